@@ -1,0 +1,2 @@
+"""Seeded synthetic input generators shared by the oracle and the CUDA library (no method arithmetic)."""
+from .inputs import *  # noqa: F401,F403

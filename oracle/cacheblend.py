@@ -1,0 +1,426 @@
+"""CPU oracle of CacheBlend's blended prefill ("cached knowledge fusion").
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product imports this module: only the
+tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+use it.  It shares no code with the CUDA library; both read their inputs from
+``harness`` (seeded generators, no method arithmetic).
+
+Everything is computed in float64 with plain numpy (matrix products are the
+only library primitive used as a step).  The one place where lower precision
+enters on purpose is the KV *storage* dtype: the cached chunk KV and the fused
+cache are rounded to the storage type (``"f64"``, ``"f32"`` or ``"bf16"``) when
+written, because that is what a cache holds.
+
+Pages cited (titles as published; sections by heading):
+
+* [P1] "論文解説: CacheBlend - RAG向けKVキャッシュ融合によるLLM推論高速化"
+  (0h-n0.github.io), an explainer of arXiv 2405.16444.
+* [P2] "KVキャッシュを再利用してLLM推論を4.49倍高速化——KVBoostが切り拓く自宅サーバーLLMの新境地".
+* [P3] "논문: CacheBlend: Fast Large Language Model Serving for RAG with Cached
+  Knowledge Fusion" (jaehun.me).
+* [P4] "LMCache: KV キャシを GPU の外へ" (ttlab.hopto.org).
+
+Readings where the pages are silent or garbled (each is restated where used):
+
+R1  RoPE pairs element i with element i + dh/2 ("rotate half"), inverse
+    frequency theta**(-2i/dh), angles evaluated in float64.
+R2  "Layer 1" of gradual filtering is the second layer (0-indexed 1): layer-0
+    K/V depend only on (token, position), so their deviation is zero.
+R3  Gradual filtering is a per-layer array of ratios of *all cached tokens*,
+    non-increasing; a negative entry means "no check: keep the previous set".
+    Layer 0 runs on every token, which supplies layer-1 inputs for the check.
+R4  The deviation of token j is the squared L2 norm of the difference of the
+    concatenated K (after re-rotation) and V rows over all KV heads.
+R5  k_i = ceil(r_i * Nc - 1e-9) over the Nc cached tokens of the request,
+    clamped to the cached candidates available; query tokens are always kept.
+R6  Top-k order: deviation descending, then token index ascending.  The
+    selected indices are returned in ascending order.
+R7  Fresh K/V of candidates that are not selected are discarded.
+R9  RMSNorm weight 1, eps 1e-5; no biases; untied LM head; no BOS token.
+R14 Selection runs on the fp32-rounded deviations, so the CUDA selection can be
+    compared bit for bit on the same fp32 array.
+
+Parity pins (tests/test_oracle_*.py) tie every function here to something other
+than itself: closed forms, invariants, the pages' printed byte counts, library
+routines (torch SDPA, complex exponentials) and brute force on tiny inputs.
+"""
+from __future__ import annotations
+
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+STORAGE_TYPES = ("f64", "f32", "bf16")
+
+
+# --------------------------------------------------------------------------- rounding
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 (8 significant bits), ties to even."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)  # x = m * 2**e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def round_storage(x: np.ndarray, storage: str) -> np.ndarray:
+    """Values as a KV cache of type ``storage`` holds them."""
+    if storage == "f64":
+        return np.asarray(x, dtype=np.float64)
+    if storage == "f32":
+        return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+    if storage == "bf16":
+        return round_bf16(x)
+    raise ValueError(storage)
+
+
+# --------------------------------------------------------------------------- RoPE
+def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
+    """Inverse frequencies theta**(-2i/dh), i < dh/2 (reading R1)."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * i / head_dim)
+
+
+def rope_rotate(x: np.ndarray, pos, theta: float) -> np.ndarray:
+    """Rotary position embedding of rows x[n, heads, dh] at positions pos[n] (or one scalar).
+
+    [P1] 技術的詳細 / 位置エンコーディングの更新: keys carry a rotation R(p) that depends on
+    their position.  Element i is paired with element i + dh/2 (reading R1):
+    (a, b) -> (a cos t - b sin t, b cos t + a sin t) with t = pos * inv_freq_i.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    n, _, dh = x.shape
+    half = dh // 2
+    pos = np.broadcast_to(np.asarray(pos, dtype=np.float64), (n,))
+    ang = pos[:, None] * rope_inv_freq(dh, theta)[None, :]  # [n, half]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def rerotate_keys(k_cached: np.ndarray, delta: int, theta: float) -> np.ndarray:
+    """K_new = R(delta) . K_cached for every row of a chunk moved by ``delta`` positions.
+
+    [P1] 技術的詳細 / 位置エンコーディングの更新, the re-rotation equation: a chunk cached at
+    positions 0..n-1 and placed at offset ``delta`` needs the extra rotation R(delta).
+    """
+    return rope_rotate(k_cached, delta, theta)
+
+
+# --------------------------------------------------------------------------- decoder pieces
+def rms_norm(x: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x**2) + eps) per row; weight 1 (reading R9)."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def causal_attention(q: np.ndarray, q_pos: Sequence[int], k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """Causal scaled-dot-product attention of sparse queries over a KV cache.
+
+    q[m, H, dh] are queries at global positions q_pos[m]; k, v[N, Hkv, dh] hold the
+    cache.  Query t attends to cache rows 0..q_pos[t] with scale 1/sqrt(dh); head h
+    reads KV head floor(h * Hkv / H) (grouped-query attention).  [P3] "어떤 토큰을
+    다시 계산하는가": selected queries attend, under the causal mask, to all available
+    K/V -- cached rows included.
+    """
+    m, H, dh = q.shape
+    Hkv = k.shape[1]
+    G = H // Hkv
+    out = np.zeros((m, H, dh), dtype=np.float64)
+    scale = 1.0 / math.sqrt(dh)
+    for t in range(m):
+        p = int(q_pos[t])
+        kk = k[: p + 1].transpose(1, 2, 0)  # [Hkv, dh, p+1]
+        vv = v[: p + 1].transpose(1, 0, 2)  # [Hkv, p+1, dh]
+        qg = q[t].reshape(Hkv, G, dh)
+        s = np.matmul(qg, kk) * scale  # [Hkv, G, p+1]
+        s = s - s.max(axis=-1, keepdims=True)
+        w = np.exp(s)
+        w = w / w.sum(axis=-1, keepdims=True)
+        out[t] = np.matmul(w, vv).reshape(H, dh)
+    return out
+
+
+def project_qkv(cfg, W: Dict[str, np.ndarray], h: np.ndarray, pos: Sequence[int]):
+    """x = RMSNorm(h); q, k, v = x W_q^T, x W_k^T, x W_v^T; RoPE on q and k at ``pos``."""
+    n = h.shape[0]
+    x = rms_norm(h, cfg.rms_eps)
+    q = (x @ W["wq"].astype(np.float64).T).reshape(n, cfg.n_heads, cfg.head_dim)
+    k = (x @ W["wk"].astype(np.float64).T).reshape(n, cfg.n_kv_heads, cfg.head_dim)
+    v = (x @ W["wv"].astype(np.float64).T).reshape(n, cfg.n_kv_heads, cfg.head_dim)
+    pos = np.asarray(pos)
+    return rope_rotate(q, pos, cfg.rope_theta), rope_rotate(k, pos, cfg.rope_theta), v
+
+
+def output_and_mlp(cfg, W: Dict[str, np.ndarray], h: np.ndarray, attn: np.ndarray) -> np.ndarray:
+    """h += attn W_o^T; h += (SiLU(x W_gate^T) * (x W_up^T)) W_down^T with x = RMSNorm(h)."""
+    n = h.shape[0]
+    h = h + attn.reshape(n, cfg.q_width) @ W["wo"].astype(np.float64).T
+    x = rms_norm(h, cfg.rms_eps)
+    g = x @ W["wgate"].astype(np.float64).T
+    u = x @ W["wup"].astype(np.float64).T
+    return h + (silu(g) * u) @ W["wdown"].astype(np.float64).T
+
+
+def first_token(cfg, weights, h_last: np.ndarray) -> int:
+    """argmax of the LM head over RMSNorm(h) of the last prompt token; ties -> lowest id."""
+    x = rms_norm(np.asarray(h_last, dtype=np.float64)[None, :], cfg.rms_eps)[0]
+    logits = weights.lm_head().astype(np.float64) @ x
+    return int(np.argmax(logits))
+
+
+# --------------------------------------------------------------------------- full prefill
+def full_prefill(cfg, weights, ids: Sequence[int], storage: str = "f64", want_logits_token: bool = True):
+    """Plain causal prefill of ``ids`` at positions 0..n-1 (the full-recompute baseline).
+
+    Returns the final hidden states [n, d], the per-layer K (with RoPE) and V as the
+    cache holds them (rounded to ``storage``), and the first generated token.
+    [P1] 実験結果 / TTFT: "Full Recompute" is the baseline CacheBlend is compared with.
+    """
+    ids = np.asarray(ids)
+    n = len(ids)
+    pos = np.arange(n)
+    h = weights.embed(ids).astype(np.float64)
+    K = np.zeros((cfg.n_layers, n, cfg.n_kv_heads, cfg.head_dim))
+    V = np.zeros_like(K)
+    for i in range(cfg.n_layers):
+        W = weights.layer(i)
+        q, k, v = project_qkv(cfg, W, h, pos)
+        K[i] = round_storage(k, storage)
+        V[i] = round_storage(v, storage)
+        attn = causal_attention(q, pos, K[i], V[i])
+        h = output_and_mlp(cfg, W, h, attn)
+    tok = first_token(cfg, weights, h[-1]) if want_logits_token else None
+    return {"hidden": h, "k": K, "v": V, "first_token": tok}
+
+
+def precompute_chunk(cfg, weights, ids: Sequence[int], storage: str):
+    """A chunk's KV cache: the chunk prefilled alone from position 0.
+
+    [P3] "어떤 문제를 해결하는가": each retrieved chunk is processed independently and its
+    KV stored; [P1] 背景と動機: each document can be precomputed on its own.
+    """
+    r = full_prefill(cfg, weights, ids, storage, want_logits_token=False)
+    return r["k"], r["v"]
+
+
+# --------------------------------------------------------------------------- HKVD
+def kv_deviation(k_new, v_new, k_fused, v_fused, mode: int = 0) -> np.ndarray:
+    """Squared KV deviation per token (reading R4).
+
+    [P1] 技術的詳細 / HKVD トークン選定: Delta_KV^(i)[j] = || KV_cached^(i)[j] - KV_full^(i)[j] ||_2.
+    The squared norm ranks tokens the same way.  mode 0: K and V together;
+    mode 1: K only; mode 2: V only.
+    """
+    n = k_new.shape[0]
+    width = int(np.prod(k_new.shape[1:]))
+    dk = (np.asarray(k_new, np.float64) - np.asarray(k_fused, np.float64)).reshape(n, width)
+    dv = (np.asarray(v_new, np.float64) - np.asarray(v_fused, np.float64)).reshape(n, width)
+    sk = np.sum(dk * dk, axis=1)
+    sv = np.sum(dv * dv, axis=1)
+    if mode == 0:
+        return sk + sv
+    if mode == 1:
+        return sk
+    if mode == 2:
+        return sv
+    raise ValueError(mode)
+
+
+def select_hkvd(dev32: np.ndarray, cand: Sequence[int], k: int) -> np.ndarray:
+    """The k candidates of highest deviation, as ascending token indices (readings R6, R14).
+
+    [P1] 段階的フィルタリングスキーム: the HKVD tokens are the top r% by deviation.
+    Order: deviation descending, then token index ascending.
+    """
+    dev32 = np.asarray(dev32, dtype=np.float32)
+    cand = np.asarray(cand, dtype=np.int64)
+    if np.any(np.isnan(dev32)):
+        raise FloatingPointError("NaN deviation")
+    if k <= 0:
+        return np.zeros(0, dtype=np.int64)
+    order = np.lexsort((cand, -dev32.astype(np.float64)))  # primary: -dev, secondary: index
+    return np.sort(cand[order[:k]])
+
+
+def k_for_ratio(r: float, n_cached: int) -> int:
+    """k = ceil(r * Nc - 1e-9) (reading R5)."""
+    if r <= 0:
+        return 0
+    return int(math.ceil(r * n_cached - 1e-9))
+
+
+def ratio_schedule(n_layers: int, r: float, schedule: str = "gradual", r1: Optional[float] = None,
+                   n_narrow: int = 3) -> List[float]:
+    """Per-layer recompute ratios of gradual filtering (reading R3).
+
+    [P1] 段階的フィルタリングスキーム: layer 1 recomputes r1 % of all tokens and measures
+    their deviation; each later layer keeps a narrower share of the previous one.
+    Layer 0: no check (all tokens).  Layer 1: r1.  Layers 2..1+n_narrow: linear from
+    r1 down to r.  Later layers: no check (the set of the last checked layer is kept).
+    ``fixed`` is r1 = r with no narrowing; ``gradual`` defaults to r1 = min(1, 2r).
+    """
+    out = [-1.0] * n_layers
+    if n_layers < 2:
+        return out
+    if schedule == "fixed":
+        out[1] = r
+        return out
+    if schedule != "gradual":
+        raise ValueError(schedule)
+    if r1 is None:
+        r1 = min(1.0, 2.0 * r)
+    out[1] = r1
+    for j in range(1, n_narrow + 1):
+        if 1 + j < n_layers:
+            out[1 + j] = r1 + (r - r1) * j / n_narrow
+    return out
+
+
+# --------------------------------------------------------------------------- blended prefill
+def _layout(segments):
+    """Offsets of each segment and the cached-token mask of the concatenated prompt."""
+    offs, ids, cached = [], [], []
+    off = 0
+    for seg in segments:
+        offs.append(off)
+        ids.append(np.asarray(seg.ids))
+        cached.append(np.full(len(seg.ids), seg.chunk >= 0))
+        off += len(seg.ids)
+    return offs, np.concatenate(ids), np.concatenate(cached)
+
+
+def init_fused_cache(cfg, segments, chunk_caches, storage: str):
+    """Fused cache before any recompute: re-rotated cached K, copied V, NaN on query rows."""
+    offs, ids, cached = _layout(segments)
+    N = len(ids)
+    Kf = np.full((cfg.n_layers, N, cfg.n_kv_heads, cfg.head_dim), np.nan)
+    Vf = np.full_like(Kf, np.nan)
+    for seg, off in zip(segments, offs):
+        if seg.chunk < 0:
+            continue
+        Kc, Vc = chunk_caches[seg.chunk]
+        n = len(seg.ids)
+        for i in range(cfg.n_layers):
+            Kf[i, off:off + n] = round_storage(rerotate_keys(Kc[i], off, cfg.rope_theta), storage)
+            Vf[i, off:off + n] = Vc[i]
+    return Kf, Vf
+
+
+def blend_prefill(cfg, weights, segments, chunk_caches, ratios: Sequence[float], storage: str = "f64",
+                  dev_mode: int = 0, force_sel: Optional[Dict[int, np.ndarray]] = None):
+    """CacheBlend's blended prefill over independently cached chunks.
+
+    Steps, in the pages' order ([P3] "어떤 토큰을 다시 계산하는가", per-layer flow; [P1]
+    選択的再計算アルゴリズム, HKVD, 段階的フィルタリング, 位置エンコーディングの更新):
+
+    1. concatenate the segments; re-rotate each cached chunk's K by its offset;
+    2. layer 0 runs on every token (reading R3);
+    3. at each layer i the tokens R_i whose layer input exists (R_i = S_{i-1}) get
+       fresh q, k, v; at a check layer (ratio >= 0) the cached ones are ranked by
+       deviation against the fused cache and the top k_i kept: S_i = Q u top-k;
+       otherwise S_i = R_i;
+    4. fresh K/V of S_i overwrite the fused cache (the rest is discarded, R7);
+    5. queries of S_i attend causally over the whole fused cache;
+    6. output projection and MLP for S_i; their hidden states go to layer i+1.
+
+    ``force_sel`` maps a check layer to the full set S_i to use instead of the top-k.
+    Returns the final hidden rows (of the last S), the sets, the deviations of each
+    check layer, the fused cache and the first token.
+    """
+    offs, ids, cached = _layout(segments)
+    N = len(ids)
+    n_cached = int(cached.sum())
+    Kf, Vf = init_fused_cache(cfg, segments, chunk_caches, storage)
+    h = np.zeros((N, cfg.d_model))
+    h[:] = weights.embed(ids).astype(np.float64)
+    R = np.arange(N)
+    sets, devs = {}, {}
+    for i in range(cfg.n_layers):
+        W = weights.layer(i)
+        q, k, v = project_qkv(cfg, W, h[R], R)
+        r_i = ratios[i]
+        if r_i >= 0:
+            is_c = cached[R]
+            cand = R[is_c]
+            dev = kv_deviation(k[is_c], v[is_c], Kf[i][cand], Vf[i][cand], dev_mode)
+            dev32 = dev.astype(np.float32)
+            devs[i] = (cand.copy(), dev32)
+            if force_sel is not None and i in force_sel:
+                S = np.asarray(force_sel[i], dtype=np.int64)
+            else:
+                kk = min(k_for_ratio(r_i, n_cached), len(cand))
+                top = select_hkvd(dev32, cand, kk)
+                S = np.union1d(top, R[~is_c]).astype(np.int64)
+        else:
+            S = R
+        loc = np.searchsorted(R, S)
+        assert np.array_equal(R[loc], S), "selected tokens must have a layer input"
+        Kf[i][S] = round_storage(k[loc], storage)
+        Vf[i][S] = round_storage(v[loc], storage)
+        attn = causal_attention(q[loc], S, Kf[i], Vf[i])
+        h[S] = output_and_mlp(cfg, W, h[S], attn)
+        sets[i] = S
+        R = S
+    tok = first_token(cfg, weights, h[N - 1])
+    return {"hidden": h[R], "rows": R, "sets": sets, "devs": devs, "k": Kf, "v": Vf,
+            "first_token": tok, "n_cached": n_cached}
+
+
+def full_reuse(cfg, weights, segments, chunk_caches, storage: str = "f64"):
+    """Full KV reuse: only the query is computed, over the re-rotated cached KV.
+
+    [P1] 実験結果 / 生成品質の評価 ("Full KV Reuse", no recompute); [P3] comparison table.
+    """
+    offs, ids, cached = _layout(segments)
+    N = len(ids)
+    Kf, Vf = init_fused_cache(cfg, segments, chunk_caches, storage)
+    Q = np.nonzero(~cached)[0]
+    h = weights.embed(ids[Q]).astype(np.float64)
+    for i in range(cfg.n_layers):
+        W = weights.layer(i)
+        q, k, v = project_qkv(cfg, W, h, Q)
+        Kf[i][Q] = round_storage(k, storage)
+        Vf[i][Q] = round_storage(v, storage)
+        attn = causal_attention(q, Q, Kf[i], Vf[i])
+        h = output_and_mlp(cfg, W, h, attn)
+    return {"hidden": h, "rows": Q, "first_token": first_token(cfg, weights, h[-1])}
+
+
+def precompute_all(cfg, weights, spec, storage: str, chunk_indices=None):
+    """Chunk caches for every chunk a workload's requests use."""
+    used = sorted({s.chunk for req in spec.requests for s in req if s.chunk >= 0})
+    if chunk_indices is not None:
+        used = [c for c in used if c in chunk_indices]
+    return {c: precompute_chunk(cfg, weights, spec.chunks[c], storage) for c in used}
+
+
+# --------------------------------------------------------------------------- cost model
+def kv_bytes_per_token(n_layers: int, n_kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    """Per-token KV size 2 * L * Hkv * dh * bytes ([P4] §4, §9-1: Qwen2.5-1.5B 28,672 B)."""
+    return 2 * n_layers * n_kv_heads * head_dim * elem_bytes
+
+
+def t_recompute(ratio: float, t_prefill: float) -> float:
+    """[P1] パイプライン化の設計: T_recompute = r% x T_prefill."""
+    return ratio * t_prefill
+
+
+def t_load(n_tokens: int, kv_bytes_token: float, n_layers_loaded: int, n_layers: int, bandwidth: float) -> float:
+    """[P1] パイプライン化の設計, T_load = PerTokenKVSize x L / StorageThroughput (reading R8:
+    the KV bytes of the request's cached tokens for the layers loaded, over the bandwidth)."""
+    return n_tokens * kv_bytes_token * (n_layers_loaded / n_layers) / bandwidth
+
+
+def pipelined_latency(t_load_layers: Sequence[float], t_rec_layers: Sequence[float]) -> float:
+    """[P3] "로딩과 재계산의 시간을 겹친다": T_layer ~ max(T_load, T_recompute), summed over layers."""
+    return float(sum(max(a, b) for a, b in zip(t_load_layers, t_rec_layers)))
+
+
+def break_even_bandwidth(kv_bytes_token: float, prefill_s_per_token: float) -> float:
+    """[P4] §5: loading beats recomputing above BW* = KV bytes per token / prefill time per token."""
+    return kv_bytes_token / prefill_s_per_token

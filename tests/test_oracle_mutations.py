@@ -1,0 +1,94 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that a pin catches each one.
+
+A pin that still passes with a wrong sign, a dropped term or an off-by-one is no pin.
+"""
+import numpy as np
+import pytest
+
+import oracle.cacheblend as ocb
+from tests import test_oracle_pins as pins
+
+
+def _rope_wrong_sign(x, pos, theta):
+    x = np.asarray(x, dtype=np.float64)
+    n, _, dh = x.shape
+    half = dh // 2
+    pos = np.broadcast_to(np.asarray(pos, dtype=np.float64), (n,))
+    ang = pos[:, None] * ocb.rope_inv_freq(dh, theta)[None, :]
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c + b * s, b * c - a * s], axis=-1)
+
+
+def _rope_adjacent_pairs(x, pos, theta):
+    x = np.asarray(x, dtype=np.float64)
+    n, _, dh = x.shape
+    pos = np.broadcast_to(np.asarray(pos, dtype=np.float64), (n,))
+    ang = pos[:, None] * ocb.rope_inv_freq(dh, theta)[None, :]
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    a, b = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = b * c + a * s
+    return out
+
+
+_orig_attention = ocb.causal_attention
+
+
+def _attention_off_by_one(q, q_pos, k, v):
+    # excludes the diagonal key except at position 0
+    return _orig_attention(q, [max(0, int(p) - 1) for p in q_pos], k, v)
+
+
+_orig_dev = ocb.kv_deviation
+
+
+def _deviation_k_only(k_new, v_new, k_fused, v_fused, mode=0):
+    return _orig_dev(k_new, v_new, k_fused, v_fused, 1)
+
+
+def _select_ties_high_index(dev32, cand, k):
+    dev32 = np.asarray(dev32, np.float32)
+    cand = np.asarray(cand, np.int64)
+    if k <= 0:
+        return np.zeros(0, np.int64)
+    order = np.lexsort((-cand, -dev32.astype(np.float64)))
+    return np.sort(cand[order[:k]])
+
+
+def _mlp_no_residual(cfg, W, h, attn):
+    n = h.shape[0]
+    h = h + attn.reshape(n, cfg.q_width) @ W["wo"].astype(np.float64).T
+    x = ocb.rms_norm(h, cfg.rms_eps)
+    return (ocb.silu(x @ W["wgate"].T) * (x @ W["wup"].T)) @ W["wdown"].T
+
+
+def _rms_no_eps_mean(x, eps):
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+MUTATIONS = [
+    ("rerotate_keys", lambda k, d, t: np.asarray(k, np.float64), [pins.test_layer0_fresh_kv_equals_rerotated_cache]),
+    ("rope_rotate", _rope_wrong_sign, [pins.test_rope_matches_complex_exponential]),
+    ("rope_rotate", _rope_adjacent_pairs, [pins.test_rope_matches_complex_exponential]),
+    ("causal_attention", _attention_off_by_one, [pins.test_attention_matches_torch_sdpa_with_sparse_queries]),
+    ("kv_deviation", _deviation_k_only, [pins.test_deviation_closed_forms]),
+    ("select_hkvd", _select_ties_high_index, [pins.test_select_exhaustive_small_with_ties]),
+    ("output_and_mlp", _mlp_no_residual, [lambda: pins.test_full_prefill_matches_torch_library_decoder(pins.TINY)]),
+    ("rms_norm", _rms_no_eps_mean, [pins.test_rms_norm_properties]),
+]
+
+
+@pytest.mark.parametrize("name,fn,tests", MUTATIONS, ids=[f"{m[0]}-{i}" for i, m in enumerate(MUTATIONS)])
+def test_planted_mistake_is_caught(monkeypatch, name, fn, tests):
+    monkeypatch.setattr(ocb, name, fn)
+    failed = 0
+    for t in tests:
+        try:
+            t()
+        except (AssertionError, FloatingPointError, ValueError):
+            failed += 1
+    assert failed == len(tests), f"mutation of {name} was not caught"
+
