@@ -1,0 +1,444 @@
+"""Blended-prefill benchmark: TTFT and context tokens/s of the blend at r = 15 % against a
+full prefill of the same prompt, with the roofline fraction of the dominant kernel.
+
+Default workload: the Mistral-7B-shaped decoder (32 layers, d 4096, 32/8 heads, FFN
+14336, bf16, random-init weights N(0, 0.02)) on a 64-token system prefix + 6 cached
+chunks of 512 tokens + a 64-token query (3200 tokens, Zipf(1.1) ids), gradual filtering
+to 15 %.  Synthetic inputs stand in for the RAG datasets of the pages.
+
+One JSON line on rank 0.  Multi-GPU (torchrun): independent replicas, one per GPU,
+no collective on the data path (weak scaling); the barrier and max-over-ranks timing
+use torch.distributed only for scalars.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "blended-prefill TTFT ms & context tok/s at r=15% vs full prefill; % roofline"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- flop / byte accounting
+def gemm_flops(cfg, rows_R, rows_S):
+    """Algorithmic flops of the projection GEMMs per layer (2 per multiply-add)."""
+    d, qw, kvw, f = cfg.d_model, cfg.q_width, cfg.kv_width, cfg.ffn_dim
+    out = {"qkv": 0.0, "oproj": 0.0, "gateup": 0.0, "down": 0.0}
+    for R, S in zip(rows_R, rows_S):
+        out["qkv"] += 2.0 * R * d * (qw + 2 * kvw)
+        out["oproj"] += 2.0 * S * qw * d
+        out["gateup"] += 2.0 * S * d * 2 * f
+        out["down"] += 2.0 * S * f * d
+    return out
+
+
+def plan_rows(cfg, n_tokens, n_cached, n_query, ratios):
+    """|R_i| and |S_i| per layer for one request (host-known sizes)."""
+    import rag_non_prefix_gb300 as cb
+
+    R, C = n_tokens, n_cached
+    rows_R, rows_S = [], []
+    for r in ratios:
+        rows_R.append(R)
+        if r >= 0:
+            k = min(cb.k_for_ratio(r, n_cached), C)
+            S, C = k + n_query, k
+        else:
+            S = R
+        rows_S.append(S)
+        R = S
+    return rows_R, rows_S
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world):
+    import torch
+
+    import harness as hz
+    import harness.device as hd
+    import rag_non_prefix_gb300 as cb
+    from rag_non_prefix_gb300 import build as cbbuild
+
+    cbbuild.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    spec = hz.workload(args.workload)
+    cfg = spec.cfg
+    ratio = spec.ratio if args.ratio is None else args.ratio
+    ratios = cb.ratio_schedule(cfg.n_layers, ratio, args.schedule or spec.schedule)
+    W = hd.device_weights(cfg, spec.seed)
+    n_tok = [spec.n_tokens(r) for r in range(len(spec.requests))]
+    T = sum(n_tok)
+    eng = cb.Engine(cfg, W, max_tokens=max(T, max(len(c) for c in spec.chunks)), max_requests=len(spec.requests),
+                    max_positions=max(n_tok) + 1)
+    used = sorted({s.chunk for req in spec.requests for s in req if s.chunk >= 0})
+    chunk_store = {}
+    for c in used:
+        ids = hd.ids_tensor(spec.chunks[c])
+        k, v = eng.precompute_chunk(ids)
+        chunk_store[c] = (ids, k, v)
+        eng.register_chunk(c, ids, k, v)
+    reqs = []
+    for req in spec.requests:
+        q = [s for s in req if s.chunk < 0][0]
+        reqs.append(eng.make_request([s.chunk for s in req if s.chunk >= 0], hd.ids_tensor(q.ids),
+                                     want_hidden=False, want_sel=False))
+    full_ids = [hd.ids_tensor(np.concatenate([s.ids for s in req])) for req in spec.requests]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 512 MiB > L2
+
+    def blend_step():
+        eng.blend_prefill(reqs, ratios, stream=stream)
+
+    def full_step():
+        for ids in full_ids:
+            eng.full_prefill(ids, want_hidden=False, stream=stream)
+
+    def timed(fn, n):
+        ts = []
+        for _ in range(n):
+            flush.fill_(1.0)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return ts
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        blend_step()
+        full_step()
+    eng.get_status()
+    eng.get_profile()  # reset launch counters
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    barrier()
+    t0 = time.perf_counter()
+    blend_ms = timed(blend_step, args.steps)
+    barrier()
+    wall = time.perf_counter() - t0
+    prof_counts = eng.get_profile()
+    full_ms = timed(full_step, args.steps)
+    barrier()
+    clocks = sampler.stop()
+    eng.get_status()
+
+    # per-phase device time of one blend (events around each phase)
+    eng.set_profiling(True)
+    flush.fill_(1.0)
+    torch.cuda.synchronize()
+    blend_step()
+    torch.cuda.synchronize()
+    phases = eng.get_profile()
+    eng.set_profiling(False)
+
+    # end to end through the public API with host buffers: query ids in, first token out
+    pinned_q = [r["query_ids"].cpu().pin_memory() for r in reqs]
+    host_tok = torch.empty(len(reqs), dtype=torch.int32).pin_memory()
+    e2e = []
+    for _ in range(args.steps):
+        flush.fill_(1.0)
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for r, pq in zip(reqs, pinned_q):
+            r["query_ids"].copy_(pq, non_blocking=True)
+        blend_step()
+        for i, r in enumerate(reqs):
+            host_tok[i:i + 1].copy_(r["first_token"], non_blocking=True)
+        torch.cuda.synchronize()
+        e2e.append((time.perf_counter() - t) * 1e3)
+    h2d = int(sum(pq.numel() * 4 for pq in pinned_q))
+    d2h = 4 * len(reqs)
+
+    # max over ranks
+    vals = torch.tensor([statistics.mean(blend_ms), statistics.mean(full_ms), statistics.mean(e2e), wall],
+                        dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
+    blend_mean, full_mean, e2e_mean, wall = [float(x) for x in vals.cpu()]
+
+    # roofline of the dominant kernel: the tcgen05 projection GEMM (all four phases)
+    rows = [plan_rows(cfg, n_tok[r], spec.n_cached(r), n_tok[r] - spec.n_cached(r), ratios) for r in range(len(reqs))]
+    rows_R = [sum(x[0][i] for x in rows) for i in range(cfg.n_layers)]
+    rows_S = [sum(x[1][i] for x in rows) for i in range(cfg.n_layers)]
+    fl = gemm_flops(cfg, rows_R, rows_S)
+    gemm_ms = sum(phases[p]["ms"] for p in ("qkv", "oproj", "gateup", "down"))
+    gemm_launches = sum(phases[p]["calls"] for p in ("qkv", "oproj", "gateup", "down"))
+    peaks = _peaks()
+    achieved = sum(fl.values()) / (gemm_ms * 1e-3) / 1e12 if gemm_ms > 0 else None
+    peak = peaks["bf16_tflops_sustained"]
+    # re-rotation of resident chunks (begin phase): K read + written, V copied
+    nc_total = sum(spec.n_cached(r) for r in range(len(reqs)))
+    es = 2 if cfg.dtype == "bf16" else 4
+    rerot_bytes = cfg.n_layers * nc_total * cfg.kv_width * es * 4  # K r/w + V r/w
+    step_launches = sum(v["launches"] for v in prof_counts.values()) / max(1, args.steps)
+    phase_ms = {k: round(v["ms"], 4) for k, v in phases.items() if v["calls"]}
+    n_total = T * world
+    ttft = blend_mean
+    out = {
+        "metric": METRIC,
+        "value": round(n_total / (ttft * 1e-3), 1),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ttft, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": cfg.dtype,
+        "data": "synthetic (harness: random-init N(0,0.02) weights, Zipf(1.1) token ids)",
+        "config": {"workload": f"{spec.name}: {cfg.n_layers}L d{cfg.d_model} H{cfg.n_heads}/{cfg.n_kv_heads} "
+                               f"ffn{cfg.ffn_dim} {cfg.dtype}; {len(reqs)} request(s) x {n_tok[0]} tokens "
+                               f"({spec.n_cached(0)} cached); r={ratio} {args.schedule or spec.schedule}",
+                   "ratio_schedule": [round(x, 4) for x in ratios], "tokens_per_step": T,
+                   "l2": "512 MiB buffer written between timed steps; weights 14+ GB > L2",
+                   "parallelism": f"replicas x{world}"},
+        "ttft_ms": {"blend": round(blend_mean, 4), "full_prefill": round(full_mean, 4),
+                    "blend_median": round(statistics.median(blend_ms), 4),
+                    "full_median": round(statistics.median(full_ms), 4)},
+        "speedup_vs_full_prefill": round(full_mean / blend_mean, 3),
+        "full_prefill_tok_s": round(n_total / (full_mean * 1e-3), 1),
+        "phase_ms": phase_ms,
+        "roofline": {"kernel": "gemm_bf16_tc (tcgen05 projections: qkv, o, gate/up, down)", "bound": "tensor",
+                     "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4) if achieved else None, "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16 sustained", "launches": gemm_launches,
+                     "flops": sum(fl.values())},
+        "rerotate": {"bytes": rerot_bytes, "ms": phase_ms.get("begin"),
+                     "gbs": round(rerot_bytes / (phase_ms["begin"] * 1e-3) / 1e9, 1) if phase_ms.get("begin") else None},
+        "e2e": {"value": round(n_total / (e2e_mean * 1e-3), 1), "unit": "tok/s", "ms": round(e2e_mean, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(step_launches * args.steps),
+        "clocks": clocks,
+    }
+    return out, spec, cfg, ratios, W
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) sample
+def oracle_sample(spec, cfg, ratios, W_dev=None, n_layers_sample=2):
+    """Times the oracle's blended prefill of the same prompt through the first
+    ``n_layers_sample`` layers and scales by algorithmic flops to the whole model.
+
+    Weights come from the harness (device generator, copied to the host: the same bits
+    as the host generator).  The cached chunk KV of the sample is harness random data of
+    the right shape: its values do not change the oracle's work.
+    """
+    import dataclasses
+
+    import torch
+
+    import harness as hz
+    import harness.device as hd
+    import oracle.cacheblend as orc
+
+    sub = dataclasses.replace(cfg, n_layers=n_layers_sample)
+
+    class SampleWeights:
+        def __init__(self):
+            self._layers = {}
+
+        def layer(self, i):
+            if i not in self._layers:
+                if W_dev is not None:
+                    src = W_dev["layers"][i]
+                    self._layers[i] = {k: v.float().cpu().numpy() for k, v in src.items()}
+                else:
+                    self._layers[i] = hz.gen_layer_weights(cfg, spec.seed, i)
+            return self._layers[i]
+
+        def embed(self, ids):
+            return hz.gen_embedding_rows(cfg, spec.seed, ids)
+
+        def lm_head(self):
+            return np.zeros((8, cfg.d_model), dtype=np.float32)  # first token is not part of the sample
+
+    Wh = SampleWeights()
+    for i in range(n_layers_sample):
+        Wh.layer(i)
+    req = spec.requests[0]
+    caches = {}
+    for s in req:
+        if s.chunk < 0:
+            continue
+        shape = (n_layers_sample, len(s.ids), cfg.n_kv_heads, cfg.head_dim)
+        if torch.cuda.is_available():
+            k = hd.synth_into(torch.empty(shape, dtype=torch.float32, device="cuda"), 0x5EED0000 + s.chunk).cpu().numpy()
+            v = hd.synth_into(torch.empty(shape, dtype=torch.float32, device="cuda"), 0x5EED8000 + s.chunk).cpu().numpy()
+        else:
+            n = int(np.prod(shape))
+            k = hz.gen_weight_fp32(0x5EED0000 + s.chunk, 0, n).reshape(shape)
+            v = hz.gen_weight_fp32(0x5EED8000 + s.chunk, 0, n).reshape(shape)
+        caches[s.chunk] = (k.astype(np.float64), v.astype(np.float64))
+    sub_ratios = ratios[:n_layers_sample]
+    t = time.perf_counter()
+    orc.blend_prefill(sub, Wh, req, caches, sub_ratios, "bf16" if cfg.dtype == "bf16" else "f32")
+    dt = time.perf_counter() - t
+    n_tok, n_c = spec.n_tokens(0), spec.n_cached(0)
+    rR, rS = plan_rows(cfg, n_tok, n_c, n_tok - n_c, ratios)
+    f_all = sum(gemm_flops(cfg, rR, rS).values())
+    f_smp = sum(gemm_flops(cfg, rR[:n_layers_sample], rS[:n_layers_sample]).values())
+    est = dt * f_all / f_smp
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+    return {"value": round(n_tok / est, 2), "unit": "tok/s", "cores": int(threads), "kind": "oracle",
+            "sample": f"oracle blend of request 0 through layers 0..{n_layers_sample - 1} ({dt:.2f} s), scaled by "
+                      f"projection flops to {cfg.n_layers} layers: est. TTFT {est:.1f} s",
+            "sample_s": round(dt, 3), "est_ttft_s": round(est, 2)}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm (CPU, rank 0 only)."""
+    import harness as hz
+    import rag_non_prefix_gb300 as cb
+
+    spec = hz.workload(args.workload)
+    cfg = spec.cfg
+    ratio = spec.ratio if args.ratio is None else args.ratio
+    ratios = cb.ratio_schedule(cfg.n_layers, ratio, args.schedule or spec.schedule)
+    W_dev = None
+    try:
+        import torch
+
+        if torch.cuda.is_available():
+            import harness.device as hd
+            from rag_non_prefix_gb300 import build as cbbuild
+
+            cbbuild.build()
+            W_dev = hd.device_weights(cfg, spec.seed, layers=2)
+    except Exception:
+        W_dev = None
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_sample(spec, cfg, ratios, W_dev)
+        if i >= args.warmup:
+            vals.append(r)
+    v = statistics.mean(x["value"] for x in vals)
+    ms = spec.n_tokens(0) / v * 1e3
+    cpu = dict(vals[-1])
+    cpu["value"] = round(v, 3)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "ratio_schedule": [round(x, 4) for x in ratios]},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(v, 3), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mistral7b")
+    ap.add_argument("--ratio", type=float, default=None)
+    ap.add_argument("--schedule", default=None, choices=[None, "fixed", "gradual"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    out, spec, cfg, ratios, W = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = oracle_sample(spec, cfg, ratios, W)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

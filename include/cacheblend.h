@@ -1,0 +1,295 @@
+/*
+ * cacheblend.h -- C ABI of the GB300 (sm_103a) blended-prefill library.
+ *
+ * CacheBlend ("cached knowledge fusion") reuses KV caches of RAG chunks that were
+ * each prefilled alone from position 0.  For a prompt made of such chunks plus a
+ * query it re-rotates the cached keys to their new positions and, layer by layer,
+ * recomputes only the tokens whose cached KV deviates most from what a full
+ * prefill would give.  Pages the comments below cite (by title and section):
+ *
+ *   [P1] "論文解説: CacheBlend - RAG向けKVキャッシュ融合によるLLM推論高速化" (0h-n0.github.io)
+ *   [P2] "KVキャッシュを再利用してLLM推論を4.49倍高速化——KVBoostが切り拓く自宅サーバーLLMの新境地"
+ *   [P3] "논문: CacheBlend: Fast Large Language Model Serving for RAG with Cached Knowledge Fusion" (jaehun.me)
+ *   [P4] "LMCache: KV キャシを GPU の外へ" (ttlab.hopto.org)
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless the argument name ends in _host.
+ *   - The caller owns every buffer (weights, KV caches, outputs, workspace) and
+ *     every stream; the library owns only the context, its events, its chunk
+ *     registry and a small rotary cos/sin table inside the workspace.
+ *   - Streams are passed as void* holding a cudaStream_t (NULL = legacy default stream).
+ *   - Calls never throw and never abort.  Arguments are checked synchronously
+ *     (null pointers, sizes, 16-byte alignment of vector I/O, dtype) and a bad one
+ *     returns an error before anything is enqueued.  Device-side problems (a NaN
+ *     deviation, an index out of range, a bounded wait that ran out) set bits of a
+ *     status word in the workspace; cb_get_status() reports them.
+ *   - Everything is asynchronous on the given stream except cb_synchronize(),
+ *     cb_get_status(), the *_size() queries, cb_create/cb_destroy and
+ *     cb_set_workspace().
+ *   - Row-major layouts; weights are [out_features][in_features].  KV caches are
+ *     [n_layers][n_tokens][n_kv_heads][head_dim] of the model dtype.
+ */
+#ifndef CACHEBLEND_H
+#define CACHEBLEND_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CB_OK = 0,
+  CB_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad enum, out-of-range scalar */
+  CB_ERR_SHAPE = 2,        /* sizes that do not fit the model or the kernels' tiling */
+  CB_ERR_DTYPE = 3,        /* dtype not supported by this entry point */
+  CB_ERR_NOT_FOUND = 4,    /* chunk id missing from the registry */
+  CB_ERR_WORKSPACE = 5,    /* no workspace, or too small for the call */
+  CB_ERR_CUDA = 6,         /* a CUDA runtime call failed (cb_last_error has its text) */
+  CB_ERR_TIMEOUT = 7,      /* a host wait passed its deadline */
+  CB_ERR_NAN = 8,          /* a deviation was NaN (reported by the device status word) */
+  CB_ERR_DEVICE = 9,       /* another device-side check failed (index range, bounded wait) */
+  CB_ERR_STATE = 10        /* call out of order (e.g. prefill_layer before blend_begin) */
+} cb_status;
+
+typedef enum { CB_F32 = 0, CB_BF16 = 1 } cb_dtype;
+
+/* Decoder shape.  head_dim must be 128 for CB_BF16 (64 or 128 for CB_F32);
+ * d_model, n_heads*head_dim and ffn_dim multiples of 128 for CB_BF16.
+ * max_positions bounds token positions (rotary table size). */
+typedef struct {
+  int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+  double rope_theta;
+  float rms_eps;
+  cb_dtype dtype;
+  int max_positions;
+} cb_model_cfg;
+
+/* Borrowed weight pointers (device, model dtype).  The per-layer members are HOST
+ * arrays of n_layers device pointers; cb_create copies the arrays, not the weights.
+ *   embed [vocab][d]   lm_head [vocab][d]
+ *   wq [H*dh][d]  wk, wv [Hkv*dh][d]  wo [d][H*dh]  wgate, wup [ffn][d]  wdown [d][ffn]
+ * RMSNorm weights are 1 and there are no biases. */
+typedef struct {
+  const void* embed;
+  const void* lm_head;
+  const void* const* wq;
+  const void* const* wk;
+  const void* const* wv;
+  const void* const* wo;
+  const void* const* wgate;
+  const void* const* wup;
+  const void* const* wdown;
+} cb_weights;
+
+typedef struct cb_ctx cb_ctx;
+
+/* --------------------------------------------------------------------- lifetime */
+cb_status cb_create(const cb_model_cfg* cfg, const cb_weights* weights, cb_ctx** out);
+cb_status cb_destroy(cb_ctx* ctx);
+const char* cb_status_string(cb_status s);
+/* Text of the last error seen by this context (or by the standalone calls if ctx is NULL). */
+const char* cb_last_error(const cb_ctx* ctx);
+
+/* Workspace: device memory the caller allocates (e.g. with torch.empty) and hands
+ * over.  max_tokens bounds the total prompt tokens of one call summed over its
+ * requests; max_requests bounds the requests of one call. */
+size_t cb_workspace_size(const cb_ctx* ctx, int max_tokens, int max_requests);
+/* Binds the workspace; writes the rotary table into it (synchronous). */
+cb_status cb_set_workspace(cb_ctx* ctx, void* ws, size_t bytes, int max_tokens, int max_requests);
+
+/* --------------------------------------------------------------------- chunk cache
+ * A chunk's KV cache is the chunk prefilled ALONE from position 0: [P3] "어떤 문제를
+ * 해결하는가" and [P1] 背景と動機 (each retrieved document is precomputed on its own).
+ * cb_precompute_chunk runs that prefill on the GPU and writes K (with rotary
+ * embedding at local positions) and V for every layer:
+ *   ids [n] int32;  k_out, v_out [n_layers][n][n_kv_heads][head_dim].  */
+cb_status cb_precompute_chunk(cb_ctx* ctx, const int32_t* ids, int n, void* k_out, void* v_out, void* stream);
+
+/* Registers a cached chunk under chunk_id (the pages key caches by text hash:
+ * [P1] vLLMとの統合, hash table in CPU memory; [P3] loading controller).
+ * ids: device int32[n] token ids (needed because layer 0 runs on every token).
+ * k, v: [n_layers][n][n_kv_heads][head_dim]; device memory if on_host == 0, else
+ * page-locked host memory (staged per layer by cb_fetch_kv).  Borrowed: the
+ * caller keeps them alive while registered.  Re-registering an id replaces it. */
+cb_status cb_register_chunk(cb_ctx* ctx, uint64_t chunk_id, const int32_t* ids, const void* k, const void* v,
+                            int n, int on_host);
+cb_status cb_unregister_chunk(cb_ctx* ctx, uint64_t chunk_id);
+int cb_registered_chunks(const cb_ctx* ctx);
+
+/* --------------------------------------------------------------------- standalone kernels */
+
+/* RoPE re-rotation of cached keys by delta_pos positions; V is copied.
+ * [P1] 技術的詳細 / 位置エンコーディングの更新: K_new[j] = R(dp_j) . K_cached[j].
+ * Rotary pairs are (i, i + head_dim/2) with angle delta_pos * theta^(-2i/head_dim),
+ * evaluated in double precision on the host; the rotation runs in fp32.
+ * k_src/k_dst, v_src/v_dst: [n_tok][n_kv_heads][head_dim] of dtype, 16-byte
+ * aligned; in place (src == dst) is allowed.  v_src/v_dst may both be NULL. */
+cb_status cb_rope_rerotate(const void* k_src, void* k_dst, const void* v_src, void* v_dst, int n_tok,
+                           int n_kv_heads, int head_dim, int delta_pos, double theta, cb_dtype dtype,
+                           void* stream);
+
+/* Squared KV deviation of fresh rows against the fused cache.
+ * [P1] 技術的詳細 / HKVD トークン選定: Delta_KV^(i)[j] = ||KV_cached^(i)[j] - KV_full^(i)[j]||_2
+ * (squared: same ranking).  k_new, v_new: fp32 [n][kv_width] (fresh, after RoPE);
+ * k_fus, v_fus: dtype [*][kv_width]; row j is compared with fused row idx[j]
+ * (idx NULL: row j).  mode 0 = K and V, 1 = K only, 2 = V only.  dev_out fp32 [n];
+ * accumulation in fp32. */
+cb_status cb_kv_deviation(const float* k_new, const float* v_new, const void* k_fus, const void* v_fus,
+                          const int32_t* idx, int n, int kv_width, int mode, cb_dtype dtype, float* dev_out,
+                          void* stream);
+
+/* HKVD selection: the k candidates of largest deviation, ties to the smaller
+ * candidate value, written to sel_out[k] in ASCENDING order.
+ * [P1] 段階的フィルタリングスキーム (top r% by deviation).  dev fp32 [n]; cand int32 [n]
+ * (token indices, distinct; NULL = 0..n-1).  n <= 65536, 0 <= k <= n.  A NaN
+ * deviation sets CB_ERR_NAN in *status (device int32, may be NULL); the NaN ranks
+ * below every number. */
+cb_status cb_select_hkvd(const float* dev, const int32_t* cand, int n, int k, int32_t* sel_out, int32_t* status,
+                         void* stream);
+
+/* Dense GEMM used by the projections: C = A . B^T with A [M][K], B [N][K] of dtype,
+ * fp32 accumulation.  epilogue 0: C fp32 [M][ldc] = acc;  1: C fp32 += acc
+ * (residual add);  2: C (dtype) [M][N/2] = SiLU(acc[:, gate]) * acc[:, up] where
+ * B2 (may not be NULL) holds the "up" rows and B the "gate" rows, each [N/2][K]
+ * (then N counts both).  bf16 runs on the tcgen05 tensor cores, fp32 on CUDA cores.
+ * bf16 needs K % 64 == 0 and N % 128 == 0 (N/2 % 64 for epilogue 2). */
+cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, int N, int K, int ldc, int epilogue,
+                  cb_dtype dtype, void* stream);
+
+/* Causal attention of sparse queries over one KV cache ([P3] "어떤 토큰을 다시 계산하는가":
+ * selected queries attend under the causal mask to all available K/V).
+ * q [m][n_heads][head_dim] dtype; q_pos int32 [m] (positions, < n_kv);
+ * k, v [n_kv][n_kv_heads][head_dim] dtype; out [m][n_heads][head_dim] dtype.
+ * Scale 1/sqrt(head_dim); head h reads KV head h / (n_heads / n_kv_heads). */
+cb_status cb_attention(const void* q, const int32_t* q_pos, int m, const void* k, const void* v, int n_kv,
+                       int n_heads, int n_kv_heads, int head_dim, void* out, cb_dtype dtype, void* stream);
+
+/* --------------------------------------------------------------------- blended prefill */
+
+/* Per-layer ratio of ALL cached tokens of a request to keep recomputed
+ * (gradual filtering, [P1] 段階的フィルタリングスキーム; [P3] §4.3 narrowing of the
+ * candidates).  layer_ratio is a HOST array [n_layers]; a negative entry means
+ * "no check: keep the previous layer's set".  Layer 0 always runs on every token.
+ * At a check layer k = ceil(r * Nc - 1e-9) cached tokens are kept (clamped to the
+ * candidates that exist); query tokens are always kept.
+ * dev_mode: 0 = K and V, 1 = K only, 2 = V only.
+ * forced_sel_host: NULL, or a host array [n_layers] of host int32 arrays: at a
+ * check layer with a non-NULL entry the given sets replace the top-k (used to
+ * separate numerics from selection).  Each entry lists, request after request,
+ * a count c followed by c ascending cached token indices of that request. */
+typedef struct {
+  int n_layers;
+  const double* layer_ratio_host;
+  int dev_mode;
+  const int32_t* const* forced_sel_host;
+} cb_blend_params;
+
+/* One prompt: cached chunks (by registry id) in order, then the query tokens
+ * (uncached, always recomputed).  A system prefix is simply the first chunk.
+ *   query_ids: device int32 [n_query] (n_query >= 1)
+ *   fused_k, fused_v: caller-owned [n_layers][N][n_kv_heads][head_dim] (N = all
+ *     prompt tokens): the blended cache, written by the call
+ *   out_hidden: NULL or fp32 [N][d_model]; rows of the final recomputed set are
+ *     written (other rows untouched)
+ *   out_sel: NULL or int32 [n_layers][N]: per layer the recomputed token indices,
+ *     ascending; out_sel_count: NULL or int32 [n_layers] (device)
+ *   out_first_token: NULL or int32 [1]: argmax of the LM head at the last token */
+typedef struct {
+  int n_chunks;
+  const uint64_t* chunk_ids_host;
+  const int32_t* query_ids;
+  int n_query;
+  void* fused_k;
+  void* fused_v;
+  float* out_hidden;
+  int32_t* out_sel;
+  int32_t* out_sel_count;
+  int32_t* out_first_token;
+} cb_request;
+
+/* Whole blended prefill of n_req prompts (batched: the projections of all
+ * requests share one GEMM per weight).  Equivalent to cb_blend_begin, then
+ * cb_fetch_kv for every layer on copy_stream, cb_prefill_layer for every layer
+ * on stream, cb_blend_finish.  copy_stream may be NULL when no chunk lives on the host. */
+cb_status cb_blend_prefill(cb_ctx* ctx, const cb_request* reqs, int n_req, const cb_blend_params* params,
+                           void* stream, void* copy_stream);
+
+/* Full prefill of ids [n] from position 0 (the full-recompute baseline, [P1] 実験結果).
+ * k_out, v_out: NULL or [n_layers][n][n_kv_heads][head_dim] (NULL: a one-layer
+ * buffer inside the workspace is used); out_hidden: NULL or fp32 [n][d_model];
+ * first_token: NULL or int32 [1]. */
+cb_status cb_full_prefill(cb_ctx* ctx, const int32_t* ids, int n, void* k_out, void* v_out, float* out_hidden,
+                          int32_t* first_token, void* stream);
+
+/* --------------------------------------------------------------------- per-layer API
+ * The pages' three calls ([P1] vLLMとの統合): fetch_kv(text, layer_id) loads a layer's
+ * cached KV, prefill_layer(input_dict, KVCache) runs the partial prefill of the
+ * selected tokens, synchronize() waits for the load.  Loading of layer i+1 overlaps
+ * the recompute of layer i ([P1] パイプライン化の設計; [P3] "로딩과 재계산의 시간을 겹친다":
+ * T_layer ~ max(T_load, T_recompute)). */
+
+/* Plans a batch (sizes of every layer's sets are fixed here), gathers embeddings,
+ * re-rotates every device-resident chunk into the fused caches (all layers). */
+cb_status cb_blend_begin(cb_ctx* ctx, const cb_request* reqs, int n_req, const cb_blend_params* params,
+                         void* stream);
+/* Enqueues on copy_stream the host->device copy of layer `layer` of every
+ * host-resident chunk of the batch into the fused caches and records an event. */
+cb_status cb_fetch_kv(cb_ctx* ctx, int layer, void* copy_stream);
+/* Host wait, with a deadline, for the copy of `layer` (CB_ERR_TIMEOUT when it passes). */
+cb_status cb_synchronize(cb_ctx* ctx, int layer, int timeout_ms);
+/* Layer `layer` of the blend on stream: waits (on the device) for its fetch,
+ * re-rotates its host-staged keys in place, then QKV for R_i, deviation and
+ * selection at check layers, scatter, attention, output projection and MLP. */
+cb_status cb_prefill_layer(cb_ctx* ctx, int layer, void* stream);
+/* cb_prefill_layer, preceded by cb_fetch_kv of the same layer on the same stream
+ * when that layer has host-resident chunks (no overlap; the simple form). */
+cb_status cb_blend_layer(cb_ctx* ctx, int layer, void* stream);
+/* Final norm, LM head and argmax of each request's last token; writes outputs. */
+cb_status cb_blend_finish(cb_ctx* ctx, void* stream);
+
+/* Waits (deadline timeout_ms) for the work enqueued so far on `stream` and reports
+ * the device status word: CB_OK, CB_ERR_NAN or CB_ERR_DEVICE.  Clears it. */
+cb_status cb_get_status(cb_ctx* ctx, void* stream, int timeout_ms);
+
+/* --------------------------------------------------------------------- profiling
+ * Per-phase device time of the batches run since the last cb_get_profile, from CUDA
+ * events recorded on the compute stream around each phase (only while profiling is
+ * enabled), and the number of kernels each phase launched (always counted). */
+enum {
+  CB_PH_BEGIN = 0,      /* embedding gather + re-rotation of device-resident chunks */
+  CB_PH_STAGED_ROT,     /* in-place re-rotation of host-staged chunks */
+  CB_PH_NORM,           /* RMSNorm (attention and MLP inputs) */
+  CB_PH_QKV,            /* q/k/v projection GEMM */
+  CB_PH_ROPE,           /* RoPE of fresh q and k */
+  CB_PH_DEVIATION,      /* KV deviation (check layers) */
+  CB_PH_SELECT,         /* HKVD top-k (check layers) */
+  CB_PH_SCATTER,        /* compaction, q conversion, KV scatter into the fused cache */
+  CB_PH_ATTENTION,      /* causal sparse-query attention */
+  CB_PH_OPROJ,          /* output projection GEMM + residual */
+  CB_PH_GATEUP,         /* gate/up GEMM + SiLU-mul */
+  CB_PH_DOWN,           /* down projection GEMM + residual */
+  CB_PH_FINISH,         /* final norm, LM head, argmax, outputs */
+  CB_N_PHASES
+};
+typedef struct {
+  float ms[CB_N_PHASES];     /* summed device time per phase (0 when profiling was off) */
+  int launches[CB_N_PHASES]; /* kernels launched per phase */
+  int calls[CB_N_PHASES];    /* timed phase instances */
+} cb_profile;
+cb_status cb_set_profiling(cb_ctx* ctx, int enable);
+/* Waits for the recorded events, fills *out and resets the counters. */
+cb_status cb_get_profile(cb_ctx* ctx, cb_profile* out);
+
+/* A context runs one batch at a time and reuses its workspace for the next one:
+ * issue consecutive batches on one stream (or synchronize between them). */
+
+/* Sizes of the current batch's sets (host values known at cb_blend_begin):
+ * counts_host [n_layers] receives |S_i| of request `request`. */
+cb_status cb_plan_counts(const cb_ctx* ctx, int request, int32_t* counts_host);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CACHEBLEND_H */

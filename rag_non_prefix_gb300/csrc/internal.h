@@ -1,0 +1,91 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cacheblend.h"
+
+namespace cb {
+
+// One re-rotation job: n_rows rows of one chunk/layer moved by `delta` positions.
+struct RerotSeg {
+  const void* k_src;
+  const void* v_src;  // may be null (no V copy)
+  void* k_dst;
+  void* v_dst;
+  int n_rows;
+  int delta;
+};
+
+// Per request, per layer: where its rows sit in the batched R and S row lists.
+struct PlanEntry {
+  int r_off, r_n;   // rows of R_i (layer input) of this request
+  int s_off, s_n;   // rows of S_i (kept / recomputed) of this request
+  int k;            // cached tokens kept at a check layer
+  int check;        // 1: deviation + selection at this layer
+  int forced_off;   // offset of forced selection (token positions) in the forced buffer, -1 if none
+  int pad;
+};
+
+// Per request: its fused cache and prompt sizes.
+struct ReqDev {
+  void* k;                 // fused K [n_layers][N][Hkv][dh] (or one layer when layer_stride == 0)
+  void* v;
+  long long layer_stride;  // elements between consecutive layers of the fused cache
+  int n_tokens;            // N
+  int n_cached;            // Nc: tokens 0..Nc-1 are cached, Nc..N-1 the query
+};
+
+// Attention work item: `count` query rows of S starting at `row0`, one request.
+struct AttnTile {
+  int req;
+  int row0;
+  int count;
+  int pad;
+};
+
+cudaError_t launch_embed(const void* embed, const int32_t* ids, int n_rows, int d, int vocab, cb_dtype dt, float* h,
+                         int32_t* status, cudaStream_t s);
+cudaError_t launch_rerotate(const RerotSeg* segs, int n_segs, int max_rows, int n_kv_heads, int head_dim,
+                            const float2* rope_table, int max_pos, cb_dtype dt, int32_t* status, cudaStream_t s);
+cudaError_t launch_rerotate_single(const void* k_src, void* k_dst, const void* v_src, void* v_dst, int n_rows,
+                                   int n_kv_heads, int head_dim, const float* cs_host, cb_dtype dt, cudaStream_t s);
+cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x, cb_dtype dt, cudaStream_t s);
+cudaError_t launch_rope_qk(float* qkv, const int32_t* pos, int n_rows, int n_heads, int n_kv_heads, int head_dim,
+                           const float2* rope_table, int max_pos, int32_t* status, cudaStream_t s);
+cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* pos, const int32_t* req,
+                                  const ReqDev* reqs, int layer, int n_heads, int n_kv_heads, int head_dim, int mode,
+                                  cb_dtype dt, float* dev, int32_t* status, cudaStream_t s);
+cudaError_t launch_deviation_plain(const float* k_new, const float* v_new, const void* k_fus, const void* v_fus,
+                                   const int32_t* idx, int n, int kv_width, int mode, cb_dtype dt, float* dev,
+                                   cudaStream_t s);
+cudaError_t launch_select_plain(const float* dev, const int32_t* cand, int n, int k, int32_t* sel_out,
+                                int32_t* status, cudaStream_t s);
+cudaError_t launch_select_batched(const float* dev, const int32_t* r_pos, const PlanEntry* plan, const ReqDev* reqs,
+                                  const int32_t* forced, int n_req, int32_t* s_src, int32_t* s_pos, int32_t* s_req,
+                                  int32_t* status, cudaStream_t s);
+cudaError_t launch_post_qkv(const float* qkv, int n_s_rows, const int32_t* s_src, const int32_t* s_pos,
+                            const int32_t* s_req, const ReqDev* reqs, int layer, int n_heads, int n_kv_heads,
+                            int head_dim, cb_dtype dt, void* q_out, const float* h_in, float* h_out, int d,
+                            int32_t* status, cudaStream_t s);
+cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, void* C,
+                        int M, int N, int K, int ldc, int mode, cb_dtype dt, int32_t* status, cudaStream_t s);
+cudaError_t launch_attention(const void* q, const int32_t* s_pos, const int32_t* s_req, const ReqDev* reqs,
+                             const AttnTile* tiles, int n_tiles, int layer, int n_heads, int n_kv_heads, int head_dim,
+                             void* out, cb_dtype dt, cudaStream_t s);
+int attention_tile_rows(int n_heads, int n_kv_heads, cb_dtype dt);
+cudaError_t launch_last_rows_norm(const float* h, const int32_t* rows, int n, int d, float eps, float* x_out,
+                                  cudaStream_t s);
+cudaError_t launch_lm_head(const float* x, int n_req, int d, const void* w, int vocab, cb_dtype dt, float* logits,
+                           cudaStream_t s);
+cudaError_t launch_argmax(const float* logits, int n_req, int vocab, int32_t* const* outs, int32_t* out_dev,
+                          cudaStream_t s);
+cudaError_t launch_write_hidden(const float* h, const int32_t* s_pos, int row0, int n, int d, float* out,
+                                cudaStream_t s);
+
+// tensor-map encoder (driver entry point, resolved once)
+bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                         uint32_t box_rows);
+
+}  // namespace cb

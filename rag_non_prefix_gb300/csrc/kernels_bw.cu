@@ -1,0 +1,556 @@
+// Bandwidth-bound kernels of the blended prefill: embedding gather, RoPE re-rotation
+// of cached keys, RMSNorm, RoPE of fresh q/k, KV deviation, compaction + KV scatter,
+// LM head and argmax.  All use 16-byte vector accesses; rows are independent.
+#include "common.cuh"
+#include "internal.h"
+
+namespace cb {
+
+static inline int grid_for(long long work, int per_block, int cap = 152 * 16) {
+  long long g = (work + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return static_cast<int>(g);
+}
+
+// ----------------------------------------------------------------------------- embedding
+template <typename T>
+__global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict__ ids, int d, int vocab,
+                             float* __restrict__ h, int32_t* status) {
+  const int row = blockIdx.x;
+  int id = ids[row];
+  if (id < 0 || id >= vocab) {  // out-of-range token id: flag it and read row 0 instead
+    if (threadIdx.x == 0) set_status(status, ST_RANGE);
+    id = 0;
+  }
+  const T* src = E + static_cast<size_t>(id) * d;
+  float* dst = h + static_cast<size_t>(row) * d;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float f[8];
+    load8(src + c, f);
+    store8(dst + c, f);
+  }
+}
+
+cudaError_t launch_embed(const void* embed, const int32_t* ids, int n_rows, int d, int vocab, cb_dtype dt, float* h,
+                         int32_t* status, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  if (dt == CB_BF16)
+    embed_kernel<bf16><<<n_rows, 128, 0, s>>>(static_cast<const bf16*>(embed), ids, d, vocab, h, status);
+  else
+    embed_kernel<float><<<n_rows, 128, 0, s>>>(static_cast<const float*>(embed), ids, d, vocab, h, status);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- re-rotation
+// K rows: pairs (i, i + dh/2) of each head rotated by the angle delta * inv_freq_i,
+// whose (cos, sin) come from cs[i].  V rows are copied.  One thread owns 8 pairs of
+// K (two 16-byte vectors of a row) or one 16-byte vector of V.
+template <typename T>
+__device__ __forceinline__ void rerotate_item(const T* __restrict__ ks, T* __restrict__ kd, const T* __restrict__ vs,
+                                              T* __restrict__ vd, long long t, int kvw, int head_dim,
+                                              const float2* __restrict__ cs) {
+  const int half = head_dim / 2;
+  const int kthreads = kvw / 16;
+  const int vthreads = vs ? kvw / 8 : 0;
+  const int per_row = kthreads + vthreads;
+  const long long row = t / per_row;
+  const int w = static_cast<int>(t - row * per_row);
+  if (w < kthreads) {
+    const int cpr = half / 8;  // 8-pair chunks per head
+    const int head = w / cpr, c = w - head * cpr;
+    const size_t base = static_cast<size_t>(row) * kvw + static_cast<size_t>(head) * head_dim + c * 8;
+    float a[8], b[8], na[8], nb[8];
+    load8(ks + base, a);
+    load8(ks + base + half, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 r = cs[c * 8 + j];
+      na[j] = a[j] * r.x - b[j] * r.y;
+      nb[j] = b[j] * r.x + a[j] * r.y;
+    }
+    store8(kd + base, na);
+    store8(kd + base + half, nb);
+  } else {
+    const size_t base = static_cast<size_t>(row) * kvw + (w - kthreads) * 8;
+    float f[8];
+    load8(vs + base, f);
+    store8(vd + base, f);
+  }
+}
+
+template <typename T>
+__global__ void rerotate_batched_kernel(const RerotSeg* __restrict__ segs, int n_kv_heads, int head_dim,
+                                        const float2* __restrict__ table, int max_pos, int32_t* status) {
+  const RerotSeg sg = segs[blockIdx.y];
+  const int kvw = n_kv_heads * head_dim;
+  if (sg.delta < 0 || sg.delta >= max_pos) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_status(status, ST_RANGE);
+    return;
+  }
+  const float2* cs = table + static_cast<size_t>(sg.delta) * (head_dim / 2);
+  const int per_row = kvw / 16 + (sg.v_src ? kvw / 8 : 0);
+  const long long total = static_cast<long long>(sg.n_rows) * per_row;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x)
+    rerotate_item<T>(static_cast<const T*>(sg.k_src), static_cast<T*>(sg.k_dst), static_cast<const T*>(sg.v_src),
+                     static_cast<T*>(sg.v_dst), t, kvw, head_dim, cs);
+}
+
+struct CosSin {
+  float2 v[64];
+};
+
+template <typename T>
+__global__ void rerotate_single_kernel(const T* __restrict__ ks, T* __restrict__ kd, const T* __restrict__ vs,
+                                       T* __restrict__ vd, int n_rows, int kvw, int head_dim, CosSin cs) {
+  const int per_row = kvw / 16 + (vs ? kvw / 8 : 0);
+  const long long total = static_cast<long long>(n_rows) * per_row;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x)
+    rerotate_item<T>(ks, kd, vs, vd, t, kvw, head_dim, cs.v);
+}
+
+cudaError_t launch_rerotate(const RerotSeg* segs, int n_segs, int max_rows, int n_kv_heads, int head_dim,
+                            const float2* rope_table, int max_pos, cb_dtype dt, int32_t* status, cudaStream_t s) {
+  if (n_segs <= 0 || max_rows <= 0) return cudaSuccess;
+  const int kvw = n_kv_heads * head_dim;
+  const long long work = static_cast<long long>(max_rows) * (kvw / 16 + kvw / 8);
+  const int gx = grid_for(work, 256, 1 << 16);
+  dim3 grid(gx, n_segs);
+  if (dt == CB_BF16)
+    rerotate_batched_kernel<bf16><<<grid, 256, 0, s>>>(segs, n_kv_heads, head_dim, rope_table, max_pos, status);
+  else
+    rerotate_batched_kernel<float><<<grid, 256, 0, s>>>(segs, n_kv_heads, head_dim, rope_table, max_pos, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rerotate_single(const void* k_src, void* k_dst, const void* v_src, void* v_dst, int n_rows,
+                                   int n_kv_heads, int head_dim, const float* cs_host, cb_dtype dt, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  CosSin cs;
+  for (int i = 0; i < head_dim / 2; ++i) cs.v[i] = make_float2(cs_host[2 * i], cs_host[2 * i + 1]);
+  const int kvw = n_kv_heads * head_dim;
+  const long long work = static_cast<long long>(n_rows) * (kvw / 16 + (v_src ? kvw / 8 : 0));
+  const int g = grid_for(work, 256, 152 * 32);
+  if (dt == CB_BF16)
+    rerotate_single_kernel<bf16><<<g, 256, 0, s>>>(static_cast<const bf16*>(k_src), static_cast<bf16*>(k_dst),
+                                                   static_cast<const bf16*>(v_src), static_cast<bf16*>(v_dst), n_rows,
+                                                   kvw, head_dim, cs);
+  else
+    rerotate_single_kernel<float><<<g, 256, 0, s>>>(static_cast<const float*>(k_src), static_cast<float*>(k_dst),
+                                                    static_cast<const float*>(v_src), static_cast<float*>(v_dst),
+                                                    n_rows, kvw, head_dim, cs);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- RMSNorm
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = (l < (blockDim.x >> 5)) ? red[l] : 0.f;
+  t = warp_sum(t);
+  __syncthreads();
+  return t;
+}
+
+template <typename T>
+__global__ void rmsnorm_kernel(const float* __restrict__ h, int d, float eps, T* __restrict__ x) {
+  __shared__ float red[32];
+  const size_t row = blockIdx.x;
+  const float* src = h + row * d;
+  float ss = 0.f;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float f[8];
+    load8(src + c, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+  }
+  ss = block_sum_256(ss, red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  T* dst = x + row * d;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float f[8];
+    load8(src + c, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] *= inv;
+    store8(dst + c, f);
+  }
+}
+
+cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x, cb_dtype dt, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  if (dt == CB_BF16)
+    rmsnorm_kernel<bf16><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<bf16*>(x));
+  else
+    rmsnorm_kernel<float><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<float*>(x));
+  return cudaGetLastError();
+}
+
+// final norm of selected rows into fp32 (LM-head input)
+__global__ void last_rows_norm_kernel(const float* __restrict__ h, const int32_t* __restrict__ rows, int d, float eps,
+                                      float* __restrict__ x) {
+  __shared__ float red[32];
+  const float* src = h + static_cast<size_t>(rows[blockIdx.x]) * d;
+  float ss = 0.f;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float f[8];
+    load8(src + c, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+  }
+  ss = block_sum_256(ss, red);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  float* dst = x + static_cast<size_t>(blockIdx.x) * d;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float f[8];
+    load8(src + c, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] *= inv;
+    store8(dst + c, f);
+  }
+}
+
+cudaError_t launch_last_rows_norm(const float* h, const int32_t* rows, int n, int d, float eps, float* x_out,
+                                  cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  last_rows_norm_kernel<<<n, 256, 0, s>>>(h, rows, d, eps, x_out);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- RoPE of fresh q and k
+// In place on the fp32 [rows][(H + 2 Hkv) dh] projection output: heads 0..H-1 (q) and
+// H..H+Hkv-1 (k) rotated at each row's position.  One thread owns 8 pairs.
+__global__ void rope_qk_kernel(float* __restrict__ qkv, const int32_t* __restrict__ pos, int n_rows, int n_heads,
+                               int n_kv_heads, int head_dim, const float2* __restrict__ table, int max_pos,
+                               int32_t* status) {
+  const int half = head_dim / 2, cpr = half / 8;
+  const int width = (n_heads + 2 * n_kv_heads) * head_dim;
+  const int per_row = (n_heads + n_kv_heads) * cpr;
+  const long long total = static_cast<long long>(n_rows) * per_row;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = t / per_row;
+    const int w = static_cast<int>(t - row * per_row);
+    const int head = w / cpr, c = w - head * cpr;
+    const int p = pos[row];
+    if (p < 0 || p >= max_pos) {
+      set_status(status, ST_RANGE);
+      continue;
+    }
+    float* base = qkv + static_cast<size_t>(row) * width + static_cast<size_t>(head) * head_dim + c * 8;
+    const float2* cs = table + static_cast<size_t>(p) * half + c * 8;
+    float a[8], b[8];
+    load8(base, a);
+    load8(base + half, b);
+    float na[8], nb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 r = cs[j];
+      na[j] = a[j] * r.x - b[j] * r.y;
+      nb[j] = b[j] * r.x + a[j] * r.y;
+    }
+    store8(base, na);
+    store8(base + half, nb);
+  }
+}
+
+cudaError_t launch_rope_qk(float* qkv, const int32_t* pos, int n_rows, int n_heads, int n_kv_heads, int head_dim,
+                           const float2* rope_table, int max_pos, int32_t* status, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  const long long work = static_cast<long long>(n_rows) * (n_heads + n_kv_heads) * (head_dim / 16);
+  rope_qk_kernel<<<grid_for(work, 256), 256, 0, s>>>(qkv, pos, n_rows, n_heads, n_kv_heads, head_dim, rope_table,
+                                                     max_pos, status);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- KV deviation
+template <typename T>
+__device__ __forceinline__ float dev_row(const float* __restrict__ kn, const float* __restrict__ vn,
+                                         const T* __restrict__ kf, const T* __restrict__ vf, int kvw, int mode) {
+  float acc = 0.f;
+  for (int c = (threadIdx.x & 31) * 8; c < kvw; c += 256) {
+    float a[8], b[8];
+    if (mode != 2) {
+      load8(kn + c, a);
+      load8(kf + c, b);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e = a[j] - b[j];
+        acc += e * e;
+      }
+    }
+    if (mode != 1) {
+      load8(vn + c, a);
+      load8(vf + c, b);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e = a[j] - b[j];
+        acc += e * e;
+      }
+    }
+  }
+  return warp_sum(acc);
+}
+
+// One warp per row of R; only cached rows (position < Nc of their request) are candidates.
+template <typename T>
+__global__ void deviation_rows_kernel(const float* __restrict__ qkv, int n_rows, const int32_t* __restrict__ pos,
+                                      const int32_t* __restrict__ req, const ReqDev* __restrict__ reqs, int layer,
+                                      int q_width, int kvw, int mode, float* __restrict__ dev, int32_t* status) {
+  const int warps = blockDim.x >> 5;
+  const int row = blockIdx.x * warps + (threadIdx.x >> 5);
+  if (row >= n_rows) return;
+  const int p = pos[row];
+  const ReqDev rq = reqs[req[row]];
+  if (p >= rq.n_cached) {
+    if ((threadIdx.x & 31) == 0) dev[row] = 0.f;
+    return;
+  }
+  if (p < 0) {
+    if ((threadIdx.x & 31) == 0) set_status(status, ST_RANGE);
+    return;
+  }
+  const size_t width = static_cast<size_t>(q_width) + 2 * kvw;
+  const float* kn = qkv + static_cast<size_t>(row) * width + q_width;
+  const float* vn = kn + kvw;
+  const size_t off = static_cast<size_t>(layer) * rq.layer_stride + static_cast<size_t>(p) * kvw;
+  const float d = dev_row<T>(kn, vn, static_cast<const T*>(rq.k) + off, static_cast<const T*>(rq.v) + off, kvw, mode);
+  if ((threadIdx.x & 31) == 0) dev[row] = d;
+}
+
+cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* pos, const int32_t* req,
+                                  const ReqDev* reqs, int layer, int n_heads, int n_kv_heads, int head_dim, int mode,
+                                  cb_dtype dt, float* dev, int32_t* status, cudaStream_t s) {
+  if (n_rows <= 0) return cudaSuccess;
+  const int blocks = (n_rows + 7) / 8;
+  if (dt == CB_BF16)
+    deviation_rows_kernel<bf16><<<blocks, 256, 0, s>>>(qkv, n_rows, pos, req, reqs, layer, n_heads * head_dim,
+                                                       n_kv_heads * head_dim, mode, dev, status);
+  else
+    deviation_rows_kernel<float><<<blocks, 256, 0, s>>>(qkv, n_rows, pos, req, reqs, layer, n_heads * head_dim,
+                                                        n_kv_heads * head_dim, mode, dev, status);
+  return cudaGetLastError();
+}
+
+template <typename T>
+__global__ void deviation_plain_kernel(const float* __restrict__ kn, const float* __restrict__ vn,
+                                       const T* __restrict__ kf, const T* __restrict__ vf,
+                                       const int32_t* __restrict__ idx, int n, int kvw, int mode,
+                                       float* __restrict__ dev) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= n) return;
+  const size_t f = static_cast<size_t>(idx ? idx[row] : row) * kvw;
+  const size_t r = static_cast<size_t>(row) * kvw;
+  const float d = dev_row<T>(kn + r, vn + r, kf + f, vf + f, kvw, mode);
+  if ((threadIdx.x & 31) == 0) dev[row] = d;
+}
+
+cudaError_t launch_deviation_plain(const float* k_new, const float* v_new, const void* k_fus, const void* v_fus,
+                                   const int32_t* idx, int n, int kv_width, int mode, cb_dtype dt, float* dev,
+                                   cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int blocks = (n + 7) / 8;
+  if (dt == CB_BF16)
+    deviation_plain_kernel<bf16><<<blocks, 256, 0, s>>>(k_new, v_new, static_cast<const bf16*>(k_fus),
+                                                        static_cast<const bf16*>(v_fus), idx, n, kv_width, mode, dev);
+  else
+    deviation_plain_kernel<float><<<blocks, 256, 0, s>>>(k_new, v_new, static_cast<const float*>(k_fus),
+                                                         static_cast<const float*>(v_fus), idx, n, kv_width, mode,
+                                                         dev);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- compaction + KV scatter
+// For every row t of S: q of its source row (RoPE applied, fp32) -> q_out[t] (model dtype);
+// fresh k, v -> fused cache row at its position; hidden state h_in[src] -> h_out[t]
+// when the set shrank (h_out != h_in).
+template <typename T>
+__global__ void post_qkv_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ s_src,
+                                const int32_t* __restrict__ s_pos, const int32_t* __restrict__ s_req,
+                                const ReqDev* __restrict__ reqs, int layer, int q_width, int kvw, T* __restrict__ q_out,
+                                const float* __restrict__ h_in, float* __restrict__ h_out, int d, int32_t* status) {
+  const int t = blockIdx.x;
+  const int src = s_src ? s_src[t] : t;
+  const int p = s_pos[t];
+  const ReqDev rq = reqs[s_req[t]];
+  if (p < 0 || p >= rq.n_tokens) {
+    if (threadIdx.x == 0) set_status(status, ST_RANGE);
+    return;
+  }
+  const size_t width = static_cast<size_t>(q_width) + 2 * kvw;
+  const float* row = qkv + static_cast<size_t>(src) * width;
+  for (int c = threadIdx.x * 8; c < q_width; c += blockDim.x * 8) {
+    float f[8];
+    load8(row + c, f);
+    store8(q_out + static_cast<size_t>(t) * q_width + c, f);
+  }
+  const size_t off = static_cast<size_t>(layer) * rq.layer_stride + static_cast<size_t>(p) * kvw;
+  T* kd = static_cast<T*>(rq.k) + off;
+  T* vd = static_cast<T*>(rq.v) + off;
+  for (int c = threadIdx.x * 8; c < kvw; c += blockDim.x * 8) {
+    float f[8];
+    load8(row + q_width + c, f);
+    store8(kd + c, f);
+    load8(row + q_width + kvw + c, f);
+    store8(vd + c, f);
+  }
+  if (h_out != h_in) {
+    const float* hs = h_in + static_cast<size_t>(src) * d;
+    float* hd = h_out + static_cast<size_t>(t) * d;
+    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+      float f[8];
+      load8(hs + c, f);
+      store8(hd + c, f);
+    }
+  }
+}
+
+cudaError_t launch_post_qkv(const float* qkv, int n_s_rows, const int32_t* s_src, const int32_t* s_pos,
+                            const int32_t* s_req, const ReqDev* reqs, int layer, int n_heads, int n_kv_heads,
+                            int head_dim, cb_dtype dt, void* q_out, const float* h_in, float* h_out, int d,
+                            int32_t* status, cudaStream_t s) {
+  if (n_s_rows <= 0) return cudaSuccess;
+  if (dt == CB_BF16)
+    post_qkv_kernel<bf16><<<n_s_rows, 256, 0, s>>>(qkv, s_src, s_pos, s_req, reqs, layer, n_heads * head_dim,
+                                                   n_kv_heads * head_dim, static_cast<bf16*>(q_out), h_in, h_out, d,
+                                                   status);
+  else
+    post_qkv_kernel<float><<<n_s_rows, 256, 0, s>>>(qkv, s_src, s_pos, s_req, reqs, layer, n_heads * head_dim,
+                                                    n_kv_heads * head_dim, static_cast<float*>(q_out), h_in, h_out, d,
+                                                    status);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- outputs
+__global__ void write_hidden_kernel(const float* __restrict__ h, const int32_t* __restrict__ s_pos, int row0, int d,
+                                    float* __restrict__ out) {
+  const int t = row0 + blockIdx.x;
+  const float* src = h + static_cast<size_t>(t) * d;
+  float* dst = out + static_cast<size_t>(s_pos[t]) * d;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float f[8];
+    load8(src + c, f);
+    store8(dst + c, f);
+  }
+}
+
+cudaError_t launch_write_hidden(const float* h, const int32_t* s_pos, int row0, int n, int d, float* out,
+                                cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  write_hidden_kernel<<<n, 256, 0, s>>>(h, s_pos, row0, d, out);
+  return cudaGetLastError();
+}
+
+constexpr int LM_MAX_REQ = 16;
+
+// logits[r][v] = <x[r], W[v]>: one warp per vocabulary row, every request at once.
+template <typename T>
+__global__ void lm_head_kernel(const float* __restrict__ x, int n_req, int d, const T* __restrict__ w, int vocab,
+                               float* __restrict__ logits) {
+  const int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (v >= vocab) return;
+  const int lane = threadIdx.x & 31;
+  float acc[LM_MAX_REQ];
+#pragma unroll
+  for (int r = 0; r < LM_MAX_REQ; ++r) acc[r] = 0.f;
+  const T* wr = w + static_cast<size_t>(v) * d;
+  for (int c = lane * 8; c < d; c += 256) {
+    float wf[8];
+    load8(wr + c, wf);
+#pragma unroll
+    for (int r = 0; r < LM_MAX_REQ; ++r) {
+      if (r < n_req) {
+        float xf[8];
+        load8(x + static_cast<size_t>(r) * d + c, xf);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[r] += wf[j] * xf[j];
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < LM_MAX_REQ; ++r) {
+    if (r < n_req) {
+      const float t = warp_sum(acc[r]);
+      if (lane == 0) logits[static_cast<size_t>(r) * vocab + v] = t;
+    }
+  }
+}
+
+cudaError_t launch_lm_head(const float* x, int n_req, int d, const void* w, int vocab, cb_dtype dt, float* logits,
+                           cudaStream_t s) {
+  if (n_req <= 0) return cudaSuccess;
+  for (int r0 = 0; r0 < n_req; r0 += LM_MAX_REQ) {
+    const int nr = n_req - r0 < LM_MAX_REQ ? n_req - r0 : LM_MAX_REQ;
+    const int blocks = (vocab + 7) / 8;
+    if (dt == CB_BF16)
+      lm_head_kernel<bf16><<<blocks, 256, 0, s>>>(x + static_cast<size_t>(r0) * d, nr, d, static_cast<const bf16*>(w),
+                                                  vocab, logits + static_cast<size_t>(r0) * vocab);
+    else
+      lm_head_kernel<float><<<blocks, 256, 0, s>>>(x + static_cast<size_t>(r0) * d, nr, d,
+                                                   static_cast<const float*>(w), vocab,
+                                                   logits + static_cast<size_t>(r0) * vocab);
+  }
+  return cudaGetLastError();
+}
+
+// argmax per request; ties go to the lowest token id; NaN logits never win.
+__global__ void argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* const* outs,
+                              int32_t* __restrict__ out_dev) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const float* l = logits + static_cast<size_t>(blockIdx.x) * vocab;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int v = threadIdx.x; v < vocab; v += blockDim.x) {
+    const float x = l[v];
+    if (x > best || (x == best && v < bi)) {
+      best = x;
+      bi = v;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ob > best || (ob == best && oi < bi)) {
+      best = ob;
+      bi = oi;
+    }
+  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sv[w] = best;
+    si[w] = bi;
+  }
+  __syncthreads();
+  if (w == 0) {
+    best = lane < (blockDim.x >> 5) ? sv[lane] : -INFINITY;
+    bi = lane < (blockDim.x >> 5) ? si[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ob > best || (ob == best && oi < bi)) {
+        best = ob;
+        bi = oi;
+      }
+    }
+    if (lane == 0) {
+      if (bi == 0x7fffffff) bi = 0;
+      if (out_dev) out_dev[blockIdx.x] = bi;
+      if (outs && outs[blockIdx.x]) *outs[blockIdx.x] = bi;
+    }
+  }
+}
+
+cudaError_t launch_argmax(const float* logits, int n_req, int vocab, int32_t* const* outs, int32_t* out_dev,
+                          cudaStream_t s) {
+  if (n_req <= 0) return cudaSuccess;
+  argmax_kernel<<<n_req, 1024, 0, s>>>(logits, vocab, outs, out_dev);
+  return cudaGetLastError();
+}
+
+}  // namespace cb

@@ -1,0 +1,105 @@
+"""Shared set-up of the GPU parity tests: the CUDA path (through the C ABI) and the
+oracle, each fed from the harness with the same seeds."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import harness as hz
+import harness.device as hd
+import oracle.cacheblend as orc
+import rag_non_prefix_gb300 as cb
+from rag_non_prefix_gb300 import build as cbbuild
+
+
+@functools.lru_cache(maxsize=None)
+def built():
+    cbbuild.build()
+    cb.load_library()
+    return True
+
+
+def storage_of(cfg) -> str:
+    return "bf16" if cfg.dtype == "bf16" else "f32"
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+class GpuWorkload:
+    """A workload on the GPU: weights, an engine, every chunk precomputed and registered."""
+
+    def __init__(self, spec: hz.PromptSpec, on_host: bool = False, max_tokens=None):
+        built()
+        self.spec = spec
+        self.cfg = spec.cfg
+        self.W = hd.device_weights(self.cfg, spec.seed)
+        total = sum(spec.n_tokens(r) for r in range(len(spec.requests)))
+        longest = max(max(len(c) for c in spec.chunks), max(spec.n_tokens(r) for r in range(len(spec.requests))))
+        self.eng = cb.Engine(self.cfg, self.W, max_tokens=max_tokens or max(total, longest),
+                             max_requests=len(spec.requests), max_positions=longest + 1)
+        self.chunk_kv = {}
+        used = sorted({s.chunk for req in spec.requests for s in req if s.chunk >= 0})
+        for c in used:
+            ids = hd.ids_tensor(spec.chunks[c])
+            k, v = self.eng.precompute_chunk(ids)
+            if on_host:
+                k, v = k.cpu().pin_memory(), v.cpu().pin_memory()
+            self.chunk_kv[c] = (ids, k, v)
+            self.eng.register_chunk(c, ids, k, v, on_host=on_host)
+        torch.cuda.synchronize()
+
+    def requests(self):
+        out = []
+        for req in self.spec.requests:
+            chunks = [s.chunk for s in req if s.chunk >= 0]
+            q = [s for s in req if s.chunk < 0][0]
+            out.append(self.eng.make_request(chunks, hd.ids_tensor(q.ids)))
+        return out
+
+    def blend(self, ratios, forced=None, copy_stream=None, dev_mode=0):
+        reqs = self.requests()
+        self.eng.blend_prefill(reqs, ratios, dev_mode=dev_mode, forced=forced,
+                               copy_stream=copy_stream)
+        self.eng.get_status()
+        torch.cuda.synchronize()
+        return reqs
+
+
+class OracleWorkload:
+    """The same workload in the oracle (fp64, KV stored in the model dtype)."""
+
+    def __init__(self, spec: hz.PromptSpec):
+        self.spec = spec
+        self.cfg = spec.cfg
+        self.W = hz.HostWeights(self.cfg, spec.seed)
+        self.storage = storage_of(self.cfg)
+        self.caches = orc.precompute_all(self.cfg, self.W, spec, self.storage)
+
+    def blend(self, r: int, ratios, force_sel=None, dev_mode=0):
+        return orc.blend_prefill(self.cfg, self.W, self.spec.requests[r], self.caches, ratios, self.storage,
+                                 dev_mode=dev_mode, force_sel=force_sel)
+
+    def full(self, r: int):
+        ids = np.concatenate([s.ids for s in self.spec.requests[r]])
+        return orc.full_prefill(self.cfg, self.W, ids, self.storage)
+
+
+def max_rel_err(gpu_rows: np.ndarray, ref_rows: np.ndarray) -> float:
+    """max over rows t of ||g_t - o_t||_inf / ||o_t||_inf."""
+    num = np.max(np.abs(gpu_rows - ref_rows), axis=1)
+    den = np.maximum(np.max(np.abs(ref_rows), axis=1), 1e-30)
+    return float(np.max(num / den))
+
+
+def forced_from_oracle(res, n_cached: int, n_layers: int, ratios):
+    """{check layer: [cached part of the oracle's S_i]} for the GPU's forced-selection mode."""
+    out = {}
+    for i in range(n_layers):
+        if ratios[i] >= 0:
+            S = res["sets"][i]
+            out[i] = [[int(x) for x in S if x < n_cached]]
+    return out

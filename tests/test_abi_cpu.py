@@ -1,0 +1,88 @@
+"""The C-ABI library loads and exports every symbol include/cacheblend.h declares; the
+binding's struct layouts match the C compiler's; host-side planning agrees with the
+oracle's reading of the pages (no GPU, no compute calls)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+import rag_non_prefix_gb300 as cb
+from rag_non_prefix_gb300 import build as cbbuild
+import oracle.cacheblend as orc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cacheblend.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbbuild.build()
+    return cb.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cb_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 20
+    out = subprocess.run(["nm", "-D", "--defined-only", cb.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (cb_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    assert sorted(cb.EXPORTED) == names
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_status_strings_without_gpu(lib):
+    assert lib.cb_status_string(0) == b"ok"
+    assert lib.cb_status_string(4) == b"chunk id not registered"
+    assert lib.cb_registered_chunks(None) == 0
+
+
+def test_struct_layout_matches_c_compiler(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "cacheblend.h"\n'
+        "int main(void){\n"
+        'printf("%zu %zu %zu %zu %zu\\n", sizeof(cb_model_cfg), offsetof(cb_model_cfg, rope_theta),'
+        " offsetof(cb_model_cfg, rms_eps), offsetof(cb_model_cfg, dtype), offsetof(cb_model_cfg, max_positions));\n"
+        'printf("%zu %zu %zu\\n", sizeof(cb_request), offsetof(cb_request, n_query), offsetof(cb_request, out_first_token));\n'
+        'printf("%zu %zu %zu\\n", sizeof(cb_blend_params), offsetof(cb_blend_params, dev_mode), offsetof(cb_blend_params, forced_sel_host));\n'
+        'printf("%zu\\n", sizeof(cb_weights));\nreturn 0;}\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    m = cb.ModelCfg
+    assert lines[0].split() == [str(v) for v in (C.sizeof(m), m.rope_theta.offset, m.rms_eps.offset, m.dtype.offset,
+                                                 m.max_positions.offset)]
+    r = cb.Request
+    assert lines[1].split() == [str(v) for v in (C.sizeof(r), r.n_query.offset, r.out_first_token.offset)]
+    p = cb.BlendParams
+    assert lines[2].split() == [str(v) for v in (C.sizeof(p), p.dev_mode.offset, p.forced_sel_host.offset)]
+    assert lines[3].strip() == str(C.sizeof(cb.Weights))
+
+
+@pytest.mark.parametrize("L,r,sched", [(2, 0.15, "fixed"), (32, 0.15, "gradual"), (60, 0.15, "gradual"),
+                                       (80, 0.1, "gradual"), (80, 0.2, "gradual"), (4, 0.5, "gradual"),
+                                       (32, 0.0, "gradual"), (32, 1.0, "fixed")])
+def test_host_schedule_matches_oracle(L, r, sched):
+    assert cb.ratio_schedule(L, r, sched) == pytest.approx(orc.ratio_schedule(L, r, sched))
+    for nc in (1, 255, 256, 3136, 4096, 8192):
+        for x in cb.ratio_schedule(L, r, sched):
+            assert cb.k_for_ratio(x, nc) == orc.k_for_ratio(x, nc)
+
+
+def test_library_fails_loudly_when_missing(tmp_path):
+    with pytest.raises(RuntimeError):
+        cb._lib = None
+        try:
+            cb.load_library(str(tmp_path / "nope.so"))
+        finally:
+            cb._lib = None

@@ -1,0 +1,244 @@
+"""End-to-end parity of the blended prefill (CUDA path through the C ABI vs the oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import harness as hz
+import harness.device as hd
+import oracle.cacheblend as orc
+import rag_non_prefix_gb300 as cb
+from tests._gpu import GpuWorkload, OracleWorkload, forced_from_oracle, max_rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def tol(cfg):
+    return TOL[cfg.dtype]
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    spec = hz.workload("tiny")
+    return spec, GpuWorkload(spec), OracleWorkload(spec)
+
+
+@pytest.fixture(scope="module")
+def small_bf16():
+    spec = hz.workload("small_bf16")
+    return spec, GpuWorkload(spec), OracleWorkload(spec)
+
+
+def _sets(req, cfg):
+    sel, cnt = req["sel"].cpu().numpy(), req["sel_count"].cpu().numpy()
+    return {i: sel[i, : cnt[i]] for i in range(cfg.n_layers)}
+
+
+# ----------------------------------------------------------------------------- chunk precompute / full prefill
+@pytest.mark.parametrize("name", ["tiny", "small_gqa_f32", "small_bf16", "small_mha_bf16"])
+def test_precompute_and_full_prefill_match_oracle(name):
+    spec = hz.workload(name)
+    g = GpuWorkload(spec)
+    o = OracleWorkload(spec)
+    t = tol(spec.cfg)
+    for c, (ids, k, v) in g.chunk_kv.items():
+        ok, ov = o.caches[c]
+        for got, ref in ((to_np(k), ok), (to_np(v), ov)):
+            err = np.max(np.abs(got - ref), axis=(2, 3)).max() / np.max(np.abs(ref))
+            assert err < t, (c, err)
+    ids = np.concatenate([s.ids for s in spec.requests[0]])
+    full = g.eng.full_prefill(hd.ids_tensor(ids))
+    torch.cuda.synchronize()
+    ref = o.full(0)
+    assert max_rel_err(to_np(full["hidden"]), ref["hidden"]) < t
+    if spec.cfg.dtype == "f32":
+        assert int(full["first_token"].item()) == ref["first_token"]
+
+
+# ----------------------------------------------------------------------------- blend, fp32 (configuration 1)
+def test_tiny_blend_matches_oracle(tiny):
+    spec, g, o = tiny
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    req = g.blend(ratios)[0]
+    ref = o.blend(0, ratios)
+    sets = _sets(req, cfg)
+    for i in range(cfg.n_layers):
+        assert np.array_equal(sets[i], ref["sets"][i]), i
+    rows = ref["rows"]
+    got = to_np(req["hidden"])[rows]
+    assert max_rel_err(got, ref["hidden"]) < 1e-4
+    assert int(req["first_token"].item()) == ref["first_token"]
+    assert len(rows) == 32 + 39
+
+
+@pytest.mark.parametrize("schedule,r", [("gradual", 0.2), ("fixed", 0.5)])
+def test_gqa_f32_blend_matches_oracle(schedule, r):
+    spec = hz.workload("small_gqa_f32")
+    g, o = GpuWorkload(spec), OracleWorkload(spec)
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, r, schedule)
+    req = g.blend(ratios)[0]
+    ref = o.blend(0, ratios)
+    sets = _sets(req, cfg)
+    for i in range(cfg.n_layers):
+        assert np.array_equal(sets[i], ref["sets"][i]), i
+    assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 1e-4
+
+
+# ----------------------------------------------------------------------------- blend, bf16
+def test_bf16_blend_forced_selection_matches_oracle(small_bf16):
+    """Numerics alone: the GPU follows the oracle's sets."""
+    spec, g, o = small_bf16
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    ref = o.blend(0, ratios)
+    forced = forced_from_oracle(ref, ref["n_cached"], cfg.n_layers, ratios)
+    req = g.blend(ratios, forced=forced)[0]
+    sets = _sets(req, cfg)
+    for i in range(cfg.n_layers):
+        assert np.array_equal(sets[i], ref["sets"][i])
+    assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 2e-2
+
+
+def test_bf16_blend_selection_overlap(small_bf16):
+    """Free-running selection: >= 99 % overlap of every checked set with the oracle's."""
+    spec, g, o = small_bf16
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    ref = o.blend(0, ratios)
+    req = g.blend(ratios)[0]
+    sets = _sets(req, cfg)
+    for i in range(cfg.n_layers):
+        inter = len(np.intersect1d(sets[i], ref["sets"][i]))
+        assert len(sets[i]) == len(ref["sets"][i])
+        assert inter / len(ref["sets"][i]) >= 0.99, (i, inter, len(ref["sets"][i]))
+    common = np.intersect1d(sets[cfg.n_layers - 1], ref["rows"])
+    got = to_np(req["hidden"])[common]
+    refh = ref["hidden"][np.searchsorted(ref["rows"], common)]
+    assert max_rel_err(got, refh) < 2e-2
+
+
+def test_mha_bf16_blend_forced(tmp_path):
+    spec = hz.workload("small_mha_bf16")
+    g, o = GpuWorkload(spec), OracleWorkload(spec)
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    ref = o.blend(0, ratios)
+    req = g.blend(ratios, forced=forced_from_oracle(ref, ref["n_cached"], cfg.n_layers, ratios))[0]
+    assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 2e-2
+
+
+# ----------------------------------------------------------------------------- special cases
+def test_full_recompute_equals_full_prefill_on_gpu(small_bf16):
+    """r = 100 %: the blend recomputes everything, which is the GPU's own full prefill."""
+    spec, g, o = small_bf16
+    cfg = spec.cfg
+    req = g.blend(orc.ratio_schedule(cfg.n_layers, 1.0, "fixed"))[0]
+    ids = np.concatenate([s.ids for s in spec.requests[0]])
+    full = g.eng.full_prefill(hd.ids_tensor(ids))
+    torch.cuda.synchronize()
+    a, b = to_np(req["hidden"]), to_np(full["hidden"])
+    assert max_rel_err(a, b) < 1e-2
+    assert int(req["first_token"].item()) == int(full["first_token"].item())
+
+
+def test_zero_ratio_equals_full_reuse_oracle(tiny):
+    spec, g, o = tiny
+    cfg = spec.cfg
+    req = g.blend(orc.ratio_schedule(cfg.n_layers, 0.0, "fixed"))[0]
+    ref = orc.full_reuse(cfg, o.W, spec.requests[0], o.caches, "f32")
+    assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 1e-4
+
+
+def test_host_staged_chunks_are_bit_identical(small_bf16):
+    spec, g, o = small_bf16
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    resident = g.blend(ratios)[0]
+    gh = GpuWorkload(spec, on_host=True)
+    cs = torch.cuda.Stream()
+    staged = gh.blend(ratios, copy_stream=cs)[0]
+    assert torch.equal(resident["hidden"], staged["hidden"])
+    assert torch.equal(resident["fused_k"], staged["fused_k"])
+    assert torch.equal(resident["sel"], staged["sel"])
+
+
+def test_per_layer_api_matches_whole_call(small_bf16):
+    spec, g, o = small_bf16
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    whole = g.blend(ratios)[0]
+    reqs = g.requests()
+    g.eng.blend_begin(reqs, ratios)
+    for i in range(cfg.n_layers):
+        g.eng.blend_layer(i)
+    g.eng.blend_finish()
+    g.eng.get_status()
+    torch.cuda.synchronize()
+    assert torch.equal(whole["hidden"], reqs[0]["hidden"])
+    assert g.eng.plan_counts(0) == whole["sel_count"].cpu().tolist()
+
+
+def test_batched_requests_match_single():
+    """Two requests sharing chunks (a pooled batch) give the same result as one at a time."""
+    base = hz.make_pooled_batch("small_bf16", 21, 6, 96, 3, 2, 24, 0.2, name="pool")
+    g = GpuWorkload(base)
+    cfg = base.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, base.ratio, base.schedule)
+    both = g.blend(ratios)
+    for r in range(2):
+        req = base.requests[r]
+        one = g.eng.make_request([s.chunk for s in req if s.chunk >= 0], hd.ids_tensor(req[-1].ids))
+        g.eng.blend_prefill([one], ratios)
+        torch.cuda.synchronize()
+        assert max_rel_err(to_np(one["hidden"])[to_np(one["sel"])[-1][: int(one["sel_count"][-1])].astype(int)],
+                           to_np(both[r]["hidden"])[to_np(both[r]["sel"])[-1][: int(both[r]["sel_count"][-1])].astype(int)]) < 1e-2
+
+
+# ----------------------------------------------------------------------------- errors and waits
+def test_errors_are_reported_not_raised_on_device(tiny):
+    spec, g, o = tiny
+    cfg = spec.cfg
+    eng = g.eng
+    bad = eng.make_request([0, 1], hd.ids_tensor(spec.requests[0][-1].ids))
+    bad["chunk_ids"] = [0, 12345]
+    with pytest.raises(cb.CacheBlendError) as e:
+        eng.blend_prefill([bad], orc.ratio_schedule(cfg.n_layers, 0.15, "fixed"))
+    assert e.value.name == "CB_ERR_NOT_FOUND"
+    # a NaN in a cached chunk reaches the deviation: the call reports CB_ERR_NAN, no trap
+    ids, k, v = g.chunk_kv[1]
+    k2 = k.clone()
+    k2[1, 5] = float("nan")
+    eng.register_chunk(99, ids, k2, v)
+    req = eng.make_request([0, 99], hd.ids_tensor(spec.requests[0][-1].ids))
+    eng.blend_prefill([req], orc.ratio_schedule(cfg.n_layers, 0.15, "fixed"))
+    with pytest.raises(cb.CacheBlendError) as e:
+        eng.get_status()
+    assert e.value.name == "CB_ERR_NAN"
+    eng.unregister_chunk(99)
+    eng.get_status()  # cleared
+
+
+def test_synchronize_deadline_on_a_stalled_copy_stream(small_bf16):
+    spec, g, o = small_bf16
+    gh = GpuWorkload(spec, on_host=True)
+    cfg = spec.cfg
+    cs = torch.cuda.Stream()
+    reqs = gh.requests()
+    gh.eng.blend_begin(reqs, orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule))
+    with torch.cuda.stream(cs):
+        torch.cuda._sleep(int(2e9))  # about a second of spinning on the copy stream (bounded)
+    gh.eng.fetch_kv(0, cs)
+    with pytest.raises(cb.CacheBlendError) as e:
+        gh.eng.synchronize(0, timeout_ms=1)
+    assert e.value.name == "CB_ERR_TIMEOUT"
+    gh.eng.synchronize(0, timeout_ms=30000)
+    for i in range(1, cfg.n_layers):
+        gh.eng.fetch_kv(i, cs)
+    for i in range(cfg.n_layers):
+        gh.eng.prefill_layer(i)
+    gh.eng.blend_finish()
+    gh.eng.get_status()
+    torch.cuda.synchronize()
