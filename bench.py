@@ -167,15 +167,17 @@ def run_ours(args, rank, world):
         for ids in full_ids:
             eng.full_prefill(ids, want_hidden=False, stream=stream)
 
-    def timed(fn, n):
+    def timed(fn, n, tag):
         ts = []
         for _ in range(n):
             flush.fill_(1.0)
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
+            torch.cuda.nvtx.range_push(tag)
             a.record(stream)
             fn()
             b.record(stream)
+            torch.cuda.nvtx.range_pop()
             b.synchronize()
             ts.append(a.elapsed_time(b))
         return ts
@@ -194,11 +196,11 @@ def run_ours(args, rank, world):
     sampler.start()
     barrier()
     t0 = time.perf_counter()
-    blend_ms = timed(blend_step, args.steps)
+    blend_ms = timed(blend_step, args.steps, "blend_timed")
     barrier()
     wall = time.perf_counter() - t0
     prof_counts = eng.get_profile()
-    full_ms = timed(full_step, args.steps)
+    full_ms = timed(full_step, args.steps, "full_timed")
     barrier()
     clocks = sampler.stop()
     eng.get_status()

@@ -1,0 +1,123 @@
+"""Per-kernel timing of the library's hot kernels through the C ABI (CUDA events).
+
+    python -m rag_non_prefix_gb300.kernel_bench gemm --M 535 --N 28672 --K 4096 --mode swiglu
+    python -m rag_non_prefix_gb300.kernel_bench attention --H 32 --Hkv 8 --N 3200 --m 535
+    python -m rag_non_prefix_gb300.kernel_bench rerotate --rows 100352 --hkv 8
+    python -m rag_non_prefix_gb300.kernel_bench select --n 3136 --k 471
+    python -m rag_non_prefix_gb300.kernel_bench deviation --n 3200 --kvw 1024
+
+Operands are random device tensors sized like one layer of the Mistral-7B-shaped
+workload; weight operands exceed the 129 MB L2 where the shape allows, and a 512 MiB
+buffer is written between timed launches.  Prints one JSON line with the average
+launch time and the achieved rate (TFLOP/s or GB/s of algorithmic traffic).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+import rag_non_prefix_gb300 as cb
+from rag_non_prefix_gb300 import build as cbbuild
+
+
+def _time(fn, iters, warmup=3, flush=None):
+    for _ in range(warmup):
+        fn()
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s = torch.cuda.current_stream()
+        a.record(s)
+        fn()
+        b.record(s)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return sum(ts) / len(ts), min(ts)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("kernel", choices=["gemm", "attention", "rerotate", "select", "deviation"])
+    ap.add_argument("--M", type=int, default=535)
+    ap.add_argument("--N", type=int, default=28672)
+    ap.add_argument("--K", type=int, default=4096)
+    ap.add_argument("--mode", default="swiglu", choices=["store", "add", "swiglu"])
+    ap.add_argument("--H", type=int, default=32)
+    ap.add_argument("--Hkv", type=int, default=8)
+    ap.add_argument("--m", type=int, default=535)
+    ap.add_argument("--rows", type=int, default=32 * 3136)
+    ap.add_argument("--hkv", type=int, default=8)
+    ap.add_argument("--n", type=int, default=3136)
+    ap.add_argument("--k", type=int, default=471)
+    ap.add_argument("--kvw", type=int, default=1024)
+    ap.add_argument("--iters", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--no-flush", action="store_true")
+    a = ap.parse_args()
+    cbbuild.build()
+    torch.manual_seed(0)
+    dev = torch.device("cuda")
+    flush = None if a.no_flush else torch.empty(128 * 1024 * 1024, dtype=torch.float32, device=dev)
+    out = {"kernel": a.kernel}
+    if a.kernel == "gemm":
+        M, N, K = a.M, a.N, a.K
+        A = (torch.randn(M, K, device=dev) * 0.5).to(torch.bfloat16)
+        if a.mode == "swiglu":
+            G = (torch.randn(N // 2, K, device=dev) * 0.02).to(torch.bfloat16)
+            U = (torch.randn(N // 2, K, device=dev) * 0.02).to(torch.bfloat16)
+            C = torch.empty(M, N // 2, dtype=torch.bfloat16, device=dev)
+            fn = lambda: cb.cb_gemm(A, G, C, 2, B2=U)  # noqa: E731
+        else:
+            B = (torch.randn(N, K, device=dev) * 0.02).to(torch.bfloat16)
+            C = torch.zeros(M, N, dtype=torch.float32, device=dev)
+            fn = lambda: cb.cb_gemm(A, B, C, 1 if a.mode == "add" else 0)  # noqa: E731
+        avg, best = _time(fn, a.iters, a.warmup, flush)
+        fl = 2.0 * M * N * K
+        out.update(shape=[M, N, K], mode=a.mode, ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12,
+                   weight_bytes=N * K * 2)
+    elif a.kernel == "attention":
+        H, Hkv, N, m = a.H, a.Hkv, a.N, a.m
+        pos = torch.sort(torch.randperm(N, device=dev)[:m]).values.to(torch.int32)
+        q = torch.randn(m, H, 128, device=dev).to(torch.bfloat16)
+        k = torch.randn(N, Hkv, 128, device=dev).to(torch.bfloat16)
+        v = torch.randn(N, Hkv, 128, device=dev).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        fn = lambda: cb.cb_attention(q, pos, k, v, o)  # noqa: E731
+        avg, best = _time(fn, a.iters, a.warmup, flush)
+        fl = 4.0 * H * 128 * float((pos.to(torch.float64) + 1).sum())
+        out.update(shape=[H, Hkv, N, m], ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12)
+    elif a.kernel == "rerotate":
+        k = torch.randn(a.rows, a.hkv, 128, device=dev).to(torch.bfloat16)
+        v = torch.randn(a.rows, a.hkv, 128, device=dev).to(torch.bfloat16)
+        kd, vd = torch.empty_like(k), torch.empty_like(v)
+        fn = lambda: cb.cb_rope_rerotate(k, kd, v, vd, 1234, 1e4)  # noqa: E731
+        avg, best = _time(fn, a.iters, a.warmup, flush)
+        by = 4 * k.numel() * 2  # K and V, read and written
+        out.update(rows=a.rows, ms=avg, best_ms=best, gbs=by / (avg * 1e-3) / 1e9, bytes=by)
+    elif a.kernel == "select":
+        d = torch.rand(a.n, device=dev)
+        cand = torch.arange(a.n, dtype=torch.int32, device=dev)
+        o = torch.empty(a.k, dtype=torch.int32, device=dev)
+        fn = lambda: cb.cb_select_hkvd(d, cand, a.k, o)  # noqa: E731
+        avg, best = _time(fn, a.iters, a.warmup, None)
+        out.update(n=a.n, k=a.k, ms=avg, best_ms=best)
+    elif a.kernel == "deviation":
+        kn = torch.randn(a.n, a.kvw, device=dev)
+        vn = torch.randn(a.n, a.kvw, device=dev)
+        kf = torch.randn(a.n, a.kvw, device=dev).to(torch.bfloat16)
+        vf = torch.randn(a.n, a.kvw, device=dev).to(torch.bfloat16)
+        dv = torch.empty(a.n, device=dev)
+        fn = lambda: cb.cb_kv_deviation(kn, vn, kf, vf, None, 0, dv)  # noqa: E731
+        avg, best = _time(fn, a.iters, a.warmup, flush)
+        by = a.n * a.kvw * (4 + 2) * 2
+        out.update(n=a.n, ms=avg, best_ms=best, gbs=by / (avg * 1e-3) / 1e9, bytes=by)
+    torch.cuda.synchronize()
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()
