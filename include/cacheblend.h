@@ -153,10 +153,15 @@ cb_status cb_select_hkvd(const float* dev, const int32_t* cand, int n, int k, in
  * fp32 accumulation.  epilogue 0: C fp32 [M][ldc] = acc;  1: C fp32 += acc
  * (residual add);  2: C (dtype) [M][N/2] = SiLU(acc[:, gate]) * acc[:, up] where
  * B2 (may not be NULL) holds the "up" rows and B the "gate" rows, each [N/2][K]
- * (then N counts both).  bf16 runs on the tcgen05 tensor cores, fp32 on CUDA cores.
- * bf16 needs K % 64 == 0 and N % 128 == 0 (N/2 % 64 for epilogue 2). */
+ * (then N counts both).  bf16 runs on the tcgen05 tensor cores (persistent, one CTA
+ * per SM), fp32 on CUDA cores.  bf16 needs K % 64 == 0 and N % 128 == 0.
+ * scratch: NULL (whole output tiles per CTA only) or cb_gemm_scratch_size() bytes of
+ * device memory, zero-filled before its first use, which lets the k-iterations of the
+ * last waves be split across CTAs (stream-K partial tiles and their flags); the call
+ * leaves it zero-filled.  Calls sharing one scratch must not overlap on the GPU. */
 cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, int N, int K, int ldc, int epilogue,
-                  cb_dtype dtype, void* stream);
+                  cb_dtype dtype, void* scratch, size_t scratch_bytes, void* stream);
+size_t cb_gemm_scratch_size(void);
 
 /* Causal attention of sparse queries over one KV cache ([P3] "어떤 토큰을 다시 계산하는가":
  * selected queries attend under the causal mask to all available K/V).

@@ -23,7 +23,8 @@ STATUS = {0: "CB_OK", 1: "CB_ERR_INVALID_ARG", 2: "CB_ERR_SHAPE", 3: "CB_ERR_DTY
           10: "CB_ERR_STATE"}
 EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_workspace_size", "cb_set_workspace",
             "cb_precompute_chunk", "cb_register_chunk", "cb_unregister_chunk", "cb_registered_chunks",
-            "cb_rope_rerotate", "cb_kv_deviation", "cb_select_hkvd", "cb_gemm", "cb_attention", "cb_blend_prefill",
+            "cb_rope_rerotate", "cb_kv_deviation", "cb_select_hkvd", "cb_gemm", "cb_gemm_scratch_size", "cb_attention",
+            "cb_blend_prefill",
             "cb_full_prefill", "cb_blend_begin", "cb_fetch_kv", "cb_synchronize", "cb_prefill_layer",
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
             "cb_get_profile")
@@ -91,7 +92,8 @@ def load_library(path: str = LIB_PATH):
         "cb_rope_rerotate": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_double, C.c_int, vp]),
         "cb_kv_deviation": (st, [vp, vp, vp, vp, i32p, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp]),
         "cb_select_hkvd": (st, [vp, i32p, C.c_int, C.c_int, i32p, i32p, vp]),
-        "cb_gemm": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp]),
+        "cb_gemm": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_size_t, vp]),
+        "cb_gemm_scratch_size": (C.c_size_t, []),
         "cb_attention": (st, [vp, i32p, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp]),
         "cb_blend_prefill": (st, [vp, C.POINTER(Request), C.c_int, C.POINTER(BlendParams), vp, vp]),
         "cb_full_prefill": (st, [vp, i32p, C.c_int, vp, vp, vp, i32p, vp]),
@@ -195,14 +197,29 @@ def cb_select_hkvd(dev: torch.Tensor, cand: Optional[torch.Tensor], k: int, out:
     return out
 
 
+_GEMM_SCRATCH = {}
+
+
+def gemm_scratch(device=None) -> torch.Tensor:
+    """A zero-filled scratch buffer for cb_gemm on ``device`` (one per device, reused)."""
+    device = torch.device("cuda") if device is None else torch.device(device)
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    if key not in _GEMM_SCRATCH:
+        n = load_library().cb_gemm_scratch_size()
+        _GEMM_SCRATCH[key] = torch.zeros(n, dtype=torch.uint8, device=torch.device("cuda", key))
+    return _GEMM_SCRATCH[key]
+
+
 def cb_gemm(A: torch.Tensor, B: torch.Tensor, C_out: torch.Tensor, epilogue: int = 0,
-            B2: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """C = A . B^T (epilogue 0), C += A . B^T (1), C = SiLU(A B^T) * (A B2^T) (2)."""
+            B2: Optional[torch.Tensor] = None, scratch: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """C = A . B^T (epilogue 0), C += A . B^T (1), C = SiLU(A B^T) * (A B2^T) (2).
+    ``scratch`` (see gemm_scratch) enables the stream-K schedule; None = whole tiles only."""
     lib = load_library()
     M, K = A.shape
     N = B.shape[0] * (2 if epilogue == 2 else 1)
     _check(lib.cb_gemm(_ptr(A), _ptr(B), _ptr(B2), _ptr(C_out), M, N, K, C_out.shape[1], epilogue,
-                       _dtype_code(A.dtype), _stream(stream)))
+                       _dtype_code(A.dtype), _ptr(scratch), 0 if scratch is None else scratch.numel(),
+                       _stream(stream)))
     return C_out
 
 

@@ -186,6 +186,8 @@ struct cb_ctx {
   void* tmp_v = nullptr;
   float* logits = nullptr;
   float* xlast = nullptr;
+  void* gemm_scratch = nullptr;
+  size_t gemm_scratch_bytes = 0;
   uint8_t* meta = nullptr;  // plan, requests, tiles, segments, row ids ... (uploaded per batch)
   size_t meta_bytes = 0;
 
@@ -304,7 +306,7 @@ bool valid_cfg(const cb_model_cfg& c, std::string* why) {
 
 struct WsLayout {
   size_t status, rope, tok, pos0, pos1, req0, req1, src, dev, h0, h1, x, qkv, q, attn, act, tmpk, tmpv, logits,
-      xlast, meta, total, meta_bytes;
+      xlast, gemm, meta, total, meta_bytes;
 };
 
 WsLayout ws_layout(const cb_model_cfg& c, int T, int R) {
@@ -338,6 +340,7 @@ WsLayout ws_layout(const cb_model_cfg& c, int T, int R) {
   w.tmpv = take(Tz * kvw * es);
   w.logits = take(static_cast<size_t>(R) * c.vocab * 4);
   w.xlast = take(static_cast<size_t>(R) * c.d_model * 4);
+  w.gemm = take(gemm_scratch_bytes());
   // metadata: plan, requests, tiles, segments, forced sets, last rows, counts, first-token pointers
   const size_t L = c.n_layers;
   size_t m = 0;
@@ -691,7 +694,7 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   {
     PhaseScope ps(ctx, CB_PH_QKV, s, 1);
     CB_CUDA(ctx, launch_gemm(ctx->x, ctx->wq[i], ctx->wk[i], ctx->wv[i], qw, qw + kvw, ctx->qkv, Rn, qw + 2 * kvw, d,
-                             qw + 2 * kvw, 0, c.dtype, ctx->status, s));
+                             qw + 2 * kvw, 0, c.dtype, ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
   }
   {
     PhaseScope ps(ctx, CB_PH_ROPE, s, 1);
@@ -739,7 +742,7 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   {
     PhaseScope ps(ctx, CB_PH_OPROJ, s, 1);
     CB_CUDA(ctx, launch_gemm(ctx->attn, ctx->wo[i], nullptr, nullptr, d, d, hS, Sn, d, qw, d, 1, c.dtype, ctx->status,
-                             s));
+                             ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
   }
   {
     PhaseScope ps(ctx, CB_PH_NORM, s, 1);
@@ -748,12 +751,12 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   {
     PhaseScope ps(ctx, CB_PH_GATEUP, s, 1);
     CB_CUDA(ctx, launch_gemm(ctx->x, ctx->wg[i], ctx->wu[i], nullptr, 0, 0, ctx->act, Sn, 2 * c.ffn_dim, d,
-                             c.ffn_dim, 2, c.dtype, ctx->status, s));
+                             c.ffn_dim, 2, c.dtype, ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
   }
   {
     PhaseScope ps(ctx, CB_PH_DOWN, s, 1);
     CB_CUDA(ctx, launch_gemm(ctx->act, ctx->wd[i], nullptr, nullptr, d, d, hS, Sn, d, c.ffn_dim, d, 1, c.dtype,
-                             ctx->status, s));
+                             ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
   }
   // 6. optional per-layer sets
   for (int r = 0; r < b.n_req; ++r) {
@@ -917,6 +920,8 @@ cb_status cb_set_workspace(cb_ctx* ctx, void* ws, size_t bytes, int max_tokens, 
   ctx->tmp_v = base + w.tmpv;
   ctx->logits = reinterpret_cast<float*>(base + w.logits);
   ctx->xlast = reinterpret_cast<float*>(base + w.xlast);
+  ctx->gemm_scratch = base + w.gemm;
+  ctx->gemm_scratch_bytes = gemm_scratch_bytes();
   ctx->meta = base + w.meta;
   ctx->meta_bytes = w.meta_bytes;
   // rotary table: (cos, sin) of p * theta^(-2i/dh), evaluated in double on the host
@@ -931,6 +936,7 @@ cb_status cb_set_workspace(cb_ctx* ctx, void* ws, size_t bytes, int max_tokens, 
   }
   CB_CUDA(ctx, cudaMemcpy(ctx->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
   CB_CUDA(ctx, cudaMemset(ctx->status, 0, 256));
+  CB_CUDA(ctx, cudaMemset(ctx->gemm_scratch, 0, ctx->gemm_scratch_bytes));
   return CB_OK;
 }
 
@@ -1001,7 +1007,7 @@ cb_status cb_select_hkvd(const float* dev, const int32_t* cand, int n, int k, in
 }
 
 cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, int N, int K, int ldc, int epilogue,
-                  cb_dtype dtype, void* stream) {
+                  cb_dtype dtype, void* scratch, size_t scratch_bytes, void* stream) {
   if (!A || !B || !C || (epilogue == 2 && !B2)) return fail(nullptr, CB_ERR_INVALID_ARG, "null pointer");
   if (epilogue < 0 || epilogue > 2) return fail(nullptr, CB_ERR_INVALID_ARG, "bad epilogue");
   if (M < 0 || N < 1 || K < 1) return fail(nullptr, CB_ERR_SHAPE, "bad sizes");
@@ -1010,14 +1016,18 @@ cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, 
         (B2 && (reinterpret_cast<uintptr_t>(B2) & 15)))
       return fail(nullptr, CB_ERR_SHAPE, "bf16 GEMM needs K % 64 == 0, N % 128 == 0 and 16-byte aligned operands");
     if (ldc % 8 || (reinterpret_cast<uintptr_t>(C) & 15)) return fail(nullptr, CB_ERR_SHAPE, "ldc % 8 and aligned C");
+    if (scratch && (reinterpret_cast<uintptr_t>(scratch) & 15))
+      return fail(nullptr, CB_ERR_INVALID_ARG, "scratch must be 16-byte aligned");
   } else if (dtype != CB_F32) {
     return fail(nullptr, CB_ERR_DTYPE, "unknown dtype");
   }
   if (epilogue == 2 ? ldc < N / 2 : ldc < N) return fail(nullptr, CB_ERR_SHAPE, "ldc too small");
   cudaError_t e = launch_gemm(A, B, epilogue == 2 ? B2 : nullptr, nullptr, N, N, C, M, N, K, ldc, epilogue, dtype,
-                              nullptr, as_stream(stream));
+                              nullptr, scratch, scratch ? scratch_bytes : 0, as_stream(stream));
   return e == cudaSuccess ? CB_OK : cuda_fail(nullptr, e, "cb_gemm");
 }
+
+size_t cb_gemm_scratch_size(void) { return gemm_scratch_bytes(); }
 
 cb_status cb_attention(const void* q, const int32_t* q_pos, int m, const void* k, const void* v, int n_kv, int n_heads,
                        int n_kv_heads, int head_dim, void* out, cb_dtype dtype, void* stream) {

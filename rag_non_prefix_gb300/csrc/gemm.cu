@@ -13,6 +13,7 @@
 //
 // fp32: a plain shared-memory-tiled FFMA kernel with the same epilogues (used by the
 // fp32 configuration, whose 1e-4 tolerance rules out TF32).
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -55,6 +56,7 @@ bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
   return r == CUDA_SUCCESS;
 }
 
+
 // ============================================================================= tcgen05 kernel
 namespace tc {
 
@@ -62,7 +64,12 @@ constexpr int BM = 128;
 constexpr int BK = 64;                    // one 128-byte swizzle atom of bf16 along K
 constexpr int A_STAGE = BM * BK * 2;      // 16 KiB
 constexpr int THREADS = 192;
+constexpr int MAX_CTAS = 256;             // bound of the persistent grid (stream-K partial slots)
 
+// Work division.  Tiles t = m + n * m_tiles (consecutive tiles share a weight tile).
+// Tiles [0, dp_tiles) go round-robin to the CTAs (data-parallel); the k-iterations of the
+// remaining tiles are split evenly over the CTAs (stream-K): CTA g owns iterations
+// [g*I/G, (g+1)*I/G) of the I = (tiles - dp_tiles) * kb_per_tile tail iterations.
 struct Params {
   int M, N, K;
   int mode;
@@ -70,6 +77,11 @@ struct Params {
   int ldc;
   int split0, split1;  // B columns [0,split0) from map 0, [split0,split1) map 1, rest map 2
   int32_t* status;
+  int m_tiles, kb_per_tile;
+  int dp_tiles, tiles;
+  long long sk_iters;
+  float* partials;     // [gridDim.x][BM][BN] fp32, stream-K partial tiles
+  int* flags;          // [gridDim.x], zero between launches
 };
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -101,6 +113,52 @@ struct Layout {
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
+enum { ITEM_FULL = 0, ITEM_PARTIAL = 1, ITEM_OWNER = 2 };
+
+struct Item {
+  int tile, kb0, kb1, kind;
+  int last;  // ITEM_OWNER: last contributing CTA
+};
+
+// The idx-th work item of CTA g (false when there is none).
+__device__ __forceinline__ bool get_item(const Params& p, int g, int G, int idx, Item& it) {
+  const int KB = p.kb_per_tile;
+  const int n_dp = p.dp_tiles > g ? (p.dp_tiles - g + G - 1) / G : 0;
+  if (idx < n_dp) {
+    it.tile = g + idx * G;
+    it.kb0 = 0;
+    it.kb1 = KB;
+    it.kind = ITEM_FULL;
+    it.last = g;
+    return true;
+  }
+  if (p.sk_iters <= 0) return false;
+  const long long I = p.sk_iters;
+  const long long a = static_cast<long long>(g) * I / G, b = static_cast<long long>(g + 1) * I / G;
+  const int j = idx - n_dp;
+  const long long start = j == 0 ? a : (a / KB + j) * KB;
+  if (start >= b) return false;
+  const long long tile_lo = (start / KB) * KB, tile_hi = tile_lo + KB;
+  const long long end = b < tile_hi ? b : tile_hi;
+  it.tile = p.dp_tiles + static_cast<int>(start / KB);
+  it.kb0 = static_cast<int>(start - tile_lo);
+  it.kb1 = static_cast<int>(end - tile_lo);
+  it.last = g;
+  if (it.kb0 == 0 && it.kb1 == KB) {
+    it.kind = ITEM_FULL;
+  } else if (it.kb0 == 0) {
+    it.kind = ITEM_OWNER;
+    int last = g;
+    while (last + 1 < G && static_cast<long long>(last + 1) * I / G < tile_hi) ++last;
+    it.last = last;
+  } else {
+    it.kind = ITEM_PARTIAL;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -110,21 +168,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* empty = full + STAGES;
-  uint64_t* accum = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* acc_full = empty + STAGES;  // [2]
+  uint64_t* acc_empty = acc_full + 2;   // [2]
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BM;
-  const int n0 = blockIdx.y * BN;
-  const int num_kb = p.K / BK;
+  const int g = blockIdx.x, G = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -134,7 +196,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (p.mode == EPI_SWIGLU || p.split0 < p.N) prefetch_tmap(&tmB1);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, BN);
+    tmem_alloc(tmem_slot, 2 * BN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -144,47 +206,51 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    const CUtensorMap* mb = &tmB0;
-    int brow = n0;
-    if (p.mode != EPI_SWIGLU) {
-      if (n0 >= p.split1) {
-        mb = &tmB2;
-        brow = n0 - p.split1;
-      } else if (n0 >= p.split0) {
-        mb = &tmB1;
-        brow = n0 - p.split0;
-      }
-    }
     int issued_phase[STAGES];
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
-    for (int kb = 0; kb < num_kb; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = static_cast<uint32_t>(kb / STAGES) & 1u;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
+    uint32_t c = 0;  // k-blocks issued so far (ring position)
+    Item it;
+    bool ok = true;
+    for (int idx = 0; ok && get_item(p, g, G, idx, it); ++idx) {
+      const int m0 = (it.tile % p.m_tiles) * BM;
+      const int n0 = (it.tile / p.m_tiles) * BN;
+      const CUtensorMap* mb = &tmB0;
+      int brow = n0;
+      if (p.mode != EPI_SWIGLU) {
+        if (n0 >= p.split1) {
+          mb = &tmB2;
+          brow = n0 - p.split1;
+        } else if (n0 >= p.split0) {
+          mb = &tmB1;
+          brow = n0 - p.split0;
+        }
+      }
+      for (int kb = it.kb0; kb < it.kb1; ++kb, ++c) {
+        const int s = static_cast<int>(c % STAGES);
+        const uint32_t ph = (c / STAGES) & 1u;
+        if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
         if (lane == 0) {
-          *abort_flag = 1;
-          set_status(p.status, ST_WAIT_TIMEOUT);
+          uint8_t* sa = smem + L::OFF_A + s * A_STAGE;
+          uint8_t* sb = smem + L::OFF_B + s * L::B_STAGE;
+          mbar_arrive_expect_tx(&full[s], A_STAGE + L::B_STAGE);
+          tma_load_2d(sa, &tmA, &full[s], kb * BK, m0);
+          if (p.mode == EPI_SWIGLU) {
+            tma_load_2d(sb, &tmB0, &full[s], kb * BK, n0 / 2);
+            tma_load_2d(sb + L::B_STAGE / 2, &tmB1, &full[s], kb * BK, n0 / 2);
+          } else {
+            tma_load_2d(sb, mb, &full[s], kb * BK, brow);
+          }
         }
-        break;
+        issued_phase[s] = static_cast<int>(ph);
+        __syncwarp();
       }
-      if (lane == 0) {
-        uint8_t* sa = smem + L::OFF_A + s * A_STAGE;
-        uint8_t* sb = smem + L::OFF_B + s * L::B_STAGE;
-        mbar_arrive_expect_tx(&full[s], A_STAGE + L::B_STAGE);
-        tma_load_2d(sa, &tmA, &full[s], kb * BK, m0);
-        if (p.mode == EPI_SWIGLU) {
-          tma_load_2d(sb, &tmB0, &full[s], kb * BK, n0 / 2);
-          tma_load_2d(sb + L::B_STAGE / 2, &tmB1, &full[s], kb * BK, n0 / 2);
-        } else {
-          tma_load_2d(sb, mb, &full[s], kb * BK, brow);
-        }
-      }
-      issued_phase[s] = static_cast<int>(ph);
-      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      set_status(p.status, ST_WAIT_TIMEOUT);
     }
     // Let every copy this warp issued land before the block can exit.
     if (lane == 0) {
@@ -195,94 +261,183 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = idesc_bf16(BN);
+    uint32_t c = 0;
+    Item it;
     bool ok = true;
-    int kb = 0;
-    for (; kb < num_kb; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t ph = static_cast<uint32_t>(kb / STAGES) & 1u;
-      if (lane == 0) ok = mbar_wait_bounded(&full[s], ph, abort_flag);
+    for (int idx = 0; ok && get_item(p, g, G, idx, it); ++idx) {
+      const int b = idx & 1;
+      const uint32_t use = static_cast<uint32_t>(idx >> 1);
+      if (lane == 0) ok = mbar_wait_bounded(&acc_empty[b], (use & 1u) ^ 1u, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        if (lane == 0) {
-          *abort_flag = 1;
-          set_status(p.status, ST_WAIT_TIMEOUT);
-        }
-        break;
-      }
+      if (!ok) break;
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sa = smem_u32(smem + L::OFF_A + s * A_STAGE);
-        const uint32_t sb = smem_u32(smem + L::OFF_B + s * L::B_STAGE);
-        const uint64_t da = sw128_desc(sa), db = sw128_desc(sb);
+      const uint32_t tacc = tmem + static_cast<uint32_t>(b * BN);
+      for (int kb = it.kb0; kb < it.kb1; ++kb, ++c) {
+        const int s = static_cast<int>(c % STAGES);
+        const uint32_t ph = (c / STAGES) & 1u;
+        if (lane == 0) ok = mbar_wait_bounded(&full[s], ph, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t da = sw128_desc(smem_u32(smem + L::OFF_A + s * A_STAGE));
+          const uint64_t db = sw128_desc(smem_u32(smem + L::OFF_B + s * L::B_STAGE));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes along K per step (encoded >> 4)
-          tc_mma_f16(tmem, da + 2 * kk, db + 2 * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
-        tc_commit(&empty[s]);  // frees the stage once these MMAs have read it
+          for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes along K per step (encoded >> 4)
+            tc_mma_f16(tacc, da + 2 * kk, db + 2 * kk, idesc, (kb > it.kb0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);  // frees the stage once these MMAs have read it
+        }
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&acc_full[b]);  // accumulator b complete
       __syncwarp();
     }
-    // Signal the epilogue (also on abort: the commit then only drains issued MMAs).
-    if (lane == 0) tc_commit(accum);
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      set_status(p.status, ST_WAIT_TIMEOUT);
+    }
+    // no MMA may still be running when the tensor memory is released
+    if (lane == 0) {
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0u, nullptr);
+    }
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue (warps 2..5)
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_bounded(accum, 0u, nullptr);
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    tc_fence_after();
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
-    const int row = m0 + quarter * 32 + lane;
-    const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool live = ok && !*abort_flag;
-    if (!ok && lane == 0) set_status(p.status, ST_WAIT_TIMEOUT);
-    if (p.mode == EPI_SWIGLU) {
-      bf16* out = static_cast<bf16*>(p.out);
-#pragma unroll 1
-      for (int c = 0; c < BN / 2; c += 32) {
-        float g[32], u[32];
-        tmem_ld32(tbase + c, g);
-        tmem_ld32(tbase + BN / 2 + c, u);
-        if (live && row < p.M) {
-          bf16* dst = out + static_cast<size_t>(row) * p.ldc + n0 / 2 + c;
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = silu_f(g[j + e]) * u[j + e];
-            store8(dst + j, f);
-          }
-        }
+    const int r_loc = quarter * 32 + lane;
+    const int et = threadIdx.x - 64;  // 0..127 within the epilogue warps
+    volatile int* go = abort_flag + 1;   // [2]: per-item decision, written by et == 0
+    Item it;
+    for (int idx = 0; get_item(p, g, G, idx, it); ++idx) {
+      const int b = idx & 1;
+      const uint32_t use = static_cast<uint32_t>(idx >> 1);
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_bounded(&acc_full[b], use & 1u, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok && lane == 0) {
+        *abort_flag = 1;
+        set_status(p.status, ST_WAIT_TIMEOUT);
       }
-    } else {
-      float* out = static_cast<float*>(p.out);
+      // one decision for all four epilogue warps, so that every named barrier below is
+      // reached by all of them: failures are recorded before the first barrier, read by
+      // one thread between the two, and the slot of item idx is rewritten at idx + 2 only
+      epi_bar();
+      if (et == 0) go[b] = !*abort_flag;
+      epi_bar();
+      if (!go[b]) break;
+      tc_fence_after();
+      const int m0 = (it.tile % p.m_tiles) * BM;
+      const int n0 = (it.tile / p.m_tiles) * BN;
+      const int row = m0 + r_loc;
+      const uint32_t tbase = tmem + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
+      if (it.kind == ITEM_PARTIAL) {
+        // write the partial accumulator of this tile to this CTA's slot, then publish it
+        float* slot = p.partials + (static_cast<size_t>(g) * BM + r_loc) * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
-        tmem_ld32(tbase + c, v);
-        if (live && row < p.M) {
-          float* dst = out + static_cast<size_t>(row) * p.ldc + n0 + c;
-          if (p.mode == EPI_ADD_F32) {
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(tbase + c, v);
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              float o[8];
-              load8(dst + j, o);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) o[e] += v[j + e];
-              store8(dst + j, o);
+          for (int j = 0; j < 32; j += 8) store8(slot + c + j, v + j);
+        }
+        __threadfence();
+        epi_bar();
+        if (et == 0) atomicExch(&p.flags[g], 1);
+      } else {
+        const int first = g + 1, last = it.kind == ITEM_OWNER ? it.last : g;
+        if (it.kind == ITEM_OWNER) {
+          // wait for the later contributors of this tile (bounded), in order
+          if (et == 0) {
+            for (int q = first; q <= last; ++q) {
+              const uint64_t t0 = global_ns();
+              while (atomicAdd(&p.flags[q], 0) == 0) {
+                if (global_ns() - t0 > 2000000000ull || *abort_flag) {
+                  set_status(p.status, ST_WAIT_TIMEOUT);
+                  break;
+                }
+              }
             }
-          } else {
+            __threadfence();
+          }
+          epi_bar();
+        }
+        auto add_partials = [&](float* v, int col) {
+          for (int q = first; q <= last; ++q) {
+            const float* src = p.partials + (static_cast<size_t>(q) * BM + r_loc) * BN + col;
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) store8(dst + j, v + j);
+            for (int j = 0; j < 32; j += 4) {
+              const float4 t = __ldcg(reinterpret_cast<const float4*>(src + j));
+              v[j] += t.x;
+              v[j + 1] += t.y;
+              v[j + 2] += t.z;
+              v[j + 3] += t.w;
+            }
+          }
+        };
+        if (p.mode == EPI_SWIGLU) {
+          bf16* out = static_cast<bf16*>(p.out);
+#pragma unroll 1
+          for (int c = 0; c < BN / 2; c += 32) {
+            float gv[32], uv[32];
+            tmem_ld32(tbase + c, gv);
+            tmem_ld32(tbase + BN / 2 + c, uv);
+            add_partials(gv, c);
+            add_partials(uv, BN / 2 + c);
+            if (row < p.M) {
+              bf16* dst = out + static_cast<size_t>(row) * p.ldc + n0 / 2 + c;
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = silu_f(gv[j + e]) * uv[j + e];
+                store8(dst + j, f);
+              }
+            }
+          }
+        } else {
+          float* out = static_cast<float*>(p.out);
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            float v[32];
+            tmem_ld32(tbase + c, v);
+            add_partials(v, c);
+            if (row < p.M) {
+              float* dst = out + static_cast<size_t>(row) * p.ldc + n0 + c;
+              if (p.mode == EPI_ADD_F32) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                  float o[8];
+                  load8(dst + j, o);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) o[e] += v[j + e];
+                  store8(dst + j, o);
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) store8(dst + j, v + j);
+              }
+            }
           }
         }
+        if (it.kind == ITEM_OWNER) {
+          epi_bar();  // every thread has read the partials
+          if (et == 0)
+            for (int q = first; q <= last; ++q) atomicExch(&p.flags[q], 0);
+        }
       }
+      // accumulator b may be overwritten once every epilogue warp has read it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, 2 * BN);
   }
 }
 
@@ -368,9 +523,23 @@ __global__ void __launch_bounds__(256) gemm_f32(const float* __restrict__ A, con
 }  // namespace simt
 
 // ============================================================================= launcher
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+size_t gemm_scratch_bytes() {
+  return static_cast<size_t>(tc::MAX_CTAS) * tc::BM * 256 * sizeof(float) + tc::MAX_CTAS * sizeof(int);
+}
+
 template <int BN, int STAGES>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
-                             const tc::Params& p, cudaStream_t s) {
+                             tc::Params p, void* scratch, size_t scratch_bytes, cudaStream_t s) {
   using L = tc::Layout<BN, STAGES>;
   static bool configured = false;
   if (!configured) {
@@ -379,17 +548,46 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid((p.M + tc::BM - 1) / tc::BM, p.N / BN);
-  tc::gemm_bf16_tc<BN, STAGES><<<grid, tc::THREADS, L::ALLOC, s>>>(a, b0, b1, b2, p);
+  // Persistent grid: one CTA per SM, whole tiles round-robin (data-parallel).  When the
+  // tiles fill at most half of the SMs, the k-iterations are instead divided evenly over
+  // all SMs (stream-K), which needs scratch for the partial tiles.  Measured on GB300:
+  // with five or more CTAs sharing each weight tile (M >= ~512), stream-K desynchronises
+  // them and re-reads weights from DRAM (1.66x the bytes), so it is kept to the sparse
+  // case where most SMs would otherwise idle.
+  const int sms = std::min(sm_count(), tc::MAX_CTAS);
+  p.m_tiles = (p.M + tc::BM - 1) / tc::BM;
+  p.kb_per_tile = p.K / tc::BK;
+  p.tiles = p.m_tiles * (p.N / BN);
+  const size_t need = static_cast<size_t>(sms) * tc::BM * BN * sizeof(float) + sms * sizeof(int);
+  const bool can_sk = scratch != nullptr && scratch_bytes >= need;
+  int G = std::min(sms, p.tiles);
+  p.dp_tiles = p.tiles;
+  p.sk_iters = 0;
+  if (can_sk && 2 * p.tiles <= sms) {
+    const long long iters = static_cast<long long>(p.tiles) * p.kb_per_tile;
+    const int g_sk = std::min(sms, 8 * p.tiles);  // at most ~8 CTAs share one tile
+    if (iters >= 8LL * g_sk) {                      // and at least 8 k-blocks per CTA
+      G = g_sk;
+      p.dp_tiles = 0;
+      p.sk_iters = iters;
+    }
+  }
+  p.partials = static_cast<float*>(scratch);
+  p.flags = scratch ? reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) +
+                                             static_cast<size_t>(sms) * tc::BM * BN * sizeof(float))
+                    : nullptr;
+  tc::gemm_bf16_tc<BN, STAGES><<<G, tc::THREADS, L::ALLOC, s>>>(a, b0, b1, b2, p);
   return cudaGetLastError();
 }
 
 // mode: EPI_STORE_F32 / EPI_ADD_F32 (C fp32 [M][ldc]) or EPI_SWIGLU (C dtype [M][ldc], N/2 columns).
 // B0/B1/B2: weight tensors [rows][K]; for STORE/ADD the output columns [0,split0) come from
 // B0, [split0,split1) from B1 and [split1,N) from B2; for SWIGLU B0 = gate, B1 = up, each
-// [N/2][K].
+// [N/2][K].  scratch (may be null: data-parallel only) holds stream-K partial tiles and
+// flags; its flags must be zero before the first use and are left zero.
 cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, void* C,
-                        int M, int N, int K, int ldc, int mode, cb_dtype dt, int32_t* status, cudaStream_t s) {
+                        int M, int N, int K, int ldc, int mode, cb_dtype dt, int32_t* status, void* scratch,
+                        size_t scratch_bytes, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   if (dt == CB_F32) {
     if (mode == EPI_SWIGLU) {
@@ -421,9 +619,18 @@ cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const voi
     if (r1 > 0 && !encode_tmap_bf16_2d(&mb1, B1, K, r1, tc::BK, BN)) return cudaErrorInvalidValue;
     if (r2 > 0 && !encode_tmap_bf16_2d(&mb2, B2, K, r2, tc::BK, BN)) return cudaErrorInvalidValue;
   }
-  tc::Params p{M, N, K, mode, C, ldc, split0, split1, status};
-  if (BN == 256) return launch_tc<256, 4>(ma, mb0, mb1, mb2, p, s);
-  return launch_tc<128, 6>(ma, mb0, mb1, mb2, p, s);
+  tc::Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.mode = mode;
+  p.out = C;
+  p.ldc = ldc;
+  p.split0 = split0;
+  p.split1 = split1;
+  p.status = status;
+  if (BN == 256) return launch_tc<256, 4>(ma, mb0, mb1, mb2, p, scratch, scratch_bytes, s);
+  return launch_tc<128, 6>(ma, mb0, mb1, mb2, p, scratch, scratch_bytes, s);
 }
 
 }  // namespace cb

@@ -70,7 +70,10 @@ cudaError_t launch_post_qkv(const float* qkv, int n_s_rows, const int32_t* s_src
                             int head_dim, cb_dtype dt, void* q_out, const float* h_in, float* h_out, int d,
                             int32_t* status, cudaStream_t s);
 cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, void* C,
-                        int M, int N, int K, int ldc, int mode, cb_dtype dt, int32_t* status, cudaStream_t s);
+                        int M, int N, int K, int ldc, int mode, cb_dtype dt, int32_t* status, void* scratch,
+                        size_t scratch_bytes, cudaStream_t s);
+// bytes of GEMM scratch (stream-K partial tiles + flags) that enable every schedule
+size_t gemm_scratch_bytes();
 cudaError_t launch_attention(const void* q, const int32_t* s_pos, const int32_t* s_req, const ReqDev* reqs,
                              const AttnTile* tiles, int n_tiles, int layer, int n_heads, int n_kv_heads, int head_dim,
                              void* out, cb_dtype dt, cudaStream_t s);

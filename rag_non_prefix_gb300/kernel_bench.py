@@ -57,6 +57,7 @@ def main():
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--no-stream-k", action="store_true", help="GEMM without scratch: whole tiles per CTA")
     a = ap.parse_args()
     cbbuild.build()
     torch.manual_seed(0)
@@ -65,19 +66,20 @@ def main():
     out = {"kernel": a.kernel}
     if a.kernel == "gemm":
         M, N, K = a.M, a.N, a.K
+        scr = None if a.no_stream_k else cb.gemm_scratch(dev)
         A = (torch.randn(M, K, device=dev) * 0.5).to(torch.bfloat16)
         if a.mode == "swiglu":
             G = (torch.randn(N // 2, K, device=dev) * 0.02).to(torch.bfloat16)
             U = (torch.randn(N // 2, K, device=dev) * 0.02).to(torch.bfloat16)
             C = torch.empty(M, N // 2, dtype=torch.bfloat16, device=dev)
-            fn = lambda: cb.cb_gemm(A, G, C, 2, B2=U)  # noqa: E731
+            fn = lambda: cb.cb_gemm(A, G, C, 2, B2=U, scratch=scr)  # noqa: E731
         else:
             B = (torch.randn(N, K, device=dev) * 0.02).to(torch.bfloat16)
             C = torch.zeros(M, N, dtype=torch.float32, device=dev)
-            fn = lambda: cb.cb_gemm(A, B, C, 1 if a.mode == "add" else 0)  # noqa: E731
+            fn = lambda: cb.cb_gemm(A, B, C, 1 if a.mode == "add" else 0, scratch=scr)  # noqa: E731
         avg, best = _time(fn, a.iters, a.warmup, flush)
         fl = 2.0 * M * N * K
-        out.update(shape=[M, N, K], mode=a.mode, ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12,
+        out.update(shape=[M, N, K], mode=a.mode, stream_k=scr is not None, ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12,
                    weight_bytes=N * K * 2)
     elif a.kernel == "attention":
         H, Hkv, N, m = a.H, a.Hkv, a.N, a.m

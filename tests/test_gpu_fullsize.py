@@ -35,7 +35,7 @@ def test_gemm_full_size_sampled_rows(M, N, K, mode):
         G = (torch.randn(N // 2, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
         U = (torch.randn(N // 2, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
         C = torch.empty(M, N // 2, dtype=torch.bfloat16, device="cuda")
-        cb.cb_gemm(A, G, C, 2, B2=U)
+        cb.cb_gemm(A, G, C, 2, B2=U, scratch=cb.gemm_scratch())
         a = to_np(A[rows])
         ref = orc.silu(a @ to_np(G).T) * (a @ to_np(U).T)
         tol = 2 ** -7
@@ -43,7 +43,7 @@ def test_gemm_full_size_sampled_rows(M, N, K, mode):
         B = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
         C0 = torch.randn(M, N, device="cuda", generator=g)
         C = C0.clone()
-        cb.cb_gemm(A, B, C, mode)
+        cb.cb_gemm(A, B, C, mode, scratch=cb.gemm_scratch())
         ref = to_np(A[rows]) @ to_np(B).T + (to_np(C0[rows]) if mode == 1 else 0)
         tol = 1e-4
     torch.cuda.synchronize()

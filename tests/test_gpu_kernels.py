@@ -146,37 +146,56 @@ def _gemm_ref(a, b):
     return a.astype(np.float64) @ b.astype(np.float64).T
 
 
+@pytest.mark.parametrize("sk", [False, True], ids=["whole-tiles", "stream-k"])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (71, 256, 512), (128, 384, 256), (300, 768, 1024), (535, 1024, 4096),
-                                   (1000, 512, 320)])
-def test_gemm_bf16_store_and_add(M, N, K):
+                                   (1000, 512, 320), (535, 4096, 4096), (535, 4096, 14336), (3000, 6144, 512),
+                                   (128, 4096, 14336), (256, 4096, 4096), (200, 2560, 8192), (64, 1024, 28672)])
+def test_gemm_bf16_store_and_add(M, N, K, sk):
+    scr = cb.gemm_scratch() if sk else None
     rng = np.random.default_rng(M + N + K)
     A = _bf16(rng.standard_normal((M, K)))
     B = _bf16(rng.standard_normal((N, K)) * 0.02)
     C0 = _f32(rng.standard_normal((M, N)))
     ref = _gemm_ref(to_np(A), to_np(B))
     out = torch.full((M, N), np.nan, dtype=torch.float32, device="cuda")
-    cb.cb_gemm(A, B, out, epilogue=0)
+    cb.cb_gemm(A, B, out, epilogue=0, scratch=scr)
     acc = C0.clone()
-    cb.cb_gemm(A, B, acc, epilogue=1)
+    cb.cb_gemm(A, B, acc, epilogue=1, scratch=scr)
     torch.cuda.synchronize()
+    if sk:  # the scratch is left zero-filled (flags reset) for the next call
+        assert int(scr.view(torch.int32)[-256:].abs().sum().item()) == 0
     scale = np.max(np.abs(ref))
     assert np.max(np.abs(to_np(out) - ref)) < 1e-4 * scale
     assert np.max(np.abs(to_np(acc) - (ref + to_np(C0)))) < 1e-4 * max(scale, 1.0) + 1e-5
 
 
-@pytest.mark.parametrize("M,F,K", [(5, 64, 128), (130, 128, 256), (535, 384, 512)])
-def test_gemm_bf16_swiglu(M, F, K):
+@pytest.mark.parametrize("sk", [False, True], ids=["whole-tiles", "stream-k"])
+@pytest.mark.parametrize("M,F,K", [(5, 64, 128), (130, 128, 256), (535, 384, 512), (535, 14336, 4096), (96, 2048, 4096)])
+def test_gemm_bf16_swiglu(M, F, K, sk):
     rng = np.random.default_rng(M + F)
     A = _bf16(rng.standard_normal((M, K)))
     G = _bf16(rng.standard_normal((F, K)) * 0.05)
     U = _bf16(rng.standard_normal((F, K)) * 0.05)
     out = torch.zeros((M, F), dtype=torch.bfloat16, device="cuda")
-    cb.cb_gemm(A, G, out, epilogue=2, B2=U)
+    cb.cb_gemm(A, G, out, epilogue=2, B2=U, scratch=cb.gemm_scratch() if sk else None)
     torch.cuda.synchronize()
     g = _gemm_ref(to_np(A), to_np(G))
     u = _gemm_ref(to_np(A), to_np(U))
     ref = orc.silu(g) * u
     assert np.max(np.abs(to_np(out) - ref)) <= 2 ** -7 * np.max(np.abs(ref)) + 1e-6
+
+
+def test_gemm_stream_k_is_deterministic():
+    rng = np.random.default_rng(99)
+    A = _bf16(rng.standard_normal((200, 14336)))  # 32 tiles: the stream-K schedule
+    B = _bf16(rng.standard_normal((4096, 14336)) * 0.02)
+    outs = []
+    for _ in range(3):
+        o = torch.zeros((200, 4096), dtype=torch.float32, device="cuda")
+        cb.cb_gemm(A, B, o, 1, scratch=cb.gemm_scratch())
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 64, 8), (77, 200, 96), (288, 1024, 256)])
