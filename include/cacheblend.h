@@ -155,10 +155,12 @@ cb_status cb_select_hkvd(const float* dev, const int32_t* cand, int n, int k, in
  * B2 (may not be NULL) holds the "up" rows and B the "gate" rows, each [N/2][K]
  * (then N counts both).  bf16 runs on the tcgen05 tensor cores (persistent, one CTA
  * per SM), fp32 on CUDA cores.  bf16 needs K % 64 == 0 and N % 128 == 0.
- * scratch: NULL (whole output tiles per CTA only) or cb_gemm_scratch_size() bytes of
- * device memory, zero-filled before its first use, which lets the k-iterations of the
- * last waves be split across CTAs (stream-K partial tiles and their flags); the call
- * leaves it zero-filled.  Calls sharing one scratch must not overlap on the GPU. */
+ * scratch: NULL (whole output tiles per CTA only) or device memory, zero-filled before
+ * its first use, for the stream-K schedule used when the output tiles would occupy at
+ * most half of the SMs: 1 KiB of flags, then one 128 KiB fp32 partial tile per CTA of
+ * the split (a smaller scratch narrows the split).  cb_gemm_scratch_size() bytes allow
+ * every split.  The call leaves the flags zeroed.  Calls sharing one scratch must not
+ * overlap on the GPU. */
 cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, int N, int K, int ldc, int epilogue,
                   cb_dtype dtype, void* scratch, size_t scratch_bytes, void* stream);
 size_t cb_gemm_scratch_size(void);

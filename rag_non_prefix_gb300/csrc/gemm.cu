@@ -64,7 +64,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;                    // one 128-byte swizzle atom of bf16 along K
 constexpr int A_STAGE = BM * BK * 2;      // 16 KiB
 constexpr int THREADS = 192;
-constexpr int MAX_CTAS = 256;             // bound of the persistent grid (stream-K partial slots)
+constexpr int MAX_CTAS = 256;             // bound of the persistent grid
+constexpr int FLAG_BYTES = MAX_CTAS * 4;  // stream-K flags at the head of the scratch, partial slots after
 
 // Work division.  Tiles t = m + n * m_tiles (consecutive tiles share a weight tile).
 // Tiles [0, dp_tiles) go round-robin to the CTAs (data-parallel); the k-iterations of the
@@ -533,8 +534,10 @@ static int sm_count() {
   return n;
 }
 
+// Scratch that lets every shape use its preferred schedule: the flags plus one 128 x 256
+// fp32 partial slot per SM.
 size_t gemm_scratch_bytes() {
-  return static_cast<size_t>(tc::MAX_CTAS) * tc::BM * 256 * sizeof(float) + tc::MAX_CTAS * sizeof(int);
+  return tc::FLAG_BYTES + static_cast<size_t>(std::min(sm_count(), tc::MAX_CTAS)) * tc::BM * 256 * sizeof(float);
 }
 
 template <int BN, int STAGES>
@@ -558,24 +561,24 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
   p.m_tiles = (p.M + tc::BM - 1) / tc::BM;
   p.kb_per_tile = p.K / tc::BK;
   p.tiles = p.m_tiles * (p.N / BN);
-  const size_t need = static_cast<size_t>(sms) * tc::BM * BN * sizeof(float) + sms * sizeof(int);
-  const bool can_sk = scratch != nullptr && scratch_bytes >= need;
+  const size_t slot_bytes = static_cast<size_t>(tc::BM) * BN * sizeof(float);
+  const long long slots =
+      scratch && scratch_bytes > static_cast<size_t>(tc::FLAG_BYTES) ? (scratch_bytes - tc::FLAG_BYTES) / slot_bytes : 0;
   int G = std::min(sms, p.tiles);
   p.dp_tiles = p.tiles;
   p.sk_iters = 0;
-  if (can_sk && 2 * p.tiles <= sms) {
+  if (2 * p.tiles <= sms) {
     const long long iters = static_cast<long long>(p.tiles) * p.kb_per_tile;
-    const int g_sk = std::min(sms, 8 * p.tiles);  // at most ~8 CTAs share one tile
-    if (iters >= 8LL * g_sk) {                      // and at least 8 k-blocks per CTA
+    // at most ~8 CTAs share one tile, one partial slot per CTA, at least 8 k-blocks each
+    const int g_sk = static_cast<int>(std::min<long long>(std::min(sms, 8 * p.tiles), slots));
+    if (g_sk >= 2 * p.tiles && iters >= 8LL * g_sk) {
       G = g_sk;
       p.dp_tiles = 0;
       p.sk_iters = iters;
     }
   }
-  p.partials = static_cast<float*>(scratch);
-  p.flags = scratch ? reinterpret_cast<int*>(static_cast<uint8_t*>(scratch) +
-                                             static_cast<size_t>(sms) * tc::BM * BN * sizeof(float))
-                    : nullptr;
+  p.flags = scratch ? static_cast<int*>(scratch) : nullptr;
+  p.partials = scratch ? reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + tc::FLAG_BYTES) : nullptr;
   tc::gemm_bf16_tc<BN, STAGES><<<G, tc::THREADS, L::ALLOC, s>>>(a, b0, b1, b2, p);
   return cudaGetLastError();
 }
