@@ -165,6 +165,23 @@ cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, 
                   cb_dtype dtype, void* scratch, size_t scratch_bytes, void* stream);
 size_t cb_gemm_scratch_size(void);
 
+/* Allocation-free variant of cb_gemm (no counterpart on the pages: an addition for
+ * callers that cannot allocate device memory, e.g. a process held to a fixed device
+ * budget after start-up, or code inside a framework that owns every allocation).
+ * Same arguments and results as cb_gemm without the scratch arguments: its stream-K
+ * scratch is a built-in device array of CB_GEMM_STATIC_SCRATCH_BYTES (4 MiB + 1 KiB:
+ * the flags and 32 partial tiles) that every GPU loading the library holds until the
+ * process exits.  Shapes whose stream-K split needs more return CB_ERR_WORKSPACE
+ * (cb_gemm_noalloc_error() has the reason); data-parallel shapes need none.  The call
+ * allocates nothing; its first call on a device looks up the array's device address
+ * (make that first call before any stream capture), and each call that uses the array
+ * zeroes its flags first.  All calls share the array, so calls that overlap on the
+ * GPU (other streams, other threads) race: order them on one stream. */
+#define CB_GEMM_STATIC_SCRATCH_BYTES ((size_t)(4u << 20) + 1024u)
+cb_status cb_gemm_noalloc(const void* A, const void* B, const void* B2, void* C, int M, int N, int K, int ldc,
+                          int epilogue, cb_dtype dtype, void* stream);
+const char* cb_gemm_noalloc_error(void);
+
 /* Causal attention of sparse queries over one KV cache ([P3] "어떤 토큰을 다시 계산하는가":
  * selected queries attend under the causal mask to all available K/V).
  * q [m][n_heads][head_dim] dtype; q_pos int32 [m] (positions, < n_kv);

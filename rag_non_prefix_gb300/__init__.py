@@ -27,7 +27,7 @@ EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_
             "cb_blend_prefill",
             "cb_full_prefill", "cb_blend_begin", "cb_fetch_kv", "cb_synchronize", "cb_prefill_layer",
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
-            "cb_get_profile")
+            "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error")
 PHASES = ("begin", "staged_rot", "norm", "qkv", "rope", "deviation", "select", "scatter", "attention", "oproj",
           "gateup", "down", "finish")
 
@@ -94,6 +94,8 @@ def load_library(path: str = LIB_PATH):
         "cb_select_hkvd": (st, [vp, i32p, C.c_int, C.c_int, i32p, i32p, vp]),
         "cb_gemm": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_size_t, vp]),
         "cb_gemm_scratch_size": (C.c_size_t, []),
+        "cb_gemm_noalloc": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp]),
+        "cb_gemm_noalloc_error": (C.c_char_p, []),
         "cb_attention": (st, [vp, i32p, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp]),
         "cb_blend_prefill": (st, [vp, C.POINTER(Request), C.c_int, C.POINTER(BlendParams), vp, vp]),
         "cb_full_prefill": (st, [vp, i32p, C.c_int, vp, vp, vp, i32p, vp]),
@@ -220,6 +222,20 @@ def cb_gemm(A: torch.Tensor, B: torch.Tensor, C_out: torch.Tensor, epilogue: int
     _check(lib.cb_gemm(_ptr(A), _ptr(B), _ptr(B2), _ptr(C_out), M, N, K, C_out.shape[1], epilogue,
                        _dtype_code(A.dtype), _ptr(scratch), 0 if scratch is None else scratch.numel(),
                        _stream(stream)))
+    return C_out
+
+
+def cb_gemm_noalloc(A: torch.Tensor, B: torch.Tensor, C_out: torch.Tensor, epilogue: int = 0,
+                    B2: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """cb_gemm without scratch arguments: for callers that cannot allocate device memory
+    (the library's built-in device array serves as stream-K scratch)."""
+    lib = load_library()
+    M, K = A.shape
+    N = B.shape[0] * (2 if epilogue == 2 else 1)
+    st = lib.cb_gemm_noalloc(_ptr(A), _ptr(B), _ptr(B2), _ptr(C_out), M, N, K, C_out.shape[1], epilogue,
+                             _dtype_code(A.dtype), _stream(stream))
+    if st != 0:
+        raise CacheBlendError(st, lib.cb_gemm_noalloc_error().decode())
     return C_out
 
 

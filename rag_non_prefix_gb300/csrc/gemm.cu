@@ -583,6 +583,20 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
   return cudaGetLastError();
 }
 
+// Scratch bytes the schedule of launch_gemm would use for a single-tensor B of N output
+// columns with unlimited scratch (0 when the shape runs data-parallel).
+size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt) {
+  if (dt != CB_BF16 || M <= 0) return 0;
+  const int BN = N % 256 == 0 ? 256 : 128;
+  const int sms = std::min(sm_count(), tc::MAX_CTAS);
+  const int tiles = ((M + tc::BM - 1) / tc::BM) * (N / BN);
+  if (2 * tiles > sms) return 0;
+  const long long iters = static_cast<long long>(tiles) * (K / tc::BK);
+  const int g_sk = std::min(sms, 8 * tiles);
+  if (g_sk < 2 * tiles || iters < 8LL * g_sk) return 0;
+  return tc::FLAG_BYTES + static_cast<size_t>(g_sk) * tc::BM * BN * sizeof(float);
+}
+
 // mode: EPI_STORE_F32 / EPI_ADD_F32 (C fp32 [M][ldc]) or EPI_SWIGLU (C dtype [M][ldc], N/2 columns).
 // B0/B1/B2: weight tensors [rows][K]; for STORE/ADD the output columns [0,split0) come from
 // B0, [split0,split1) from B1 and [split1,N) from B2; for SWIGLU B0 = gate, B1 = up, each
