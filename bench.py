@@ -145,12 +145,20 @@ def run_ours(args, rank, world):
     eng = cb.Engine(cfg, W, max_tokens=max(T, max(len(c) for c in spec.chunks)), max_requests=len(spec.requests),
                     max_positions=max(n_tok) + 1)
     used = sorted({s.chunk for req in spec.requests for s in req if s.chunk >= 0})
+    staged = args.staged if args.staged is not None else spec.name == "llama7b"
     chunk_store = {}
     for c in used:
         ids = hd.ids_tensor(spec.chunks[c])
         k, v = eng.precompute_chunk(ids)
         chunk_store[c] = (ids, k, v)
         eng.register_chunk(c, ids, k, v)
+    host_store = {}
+    if staged:  # the cached KV lives in page-locked host memory and is staged layer by layer
+        for c in used:
+            ids, k, v = chunk_store[c]
+            host_store[c] = (ids, k.cpu().pin_memory(), v.cpu().pin_memory())
+            eng.register_chunk(c, ids, host_store[c][1], host_store[c][2], on_host=True)
+    copy_stream = torch.cuda.Stream() if staged else None
     reqs = []
     for req in spec.requests:
         q = [s for s in req if s.chunk < 0][0]
@@ -160,8 +168,8 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 512 MiB > L2
 
-    def blend_step():
-        eng.blend_prefill(reqs, ratios, stream=stream)
+    def blend_step(rat=None):
+        eng.blend_prefill(reqs, ratios if rat is None else rat, stream=stream, copy_stream=copy_stream)
 
     def full_step():
         for ids in full_ids:
@@ -213,6 +221,50 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     phases = eng.get_profile()
     eng.set_profiling(False)
+
+    # ratio sweep (configuration 3: 0..100 %), each point timed like the headline
+    sweep = None
+    if args.sweep:
+        sweep = []
+        for r in (0.0, 0.05, 0.10, 0.15, 0.20, 0.50, 1.0):
+            rat = cb.ratio_schedule(cfg.n_layers, r, args.schedule or spec.schedule)
+            for _ in range(2):
+                blend_step(rat)
+            ts = timed(lambda: blend_step(rat), max(3, args.steps // 2), "sweep")
+            sweep.append({"ratio": r, "ttft_ms": round(statistics.mean(ts), 4)})
+    staging = None
+    if staged:
+        # T_load: host->device bandwidth of the chunk KV measured on the copy stream
+        ids0, kh, vh = host_store[used[0]]
+        dst = torch.empty_like(kh, device=dev)
+        torch.cuda.synchronize()
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(copy_stream):
+            a_ev.record(copy_stream)
+            for _ in range(3):
+                dst.copy_(kh, non_blocking=True)
+            b_ev.record(copy_stream)
+        b_ev.synchronize()
+        h2d_gbs = 3 * kh.numel() * kh.element_size() / (a_ev.elapsed_time(b_ev) * 1e-3) / 1e9
+        total_bytes = sum(2 * host_store[c][1].numel() * host_store[c][1].element_size()
+                          for req in spec.requests for c in [s_.chunk for s_ in req if s_.chunk >= 0])
+        t_load = total_bytes / (h2d_gbs * 1e9) * 1e3
+        # the same blend with the cached KV resident in HBM: T_recompute
+        for c in used:
+            ids, k, v = chunk_store[c]
+            eng.register_chunk(c, ids, k, v)
+        cs_saved = copy_stream
+        copy_stream = None
+        for _ in range(2):
+            blend_step()
+        res_ms = statistics.mean(timed(blend_step, args.steps, "resident"))
+        copy_stream = cs_saved
+        for c in used:
+            ids, kh_, vh_ = host_store[c]
+            eng.register_chunk(c, ids, kh_, vh_, on_host=True)
+        staging = {"h2d_gbs": round(h2d_gbs, 1), "staged_bytes": total_bytes, "t_load_ms": round(t_load, 3),
+                   "t_recompute_ms": round(res_ms, 3), "max_load_recompute_ms": round(max(t_load, res_ms), 3),
+                   "ttft_staged_ms": round(statistics.mean(blend_ms), 3)}
 
     # end to end through the public API with host buffers: query ids in, first token out
     pinned_q = [r["query_ids"].cpu().pin_memory() for r in reqs]
@@ -292,6 +344,8 @@ def run_ours(args, rank, world):
         "e2e": {"value": round(n_total / (e2e_mean * 1e-3), 1), "unit": "tok/s", "ms": round(e2e_mean, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(step_launches * args.steps),
+        "sweep": sweep,
+        "staging": staging,
         "clocks": clocks,
     }
     return out, spec, cfg, ratios, W
@@ -416,6 +470,9 @@ def main():
     ap.add_argument("--ratio", type=float, default=None)
     ap.add_argument("--schedule", default=None, choices=[None, "fixed", "gradual"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="also time r in {0, 5, 10, 15, 20, 50, 100} %%")
+    ap.add_argument("--staged", default=None, action=argparse.BooleanOptionalAction,
+                    help="cached KV in pinned host memory, staged per layer (default: on for llama7b)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
