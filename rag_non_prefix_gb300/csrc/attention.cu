@@ -1,250 +1,413 @@
 // Causal attention of sparse (selected) queries over a fused KV cache.
 //
-// bf16, head_dim 128: flash-attention style.  A tile packs QT queries x G heads of one
-// KV group into 64 rows (G = n_heads / n_kv_heads, QT = 64 / G), so the group's K/V
-// blocks are read once for all its heads.  Four warps, 16 rows each; S = Q K^T and
-// O += P V on mma.sync m16n8k16 (bf16 in, fp32 accumulate); 64-key K/V blocks are
-// double-buffered in shared memory with cp.async (16-byte chunks, XOR-swizzled rows);
-// online softmax in fp32 with exp2f.  The mask is per row: key j is visible to the row
-// iff j <= the row's token position.  Tiles run longest-first (reverse launch order).
+// bf16, head_dim 128, on the tcgen05 tensor cores.  One CTA per (tile, KV head): a tile
+// packs QT queries x G heads of one KV group into the 128 rows of the MMA (G = n_heads /
+// n_kv_heads, QT = 128 / G), so each K/V block is read once for all heads of the group.
+//   warp 0: TMA producer -- 4-D tensor maps over the fused cache [L][N][Hkv][dh] bring
+//           128-key K and V blocks (128-byte swizzle) into a two-stage ring
+//   warp 1: TMEM owner + MMA issuer -- S_j = Q K_j^T into one of two TMEM buffers, then
+//           O += P_{j-1} V_{j-1} (V as an MN-major operand) accumulated in TMEM
+//   warps 2-5: one query row per thread -- read S_j from TMEM, apply the causal mask (key
+//           j is visible iff j <= the row's token position) and the online softmax in fp32
+//           (exp2f), and write P_j (bf16) to one of two shared-memory buffers.  P is taken
+//           relative to a reference max that moves only when a row's max grows by more
+//           than 2^8; then the row of O in TMEM is rescaled (rarely).  Finally O / l -> bf16.
+// Every mbarrier wait is bounded: on timeout the CTA records ST_WAIT_TIMEOUT and leaves.
 //
 // fp32 (any head_dim multiple of 32 up to 128): one warp per (query, head); lanes split
 // 32 keys at a time for the scores and head_dim for the output; expf softmax.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace cb {
 
-constexpr int AT_ROWS = 64;
-constexpr int AT_KB = 64;
-constexpr int AT_DH = 128;
-constexpr int AT_THREADS = 128;
-constexpr int AT_SMEM = (AT_ROWS * AT_DH + 4 * AT_KB * AT_DH) * 2;  // Q + 2 x (K, V)
+namespace ta {
 
-struct AttnArgs {
+constexpr int ROWS = 128;    // MMA M: (query, head) rows of a tile
+constexpr int BKV = 128;     // keys per block (MMA N of S, K of PV)
+constexpr int DH = 128;
+constexpr int THREADS = 320;   // producer, MMA, two softmax warpgroups
+constexpr int MAXREQ = 16;   // requests (tensor-map pairs) per launch
+constexpr int ATOM = ROWS * 64 * 2;          // one [128][64] bf16 swizzle-atom column: 16 KiB
+constexpr int OFF_Q = 0;                     // Q: 2 atom columns (head_dim 0-63, 64-127)
+constexpr int OFF_P = OFF_Q + 2 * ATOM;      // P[2]: 2 atom columns each (keys 0-63, 64-127)
+constexpr int OFF_KV = OFF_P + 4 * ATOM;     // stages of K (2 columns) then V (2 columns)
+constexpr int STAGE = 4 * ATOM;              // 64 KiB
+constexpr int STAGES = 2;
+constexpr int OFF_BAR = OFF_KV + STAGES * STAGE;
+constexpr int SMEM = OFF_BAR + 3072;         // barriers, row positions, max exchange: the 227 KiB limit
+// The operand tiles fill shared memory, leaving no slack to realign the base: the kernel
+// relies on the dynamic shared memory starting 1024-byte aligned (it checks, and reports
+// ST_RANGE instead of computing when it is not).
+constexpr uint32_t TMEM_COLS = 512;          // S[2] at columns 0 and 128, O at 256
+constexpr uint32_t O_COL = 256;
+constexpr float RESCALE_LOG2 = 8.0f;         // O is rescaled only when a row max grows by > 2^8
+
+struct Args {
+  CUtensorMap kmap[MAXREQ];
+  CUtensorMap vmap[MAXREQ];
+  int n_kv[MAXREQ];
+  int layer_coord[MAXREQ];  // 4th coordinate of the maps (0 for a one-layer cache)
   const bf16* q;
   const int32_t* s_pos;
-  const int32_t* s_req;
-  const ReqDev* reqs;
-  const AttnTile* tiles;
-  // direct mode (reqs == nullptr): one cache, tiles implied by m
-  const bf16* k_direct;
-  const bf16* v_direct;
-  int n_kv_direct;
-  int m_direct;
-  int layer, H, Hkv, G, QT;
+  const AttnTile* tiles;    // null: direct mode (one request, tiles of QT rows over m queries)
+  int req_base;
+  int n_tiles;
+  int direct_m;
+  int H, Hkv, G, QT;
   bf16* out;
   float scale_log2;
+  int32_t* status;
 };
 
-// element offset of 16-byte chunk `ch` of row `r` in a [rows][128] bf16 tile, swizzled
-__device__ __forceinline__ int swz(int r, int ch) { return r * AT_DH + ((ch ^ (r & 7)) << 3); }
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {  // K-major, 128-byte swizzle
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+// MN-major, 128-byte swizzle: 64-element column blocks lbo bytes apart, 8-row groups 1 KiB apart
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr, uint32_t lbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// kind::f16, bf16 inputs, fp32 accumulator, M = 128, N = 128; B MN-major when b_mn
+__host__ __device__ constexpr uint32_t idesc(bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+}
 
-__global__ void __launch_bounds__(AT_THREADS) attn_bf16_kernel(AttnArgs a) {
-  extern __shared__ __align__(128) uint8_t at_smem[];
-  bf16* Qs = reinterpret_cast<bf16*>(at_smem);
-  bf16* Ks = Qs + AT_ROWS * AT_DH;
-  bf16* Vs = Ks + 2 * AT_KB * AT_DH;
-  __shared__ int rowpos[AT_ROWS];
-  __shared__ int s_maxpos;
+// Barriers (phase of use u of a two-slot barrier b[x & 1] is (x >> 1) & 1):
+//   q_full            softmax warps stored Q                       (4 arrivals)
+//   k_full[2]         K_j landed                                   (TMA bytes)
+//   k_empty[2]        S_j done: K slot free                        (MMA commit)
+//   v_full[2]         V_j landed                                   (TMA bytes)
+//   v_empty[2]        PV_j done: V slot free                       (MMA commit)
+//   s_full[2]         S_j in TMEM                                  (MMA commit)
+//   s_empty[2]        S_j read into registers                      (4 arrivals)
+//   p_full[2]         P_j in shared memory (and O rescaled)        (4 arrivals)
+//   pv_done[2]        PV_j accumulated into O                      (MMA commit)
+__global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_constant__ Args a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // uniform across the block
+    if (threadIdx.x == 0) set_status(a.status, ST_RANGE);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* q_full = bar;
+  uint64_t* k_full = bar + 1;
+  uint64_t* k_empty = bar + 3;
+  uint64_t* s_full = bar + 5;
+  uint64_t* s_empty = bar + 7;
+  uint64_t* p_full = bar + 9;
+  uint64_t* pv_done = bar + 11;
+  uint64_t* drain = bar + 13;
+  uint64_t* v_full = bar + 14;
+  uint64_t* v_empty = bar + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_maxpos = reinterpret_cast<int*>(tmem_slot + 2);
+  int* rowpos = reinterpret_cast<int*>(bar + 20);  // [128] (bar + 18: slot, abort flag, max position)
+  float* xmax = reinterpret_cast<float*>(rowpos + ROWS);  // [2][2][128]: per block parity, per half
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.y;
   AttnTile t;
-  const bf16* Kc;
-  const bf16* Vc;
-  int n_kv;
-  if (a.reqs) {
-    t = a.tiles[gridDim.x - 1 - blockIdx.x];
-    const ReqDev rq = a.reqs[t.req];
-    const size_t off = static_cast<size_t>(a.layer) * rq.layer_stride;
-    Kc = static_cast<const bf16*>(rq.k) + off;
-    Vc = static_cast<const bf16*>(rq.v) + off;
-    n_kv = rq.n_tokens;
+  if (a.tiles) {
+    t = a.tiles[a.n_tiles - 1 - blockIdx.x];  // longest tiles first
+    t.req -= a.req_base;
   } else {
-    const int b = gridDim.x - 1 - blockIdx.x;
+    const int b = a.n_tiles - 1 - blockIdx.x;
     t.req = 0;
     t.row0 = b * a.QT;
-    t.count = min(a.QT, a.m_direct - t.row0);
-    Kc = a.k_direct;
-    Vc = a.v_direct;
-    n_kv = a.n_kv_direct;
+    t.count = min(a.QT, a.direct_m - t.row0);
   }
-  const int G = a.G, QT = a.QT, H = a.H, Hkv = a.Hkv;
+  const int G = a.G, QT = a.QT, H = a.H;
+  const int n_kv = a.n_kv[t.req];
 
-  if (tid < AT_ROWS) {
-    const int qi = tid / G;
-    int p = -1;
-    if (qi < t.count && tid < QT * G) {
-      p = a.s_pos[t.row0 + qi];
-      if (p >= n_kv) p = n_kv - 1;  // positions are < n_kv by construction; clamp defensively
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 8);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 8);
+      mbar_init(&p_full[i], 8);
+      mbar_init(&pv_done[i], 1);
     }
-    rowpos[tid] = p;
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  // Q tile: 64 rows x 16 chunks
-  for (int c = tid; c < AT_ROWS * 16; c += AT_THREADS) {
-    const int r = c >> 4, ch = c & 15;
+  if (threadIdx.x >= 64 && threadIdx.x < 64 + ROWS) {  // row positions (-1: no query in this row)
+    const int r = threadIdx.x - 64;
+    const int qi = r / G;
+    int p = -1;
+    if (qi < t.count && r < QT * G) p = min(a.s_pos[t.row0 + qi], n_kv - 1);
+    rowpos[r] = p;
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    int mp = -1;
+    for (int r = 0; r < ROWS; ++r) mp = max(mp, rowpos[r]);
+    *s_maxpos = mp;
+  }
+  __syncthreads();
+  const uint32_t tmem = *tmem_slot;
+  const int n_blk = *s_maxpos < 0 ? 0 : *s_maxpos / BKV + 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const CUtensorMap* km = &a.kmap[t.req];
+      const CUtensorMap* vm = &a.vmap[t.req];
+      const int lc = a.layer_coord[t.req];
+      int issued_k = 0, issued_v = 0;
+      for (int j = 0; j < n_blk; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = ((j >> 1) & 1) ^ 1;
+        uint8_t* kd = smem + OFF_KV + st * STAGE;
+        // K_j once S_{j-2} is done with its slot; V_j once PV_{j-2} is
+        if (!mbar_wait_bounded(&k_empty[st], ph, abort_flag)) break;
+        mbar_arrive_expect_tx(&k_full[st], 2 * ATOM);
+        tma_load_4d(kd, km, &k_full[st], 0, kvh, j * BKV, lc);
+        tma_load_4d(kd + ATOM, km, &k_full[st], 64, kvh, j * BKV, lc);
+        issued_k = j + 1;
+        if (!mbar_wait_bounded(&v_empty[st], ph, abort_flag)) break;
+        mbar_arrive_expect_tx(&v_full[st], 2 * ATOM);
+        tma_load_4d(kd + 2 * ATOM, vm, &v_full[st], 0, kvh, j * BKV, lc);
+        tma_load_4d(kd + 3 * ATOM, vm, &v_full[st], 64, kvh, j * BKV, lc);
+        issued_v = j + 1;
+      }
+      if (issued_v < n_blk && !*abort_flag) {
+        *abort_flag = 1;
+        set_status(a.status, ST_WAIT_TIMEOUT);
+      }
+      // copies issued into slots that nobody consumed must land before the block exits
+      for (int j = max(0, issued_k - 2); j < issued_k; ++j) mbar_wait_bounded(&k_full[j & 1], (j >> 1) & 1, nullptr);
+      for (int j = max(0, issued_v - 2); j < issued_v; ++j) mbar_wait_bounded(&v_full[j & 1], (j >> 1) & 1, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    const uint32_t sq = smem_u32(smem + OFF_Q);
+    bool ok = true;
+    auto wait = [&](uint64_t* b, uint32_t ph) {
+      if (ok && lane == 0) ok = mbar_wait_bounded(b, ph, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      return ok;
+    };
+    auto issue_pv = [&](int i) {  // O (+)= P_i V_i
+      const int st = i & 1;
+      if (!wait(&p_full[st], (i >> 1) & 1) || !wait(&v_full[st], (i >> 1) & 1)) return;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sp = smem_u32(smem + OFF_P + st * 2 * ATOM);
+        const uint32_t sv = smem_u32(smem + OFF_KV + st * STAGE + 2 * ATOM);
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk) {  // 16 keys per step: P columns, V rows
+          const uint64_t da = desc_kmajor(sp + (kk >> 2) * ATOM) + 2 * (kk & 3);
+          const uint64_t db = desc_mnmajor(sv + kk * 16 * 128, ATOM);
+          tc_mma_f16(tmem + O_COL, da, db, idesc(true), (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&pv_done[st]);
+        tc_commit(&v_empty[st]);
+      }
+      __syncwarp();
+    };
+    wait(q_full, 0);
+    for (int j = 0; ok && j < n_blk; ++j) {
+      const int st = j & 1;
+      if (!wait(&k_full[st], (j >> 1) & 1) || !wait(&s_empty[st], ((j >> 1) & 1) ^ 1)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sk = smem_u32(smem + OFF_KV + st * STAGE);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {  // 16 head-dim elements per step
+          const uint64_t da = desc_kmajor(sq + (kk >> 2) * ATOM) + 2 * (kk & 3);
+          const uint64_t db = desc_kmajor(sk + (kk >> 2) * ATOM) + 2 * (kk & 3);
+          tc_mma_f16(tmem + st * 128, da, db, idesc(false), kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[st]);
+        tc_commit(&k_empty[st]);
+      }
+      __syncwarp();
+      if (j >= 1) issue_pv(j - 1);
+    }
+    if (ok && n_blk > 0) issue_pv(n_blk - 1);
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      set_status(a.status, ST_WAIT_TIMEOUT);
+    }
+    if (lane == 0) {  // no MMA may run when the tensor memory is released
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0u, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax / output (warps 2..9)
+    // Two warpgroups: half h handles columns 64h..64h+63 of every row of S, P and O.
+    const int sw = warp - 2;           // 0..7
+    const int half = sw >> 2;
+    const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31 belong to this warp
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half * 64);
     const int qi = r / G, g = r - qi * G;
     const bool valid = qi < t.count && r < QT * G;
-    const bf16* src = valid ? a.q + (static_cast<size_t>(t.row0 + qi) * H + kvh * G + g) * AT_DH + ch * 8 : a.q;
-    cp_async16(smem_u32(Qs + swz(r, ch)), src, valid ? 16 : 0);
-  }
-  cp_async_commit();
-  __syncthreads();
-  if (tid == 0) {
-    int mp = -1;
-    for (int r = 0; r < AT_ROWS; ++r) mp = max(mp, rowpos[r]);
-    s_maxpos = mp;
-  }
-  __syncthreads();
-  const int maxpos = s_maxpos;
-  const int n_kb = maxpos < 0 ? 0 : maxpos / AT_KB + 1;
-
-  auto load_kv = [&](int kb, int buf) {
-    bf16* kd = Ks + buf * AT_KB * AT_DH;
-    bf16* vd = Vs + buf * AT_KB * AT_DH;
-    for (int c = tid; c < AT_KB * 16; c += AT_THREADS) {
-      const int r = c >> 4, ch = c & 15;
-      const int key = kb * AT_KB + r;
-      const bool valid = key < n_kv;
-      const size_t off = (static_cast<size_t>(valid ? key : 0) * Hkv + kvh) * AT_DH + ch * 8;
-      cp_async16(smem_u32(kd + swz(r, ch)), Kc + off, valid ? 16 : 0);
-      cp_async16(smem_u32(vd + swz(r, ch)), Vc + off, valid ? 16 : 0);
+    // Q: half h stores head_dim atom h of its rows
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + (static_cast<size_t>(t.row0 + (valid ? qi : 0)) * H + kvh * G + g) * DH + half * 64);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = valid ? src[c] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(smem + OFF_Q + half * ATOM + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
     }
-  };
-  if (n_kb > 0) load_kv(0, 0);
-  cp_async_commit();
-  cp_async_wait<1>();  // Q has landed
-  __syncthreads();
-
-  // Q fragments of this warp's 16 rows: 8 k-steps of 16 over head_dim
-  uint32_t qf[8][4];
-  {
-    const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int pos = rowpos[r];
+    float m = -1e30f, l = 0.f;  // reference max of P (log2 units, scaled); this half's row sum
+    // A failed (bounded) wait clears ok and skips the work that depends on it, but never the
+    // named barriers: both halves run the same barriers in the same order, and every later
+    // wait returns at once (ok stays false), so the loop still ends.
+    bool ok = true;
+    auto wait = [&](uint64_t* b, uint32_t ph) {
+      if (ok && lane == 0) ok = mbar_wait_bounded(b, ph, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    };
+    auto sm_bar = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };  // the eight softmax warps
+    for (int j = 0; j < n_blk; ++j) {
+      const int st = j & 1;
+      wait(&s_full[st], (j >> 1) & 1);
+      uint32_t sv[64];
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int ch = ks * 2 + (lane >> 4);
-      ldsm_x4(smem_u32(Qs + swz(r, ch)), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+        for (int c = 0; c < 64; c += 16) tmem_ld16_nowait(tmem + st * 128 + col0 + lane_off + c, sv + c);
+        tmem_wait_ld();
+        tc_fence_before();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) sv[e] = 0u;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[st]);
+      const int k0 = j * BKV + half * 64;
+      const bool full = k0 + 63 <= pos;
+      float mx = -INFINITY;
+      if (full) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(sv[e]));
+        mx *= a.scale_log2;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (k0 + e <= pos) mx = fmaxf(mx, __uint_as_float(sv[e]) * a.scale_log2);
+      }
+      // row max over both halves (slots by block parity: a slot is rewritten two blocks later,
+      // after the barrier of the next block, so the partner has read it)
+      xmax[(st * 2 + half) * ROWS + r] = mx;
+      sm_bar();
+      mx = fmaxf(mx, xmax[(st * 2 + (half ^ 1)) * ROWS + r]);
+      // lazy rescale: move the reference max only when this block exceeds it by > 2^8
+      const bool need = mx > m + RESCALE_LOG2;
+      const float m_new = need ? mx : m;
+      const float alpha = exp2f(m - m_new);
+      if (__any_sync(0xffffffffu, need) && j > 0) {  // same rows, same decision in both halves
+        // O holds PV_0..PV_{j-1}: wait for the last of them, then scale this warp's part
+        wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) {
+            uint32_t ov[16];
+            tmem_ld16_nowait(tmem + O_COL + col0 + lane_off + c, ov);
+            tmem_wait_ld();
+            float f[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(ov[e]) * alpha;
+            tmem_st16(tmem + O_COL + col0 + lane_off + c, f);
+          }
+          tmem_wait_st();
+        }
+      }
+      l *= alpha;
+      m = m_new;
+      // P_j (this half's 64 keys = one swizzle atom) -> its buffer, free once PV_{j-2} is done
+      if (j >= 2) wait(&pv_done[st], ((j - 2) >> 1) & 1);
+      if (ok) {
+        uint8_t* pb = smem + OFF_P + st * 2 * ATOM + half * ATOM;
+#pragma unroll
+        for (int c = 0; c < 64; c += 8) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const int x = c + e;
+            const float p0 = (full || k0 + x <= pos) ? exp2f(__uint_as_float(sv[x]) * a.scale_log2 - m) : 0.f;
+            const float p1 =
+                (full || k0 + x + 1 <= pos) ? exp2f(__uint_as_float(sv[x + 1]) * a.scale_log2 - m) : 0.f;
+            l += p0 + p1;
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(pb + r * 128 + (((c >> 3) ^ (r & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[st]);
     }
-  }
-  const int r_lo = warp * 16 + (lane >> 2), r_hi = r_lo + 8;
-  const int pos_lo = rowpos[r_lo], pos_hi = rowpos[r_hi];
-  float m_lo = -1e30f, m_hi = -1e30f, l_lo = 0.f, l_hi = 0.f;
-  float o[16][4];
+    // O = PV_0 + ... + PV_{n-1} (at the reference max) / (row sum of both halves); the sums go
+    // to the exchange slots of parity n_blk, last read before the previous block's barrier
+    float* xsum = xmax + (n_blk & 1) * 2 * ROWS;
+    xsum[half * ROWS + r] = l;
+    if (n_blk > 0) wait(&pv_done[(n_blk - 1) & 1], ((n_blk - 1) >> 1) & 1);
+    sm_bar();
+    const float l_all = xsum[r] + xsum[ROWS + r];  // same order in both halves
+    if (ok && n_blk > 0) {
+      tc_fence_after();
+      const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
+      bf16* dst = a.out + (static_cast<size_t>(t.row0 + (valid ? qi : 0)) * H + kvh * G + g) * DH + half * 64;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
-  for (int kb = 0; kb < n_kb; ++kb) {
-    const int buf = kb & 1;
-    if (kb + 1 < n_kb) load_kv(kb + 1, buf ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-    const bf16* kt = Ks + buf * AT_KB * AT_DH;
-    const bf16* vt = Vs + buf * AT_KB * AT_DH;
-    float s[8][4];
+      for (int c = 0; c < 64; c += 16) {
+        uint32_t ov[16];
+        tmem_ld16_nowait(tmem + O_COL + col0 + lane_off + c, ov);
+        tmem_wait_ld();
+        if (valid) {
+          float f[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-      for (int nb2 = 0; nb2 < 4; ++nb2) {
-        const int key = nb2 * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int ch = ks * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(kt + swz(key, ch)), b0, b1, b2, b3);
-        mma_bf16_16816(s[2 * nb2], qf[ks], b0, b1);
-        mma_bf16_16816(s[2 * nb2 + 1], qf[ks], b2, b3);
+          for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(ov[e]) * inv;
+          store8(dst + c, f);
+          store8(dst + c + 8, f + 8);
+        }
       }
     }
-    // mask, scale, online softmax
-    float mx_lo = -INFINITY, mx_hi = -INFINITY;
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = kb * AT_KB + nb * 8 + 2 * (lane & 3) + (e & 1);
-        const int pos = e < 2 ? pos_lo : pos_hi;
-        float v = s[nb][e] * a.scale_log2;
-        if (key > pos) v = -INFINITY;
-        s[nb][e] = v;
-        if (e < 2)
-          mx_lo = fmaxf(mx_lo, v);
-        else
-          mx_hi = fmaxf(mx_hi, v);
-      }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      set_status(a.status, ST_WAIT_TIMEOUT);
     }
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-    const float al_lo = exp2f(m_lo - mn_lo), al_hi = exp2f(m_hi - mn_hi);
-    m_lo = mn_lo;
-    m_hi = mn_hi;
-    float ps_lo = 0.f, ps_hi = 0.f;
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb) {
-      s[nb][0] = exp2f(s[nb][0] - mn_lo);
-      s[nb][1] = exp2f(s[nb][1] - mn_lo);
-      s[nb][2] = exp2f(s[nb][2] - mn_hi);
-      s[nb][3] = exp2f(s[nb][3] - mn_hi);
-      ps_lo += s[nb][0] + s[nb][1];
-      ps_hi += s[nb][2] + s[nb][3];
-    }
-    l_lo = l_lo * al_lo + ps_lo;
-    l_hi = l_hi * al_hi + ps_hi;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= al_lo;
-      o[i][1] *= al_lo;
-      o[i][2] *= al_hi;
-      o[i][3] *= al_hi;
-    }
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-      for (int dn2 = 0; dn2 < 8; ++dn2) {
-        const int key = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int ch = dn2 * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(vt + swz(key, ch)), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * dn2], pa, b0, b1);
-        mma_bf16_16816(o[2 * dn2 + 1], pa, b2, b3);
-      }
-    }
-    __syncthreads();  // this buffer is refilled by the next iteration's prefetch
   }
-  cp_async_wait<0>();
-
-  // finalize: full row sums across the quad, normalise, store bf16
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
-  const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int r = half ? r_hi : r_lo;
-    const int qi = r / G, g = r - qi * G;
-    if (qi >= t.count || r >= QT * G) continue;
-    const float inv = half ? inv_hi : inv_lo;
-    bf16* dst = a.out + (static_cast<size_t>(t.row0 + qi) * H + kvh * G + g) * AT_DH;
-#pragma unroll
-    for (int nb = 0; nb < 16; ++nb) {
-      const int col = nb * 8 + 2 * (lane & 3);
-      *reinterpret_cast<__nv_bfloat162*>(dst + col) =
-          __floats2bfloat162_rn(o[nb][2 * half] * inv, o[nb][2 * half + 1] * inv);
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
+
+}  // namespace ta
 
 // ----------------------------------------------------------------------------- fp32
 struct AttnArgsF32 {
@@ -328,42 +491,91 @@ __global__ void __launch_bounds__(256) attn_f32_kernel(AttnArgsF32 a) {
 int attention_tile_rows(int n_heads, int n_kv_heads, cb_dtype dt) {
   if (dt == CB_F32) return 1;
   const int G = n_heads / n_kv_heads;
-  return G >= AT_ROWS ? 1 : AT_ROWS / G;
+  return G >= ta::ROWS ? 1 : ta::ROWS / G;
 }
 
-static cudaError_t attn_bf16_launch(const AttnArgs& args, int n_tiles, cudaStream_t s) {
+typedef CUresult (*EncodeTiledFn4)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// 4-D map over a KV cache [L][N][Hkv][128] (bf16): box {64, 1, 128 keys, 1}, 128-byte swizzle.
+bool encode_kv_map(CUtensorMap* map, const void* base, int n_layers, int n_tokens, int n_kv_heads,
+                   long long layer_stride_elems) {
+  static EncodeTiledFn4 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<EncodeTiledFn4>(p);
+  }
+  const uint64_t row = static_cast<uint64_t>(n_kv_heads) * ta::DH * 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(ta::DH), static_cast<cuuint64_t>(n_kv_heads),
+                        static_cast<cuuint64_t>(n_tokens), static_cast<cuuint64_t>(layer_stride_elems ? n_layers : 1)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(ta::DH * 2), row,
+                           layer_stride_elems ? static_cast<cuuint64_t>(layer_stride_elems) * 2 : row * n_tokens};
+  cuuint32_t box[4] = {64, 1, ta::BKV, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static cudaError_t tc_launch(ta::Args& args, int n_tiles, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(ta::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ta::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  if (n_tiles <= 0) return cudaSuccess;
+  args.n_tiles = n_tiles;
   dim3 grid(n_tiles, args.Hkv);
-  attn_bf16_kernel<<<grid, AT_THREADS, AT_SMEM, s>>>(args);
+  ta::attn_tc_kernel<<<grid, ta::THREADS, ta::SMEM, s>>>(args);
   return cudaGetLastError();
 }
 
-// Batched: tiles (bf16) or all rows (fp32, n_tiles = number of S rows) of one layer.
+// Batched (bf16): one launch per group of at most MAXREQ requests; tiles of request r are
+// tiles[tile_off[r] .. tile_off[r+1]).
+cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const AttnTile* tiles, const int* tile_off,
+                                  const CUtensorMap* kmaps, const CUtensorMap* vmaps, const int* n_kv,
+                                  const int* one_layer, int n_req, int layer, int n_heads, int n_kv_heads, void* out,
+                                  int32_t* status, cudaStream_t s) {
+  ta::Args a;
+  a.q = static_cast<const bf16*>(q);
+  a.s_pos = s_pos;
+  a.H = n_heads;
+  a.Hkv = n_kv_heads;
+  a.G = n_heads / n_kv_heads;
+  a.QT = attention_tile_rows(n_heads, n_kv_heads, CB_BF16);
+  a.out = static_cast<bf16*>(out);
+  a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(ta::DH));
+  a.status = status;
+  a.direct_m = 0;
+  for (int r0 = 0; r0 < n_req; r0 += ta::MAXREQ) {
+    const int r1 = std::min(n_req, r0 + ta::MAXREQ);
+    for (int r = r0; r < r1; ++r) {
+      a.kmap[r - r0] = kmaps[r];
+      a.vmap[r - r0] = vmaps[r];
+      a.n_kv[r - r0] = n_kv[r];
+      a.layer_coord[r - r0] = one_layer[r] ? 0 : layer;
+    }
+    a.req_base = r0;
+    a.tiles = tiles + tile_off[r0];
+    cudaError_t e = tc_launch(a, tile_off[r1] - tile_off[r0], s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// fp32 (all rows of S).
 cudaError_t launch_attention(const void* q, const int32_t* s_pos, const int32_t* s_req, const ReqDev* reqs,
                              const AttnTile* tiles, int n_tiles, int layer, int n_heads, int n_kv_heads, int head_dim,
                              void* out, cb_dtype dt, cudaStream_t s) {
+  (void)tiles;
   if (n_tiles <= 0) return cudaSuccess;
-  if (dt == CB_BF16) {
-    AttnArgs a{};
-    a.q = static_cast<const bf16*>(q);
-    a.s_pos = s_pos;
-    a.s_req = s_req;
-    a.reqs = reqs;
-    a.tiles = tiles;
-    a.layer = layer;
-    a.H = n_heads;
-    a.Hkv = n_kv_heads;
-    a.G = n_heads / n_kv_heads;
-    a.QT = attention_tile_rows(n_heads, n_kv_heads, dt);
-    a.out = static_cast<bf16*>(out);
-    a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(head_dim));
-    return attn_bf16_launch(a, n_tiles, s);
-  }
+  if (dt != CB_F32) return cudaErrorInvalidValue;
   AttnArgsF32 a{};
   a.q = static_cast<const float*>(q);
   a.s_pos = s_pos;
@@ -387,20 +599,24 @@ cudaError_t launch_attention_direct(const void* q, const int32_t* q_pos, int m, 
                                    cudaStream_t s) {
   if (m <= 0) return cudaSuccess;
   if (dt == CB_BF16) {
-    AttnArgs a{};
+    ta::Args a;
+    if (!encode_kv_map(&a.kmap[0], k, 1, n_kv, n_kv_heads, 0) || !encode_kv_map(&a.vmap[0], v, 1, n_kv, n_kv_heads, 0))
+      return cudaErrorInvalidValue;
+    a.n_kv[0] = n_kv;
+    a.layer_coord[0] = 0;
     a.q = static_cast<const bf16*>(q);
     a.s_pos = q_pos;
-    a.k_direct = static_cast<const bf16*>(k);
-    a.v_direct = static_cast<const bf16*>(v);
-    a.n_kv_direct = n_kv;
-    a.m_direct = m;
+    a.tiles = nullptr;
+    a.req_base = 0;
+    a.direct_m = m;
     a.H = n_heads;
     a.Hkv = n_kv_heads;
     a.G = n_heads / n_kv_heads;
-    a.QT = attention_tile_rows(n_heads, n_kv_heads, dt);
+    a.QT = attention_tile_rows(n_heads, n_kv_heads, CB_BF16);
     a.out = static_cast<bf16*>(out);
     a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(head_dim));
-    return attn_bf16_launch(a, (m + a.QT - 1) / a.QT, s);
+    a.status = nullptr;
+    return tc_launch(a, (m + a.QT - 1) / a.QT, s);
   }
   AttnArgsF32 a{};
   a.q = static_cast<const float*>(q);

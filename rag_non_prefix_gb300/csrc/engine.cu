@@ -152,6 +152,10 @@ struct Batch {
   int next_layer = 0;
   bool has_forced = false;
   int dev_mode = 0;
+  // tcgen05 attention: per request K/V tensor maps, sizes, and per layer the tile range of each request
+  std::vector<CUtensorMap> kmaps, vmaps;
+  std::vector<int> n_kv, one_layer;
+  std::vector<int> req_tile_off;  // [L][n_req + 1]
 };
 
 }  // namespace
@@ -508,20 +512,37 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
     b.rows_S[i] = soff;
   }
 
-  // ---- attention tiles per layer
+  // ---- attention tiles per layer (request by request), and the K/V tensor maps
   std::vector<AttnTile> tiles;
   b.tile_off.assign(L, 0);
   b.tile_n.assign(L, 0);
+  b.req_tile_off.assign(static_cast<size_t>(L) * (n_req + 1), 0);
   const int QT = attention_tile_rows(c.n_heads, c.n_kv_heads, c.dtype);
   for (int i = 0; i < L; ++i) {
     b.tile_off[i] = static_cast<int>(tiles.size());
     if (c.dtype == CB_BF16) {
       for (int r = 0; r < n_req; ++r) {
+        b.req_tile_off[static_cast<size_t>(i) * (n_req + 1) + r] = static_cast<int>(tiles.size()) - b.tile_off[i];
         const PlanEntry& pe = b.plan[static_cast<size_t>(i) * n_req + r];
         for (int q0 = 0; q0 < pe.s_n; q0 += QT) tiles.push_back(AttnTile{r, pe.s_off + q0, std::min(QT, pe.s_n - q0), 0});
       }
+      b.req_tile_off[static_cast<size_t>(i) * (n_req + 1) + n_req] = static_cast<int>(tiles.size()) - b.tile_off[i];
     }
     b.tile_n[i] = static_cast<int>(tiles.size()) - b.tile_off[i];
+  }
+  if (c.dtype == CB_BF16) {
+    b.kmaps.resize(n_req);
+    b.vmaps.resize(n_req);
+    b.n_kv.resize(n_req);
+    b.one_layer.resize(n_req);
+    for (int r = 0; r < n_req; ++r) {
+      const ReqHost& rh = b.reqs[r];
+      if (!encode_kv_map(&b.kmaps[r], rh.fused_k, L, rh.N, c.n_kv_heads, rh.layer_stride) ||
+          !encode_kv_map(&b.vmaps[r], rh.fused_v, L, rh.N, c.n_kv_heads, rh.layer_stride))
+        return fail(ctx, CB_ERR_INVALID_ARG, "cannot describe the fused cache to the tensor memory accelerator");
+      b.n_kv[r] = rh.N;
+      b.one_layer[r] = rh.layer_stride == 0 ? 1 : 0;
+    }
   }
 
   // ---- re-rotation segments: resident chunks (all layers, once) then host chunks per layer
@@ -734,9 +755,14 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   // 4. causal attention of S over the fused cache
   {
     PhaseScope ps(ctx, CB_PH_ATTENTION, s, 1);
-    const int n_items = c.dtype == CB_BF16 ? b.tile_n[i] : Sn;
-    CB_CUDA(ctx, launch_attention(ctx->q, posS, reqS, ctx->d_reqs, ctx->d_tiles + b.tile_off[i], n_items, i, H, Hkv,
-                                  dh, ctx->attn, c.dtype, s));
+    if (c.dtype == CB_BF16)
+      CB_CUDA(ctx, launch_attention_bf16(ctx->q, posS, ctx->d_tiles + b.tile_off[i],
+                                         b.req_tile_off.data() + static_cast<size_t>(i) * (b.n_req + 1),
+                                         b.kmaps.data(), b.vmaps.data(), b.n_kv.data(), b.one_layer.data(), b.n_req,
+                                         i, H, Hkv, ctx->attn, ctx->status, s));
+    else
+      CB_CUDA(ctx, launch_attention(ctx->q, posS, reqS, ctx->d_reqs, nullptr, Sn, i, H, Hkv, dh, ctx->attn, c.dtype,
+                                    s));
   }
   // 5. h_S += attn W_o^T;  h_S += W_down(SiLU(x W_gate^T) * x W_up^T), x = RMSNorm(h_S)
   {

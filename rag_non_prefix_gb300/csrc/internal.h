@@ -80,6 +80,14 @@ cudaError_t launch_attention(const void* q, const int32_t* s_pos, const int32_t*
                              const AttnTile* tiles, int n_tiles, int layer, int n_heads, int n_kv_heads, int head_dim,
                              void* out, cb_dtype dt, cudaStream_t s);
 int attention_tile_rows(int n_heads, int n_kv_heads, cb_dtype dt);
+// tcgen05 attention (bf16, head_dim 128): tiles of request r are tiles[tile_off[r] .. tile_off[r+1])
+cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const AttnTile* tiles, const int* tile_off,
+                                  const CUtensorMap* kmaps, const CUtensorMap* vmaps, const int* n_kv,
+                                  const int* one_layer, int n_req, int layer, int n_heads, int n_kv_heads, void* out,
+                                  int32_t* status, cudaStream_t s);
+// 4-D tensor map over a bf16 KV cache [L][N][Hkv][128] (layer_stride_elems 0: one layer)
+bool encode_kv_map(CUtensorMap* map, const void* base, int n_layers, int n_tokens, int n_kv_heads,
+                   long long layer_stride_elems);
 cudaError_t launch_last_rows_norm(const float* h, const int32_t* rows, int n, int d, float eps, float* x_out,
                                   cudaStream_t s);
 cudaError_t launch_lm_head(const float* x, int n_req, int d, const void* w, int vocab, cb_dtype dt, float* logits,
