@@ -29,6 +29,22 @@ sys.path.insert(0, ROOT)
 METRIC = "blended-prefill TTFT ms & context tok/s at r=15% vs full prefill; % roofline"
 
 
+def _gemm_traffic():
+    """Per-launch DRAM bytes of the GEMM from the committed ncu capture, if the kernel is unchanged."""
+    import hashlib
+
+    p = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for src in d["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return d["bytes_per_launch"] if h.hexdigest() == d["source_sha256"] else None
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -103,6 +119,21 @@ def gemm_flops(cfg, rows_R, rows_S):
         out["gateup"] += 2.0 * S * d * 2 * f
         out["down"] += 2.0 * S * f * d
     return out
+
+
+def gemm_algorithmic_bytes(cfg, rows_R, rows_S):
+    """Bytes the projection GEMMs must move per blend: weights once per layer, A read, C written
+    (fp32 q|k|v; residual read + written; bf16 SwiGLU output)."""
+    d, qw, kvw, f = cfg.d_model, cfg.q_width, cfg.kv_width, cfg.ffn_dim
+    es = 2 if cfg.dtype == "bf16" else 4
+    total = 0
+    for R, S in zip(rows_R, rows_S):
+        total += es * ((qw + 2 * kvw) * d + qw * d + 2 * f * d + f * d)  # weights
+        total += R * d * es + R * (qw + 2 * kvw) * 4                       # q|k|v
+        total += S * qw * es + 2 * S * d * 4                               # output projection + residual
+        total += S * d * es + S * f * es                                   # gate/up + SwiGLU
+        total += S * f * es + 2 * S * d * 4                                # down + residual
+    return total
 
 
 def plan_rows(cfg, n_tokens, n_cached, n_query, ratios):
@@ -296,6 +327,7 @@ def run_ours(args, rank, world):
     rows_R = [sum(x[0][i] for x in rows) for i in range(cfg.n_layers)]
     rows_S = [sum(x[1][i] for x in rows) for i in range(cfg.n_layers)]
     fl = gemm_flops(cfg, rows_R, rows_S)
+    gemm_bytes = gemm_algorithmic_bytes(cfg, rows_R, rows_S)
     gemm_ms = sum(phases[p]["ms"] for p in ("qkv", "oproj", "gateup", "down"))
     gemm_launches = sum(phases[p]["calls"] for p in ("qkv", "oproj", "gateup", "down"))
     peaks = _peaks()
@@ -336,7 +368,8 @@ def run_ours(args, rank, world):
         "phase_ms": phase_ms,
         "roofline": {"kernel": "gemm_bf16_tc (tcgen05 projections: qkv, o, gate/up, down)", "bound": "tensor",
                      "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4) if achieved else None, "traffic": None,
+                     "frac": round(achieved / peak, 4) if achieved else None, "traffic": _gemm_traffic(),
+                     "algorithmic_bytes_per_launch": round(gemm_bytes / max(1, gemm_launches)),
                      "peak_source": f"{peaks['source']} bf16 sustained", "launches": gemm_launches,
                      "flops": sum(fl.values())},
         "rerotate": {"bytes": rerot_bytes, "ms": phase_ms.get("begin"),
