@@ -165,6 +165,15 @@ cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, 
                   cb_dtype dtype, void* scratch, size_t scratch_bytes, void* stream);
 size_t cb_gemm_scratch_size(void);
 
+/* Tile orientation of the bf16 GEMMs, process-wide (a tuning and test hook; default 0).
+ * 0: chosen per shape by the library's time model; 1: tokens (rows of A) as the 128
+ * rows of each tensor-core tile; 2: output features (rows of B) as the tile rows and
+ * tokens as its columns, in tiles of a multiple of 16 tokens (used where the q|k|v
+ * split points are multiples of 128; otherwise 1); 16..256, a multiple of 16: as 2 with
+ * that many tokens per tile.  Results agree to fp32 rounding of the same sums.  Other
+ * values: CB_ERR_INVALID_ARG. */
+cb_status cb_gemm_set_orientation(int orientation);
+
 /* Allocation-free variant of cb_gemm (no counterpart on the pages: an addition for
  * callers that cannot allocate device memory, e.g. a process held to a fixed device
  * budget after start-up, or code inside a framework that owns every allocation).

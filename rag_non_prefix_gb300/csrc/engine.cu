@@ -1055,6 +1055,14 @@ cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, 
 
 size_t cb_gemm_scratch_size(void) { return gemm_scratch_bytes(); }
 
+cb_status cb_gemm_set_orientation(int orientation) {
+  const bool tile = orientation >= 16 && orientation <= 256 && orientation % 16 == 0;
+  if ((orientation < 0 || orientation > 2) && !tile)
+    return fail(nullptr, CB_ERR_INVALID_ARG, "orientation must be 0, 1, 2 or a token tile 16..256 (multiple of 16)");
+  gemm_set_orientation(orientation);
+  return CB_OK;
+}
+
 cb_status cb_attention(const void* q, const int32_t* q_pos, int m, const void* k, const void* v, int n_kv, int n_heads,
                        int n_kv_heads, int head_dim, void* out, cb_dtype dtype, void* stream) {
   if (!q || !q_pos || !k || !v || !out) return fail(nullptr, CB_ERR_INVALID_ARG, "null pointer");

@@ -1,10 +1,13 @@
 // Dense projections C = A . B^T of the blended prefill.
 //
 // bf16: a tcgen05 kernel.  One 128 x BN output tile per CTA; operands staged by TMA
-// (128-byte swizzle, K-major) through a STAGES-deep shared-memory ring guarded by
+// (128-byte swizzle, K-major) through a shared-memory ring guarded by
 // mbarriers; one elected thread issues tcgen05.mma (kind::f16, M=128, N=BN, K=16) into a
-// fp32 accumulator in tensor memory; four epilogue warps read it back with tcgen05.ld and
-// apply the fused epilogue (store fp32, residual add, or SiLU(gate) * up -> bf16).
+// fp32 accumulator in tensor memory; four epilogue warps read it back with tcgen05.ld,
+// apply the fused epilogue (store fp32, residual add, or SiLU(gate) * up -> bf16).  The
+// fp32 epilogues stage each 32-column slab of the tile in shared memory, from where one
+// thread writes it with a TMA tile store (residual add: a TMA fp32 add-reduction), so
+// that global writes are whole lines instead of one 32-byte piece per row.
 //   warp 0: TMA producer   warp 1: TMEM owner + MMA issuer   warps 2-5: epilogue
 // The B operand may come from up to three tensors split along N (q | k | v weights), or
 // from two tensors interleaved per tile (gate rows then up rows) for the SwiGLU epilogue.
@@ -14,6 +17,7 @@
 // fp32: a plain shared-memory-tiled FFMA kernel with the same epilogues (used by the
 // fp32 configuration, whose 1e-4 tolerance rules out TF32).
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -40,6 +44,21 @@ static EncodeTiledFn get_encoder() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   });
   return fn;
+}
+
+// Row-major [rows][inner] tensor with a row pitch of `pitch` bytes (default: 128-byte swizzle).
+static bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                           uint64_t pitch, uint32_t box_inner, uint32_t box_rows,
+                           CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  EncodeTiledFn fn = get_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
@@ -83,6 +102,9 @@ struct Params {
   long long sk_iters;
   float* partials;     // [gridDim.x][BM][BN] fp32, stream-K partial tiles
   int* flags;          // [gridDim.x], zero between launches
+  int bt;              // weight-rows orientation: tokens per tile (multiple of 16, <= 256)
+  int stages;          // ring depth
+  int stage_bytes;     // A_STAGE + slot B bytes (a multiple of 2 KiB)
 };
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -102,15 +124,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int bn) {
          (static_cast<uint32_t>(BM >> 4) << 24);
 }
 
-template <int BN, int STAGES>
-struct Layout {
-  static constexpr int B_STAGE = BN * BK * 2;
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = STAGES * A_STAGE;
-  static constexpr int OFF_BAR = OFF_B + STAGES * B_STAGE;
-  static constexpr int BYTES = OFF_BAR + 256;
-  static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024 B
-};
+// Shared memory: barriers, the epilogue's staging buffer, then the operand ring.  A ring
+// stage is slot A (128 rows x 64 bf16 = 16 KiB) followed by slot B (rows x 64 bf16); its
+// depth is what fits (at most MAX_STAGES): the deeper the ring, the more weight bytes are
+// in flight per SM, which is what bounds a launch whose tiles stream weights from DRAM.
+constexpr int MAX_STAGES = 12;
+constexpr int OFF_BAR = 0;
+constexpr int OFF_STG = 1024;          // epilogue staging: 16 KiB
+constexpr int STG_BYTES = 16384;
+constexpr int OFF_RING = OFF_STG + STG_BYTES;
+constexpr int SMEM_ALLOC = 232448;     // the per-block maximum (227 KiB)
+constexpr int RING_BYTES = SMEM_ALLOC - 1024 - OFF_RING;  // 1 KiB of slack aligns the base
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
@@ -160,16 +184,39 @@ __device__ __forceinline__ bool get_item(const Params& p, int g, int G, int idx,
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <int BN, int STAGES>
+// Adds the stream-K partial tiles of CTAs first..last (row r_loc, columns col..col+W-1).
+template <int W, int BN>
+__device__ __forceinline__ void add_partial_slots(const Params& p, float* v, int first, int last, int r_loc, int col) {
+  for (int q = first; q <= last; ++q) {
+    const float* src = p.partials + (static_cast<size_t>(q) * BM + r_loc) * BN + col;
+#pragma unroll
+    for (int j = 0; j < W; j += 4) {
+      const float4 t = __ldcg(reinterpret_cast<const float4*>(src + j));
+      v[j] += t.x;
+      v[j + 1] += t.y;
+      v[j + 2] += t.z;
+      v[j + 3] += t.w;
+    }
+  }
+}
+
+// Two tile orientations.  TOKEN_ROWS (WROWS = false): the MMA's 128 rows are tokens
+// (rows of A) and its N = BN columns are output features.  WEIGHT_ROWS (WROWS = true): the
+// MMA's 128 rows are output features (rows of B; for SwiGLU 64 gate rows then the 64 up
+// rows of the same features) and its N = p.bt columns are tokens, so that a token count
+// that is not a multiple of 128 is covered in steps of 16 and a few hundred tokens still
+// yield one tile per SM.  In both, shared-memory slot A holds the MMA's rows (128 x 64 bf16)
+// and slot B its columns (<= 256 x 64 bf16).
+template <int BN, bool WROWS>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, Params p) {
-  using L = Layout<BN, STAGES>;
+                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+                 const __grid_constant__ CUtensorMap tmC, Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* empty = full + STAGES;
-  uint64_t* acc_full = empty + STAGES;  // [2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* acc_full = empty + MAX_STAGES;  // [2]
   uint64_t* acc_empty = acc_full + 2;   // [2]
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -178,8 +225,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x, G = gridDim.x;
 
+  const uint32_t stages = static_cast<uint32_t>(p.stages);
+  uint8_t* ring = smem + OFF_RING;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -195,6 +244,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB0);
     if (p.mode == EPI_SWIGLU || p.split0 < p.N) prefetch_tmap(&tmB1);
+    if (p.mode != EPI_SWIGLU) prefetch_tmap(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 2 * BN);
@@ -207,15 +257,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    int issued_phase[STAGES];
-#pragma unroll
-    for (int s = 0; s < STAGES; ++s) issued_phase[s] = -1;
-    uint32_t c = 0;  // k-blocks issued so far (ring position)
+    uint32_t c = 0;            // k-blocks issued so far
+    uint32_t s = 0, ph = 0;    // ring position of k-block c (no division in the loop)
     Item it;
     bool ok = true;
+    // rows of the tile in the token dimension (TOKEN_ROWS: 128; WEIGHT_ROWS: p.bt)
+    const int tok_rows = WROWS ? p.bt : BM;
+    const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
     for (int idx = 0; ok && get_item(p, g, G, idx, it); ++idx) {
-      const int m0 = (it.tile % p.m_tiles) * BM;
-      const int n0 = (it.tile / p.m_tiles) * BN;
+      const int t0 = (it.tile % p.m_tiles) * tok_rows;  // first token of the tile
+      const int wt = it.tile / p.m_tiles;               // weight tile
+      // weight rows: WEIGHT_ROWS takes 128 output features (SwiGLU: 64 gate + 64 up),
+      // TOKEN_ROWS BN of them (SwiGLU: BN/2 + BN/2)
+      const int w_rows = WROWS ? BM : BN;
+      const int n0 = wt * w_rows;  // first output column (of the gate|up concatenation for SwiGLU)
       const CUtensorMap* mb = &tmB0;
       int brow = n0;
       if (p.mode != EPI_SWIGLU) {
@@ -227,42 +282,49 @@ __global__ void __launch_bounds__(THREADS, 1)
           brow = n0 - p.split0;
         }
       }
-      for (int kb = it.kb0; kb < it.kb1; ++kb, ++c) {
-        const int s = static_cast<int>(c % STAGES);
-        const uint32_t ph = (c / STAGES) & 1u;
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
-          uint8_t* sa = smem + L::OFF_A + s * A_STAGE;
-          uint8_t* sb = smem + L::OFF_B + s * L::B_STAGE;
-          mbar_arrive_expect_tx(&full[s], A_STAGE + L::B_STAGE);
-          tma_load_2d(sa, &tmA, &full[s], kb * BK, m0);
+          uint8_t* sa = ring + s * stage_bytes;
+          uint8_t* sb = sa + A_STAGE;
+          uint8_t* sw_dst = WROWS ? sa : sb;  // weights
+          uint8_t* sx_dst = WROWS ? sb : sa;  // tokens
+          const int w_half = WROWS ? A_STAGE / 2 : BN * BK;  // SwiGLU: where the up rows start
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          tma_load_2d(sx_dst, &tmA, &full[s], kb * BK, t0);
           if (p.mode == EPI_SWIGLU) {
-            tma_load_2d(sb, &tmB0, &full[s], kb * BK, n0 / 2);
-            tma_load_2d(sb + L::B_STAGE / 2, &tmB1, &full[s], kb * BK, n0 / 2);
+            tma_load_2d(sw_dst, &tmB0, &full[s], kb * BK, n0 / 2);
+            tma_load_2d(sw_dst + w_half, &tmB1, &full[s], kb * BK, n0 / 2);
           } else {
-            tma_load_2d(sb, mb, &full[s], kb * BK, brow);
+            tma_load_2d(sw_dst, mb, &full[s], kb * BK, brow);
           }
         }
-        issued_phase[s] = static_cast<int>(ph);
         __syncwarp();
+        ++c;
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
     if (!ok && lane == 0) {
       *abort_flag = 1;
       set_status(p.status, ST_WAIT_TIMEOUT);
     }
-    // Let every copy this warp issued land before the block can exit.
+    // Let every copy this warp issued land before the block can exit: only the last
+    // `stages` k-blocks can still be in flight (an earlier one's stage was reused).
     if (lane == 0) {
-      for (int s = 0; s < STAGES; ++s)
-        if (issued_phase[s] >= 0) mbar_wait_bounded(&full[s], static_cast<uint32_t>(issued_phase[s]), nullptr);
+      for (uint32_t j = c > stages ? c - stages : 0; j < c; ++j)
+        mbar_wait_bounded(&full[j % stages], (j / stages) & 1u, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(BN);
-    uint32_t c = 0;
+    const uint32_t idesc = idesc_bf16(WROWS ? p.bt : BN);
+    const uint32_t ring_u32 = smem_u32(ring);
+    uint32_t s = 0, ph = 0, sa = ring_u32;  // ring position and its slot-A address
     Item it;
     bool ok = true;
     for (int idx = 0; ok && get_item(p, g, G, idx, it); ++idx) {
@@ -273,22 +335,26 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem + static_cast<uint32_t>(b * BN);
-      for (int kb = it.kb0; kb < it.kb1; ++kb, ++c) {
-        const int s = static_cast<int>(c % STAGES);
-        const uint32_t ph = (c / STAGES) & 1u;
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (lane == 0) ok = mbar_wait_bounded(&full[s], ph, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint64_t da = sw128_desc(smem_u32(smem + L::OFF_A + s * A_STAGE));
-          const uint64_t db = sw128_desc(smem_u32(smem + L::OFF_B + s * L::B_STAGE));
+          const uint64_t da = sw128_desc(sa);
+          const uint64_t db = sw128_desc(sa + A_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes along K per step (encoded >> 4)
             tc_mma_f16(tacc, da + 2 * kk, db + 2 * kk, idesc, (kb > it.kb0 || kk > 0) ? 1u : 0u);
           tc_commit(&empty[s]);  // frees the stage once these MMAs have read it
         }
         __syncwarp();
+        sa += static_cast<uint32_t>(p.stage_bytes);
+        if (++s == stages) {
+          s = 0;
+          ph ^= 1u;
+          sa = ring_u32;
+        }
       }
       if (!ok) break;
       if (lane == 0) tc_commit(&acc_full[b]);  // accumulator b complete
@@ -310,6 +376,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r_loc = quarter * 32 + lane;
     const int et = threadIdx.x - 64;  // 0..127 within the epilogue warps
     volatile int* go = abort_flag + 1;   // [2]: per-item decision, written by et == 0
+    int slab = 0;                        // staging slabs issued (double buffer parity)
     Item it;
     for (int idx = 0; get_item(p, g, G, idx, it); ++idx) {
       const int b = idx & 1;
@@ -336,8 +403,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (it.kind == ITEM_PARTIAL) {
         // write the partial accumulator of this tile to this CTA's slot, then publish it
         float* slot = p.partials + (static_cast<size_t>(g) * BM + r_loc) * BN;
+        const int ncols = WROWS ? ((p.bt + 31) & ~31) : BN;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < ncols; c += 32) {
           float v[32];
           tmem_ld32(tbase + c, v);
 #pragma unroll
@@ -364,20 +432,92 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           epi_bar();
         }
-        auto add_partials = [&](float* v, int col) {
-          for (int q = first; q <= last; ++q) {
-            const float* src = p.partials + (static_cast<size_t>(q) * BM + r_loc) * BN + col;
+        auto add_partials = [&](float* v, int col) { add_partial_slots<32, BN>(p, v, first, last, r_loc, col); };
+        if (WROWS) {
+          // lanes = output features, columns = the tile's tokens t0 .. t0 + nt - 1
+          const int t0 = (it.tile % p.m_tiles) * p.bt;
+          const int nt = min(p.bt, p.M - t0);
+          const int wt = it.tile / p.m_tiles;
+          if (p.mode == EPI_SWIGLU) {
+            // lanes 0-63 hold the gate and lanes 64-127 the up projection of features
+            // f0 .. f0 + 63: the up warps pass their values through shared memory
+            float* xch = reinterpret_cast<float*>(smem + OFF_STG);  // [64][17]
+            const int f0 = wt * (BM / 2);
+            bf16* out = static_cast<bf16*>(p.out);
+#pragma unroll 1
+            for (int c = 0; c < nt; c += 16) {
+              float v[16];
+              tmem_ld16(tbase + c, v);
+              add_partial_slots<16, BN>(p, v, first, last, r_loc, c);
+              if (quarter >= 2) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 t = __ldcg(reinterpret_cast<const float4*>(src + j));
-              v[j] += t.x;
-              v[j + 1] += t.y;
-              v[j + 2] += t.z;
-              v[j + 3] += t.w;
+                for (int j = 0; j < 16; ++j) xch[(r_loc - 64) * 17 + j] = v[j];
+              }
+              epi_bar();
+              if (quarter < 2) {
+                bf16* dst = out + static_cast<size_t>(t0 + c) * p.ldc + f0 + r_loc;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (c + j < nt)
+                    dst[static_cast<size_t>(j) * p.ldc] = __float2bfloat16_rn(silu_f(v[j]) * xch[r_loc * 17 + j]);
+              }
+              epi_bar();
+            }
+          } else {
+            // 16-token x 128-feature fp32 slabs, double-buffered, one TMA store (or
+            // add-reduction) each
+            const int f0 = wt * BM;
+            float* stg = reinterpret_cast<float*>(smem + OFF_STG);
+#pragma unroll 1
+            for (int c = 0; c < nt; c += 16, ++slab) {
+              float v[16];
+              tmem_ld16(tbase + c, v);
+              add_partial_slots<16, BN>(p, v, first, last, r_loc, c);
+              float* sbuf = stg + (slab & 1) * (16 * BM);
+              if (et == 0) bulk_wait_read_all_but_1();  // the store from this buffer two slabs ago
+              epi_bar();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) sbuf[j * BM + r_loc] = v[j];
+              fence_proxy_async_smem();
+              epi_bar();
+              if (et == 0) {
+                if (p.mode == EPI_ADD_F32)
+                  tma_reduce_add_2d(&tmC, sbuf, f0, t0 + c);
+                else
+                  tma_store_2d(&tmC, sbuf, f0, t0 + c);
+                bulk_commit();
+              }
             }
           }
-        };
-        if (p.mode == EPI_SWIGLU) {
+        } else if (p.mode != EPI_SWIGLU) {
+          // stage a 128-row x 32-column slab in shared memory (128-byte swizzle: 16-byte
+          // chunk q of row r at chunk q ^ (r & 7), conflict-free), then one thread stores
+          // it; the staging buffer is reused once the previous store has read it
+          uint8_t* stg = smem + OFF_STG;
+          uint8_t* srow = stg + r_loc * 128;
+          const int sw = r_loc & 7;
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 32) {
+            float v[32];
+            tmem_ld32(tbase + c, v);
+            add_partials(v, c);
+            if (et == 0) bulk_wait_read_all();
+            epi_bar();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<float4*>(srow + ((q ^ sw) << 4)) =
+                  make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            fence_proxy_async_smem();
+            epi_bar();
+            if (et == 0) {
+              if (p.mode == EPI_ADD_F32)
+                tma_reduce_add_2d(&tmC, stg, n0 + c, m0);
+              else
+                tma_store_2d(&tmC, stg, n0 + c, m0);
+              bulk_commit();
+            }
+          }
+        } else {  // EPI_SWIGLU, direct stores
           bf16* out = static_cast<bf16*>(p.out);
 #pragma unroll 1
           for (int c = 0; c < BN / 2; c += 32) {
@@ -397,30 +537,6 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           }
-        } else {
-          float* out = static_cast<float*>(p.out);
-#pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
-            float v[32];
-            tmem_ld32(tbase + c, v);
-            add_partials(v, c);
-            if (row < p.M) {
-              float* dst = out + static_cast<size_t>(row) * p.ldc + n0 + c;
-              if (p.mode == EPI_ADD_F32) {
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                  float o[8];
-                  load8(dst + j, o);
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) o[e] += v[j + e];
-                  store8(dst + j, o);
-                }
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) store8(dst + j, v + j);
-              }
-            }
-          }
         }
         if (it.kind == ITEM_OWNER) {
           epi_bar();  // every thread has read the partials
@@ -433,6 +549,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[b]);
     }
+    if (et == 0) bulk_wait_all();  // the tile stores have completed before the grid does
   }
   tc_fence_before();
   __syncthreads();
@@ -540,46 +657,142 @@ size_t gemm_scratch_bytes() {
   return tc::FLAG_BYTES + static_cast<size_t>(std::min(sm_count(), tc::MAX_CTAS)) * tc::BM * 256 * sizeof(float);
 }
 
-template <int BN, int STAGES>
+// 0: time model; 1: token rows; 2: weight rows with the model's token tile; 16..256
+// (multiple of 16): weight rows with that token tile.
+static std::atomic<int> g_orientation{0};
+void gemm_set_orientation(int o) { g_orientation.store(o); }
+
+// Schedule of one bf16 GEMM.
+struct GemmPlan {
+  bool wrows;     // weight-rows orientation
+  int bn;         // token-rows: output features per tile (256 or 128)
+  int bt;         // weight-rows: tokens per tile
+  int tok_tiles;  // tiles along the tokens
+  int tiles;
+  int grid;
+  int dp_tiles;
+  long long sk_iters;
+  size_t scratch_used;  // bytes of scratch the stream-K split touches (0: data-parallel)
+};
+
+// Time model used to pick the orientation, the token tile and the schedule.  A tile takes
+// K/64 k-blocks.  Measured on GB300 (one CTA per SM): the four MMAs of a k-block take
+// ~0.31 us whatever N below 256 (0.336 us at N = 256, the bf16 peak), so narrow tiles buy
+// no MMA time; the stage copies alone take ~0.24 us per k-block and are hidden behind
+// the MMAs.  A k-block therefore costs about max(0.336 * N / 256, 0.31) us (with a slight
+// slope below the floor, so that of two plans with as many waves the one spreading the
+// tokens over more SMs wins), and the choice is about padding and filling the SMs.
+// Data-parallel: tiles go round-robin over at most one CTA per SM, ceil(tiles / SMs) tile
+// times.  Stream-K (when the tiles fill at most half of the SMs): the k-blocks of all tiles
+// are divided evenly over up to 8 CTAs per tile, and every token tile of a weight tile
+// then streams that weight tile from DRAM on its own (6.5 TB/s).  Token rows pad the
+// tokens to a multiple of 128; weight rows pad them to a multiple of 16 per tile.
+static double kblock_us(int n_cols) { return std::max(0.336 * n_cols / 256.0, 0.31 + 0.02 * n_cols / 256.0); }
+
+struct Sched {
+  int grid, dp_tiles;
+  long long sk_iters;
+  size_t scratch;
+  double us;
+};
+
+// tiles = tok_tiles x w_tiles, each of kb k-blocks; weight_bytes read once per token tile
+// under stream-K.
+static Sched schedule(int tok_tiles, int w_tiles, int kb, double kb_us, double weight_bytes, int sms,
+                      long long slots) {
+  Sched r{};
+  const int tiles = tok_tiles * w_tiles;
+  r.grid = std::min(sms, tiles);
+  r.dp_tiles = tiles;
+  r.sk_iters = 0;
+  r.scratch = 0;
+  r.us = ((tiles + sms - 1) / sms) * kb * kb_us;
+  if (2 * tiles <= sms) {
+    const long long iters = static_cast<long long>(tiles) * kb;
+    // at most ~8 CTAs share one tile, one partial slot per CTA, at least 8 k-blocks each
+    const int g_sk = static_cast<int>(std::min<long long>(std::min(sms, 8 * tiles), slots));
+    if (g_sk >= 2 * tiles && iters >= 8LL * g_sk) {
+      r.grid = g_sk;
+      r.dp_tiles = 0;
+      r.sk_iters = iters;
+      r.scratch = tc::FLAG_BYTES + static_cast<size_t>(g_sk) * tc::BM * 256 * sizeof(float);
+      // (+0.5 us per extra token tile: their CTAs no longer share the weight stream)
+      r.us = std::max(((iters + g_sk - 1) / g_sk) * kb_us, weight_bytes * tok_tiles / 6.5e6) + 0.5 * (tok_tiles - 1);
+    }
+  }
+  return r;
+}
+
+static GemmPlan plan_gemm(int M, int N, int K, int split0, int split1, long long slots) {
+  const int sms = std::min(sm_count(), tc::MAX_CTAS);
+  const int kb = K / tc::BK;
+  const double wbytes = 2.0 * N * K;
+  GemmPlan g{};
+  g.bn = (N % 256 == 0 && split0 % 256 == 0 && split1 % 256 == 0) ? 256 : 128;
+  const int mt = (M + tc::BM - 1) / tc::BM;
+  const Sched st = schedule(mt, N / g.bn, kb, kblock_us(g.bn), wbytes, sms, slots);
+  const int nw = N / tc::BM;
+  const int forced = g_orientation.load();
+  const bool w_ok = split0 % tc::BM == 0 && split1 % tc::BM == 0;
+  Sched sw{};
+  int best_bt = 0;
+  if (w_ok) {
+    for (int t = (M + 255) / 256; t <= M; ++t) {
+      const int bt = ((M + t - 1) / t + 15) / 16 * 16;
+      if (bt > 256) continue;
+      if (forced >= 16 && bt != forced) {
+        if (bt <= 16) break;
+        continue;
+      }
+      const Sched c = schedule((M + bt - 1) / bt, nw, kb, kblock_us(bt), wbytes, sms,
+                               slots);
+      if (best_bt == 0 || c.us < sw.us) {
+        sw = c;
+        best_bt = bt;
+      }
+      if (bt <= 16) break;
+    }
+    if (forced >= 16 && best_bt == 0) {  // a forced tile the enumeration did not produce
+      best_bt = forced;
+      sw = schedule((M + forced - 1) / forced, nw, kb, kblock_us(forced), wbytes,
+                    sms, slots);
+    }
+  }
+  g.wrows = best_bt > 0 && (forced >= 2 || (forced == 0 && sw.us < st.us));
+  const Sched& c = g.wrows ? sw : st;
+  g.bt = g.wrows ? best_bt : 0;
+  g.tok_tiles = g.wrows ? (M + g.bt - 1) / g.bt : mt;
+  g.tiles = g.tok_tiles * (g.wrows ? nw : N / g.bn);
+  g.grid = c.grid;
+  g.dp_tiles = c.dp_tiles;
+  g.sk_iters = c.sk_iters;
+  g.scratch_used = c.scratch;
+  return g;
+}
+
+template <int BN, bool WROWS>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
-                             tc::Params p, void* scratch, size_t scratch_bytes, cudaStream_t s) {
-  using L = tc::Layout<BN, STAGES>;
+                             const CUtensorMap& c, tc::Params p, const GemmPlan& g, void* scratch, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc::gemm_bf16_tc<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(tc::gemm_bf16_tc<BN, WROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tc::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  // Persistent grid: one CTA per SM, whole tiles round-robin (data-parallel).  When the
-  // tiles fill at most half of the SMs, the k-iterations are instead divided evenly over
-  // all SMs (stream-K), which needs scratch for the partial tiles.  Measured on GB300:
-  // with five or more CTAs sharing each weight tile (M >= ~512), stream-K desynchronises
-  // them and re-reads weights from DRAM (1.66x the bytes), so it is kept to the sparse
-  // case where most SMs would otherwise idle.
-  const int sms = std::min(sm_count(), tc::MAX_CTAS);
-  p.m_tiles = (p.M + tc::BM - 1) / tc::BM;
+  p.m_tiles = g.tok_tiles;
   p.kb_per_tile = p.K / tc::BK;
-  p.tiles = p.m_tiles * (p.N / BN);
-  const size_t slot_bytes = static_cast<size_t>(tc::BM) * BN * sizeof(float);
-  const long long slots =
-      scratch && scratch_bytes > static_cast<size_t>(tc::FLAG_BYTES) ? (scratch_bytes - tc::FLAG_BYTES) / slot_bytes : 0;
-  int G = std::min(sms, p.tiles);
-  p.dp_tiles = p.tiles;
-  p.sk_iters = 0;
-  if (2 * p.tiles <= sms) {
-    const long long iters = static_cast<long long>(p.tiles) * p.kb_per_tile;
-    // at most ~8 CTAs share one tile, one partial slot per CTA, at least 8 k-blocks each
-    const int g_sk = static_cast<int>(std::min<long long>(std::min(sms, 8 * p.tiles), slots));
-    if (g_sk >= 2 * p.tiles && iters >= 8LL * g_sk) {
-      G = g_sk;
-      p.dp_tiles = 0;
-      p.sk_iters = iters;
-    }
-  }
+  p.tiles = g.tiles;
+  p.dp_tiles = g.dp_tiles;
+  p.sk_iters = g.sk_iters;
+  p.bt = g.bt;
+  p.stage_bytes = tc::A_STAGE + (WROWS ? g.bt : BN) * tc::BK * 2;
+  p.stages = std::min(tc::MAX_STAGES, tc::RING_BYTES / p.stage_bytes);
   p.flags = scratch ? static_cast<int*>(scratch) : nullptr;
   p.partials = scratch ? reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + tc::FLAG_BYTES) : nullptr;
-  tc::gemm_bf16_tc<BN, STAGES><<<G, tc::THREADS, L::ALLOC, s>>>(a, b0, b1, b2, p);
+  // request only what the ring uses (+1 KiB to align the base)
+  const int smem = tc::OFF_RING + p.stages * p.stage_bytes + 1024;
+  tc::gemm_bf16_tc<BN, WROWS><<<g.grid, tc::THREADS, smem, s>>>(a, b0, b1, b2, c, p);
   return cudaGetLastError();
 }
 
@@ -587,14 +800,7 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
 // columns with unlimited scratch (0 when the shape runs data-parallel).
 size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt) {
   if (dt != CB_BF16 || M <= 0) return 0;
-  const int BN = N % 256 == 0 ? 256 : 128;
-  const int sms = std::min(sm_count(), tc::MAX_CTAS);
-  const int tiles = ((M + tc::BM - 1) / tc::BM) * (N / BN);
-  if (2 * tiles > sms) return 0;
-  const long long iters = static_cast<long long>(tiles) * (K / tc::BK);
-  const int g_sk = std::min(sms, 8 * tiles);
-  if (g_sk < 2 * tiles || iters < 8LL * g_sk) return 0;
-  return tc::FLAG_BYTES + static_cast<size_t>(g_sk) * tc::BM * BN * sizeof(float);
+  return plan_gemm(M, N, K, N, N, 1LL << 40).scratch_used;
 }
 
 // mode: EPI_STORE_F32 / EPI_ADD_F32 (C fp32 [M][ldc]) or EPI_SWIGLU (C dtype [M][ldc], N/2 columns).
@@ -621,21 +827,47 @@ cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const voi
     return cudaGetLastError();
   }
   // bf16 on tcgen05
-  const int BN = (N % 256 == 0 && split0 % 256 == 0 && split1 % 256 == 0) ? 256 : 128;
+  const size_t slot_bytes = static_cast<size_t>(tc::BM) * 256 * sizeof(float);
+  const long long slots = scratch && scratch_bytes > static_cast<size_t>(tc::FLAG_BYTES)
+                              ? static_cast<long long>((scratch_bytes - tc::FLAG_BYTES) / slot_bytes)
+                              : 0;
+  const GemmPlan g = plan_gemm(M, N, K, split0, split1, slots);
+  const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  // token rows: A box 128 rows, weight box BN rows (SwiGLU BN/2 + BN/2);
+  // weight rows: A box bt rows, weight box 128 rows (SwiGLU 64 + 64)
+  const uint32_t a_rows = g.wrows ? static_cast<uint32_t>(g.bt) : static_cast<uint32_t>(tc::BM);
+  const uint32_t w_rows = g.wrows ? static_cast<uint32_t>(tc::BM) : static_cast<uint32_t>(g.bn);
   CUtensorMap ma, mb0, mb1, mb2;
-  if (!encode_tmap_bf16_2d(&ma, A, K, M, tc::BK, tc::BM)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&ma, BF, A, K, M, static_cast<uint64_t>(K) * 2, tc::BK, a_rows, SW)) return cudaErrorInvalidValue;
   if (mode == EPI_SWIGLU) {
-    if (!encode_tmap_bf16_2d(&mb0, B0, K, N / 2, tc::BK, BN / 2)) return cudaErrorInvalidValue;
-    if (!encode_tmap_bf16_2d(&mb1, B1, K, N / 2, tc::BK, BN / 2)) return cudaErrorInvalidValue;
+    if (!encode_tmap_2d(&mb0, BF, B0, K, N / 2, static_cast<uint64_t>(K) * 2, tc::BK, w_rows / 2, SW))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap_2d(&mb1, BF, B1, K, N / 2, static_cast<uint64_t>(K) * 2, tc::BK, w_rows / 2, SW))
+      return cudaErrorInvalidValue;
     mb2 = mb1;
   } else {
     const int r0 = split0, r1 = split1 - split0, r2 = N - split1;
-    if (!encode_tmap_bf16_2d(&mb0, B0, K, r0, tc::BK, BN)) return cudaErrorInvalidValue;
+    if (!encode_tmap_2d(&mb0, BF, B0, K, r0, static_cast<uint64_t>(K) * 2, tc::BK, w_rows, SW))
+      return cudaErrorInvalidValue;
     mb1 = mb0;
     mb2 = mb0;
-    if (r1 > 0 && !encode_tmap_bf16_2d(&mb1, B1, K, r1, tc::BK, BN)) return cudaErrorInvalidValue;
-    if (r2 > 0 && !encode_tmap_bf16_2d(&mb2, B2, K, r2, tc::BK, BN)) return cudaErrorInvalidValue;
+    if (r1 > 0 && !encode_tmap_2d(&mb1, BF, B1, K, r1, static_cast<uint64_t>(K) * 2, tc::BK, w_rows, SW))
+      return cudaErrorInvalidValue;
+    if (r2 > 0 && !encode_tmap_2d(&mb2, BF, B2, K, r2, static_cast<uint64_t>(K) * 2, tc::BK, w_rows, SW))
+      return cudaErrorInvalidValue;
   }
+  // fp32 output tensor map: token rows store 128 tokens x 32 features (128-byte swizzle),
+  // weight rows 16 tokens x 128 features.  SwiGLU keeps direct stores: in token rows its
+  // CTAs run several tiles, so the epilogue overlaps the next tile's main loop, and it
+  // measured slower with TMA stores sharing the copy unit with the loads.
+  // (fp32 C: 16-byte aligned, ldc % 4 == 0)
+  CUtensorMap mc = ma;
+  if (mode != EPI_SWIGLU &&
+      ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || ldc % 4 != 0 ||
+       !encode_tmap_2d(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, static_cast<uint64_t>(ldc) * 4,
+                       g.wrows ? tc::BM : 32, g.wrows ? 16 : tc::BM, g.wrows ? CU_TENSOR_MAP_SWIZZLE_NONE : SW)))
+    return cudaErrorInvalidValue;
   tc::Params p{};
   p.M = M;
   p.N = N;
@@ -646,8 +878,9 @@ cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const voi
   p.split0 = split0;
   p.split1 = split1;
   p.status = status;
-  if (BN == 256) return launch_tc<256, 4>(ma, mb0, mb1, mb2, p, scratch, scratch_bytes, s);
-  return launch_tc<128, 6>(ma, mb0, mb1, mb2, p, scratch, scratch_bytes, s);
+  if (g.wrows) return launch_tc<256, true>(ma, mb0, mb1, mb2, mc, p, g, scratch, s);
+  if (g.bn == 256) return launch_tc<256, false>(ma, mb0, mb1, mb2, mc, p, g, scratch, s);
+  return launch_tc<128, false>(ma, mb0, mb1, mb2, mc, p, g, scratch, s);
 }
 
 }  // namespace cb

@@ -74,6 +74,7 @@ cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const voi
                         size_t scratch_bytes, cudaStream_t s);
 // bytes of GEMM scratch (stream-K partial tiles + flags) that enable every schedule
 size_t gemm_scratch_bytes();
+void gemm_set_orientation(int o);  // 0 model, 1 token rows, 2 weight rows
 // scratch the schedule of one single-B GEMM uses when scratch is unlimited (0: none)
 size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt);
 cudaError_t launch_attention(const void* q, const int32_t* s_pos, const int32_t* s_req, const ReqDev* reqs,

@@ -22,7 +22,10 @@ import rag_non_prefix_gb300 as cb
 from rag_non_prefix_gb300 import build as cbbuild
 
 
-def _time(fn, iters, warmup=3, flush=None):
+def _time(fn, iters, warmup=3, flush=None, batch=1):
+    """Average and best time of one launch; with batch > 1, `batch` launches run back to
+    back between the events and the time is divided by `batch` (launch gaps included, host
+    launch latency hidden behind the queue)."""
     for _ in range(warmup):
         fn()
     ts = []
@@ -31,11 +34,14 @@ def _time(fn, iters, warmup=3, flush=None):
             flush.fill_(1.0)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s = torch.cuda.current_stream()
+        if batch > 1:
+            torch.cuda._sleep(2_000_000)  # keeps the GPU busy while the launches queue up
         a.record(s)
-        fn()
+        for _ in range(batch):
+            fn()
         b.record(s)
         b.synchronize()
-        ts.append(a.elapsed_time(b))
+        ts.append(a.elapsed_time(b) / batch)
     return sum(ts) / len(ts), min(ts)
 
 
@@ -57,7 +63,11 @@ def main():
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--batch", type=int, default=1, help="launches per timed region")
     ap.add_argument("--no-stream-k", action="store_true", help="GEMM without scratch: whole tiles per CTA")
+    ap.add_argument("--orientation", type=int, default=0,
+                    help="GEMM tiles: 0 by the time model, 1 token rows, 2 weight rows, 16..256 weight rows "
+                         "with that many tokens per tile")
     a = ap.parse_args()
     cbbuild.build()
     torch.manual_seed(0)
@@ -67,6 +77,7 @@ def main():
     if a.kernel == "gemm":
         M, N, K = a.M, a.N, a.K
         scr = None if a.no_stream_k else cb.gemm_scratch(dev)
+        cb.cb_gemm_set_orientation(a.orientation)
         A = (torch.randn(M, K, device=dev) * 0.5).to(torch.bfloat16)
         if a.mode == "swiglu":
             G = (torch.randn(N // 2, K, device=dev) * 0.02).to(torch.bfloat16)
@@ -77,9 +88,9 @@ def main():
             B = (torch.randn(N, K, device=dev) * 0.02).to(torch.bfloat16)
             C = torch.zeros(M, N, dtype=torch.float32, device=dev)
             fn = lambda: cb.cb_gemm(A, B, C, 1 if a.mode == "add" else 0, scratch=scr)  # noqa: E731
-        avg, best = _time(fn, a.iters, a.warmup, flush)
+        avg, best = _time(fn, a.iters, a.warmup, flush, a.batch)
         fl = 2.0 * M * N * K
-        out.update(shape=[M, N, K], mode=a.mode, stream_k=scr is not None, ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12,
+        out.update(shape=[M, N, K], mode=a.mode, stream_k=scr is not None, orientation=a.orientation, ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12,
                    weight_bytes=N * K * 2)
     elif a.kernel == "attention":
         H, Hkv, N, m = a.H, a.Hkv, a.N, a.m
@@ -89,7 +100,7 @@ def main():
         v = torch.randn(N, Hkv, 128, device=dev).to(torch.bfloat16)
         o = torch.empty_like(q)
         fn = lambda: cb.cb_attention(q, pos, k, v, o)  # noqa: E731
-        avg, best = _time(fn, a.iters, a.warmup, flush)
+        avg, best = _time(fn, a.iters, a.warmup, flush, a.batch)
         fl = 4.0 * H * 128 * float((pos.to(torch.float64) + 1).sum())
         out.update(shape=[H, Hkv, N, m], ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12)
     elif a.kernel == "rerotate":
@@ -97,7 +108,7 @@ def main():
         v = torch.randn(a.rows, a.hkv, 128, device=dev).to(torch.bfloat16)
         kd, vd = torch.empty_like(k), torch.empty_like(v)
         fn = lambda: cb.cb_rope_rerotate(k, kd, v, vd, 1234, 1e4)  # noqa: E731
-        avg, best = _time(fn, a.iters, a.warmup, flush)
+        avg, best = _time(fn, a.iters, a.warmup, flush, a.batch)
         by = 4 * k.numel() * 2  # K and V, read and written
         out.update(rows=a.rows, ms=avg, best_ms=best, gbs=by / (avg * 1e-3) / 1e9, bytes=by)
     elif a.kernel == "select":
@@ -105,7 +116,7 @@ def main():
         cand = torch.arange(a.n, dtype=torch.int32, device=dev)
         o = torch.empty(a.k, dtype=torch.int32, device=dev)
         fn = lambda: cb.cb_select_hkvd(d, cand, a.k, o)  # noqa: E731
-        avg, best = _time(fn, a.iters, a.warmup, None)
+        avg, best = _time(fn, a.iters, a.warmup, None, a.batch)
         out.update(n=a.n, k=a.k, ms=avg, best_ms=best)
     elif a.kernel == "deviation":
         kn = torch.randn(a.n, a.kvw, device=dev)
@@ -114,7 +125,7 @@ def main():
         vf = torch.randn(a.n, a.kvw, device=dev).to(torch.bfloat16)
         dv = torch.empty(a.n, device=dev)
         fn = lambda: cb.cb_kv_deviation(kn, vn, kf, vf, None, 0, dv)  # noqa: E731
-        avg, best = _time(fn, a.iters, a.warmup, flush)
+        avg, best = _time(fn, a.iters, a.warmup, flush, a.batch)
         by = a.n * a.kvw * (4 + 2) * 2
         out.update(n=a.n, ms=avg, best_ms=best, gbs=by / (avg * 1e-3) / 1e9, bytes=by)
     torch.cuda.synchronize()

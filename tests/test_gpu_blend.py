@@ -88,8 +88,18 @@ def test_gqa_f32_blend_matches_oracle(schedule, r):
 
 
 # ----------------------------------------------------------------------------- blend, bf16
-def test_bf16_blend_forced_selection_matches_oracle(small_bf16):
-    """Numerics alone: the GPU follows the oracle's sets."""
+@pytest.mark.parametrize("orientation", [0, 1, 2], ids=["model", "token-rows", "weight-rows"])
+def test_bf16_blend_forced_selection_matches_oracle(small_bf16, orientation):
+    """Numerics alone: the GPU follows the oracle's sets (under each GEMM tile orientation:
+    the q|k|v weights split along the output features, SwiGLU, residual add)."""
+    cb.cb_gemm_set_orientation(orientation)
+    try:
+        _forced_bf16(small_bf16)
+    finally:
+        cb.cb_gemm_set_orientation(0)
+
+
+def _forced_bf16(small_bf16):
     spec, g, o = small_bf16
     cfg = spec.cfg
     ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)

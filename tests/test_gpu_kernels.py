@@ -146,11 +146,19 @@ def _gemm_ref(a, b):
     return a.astype(np.float64) @ b.astype(np.float64).T
 
 
+@pytest.fixture(params=[0, 1, 2], ids=["model", "token-rows", "weight-rows"])
+def orientation(request):
+    """Runs a GEMM test under each tile orientation (process-wide setting, reset after)."""
+    cb.cb_gemm_set_orientation(request.param)
+    yield request.param
+    cb.cb_gemm_set_orientation(0)
+
+
 @pytest.mark.parametrize("sk", [False, True], ids=["whole-tiles", "stream-k"])
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (71, 256, 512), (128, 384, 256), (300, 768, 1024), (535, 1024, 4096),
                                    (1000, 512, 320), (535, 4096, 4096), (535, 4096, 14336), (3000, 6144, 512),
                                    (128, 4096, 14336), (256, 4096, 4096), (200, 2560, 8192), (64, 1024, 28672)])
-def test_gemm_bf16_store_and_add(M, N, K, sk):
+def test_gemm_bf16_store_and_add(M, N, K, sk, orientation):
     scr = cb.gemm_scratch() if sk else None
     rng = np.random.default_rng(M + N + K)
     A = _bf16(rng.standard_normal((M, K)))
@@ -170,8 +178,9 @@ def test_gemm_bf16_store_and_add(M, N, K, sk):
 
 
 @pytest.mark.parametrize("sk", [False, True], ids=["whole-tiles", "stream-k"])
-@pytest.mark.parametrize("M,F,K", [(5, 64, 128), (130, 128, 256), (535, 384, 512), (535, 14336, 4096), (96, 2048, 4096)])
-def test_gemm_bf16_swiglu(M, F, K, sk):
+@pytest.mark.parametrize("M,F,K", [(5, 64, 128), (130, 128, 256), (535, 384, 512), (535, 14336, 4096), (96, 2048, 4096),
+                                   (3200, 1024, 256), (1005, 3584, 1024)])
+def test_gemm_bf16_swiglu(M, F, K, sk, orientation):
     rng = np.random.default_rng(M + F)
     A = _bf16(rng.standard_normal((M, K)))
     G = _bf16(rng.standard_normal((F, K)) * 0.05)
@@ -183,6 +192,23 @@ def test_gemm_bf16_swiglu(M, F, K, sk):
     u = _gemm_ref(to_np(A), to_np(U))
     ref = orc.silu(g) * u
     assert np.max(np.abs(to_np(out) - ref)) <= 2 ** -7 * np.max(np.abs(ref)) + 1e-6
+
+
+@pytest.mark.parametrize("ldc_extra", [0, 8, 136], ids=["dense", "pitch+8", "pitch+136"])
+def test_gemm_bf16_strided_output(ldc_extra, orientation):
+    """Output rows with a pitch larger than N (the tile stores go through a tensor map
+    with that pitch): columns past N stay untouched."""
+    M, N, K = 535, 1024, 512
+    rng = np.random.default_rng(7)
+    A = _bf16(rng.standard_normal((M, K)))
+    B = _bf16(rng.standard_normal((N, K)) * 0.02)
+    ref = _gemm_ref(to_np(A), to_np(B))
+    big = torch.full((M, N + ldc_extra), 3.0, dtype=torch.float32, device="cuda")
+    cb.cb_gemm(A, B, big, epilogue=1, scratch=cb.gemm_scratch())
+    torch.cuda.synchronize()
+    got = to_np(big)
+    assert np.max(np.abs(got[:, :N] - (ref + 3.0))) < 1e-4 * np.max(np.abs(ref)) + 1e-5
+    assert np.all(got[:, N:] == 3.0)
 
 
 def test_gemm_stream_k_is_deterministic():

@@ -23,9 +23,9 @@ def _build():
     built()
 
 
-# (M, N, K, epilogue): stream-K splits that fit the built-in array, and a
-# data-parallel shape that needs no scratch at all
-SHAPES = [(128, 1024, 28672, 1), (100, 512, 14336, 0), (64, 1024, 8192, 2), (535, 4096, 4096, 1)]
+# (M, N, K, epilogue): stream-K splits over 32 CTAs (4 output tiles), which fit the
+# built-in array, and a data-parallel shape that needs no scratch at all
+SHAPES = [(64, 512, 28672, 1), (48, 512, 14336, 0), (64, 512, 8192, 2), (535, 4096, 4096, 1)]
 
 
 @pytest.mark.parametrize("M,N,K,epi", SHAPES)
@@ -56,7 +56,7 @@ def test_noalloc_gemm_matches_cb_gemm_on_two_calls(M, N, K, epi):
 
 
 def test_noalloc_gemm_rejects_a_split_larger_than_its_array():
-    # 16 output tiles of 128 x 256 would be split over 128 CTAs: 16 MiB of partial tiles
+    # 16 output tiles would be split over 128 CTAs: 16 MiB of partial tiles
     A = torch.zeros(200, 14336, dtype=torch.bfloat16, device="cuda")
     B = torch.zeros(2048, 14336, dtype=torch.bfloat16, device="cuda")
     C = torch.zeros(200, 2048, dtype=torch.float32, device="cuda")
