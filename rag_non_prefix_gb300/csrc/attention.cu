@@ -9,7 +9,7 @@
 //           O += P_{j-1} V_{j-1} (V as an MN-major operand) accumulated in TMEM
 //   warps 2-5: one query row per thread -- read S_j from TMEM, apply the causal mask (key
 //           j is visible iff j <= the row's token position) and the online softmax in fp32
-//           (exp2f), and write P_j (bf16) to one of two shared-memory buffers.  P is taken
+//           (ex2.approx), and write P_j (bf16) to one of two shared-memory buffers.  P is taken
 //           relative to a reference max that moves only when a row's max grows by more
 //           than 2^8; then the row of O in TMEM is rescaled (rarely).  Finally O / l -> bf16.
 // Every mbarrier wait is bounded: on timeout the CTA records ST_WAIT_TIMEOUT and leaves.
@@ -44,6 +44,16 @@ constexpr int SMEM = OFF_BAR + 3072;         // barriers, row positions, max exc
 constexpr uint32_t TMEM_COLS = 512;          // S[2] at columns 0 and 128, O at 256
 constexpr uint32_t O_COL = 256;
 constexpr float RESCALE_LOG2 = 8.0f;         // O is rescaled only when a row max grows by > 2^8
+
+// 2^x with the PTX ex2.approx.ftz.f32 instruction (relative error ~2^-22; results below
+// 2^-126 flush to 0, which for a softmax numerator next to a row sum >= 1 is below the
+// bf16 rounding of P).  The library exp2f adds range fix-ups around the same instruction
+// that this kernel does not need, and they made the softmax twice as slow.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 struct Args {
   CUtensorMap kmap[MAXREQ];
@@ -305,16 +315,20 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&s_empty[st]);
       const int k0 = j * BKV + half * 64;
       const bool full = k0 + 63 <= pos;
-      float mx = -INFINITY;
+      // row max of this half: eight independent chains, then a tree
+      float pm[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(sv[e]));
-        mx *= a.scale_log2;
+        for (int e = 0; e < 64; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(sv[e]));
       } else {
 #pragma unroll
         for (int e = 0; e < 64; ++e)
-          if (k0 + e <= pos) mx = fmaxf(mx, __uint_as_float(sv[e]) * a.scale_log2);
+          if (k0 + e <= pos) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(sv[e]));
       }
+      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      mx *= a.scale_log2;  // scale > 0: the max commutes with it
       // row max over both halves (slots by block parity: a slot is rewritten two blocks later,
       // after the barrier of the next block, so the partner has read it)
       xmax[(st * 2 + half) * ROWS + r] = mx;
@@ -323,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       // lazy rescale: move the reference max only when this block exceeds it by > 2^8
       const bool need = mx > m + RESCALE_LOG2;
       const float m_new = need ? mx : m;
-      const float alpha = exp2f(m - m_new);
+      const float alpha = ex2(m - m_new);
       if (__any_sync(0xffffffffu, need) && j > 0) {  // same rows, same decision in both halves
         // O holds PV_0..PV_{j-1}: wait for the last of them, then scale this warp's part
         wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1);
@@ -348,21 +362,23 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       if (j >= 2) wait(&pv_done[st], ((j - 2) >> 1) & 1);
       if (ok) {
         uint8_t* pb = smem + OFF_P + st * 2 * ATOM + half * ATOM;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial row sums
 #pragma unroll
         for (int c = 0; c < 64; c += 8) {
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
             const int x = c + e;
-            const float p0 = (full || k0 + x <= pos) ? exp2f(__uint_as_float(sv[x]) * a.scale_log2 - m) : 0.f;
+            const float p0 = (full || k0 + x <= pos) ? ex2(fmaf(__uint_as_float(sv[x]), a.scale_log2, -m)) : 0.f;
             const float p1 =
-                (full || k0 + x + 1 <= pos) ? exp2f(__uint_as_float(sv[x + 1]) * a.scale_log2 - m) : 0.f;
-            l += p0 + p1;
+                (full || k0 + x + 1 <= pos) ? ex2(fmaf(__uint_as_float(sv[x + 1]), a.scale_log2, -m)) : 0.f;
+            ls[e >> 1] += p0 + p1;
             pk[e >> 1] = pack_bf16x2(p0, p1);
           }
           *reinterpret_cast<uint4*>(pb + r * 128 + (((c >> 3) ^ (r & 7)) << 4)) =
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         fence_proxy_async_smem();
         tc_fence_before();
       }
