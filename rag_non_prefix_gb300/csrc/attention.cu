@@ -3,8 +3,8 @@
 // bf16, head_dim 128, on the tcgen05 tensor cores.  One CTA per (tile, KV head): a tile
 // packs QT queries x G heads of one KV group into the 128 rows of the MMA (G = n_heads /
 // n_kv_heads, QT = 128 / G), so each K/V block is read once for all heads of the group.
-//   warp 0: TMA producer -- 4-D tensor maps over the fused cache [L][N][Hkv][dh] bring
-//           128-key K and V blocks (128-byte swizzle) into a two-stage ring
+//   warp 0: TMA producers (lane 0: K, lane 1: V) -- 4-D tensor maps over the fused cache
+//           [L][N][Hkv][dh] bring 128-key K and V blocks (128-byte swizzle) into two-slot rings
 //   warp 1: TMEM owner + MMA issuer -- S_j = Q K_j^T into one of two TMEM buffers, then
 //           O += P_{j-1} V_{j-1} (V as an MN-major operand) accumulated in TMEM
 //   warps 2-5: one query row per thread -- read S_j from TMEM, apply the causal mask (key
@@ -176,34 +176,32 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const CUtensorMap* km = &a.kmap[t.req];
-      const CUtensorMap* vm = &a.vmap[t.req];
+    // Lane 0 streams K, lane 1 streams V, each at the pace its own slots free up (K_j
+    // once S_{j-2} is done with its slot, V_j once PV_{j-2} is), so that a K load never
+    // queues behind a V slot that the previous PV still holds.
+    if (lane < 2) {
+      const bool is_v = lane == 1;
+      const CUtensorMap* map = is_v ? &a.vmap[t.req] : &a.kmap[t.req];
+      uint64_t* empty = is_v ? v_empty : k_empty;
+      uint64_t* full = is_v ? v_full : k_full;
       const int lc = a.layer_coord[t.req];
-      int issued_k = 0, issued_v = 0;
+      int issued = 0;
       for (int j = 0; j < n_blk; ++j) {
         const int st = j & 1;
         const uint32_t ph = ((j >> 1) & 1) ^ 1;
-        uint8_t* kd = smem + OFF_KV + st * STAGE;
-        // K_j once S_{j-2} is done with its slot; V_j once PV_{j-2} is
-        if (!mbar_wait_bounded(&k_empty[st], ph, abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[st], 2 * ATOM);
-        tma_load_4d(kd, km, &k_full[st], 0, kvh, j * BKV, lc);
-        tma_load_4d(kd + ATOM, km, &k_full[st], 64, kvh, j * BKV, lc);
-        issued_k = j + 1;
-        if (!mbar_wait_bounded(&v_empty[st], ph, abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full[st], 2 * ATOM);
-        tma_load_4d(kd + 2 * ATOM, vm, &v_full[st], 0, kvh, j * BKV, lc);
-        tma_load_4d(kd + 3 * ATOM, vm, &v_full[st], 64, kvh, j * BKV, lc);
-        issued_v = j + 1;
+        uint8_t* dst = smem + OFF_KV + st * STAGE + (is_v ? 2 * ATOM : 0);
+        if (!mbar_wait_bounded(&empty[st], ph, abort_flag)) break;
+        mbar_arrive_expect_tx(&full[st], 2 * ATOM);
+        tma_load_4d(dst, map, &full[st], 0, kvh, j * BKV, lc);
+        tma_load_4d(dst + ATOM, map, &full[st], 64, kvh, j * BKV, lc);
+        issued = j + 1;
       }
-      if (issued_v < n_blk && !*abort_flag) {
+      if (issued < n_blk && !*abort_flag) {
         *abort_flag = 1;
         set_status(a.status, ST_WAIT_TIMEOUT);
       }
       // copies issued into slots that nobody consumed must land before the block exits
-      for (int j = max(0, issued_k - 2); j < issued_k; ++j) mbar_wait_bounded(&k_full[j & 1], (j >> 1) & 1, nullptr);
-      for (int j = max(0, issued_v - 2); j < issued_v; ++j) mbar_wait_bounded(&v_full[j & 1], (j >> 1) & 1, nullptr);
+      for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait_bounded(&full[j & 1], (j >> 1) & 1, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
