@@ -295,10 +295,10 @@ enum {
   CB_PH_STAGED_ROT,     /* in-place re-rotation of host-staged chunks */
   CB_PH_NORM,           /* RMSNorm (attention and MLP inputs) */
   CB_PH_QKV,            /* q/k/v projection GEMM */
-  CB_PH_ROPE,           /* RoPE of fresh q and k */
-  CB_PH_DEVIATION,      /* KV deviation (check layers) */
+  CB_PH_ROPE,           /* (unused: RoPE of fresh q and k runs inside the deviation and scatter) */
+  CB_PH_DEVIATION,      /* KV deviation with RoPE of the fresh k (check layers) */
   CB_PH_SELECT,         /* HKVD top-k (check layers) */
-  CB_PH_SCATTER,        /* compaction, q conversion, KV scatter into the fused cache */
+  CB_PH_SCATTER,        /* RoPE of q and k, compaction, q conversion, KV scatter into the fused cache */
   CB_PH_ATTENTION,      /* causal sparse-query attention */
   CB_PH_OPROJ,          /* output projection GEMM + residual */
   CB_PH_GATEUP,         /* gate/up GEMM + SiLU-mul */

@@ -707,7 +707,8 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   int32_t* posR = ctx->pos[cur];
   int32_t* reqR = ctx->req[cur];
   float* hR = ctx->h[cur];
-  // 1. QKV of R: x = RMSNorm(h_R); [q | k | v] = x W^T; RoPE on q, k
+  // 1. QKV of R: x = RMSNorm(h_R); [q | k | v] = x W^T (RoPE of q and k is applied where
+  //    they are consumed: the deviation and the scatter)
   {
     PhaseScope ps(ctx, CB_PH_NORM, s, 1);
     CB_CUDA(ctx, launch_rmsnorm(hR, Rn, d, c.rms_eps, ctx->x, c.dtype, s));
@@ -717,10 +718,6 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
     CB_CUDA(ctx, launch_gemm(ctx->x, ctx->wq[i], ctx->wk[i], ctx->wv[i], qw, qw + kvw, ctx->qkv, Rn, qw + 2 * kvw, d,
                              qw + 2 * kvw, 0, c.dtype, ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
   }
-  {
-    PhaseScope ps(ctx, CB_PH_ROPE, s, 1);
-    CB_CUDA(ctx, launch_rope_qk(ctx->qkv, posR, Rn, H, Hkv, dh, ctx->rope, c.max_positions, ctx->status, s));
-  }
   int32_t* posS = posR;
   int32_t* reqS = reqR;
   float* hS = hR;
@@ -729,8 +726,8 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
     // 2. deviation of the cached rows of R against the fused cache, then top-k per request
     {
       PhaseScope ps(ctx, CB_PH_DEVIATION, s, 1);
-      CB_CUDA(ctx, launch_deviation_rows(ctx->qkv, Rn, posR, reqR, ctx->d_reqs, i, H, Hkv, dh, b.dev_mode, c.dtype,
-                                         ctx->dev, ctx->status, s));
+      CB_CUDA(ctx, launch_deviation_rows(ctx->qkv, Rn, posR, reqR, ctx->d_reqs, i, H, Hkv, dh, b.dev_mode, ctx->rope,
+                                         c.max_positions, c.dtype, ctx->dev, ctx->status, s));
     }
     posS = ctx->pos[cur ^ 1];
     reqS = ctx->req[cur ^ 1];
@@ -743,14 +740,14 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
     // 3. compact S, scatter fresh K/V of S into the fused cache, q of S in the model dtype
     {
       PhaseScope ps(ctx, CB_PH_SCATTER, s, 1);
-      CB_CUDA(ctx, launch_post_qkv(ctx->qkv, Sn, ctx->src, posS, reqS, ctx->d_reqs, i, H, Hkv, dh, c.dtype, ctx->q, hR,
-                                   hS, d, ctx->status, s));
+      CB_CUDA(ctx, launch_post_qkv(ctx->qkv, Sn, ctx->src, posS, reqS, ctx->d_reqs, i, H, Hkv, dh, ctx->rope,
+                                   c.max_positions, c.dtype, ctx->q, hR, hS, d, ctx->status, s));
     }
     b.cur ^= 1;
   } else {
     PhaseScope ps(ctx, CB_PH_SCATTER, s, 1);
-    CB_CUDA(ctx, launch_post_qkv(ctx->qkv, Sn, nullptr, posS, reqS, ctx->d_reqs, i, H, Hkv, dh, c.dtype, ctx->q, hR, hR,
-                                 d, ctx->status, s));
+    CB_CUDA(ctx, launch_post_qkv(ctx->qkv, Sn, nullptr, posS, reqS, ctx->d_reqs, i, H, Hkv, dh, ctx->rope,
+                                 c.max_positions, c.dtype, ctx->q, hR, hR, d, ctx->status, s));
   }
   // 4. causal attention of S over the fused cache
   {

@@ -52,11 +52,11 @@ cudaError_t launch_rerotate(const RerotSeg* segs, int n_segs, int max_rows, int 
 cudaError_t launch_rerotate_single(const void* k_src, void* k_dst, const void* v_src, void* v_dst, int n_rows,
                                    int n_kv_heads, int head_dim, const float* cs_host, cb_dtype dt, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x, cb_dtype dt, cudaStream_t s);
-cudaError_t launch_rope_qk(float* qkv, const int32_t* pos, int n_rows, int n_heads, int n_kv_heads, int head_dim,
-                           const float2* rope_table, int max_pos, int32_t* status, cudaStream_t s);
+// (both rotate the fresh q / k of the fp32 projection output at each row's position)
 cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* pos, const int32_t* req,
                                   const ReqDev* reqs, int layer, int n_heads, int n_kv_heads, int head_dim, int mode,
-                                  cb_dtype dt, float* dev, int32_t* status, cudaStream_t s);
+                                  const float2* rope_table, int max_pos, cb_dtype dt, float* dev, int32_t* status,
+                                  cudaStream_t s);
 cudaError_t launch_deviation_plain(const float* k_new, const float* v_new, const void* k_fus, const void* v_fus,
                                    const int32_t* idx, int n, int kv_width, int mode, cb_dtype dt, float* dev,
                                    cudaStream_t s);
@@ -67,8 +67,8 @@ cudaError_t launch_select_batched(const float* dev, const int32_t* r_pos, const 
                                   int32_t* status, cudaStream_t s);
 cudaError_t launch_post_qkv(const float* qkv, int n_s_rows, const int32_t* s_src, const int32_t* s_pos,
                             const int32_t* s_req, const ReqDev* reqs, int layer, int n_heads, int n_kv_heads,
-                            int head_dim, cb_dtype dt, void* q_out, const float* h_in, float* h_out, int d,
-                            int32_t* status, cudaStream_t s);
+                            int head_dim, const float2* rope_table, int max_pos, cb_dtype dt, void* q_out,
+                            const float* h_in, float* h_out, int d, int32_t* status, cudaStream_t s);
 cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, void* C,
                         int M, int N, int K, int ldc, int mode, cb_dtype dt, int32_t* status, void* scratch,
                         size_t scratch_bytes, cudaStream_t s);

@@ -156,36 +156,72 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
   return t;
 }
 
-template <typename T>
-__global__ void rmsnorm_kernel(const float* __restrict__ h, int d, float eps, T* __restrict__ x) {
+// One CTA of 256 threads per row.  Rows of up to 8192 (= 256 x 8 x CH) elements stay in
+// registers between the sum of squares and the scaled write (one read of h); longer rows
+// are read twice.  Thread t always owns chunks t, t + 256, ... of 8 elements.
+template <typename T, bool IN_REGS>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ h, int d, float eps, T* __restrict__ x) {
+  constexpr int CH = 4;
   __shared__ float red[32];
   const size_t row = blockIdx.x;
   const float* src = h + row * d;
-  float ss = 0.f;
-  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
-    float f[8];
-    load8(src + c, f);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
-  }
-  ss = block_sum_256(ss, red);
-  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
   T* dst = x + row * d;
-  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
-    float f[8];
-    load8(src + c, f);
+  float ss = 0.f;
+  if (IN_REGS) {
+    float f[CH][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) f[j] *= inv;
-    store8(dst + c, f);
+    for (int k = 0; k < CH; ++k) {
+      const int c = (threadIdx.x + k * 256) * 8;
+      if (c < d) {
+        load8(src + c, f[k]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss += f[k][j] * f[k][j];
+      }
+    }
+    ss = block_sum_256(ss, red);
+    const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      const int c = (threadIdx.x + k * 256) * 8;
+      if (c < d) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[k][j] *= inv;
+        store8(dst + c, f[k]);
+      }
+    }
+  } else {
+    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+      float f[8];
+      load8(src + c, f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss += f[j] * f[j];
+    }
+    ss = block_sum_256(ss, red);
+    const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+      float f[8];
+      load8(src + c, f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] *= inv;
+      store8(dst + c, f);
+    }
   }
 }
 
 cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x, cb_dtype dt, cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
-  if (dt == CB_BF16)
-    rmsnorm_kernel<bf16><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<bf16*>(x));
-  else
-    rmsnorm_kernel<float><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<float*>(x));
+  const bool regs = d <= 256 * 8 * 4;
+  if (dt == CB_BF16) {
+    if (regs)
+      rmsnorm_kernel<bf16, true><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<bf16*>(x));
+    else
+      rmsnorm_kernel<bf16, false><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<bf16*>(x));
+  } else {
+    if (regs)
+      rmsnorm_kernel<float, true><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<float*>(x));
+    else
+      rmsnorm_kernel<float, false><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<float*>(x));
+  }
   return cudaGetLastError();
 }
 
@@ -221,49 +257,17 @@ cudaError_t launch_last_rows_norm(const float* h, const int32_t* rows, int n, in
 }
 
 // ----------------------------------------------------------------------------- RoPE of fresh q and k
-// In place on the fp32 [rows][(H + 2 Hkv) dh] projection output: heads 0..H-1 (q) and
-// H..H+Hkv-1 (k) rotated at each row's position.  One thread owns 8 pairs.
-__global__ void rope_qk_kernel(float* __restrict__ qkv, const int32_t* __restrict__ pos, int n_rows, int n_heads,
-                               int n_kv_heads, int head_dim, const float2* __restrict__ table, int max_pos,
-                               int32_t* status) {
-  const int half = head_dim / 2, cpr = half / 8;
-  const int width = (n_heads + 2 * n_kv_heads) * head_dim;
-  const int per_row = (n_heads + n_kv_heads) * cpr;
-  const long long total = static_cast<long long>(n_rows) * per_row;
-  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
-       t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = t / per_row;
-    const int w = static_cast<int>(t - row * per_row);
-    const int head = w / cpr, c = w - head * cpr;
-    const int p = pos[row];
-    if (p < 0 || p >= max_pos) {
-      set_status(status, ST_RANGE);
-      continue;
-    }
-    float* base = qkv + static_cast<size_t>(row) * width + static_cast<size_t>(head) * head_dim + c * 8;
-    const float2* cs = table + static_cast<size_t>(p) * half + c * 8;
-    float a[8], b[8];
-    load8(base, a);
-    load8(base + half, b);
-    float na[8], nb[8];
+// Rotate-half RoPE of one head: elements j..j+7 (a) and j+dh/2..j+dh/2+7 (b) turn by the
+// angles of pairs j..j+7 at the row's position (cs = the table row of that position).
+// Applied where the fresh q and k are consumed (deviation, scatter), so the projection
+// output is read once.
+__device__ __forceinline__ void rope8(const float* a, const float* b, const float2* cs, float* ra, float* rb) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float2 r = cs[j];
-      na[j] = a[j] * r.x - b[j] * r.y;
-      nb[j] = b[j] * r.x + a[j] * r.y;
-    }
-    store8(base, na);
-    store8(base + half, nb);
+  for (int e = 0; e < 8; ++e) {
+    const float2 r = cs[e];
+    ra[e] = a[e] * r.x - b[e] * r.y;
+    rb[e] = b[e] * r.x + a[e] * r.y;
   }
-}
-
-cudaError_t launch_rope_qk(float* qkv, const int32_t* pos, int n_rows, int n_heads, int n_kv_heads, int head_dim,
-                           const float2* rope_table, int max_pos, int32_t* status, cudaStream_t s) {
-  if (n_rows <= 0) return cudaSuccess;
-  const long long work = static_cast<long long>(n_rows) * (n_heads + n_kv_heads) * (head_dim / 16);
-  rope_qk_kernel<<<grid_for(work, 256), 256, 0, s>>>(qkv, pos, n_rows, n_heads, n_kv_heads, head_dim, rope_table,
-                                                     max_pos, status);
-  return cudaGetLastError();
 }
 
 // ----------------------------------------------------------------------------- KV deviation
@@ -296,42 +300,83 @@ __device__ __forceinline__ float dev_row(const float* __restrict__ kn, const flo
 }
 
 // One warp per row of R; only cached rows (position < Nc of their request) are candidates.
+// The fresh k of the projection output is rotated to the row's position here (RoPE), then
+// compared with the fused cache, whose cached rows were re-rotated to the same position.
 template <typename T>
 __global__ void deviation_rows_kernel(const float* __restrict__ qkv, int n_rows, const int32_t* __restrict__ pos,
                                       const int32_t* __restrict__ req, const ReqDev* __restrict__ reqs, int layer,
-                                      int q_width, int kvw, int mode, float* __restrict__ dev, int32_t* status) {
+                                      int q_width, int kvw, int head_dim, int mode, const float2* __restrict__ table,
+                                      int max_pos, float* __restrict__ dev, int32_t* status) {
   const int warps = blockDim.x >> 5;
   const int row = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (row >= n_rows) return;
   const int p = pos[row];
   const ReqDev rq = reqs[req[row]];
   if (p >= rq.n_cached) {
-    if ((threadIdx.x & 31) == 0) dev[row] = 0.f;
+    if (lane == 0) dev[row] = 0.f;
     return;
   }
-  if (p < 0) {
-    if ((threadIdx.x & 31) == 0) set_status(status, ST_RANGE);
+  if (p < 0 || p >= max_pos) {
+    if (lane == 0) set_status(status, ST_RANGE);
     return;
   }
   const size_t width = static_cast<size_t>(q_width) + 2 * kvw;
   const float* kn = qkv + static_cast<size_t>(row) * width + q_width;
   const float* vn = kn + kvw;
   const size_t off = static_cast<size_t>(layer) * rq.layer_stride + static_cast<size_t>(p) * kvw;
-  const float d = dev_row<T>(kn, vn, static_cast<const T*>(rq.k) + off, static_cast<const T*>(rq.v) + off, kvw, mode);
-  if ((threadIdx.x & 31) == 0) dev[row] = d;
+  const T* kf = static_cast<const T*>(rq.k) + off;
+  const T* vf = static_cast<const T*>(rq.v) + off;
+  const int half = head_dim / 2, cpr = half / 8;
+  const float2* cs = table + static_cast<size_t>(p) * half;
+  float acc = 0.f;
+  if (mode != 2) {
+    for (int w = lane; w < kvw / 16; w += 32) {  // 8 rotation pairs per step
+      const int head = w / cpr, j = (w - head * cpr) * 8;
+      const int o = head * head_dim + j;
+      float a[8], b[8], ra[8], rb[8], fa[8], fb[8];
+      load8(kn + o, a);
+      load8(kn + o + half, b);
+      rope8(a, b, cs + j, ra, rb);
+      load8(kf + o, fa);
+      load8(kf + o + half, fb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = ra[e] - fa[e], y = rb[e] - fb[e];
+        acc += x * x + y * y;
+      }
+    }
+  }
+  if (mode != 1) {
+    for (int c = lane * 8; c < kvw; c += 256) {
+      float a[8], b[8];
+      load8(vn + c, a);
+      load8(vf + c, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = a[e] - b[e];
+        acc += x * x;
+      }
+    }
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) dev[row] = acc;
 }
 
 cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* pos, const int32_t* req,
                                   const ReqDev* reqs, int layer, int n_heads, int n_kv_heads, int head_dim, int mode,
-                                  cb_dtype dt, float* dev, int32_t* status, cudaStream_t s) {
+                                  const float2* rope_table, int max_pos, cb_dtype dt, float* dev, int32_t* status,
+                                  cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
   const int blocks = (n_rows + 7) / 8;
   if (dt == CB_BF16)
     deviation_rows_kernel<bf16><<<blocks, 256, 0, s>>>(qkv, n_rows, pos, req, reqs, layer, n_heads * head_dim,
-                                                       n_kv_heads * head_dim, mode, dev, status);
+                                                       n_kv_heads * head_dim, head_dim, mode, rope_table, max_pos,
+                                                       dev, status);
   else
     deviation_rows_kernel<float><<<blocks, 256, 0, s>>>(qkv, n_rows, pos, req, reqs, layer, n_heads * head_dim,
-                                                        n_kv_heads * head_dim, mode, dev, status);
+                                                        n_kv_heads * head_dim, head_dim, mode, rope_table, max_pos,
+                                                        dev, status);
   return cudaGetLastError();
 }
 
@@ -364,36 +409,48 @@ cudaError_t launch_deviation_plain(const float* k_new, const float* v_new, const
 }
 
 // ----------------------------------------------------------------------------- compaction + KV scatter
-// For every row t of S: q of its source row (RoPE applied, fp32) -> q_out[t] (model dtype);
-// fresh k, v -> fused cache row at its position; hidden state h_in[src] -> h_out[t]
-// when the set shrank (h_out != h_in).
+// For every row t of S: q and k of its source row rotated at the row's position (RoPE),
+// q -> q_out[t] (model dtype), k and v -> the fused cache row at that position; hidden
+// state h_in[src] -> h_out[t] when the set shrank (h_out != h_in).
 template <typename T>
 __global__ void post_qkv_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ s_src,
                                 const int32_t* __restrict__ s_pos, const int32_t* __restrict__ s_req,
-                                const ReqDev* __restrict__ reqs, int layer, int q_width, int kvw, T* __restrict__ q_out,
+                                const ReqDev* __restrict__ reqs, int layer, int q_width, int kvw, int head_dim,
+                                const float2* __restrict__ table, int max_pos, T* __restrict__ q_out,
                                 const float* __restrict__ h_in, float* __restrict__ h_out, int d, int32_t* status) {
   const int t = blockIdx.x;
   const int src = s_src ? s_src[t] : t;
   const int p = s_pos[t];
   const ReqDev rq = reqs[s_req[t]];
-  if (p < 0 || p >= rq.n_tokens) {
+  if (p < 0 || p >= rq.n_tokens || p >= max_pos) {
     if (threadIdx.x == 0) set_status(status, ST_RANGE);
     return;
   }
   const size_t width = static_cast<size_t>(q_width) + 2 * kvw;
   const float* row = qkv + static_cast<size_t>(src) * width;
-  for (int c = threadIdx.x * 8; c < q_width; c += blockDim.x * 8) {
-    float f[8];
-    load8(row + c, f);
-    store8(q_out + static_cast<size_t>(t) * q_width + c, f);
-  }
   const size_t off = static_cast<size_t>(layer) * rq.layer_stride + static_cast<size_t>(p) * kvw;
   T* kd = static_cast<T*>(rq.k) + off;
   T* vd = static_cast<T*>(rq.v) + off;
+  T* qd = q_out + static_cast<size_t>(t) * q_width;
+  const int half = head_dim / 2, cpr = half / 8;
+  const float2* cs = table + static_cast<size_t>(p) * half;
+  const int qsteps = q_width / 16, steps = qsteps + kvw / 16;
+  for (int w = threadIdx.x; w < steps; w += blockDim.x) {  // 8 rotation pairs of q or k per step
+    const bool is_k = w >= qsteps;
+    const int ww = is_k ? w - qsteps : w;
+    const int head = ww / cpr, j = (ww - head * cpr) * 8;
+    const int o = head * head_dim + j;
+    const float* a = row + (is_k ? q_width : 0) + o;
+    float fa[8], fb[8], ra[8], rb[8];
+    load8(a, fa);
+    load8(a + half, fb);
+    rope8(fa, fb, cs + j, ra, rb);
+    T* dst = (is_k ? kd : qd) + o;
+    store8(dst, ra);
+    store8(dst + half, rb);
+  }
   for (int c = threadIdx.x * 8; c < kvw; c += blockDim.x * 8) {
     float f[8];
-    load8(row + q_width + c, f);
-    store8(kd + c, f);
     load8(row + q_width + kvw + c, f);
     store8(vd + c, f);
   }
@@ -410,17 +467,17 @@ __global__ void post_qkv_kernel(const float* __restrict__ qkv, const int32_t* __
 
 cudaError_t launch_post_qkv(const float* qkv, int n_s_rows, const int32_t* s_src, const int32_t* s_pos,
                             const int32_t* s_req, const ReqDev* reqs, int layer, int n_heads, int n_kv_heads,
-                            int head_dim, cb_dtype dt, void* q_out, const float* h_in, float* h_out, int d,
-                            int32_t* status, cudaStream_t s) {
+                            int head_dim, const float2* rope_table, int max_pos, cb_dtype dt, void* q_out,
+                            const float* h_in, float* h_out, int d, int32_t* status, cudaStream_t s) {
   if (n_s_rows <= 0) return cudaSuccess;
   if (dt == CB_BF16)
     post_qkv_kernel<bf16><<<n_s_rows, 256, 0, s>>>(qkv, s_src, s_pos, s_req, reqs, layer, n_heads * head_dim,
-                                                   n_kv_heads * head_dim, static_cast<bf16*>(q_out), h_in, h_out, d,
-                                                   status);
+                                                   n_kv_heads * head_dim, head_dim, rope_table, max_pos,
+                                                   static_cast<bf16*>(q_out), h_in, h_out, d, status);
   else
     post_qkv_kernel<float><<<n_s_rows, 256, 0, s>>>(qkv, s_src, s_pos, s_req, reqs, layer, n_heads * head_dim,
-                                                    n_kv_heads * head_dim, static_cast<float*>(q_out), h_in, h_out, d,
-                                                    status);
+                                                    n_kv_heads * head_dim, head_dim, rope_table, max_pos,
+                                                    static_cast<float*>(q_out), h_in, h_out, d, status);
   return cudaGetLastError();
 }
 
