@@ -1,0 +1,116 @@
+"""Summarise an ncu launch list (``ncu --csv --log-file``) of the blended prefill.
+
+    python -m rag_non_prefix_gb300.ncu_summary launches.csv --steps 2 \\
+        --markdown out.md --traffic-json profiles/gemm_traffic.json --command "<the ncu command>"
+
+Per kernel: launches, total device time, share of the listed time and, when the capture
+has ``dram__bytes_read.sum`` / ``dram__bytes_write.sum``, the average DRAM bytes per
+launch.  ``--traffic-json`` records the projection GEMM's average bytes per launch with a
+hash of its sources, which ``bench.py`` reports as ``roofline.traffic`` only while the
+kernel source is unchanged.  Durations under ncu are serialised and cold-cache: compare
+shares, not absolute times.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import json
+import os
+import re
+from collections import OrderedDict
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GEMM_SOURCES = ["rag_non_prefix_gb300/csrc/gemm.cu", "rag_non_prefix_gb300/csrc/common.cuh"]
+_UNIT = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "ns": 1e-3, "us": 1.0, "usecond": 1.0,
+         "nsecond": 1e-3, "msecond": 1e3, "ms": 1e3}
+
+
+def short_name(name: str) -> str:
+    """'void cb::tc::gemm_bf16_tc<256, true>(CUtensorMap_st, ...)' -> 'tc::gemm_bf16_tc<256, true>'."""
+    n = re.sub(r"^void\s+", "", name)
+    n = n.split("(")[0]
+    return n.replace("cb::", "")
+
+
+def read_launches(path: str):
+    """Rows of (launch id, kernel, metric, value in us or bytes)."""
+    with open(path) as f:
+        lines = f.read().splitlines()
+    start = next(i for i, l in enumerate(lines) if l.startswith('"ID"'))
+    rows = list(csv.DictReader(lines[start:]))
+    out = []
+    for r in rows:
+        unit = r.get("Metric Unit", "")
+        val = float(r["Metric Value"].replace(",", ""))
+        out.append((int(r["ID"]), r["Kernel Name"], r["Metric Name"], val * _UNIT.get(unit, 1.0)))
+    return out
+
+
+def summarise(path: str):
+    per = OrderedDict()
+    launches = {}
+    for lid, kern, metric, val in read_launches(path):
+        k = short_name(kern)
+        launches.setdefault(k, set()).add(lid)
+        d = per.setdefault(k, {"us": 0.0, "dram": 0.0, "has_dram": False})
+        if metric == "gpu__time_duration.sum":
+            d["us"] += val
+        elif metric in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            d["dram"] += val
+            d["has_dram"] = True
+    total = sum(d["us"] for d in per.values())
+    table = []
+    for k, d in sorted(per.items(), key=lambda kv: -kv[1]["us"]):
+        n = len(launches[k])
+        table.append({"kernel": k, "launches": n, "total_us": round(d["us"], 1),
+                      "share": round(100.0 * d["us"] / total, 2) if total else 0.0,
+                      "dram_mb_per_launch": round(d["dram"] / n / 1e6, 1) if d["has_dram"] else None})
+    return table, total
+
+
+def sources_sha256(sources) -> str:
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("csv")
+    ap.add_argument("--steps", type=int, default=1, help="timed steps the capture covers (per-step figures)")
+    ap.add_argument("--markdown", default=None)
+    ap.add_argument("--traffic-json", default=None)
+    ap.add_argument("--command", default="")
+    a = ap.parse_args()
+    table, total = summarise(a.csv)
+    lines = ["| kernel | launches | total us | share | DRAM MB / launch |", "|---|---:|---:|---:|---:|"]
+    for r in table:
+        mb = "" if r["dram_mb_per_launch"] is None else f"{r['dram_mb_per_launch']}"
+        lines.append(f"| {r['kernel']} | {r['launches']} | {r['total_us']} | {r['share']} % | {mb} |")
+    lines.append(f"\n{sum(r['launches'] for r in table)} launches, {total / 1e3:.2f} ms listed "
+                 f"({total / 1e3 / max(1, a.steps):.2f} ms per step).")
+    text = "\n".join(lines)
+    print(text)
+    if a.markdown:
+        with open(a.markdown, "w") as f:
+            f.write(text + "\n")
+    if a.traffic_json:
+        gemm = [r for r in table if "gemm_bf16_tc" in r["kernel"]]
+        n = sum(r["launches"] for r in gemm)
+        if n and all(r["dram_mb_per_launch"] is not None for r in gemm):
+            byts = sum(r["dram_mb_per_launch"] * 1e6 * r["launches"] for r in gemm) / n
+            rec = {"kernel": "tc::gemm_bf16_tc (all instantiations)", "source_sha256": sources_sha256(GEMM_SOURCES),
+                   "sources": GEMM_SOURCES, "bytes_per_launch": round(byts), "launches": n,
+                   "metrics": "dram__bytes_read.sum + dram__bytes_write.sum, averaged over the GEMM launches "
+                              "of the captured blend steps",
+                   "command": a.command}
+            with open(a.traffic_json, "w") as f:
+                json.dump(rec, f, indent=1)
+                f.write("\n")
+
+
+if __name__ == "__main__":
+    main()
