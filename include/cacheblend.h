@@ -156,11 +156,12 @@ cb_status cb_select_hkvd(const float* dev, const int32_t* cand, int n, int k, in
  * (then N counts both).  bf16 runs on the tcgen05 tensor cores (persistent, one CTA
  * per SM), fp32 on CUDA cores.  bf16 needs K % 64 == 0 and N % 128 == 0.
  * scratch: NULL (whole output tiles per CTA only) or device memory, zero-filled before
- * its first use, for the stream-K schedule used when the output tiles would occupy at
- * most half of the SMs: 1 KiB of flags, then one 128 KiB fp32 partial tile per CTA of
- * the split (a smaller scratch narrows the split).  cb_gemm_scratch_size() bytes allow
- * every split.  The call leaves the flags zeroed.  Calls sharing one scratch must not
- * overlap on the GPU. */
+ * its first use, for the stream-K schedules (the k-iterations of the output tiles
+ * divided evenly over the SMs, when whole tiles would leave SMs idle or a last wave
+ * ragged; the sums of split tiles are formed in a fixed order, so results repeat
+ * exactly): 1 KiB of flags, then one 128 KiB fp32 partial slot per CTA of the split (a smaller
+ * scratch narrows the split).  cb_gemm_scratch_size() bytes allow every split.  The
+ * call leaves the flags zeroed.  Calls sharing one scratch must not overlap on the GPU. */
 cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, int N, int K, int ldc, int epilogue,
                   cb_dtype dtype, void* scratch, size_t scratch_bytes, void* stream);
 size_t cb_gemm_scratch_size(void);
@@ -179,7 +180,7 @@ cb_status cb_gemm_set_orientation(int orientation);
  * budget after start-up, or code inside a framework that owns every allocation).
  * Same arguments and results as cb_gemm without the scratch arguments: its stream-K
  * scratch is a built-in device array of CB_GEMM_STATIC_SCRATCH_BYTES (4 MiB + 1 KiB:
- * the flags and 32 partial tiles) that every GPU loading the library holds until the
+ * the flags and the partial slots of a 32-CTA split) that every GPU loading the library holds until the
  * process exits.  Shapes whose stream-K split needs more return CB_ERR_WORKSPACE
  * (cb_gemm_noalloc_error() has the reason); data-parallel shapes need none.  The call
  * allocates nothing; its first call on a device looks up the array's device address

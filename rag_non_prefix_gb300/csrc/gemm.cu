@@ -87,9 +87,11 @@ constexpr int MAX_CTAS = 256;             // bound of the persistent grid
 constexpr int FLAG_BYTES = MAX_CTAS * 4;  // stream-K flags at the head of the scratch, partial slots after
 
 // Work division.  Tiles t = m + n * m_tiles (consecutive tiles share a weight tile).
-// Tiles [0, dp_tiles) go round-robin to the CTAs (data-parallel); the k-iterations of the
-// remaining tiles are split evenly over the CTAs (stream-K): CTA g owns iterations
-// [g*I/G, (g+1)*I/G) of the I = (tiles - dp_tiles) * kb_per_tile tail iterations.
+// Tiles [0, dp_tiles) go round-robin to the CTAs (data-parallel).  The k-iterations of the
+// rest are split evenly (stream-K) over groups of sk_group CTAs: with sk_group = 1 over the
+// remaining tiles; with sk_group = m_tiles (and no data-parallel tiles) over the weight
+// tiles n, the CTAs of a group taking the m_tiles token tiles of the same weight tile and
+// k-range at the same time, so that the weight stream is still read from DRAM once.
 struct Params {
   int M, N, K;
   int mode;
@@ -100,11 +102,12 @@ struct Params {
   int m_tiles, kb_per_tile;
   int dp_tiles, tiles;
   long long sk_iters;
-  float* partials;     // [gridDim.x][BM][BN] fp32, stream-K partial tiles
+  float* partials;     // [gridDim.x][128 KiB] fp32: stream-K partial tiles
   int* flags;          // [gridDim.x], zero between launches
   int bt;              // weight-rows orientation: tokens per tile (multiple of 16, <= 256)
   int stages;          // ring depth
   int stage_bytes;     // A_STAGE + slot B bytes (a multiple of 2 KiB)
+  int sk_group;        // stream-K: CTAs that move through the k-iterations in lockstep
 };
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -129,9 +132,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int bn) {
 // depth is what fits (at most MAX_STAGES): the deeper the ring, the more weight bytes are
 // in flight per SM, which is what bounds a launch whose tiles stream weights from DRAM.
 constexpr int MAX_STAGES = 12;
+constexpr int FIX_BUFS = 16;  // stream-K fix-up: slab steps in flight
 constexpr int OFF_BAR = 0;
-constexpr int OFF_STG = 1024;          // epilogue staging: 16 KiB
-constexpr int STG_BYTES = 16384;
+constexpr int OFF_STG = 1024;          // epilogue staging: two 16 KiB buffers
+constexpr int STG_BYTES = 32768;
 constexpr int OFF_RING = OFF_STG + STG_BYTES;
 constexpr int SMEM_ALLOC = 232448;     // the per-block maximum (227 KiB)
 constexpr int RING_BYTES = SMEM_ALLOC - 1024 - OFF_RING;  // 1 KiB of slack aligns the base
@@ -142,7 +146,9 @@ enum { ITEM_FULL = 0, ITEM_PARTIAL = 1, ITEM_OWNER = 2 };
 
 struct Item {
   int tile, kb0, kb1, kind;
-  int last;  // ITEM_OWNER: last contributing CTA
+  // contributors of an ITEM_OWNER tile: CTAs first, first + stride, ..., last (none when
+  // first > last)
+  int first, last, stride;
 };
 
 // The idx-th work item of CTA g (false when there is none).
@@ -154,28 +160,35 @@ __device__ __forceinline__ bool get_item(const Params& p, int g, int G, int idx,
     it.kb0 = 0;
     it.kb1 = KB;
     it.kind = ITEM_FULL;
+    it.first = g + 1;
     it.last = g;
+    it.stride = 1;
     return true;
   }
   if (p.sk_iters <= 0) return false;
+  const int S = p.sk_group;
+  const int NG = G / S, gi = g / S, mem = g - gi * S;
+  if (gi >= NG) return false;
   const long long I = p.sk_iters;
-  const long long a = static_cast<long long>(g) * I / G, b = static_cast<long long>(g + 1) * I / G;
+  const long long a = static_cast<long long>(gi) * I / NG, b = static_cast<long long>(gi + 1) * I / NG;
   const int j = idx - n_dp;
   const long long start = j == 0 ? a : (a / KB + j) * KB;
   if (start >= b) return false;
   const long long tile_lo = (start / KB) * KB, tile_hi = tile_lo + KB;
   const long long end = b < tile_hi ? b : tile_hi;
-  it.tile = p.dp_tiles + static_cast<int>(start / KB);
+  it.tile = p.dp_tiles + mem + static_cast<int>(start / KB) * S;
   it.kb0 = static_cast<int>(start - tile_lo);
   it.kb1 = static_cast<int>(end - tile_lo);
+  it.first = g + S;
   it.last = g;
+  it.stride = S;
   if (it.kb0 == 0 && it.kb1 == KB) {
     it.kind = ITEM_FULL;
   } else if (it.kb0 == 0) {
     it.kind = ITEM_OWNER;
-    int last = g;
-    while (last + 1 < G && static_cast<long long>(last + 1) * I / G < tile_hi) ++last;
-    it.last = last;
+    int gl = gi;
+    while (gl + 1 < NG && static_cast<long long>(gl + 1) * I / NG < tile_hi) ++gl;
+    it.last = gl * S + mem;
   } else {
     it.kind = ITEM_PARTIAL;
   }
@@ -184,21 +197,6 @@ __device__ __forceinline__ bool get_item(const Params& p, int g, int G, int idx,
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Adds the stream-K partial tiles of CTAs first..last (row r_loc, columns col..col+W-1).
-template <int W, int BN>
-__device__ __forceinline__ void add_partial_slots(const Params& p, float* v, int first, int last, int r_loc, int col) {
-  for (int q = first; q <= last; ++q) {
-    const float* src = p.partials + (static_cast<size_t>(q) * BM + r_loc) * BN + col;
-#pragma unroll
-    for (int j = 0; j < W; j += 4) {
-      const float4 t = __ldcg(reinterpret_cast<const float4*>(src + j));
-      v[j] += t.x;
-      v[j + 1] += t.y;
-      v[j + 2] += t.z;
-      v[j + 3] += t.w;
-    }
-  }
-}
 
 // Two tile orientations.  TOKEN_ROWS (WROWS = false): the MMA's 128 rows are tokens
 // (rows of A) and its N = BN columns are output features.  WEIGHT_ROWS (WROWS = true): the
@@ -221,6 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* fix_full = reinterpret_cast<uint64_t*>(smem + OFF_BAR + 256);  // [FIX_BUFS] stream-K fix-up slabs
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x, G = gridDim.x;
@@ -237,6 +236,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
+    for (int f = 0; f < FIX_BUFS; ++f) mbar_init(&fix_full[f], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -376,7 +376,179 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r_loc = quarter * 32 + lane;
     const int et = threadIdx.x - 64;  // 0..127 within the epilogue warps
     volatile int* go = abort_flag + 1;   // [2]: per-item decision, written by et == 0
-    int slab = 0;                        // staging slabs issued (double buffer parity)
+    int slab_par = 0;                    // staging slabs issued (double buffer parity)
+    // Stream-K partial slot of CTA `slot` (128 KiB), written straight from registers in a
+    // layout where each warp store covers 512 contiguous bytes: token rows as 32-column
+    // chunks [chunk][8 float4 groups][128 rows], weight rows as 16-token chunks
+    // [chunk][4 float4 groups][128 features].  A chunk (16 / 8 KiB) is contiguous, so the
+    // owner fetches it with one bulk copy.
+    auto write_slot = [&](uint32_t tb, int slot) {
+      float4* base = reinterpret_cast<float4*>(p.partials + static_cast<size_t>(slot) * (BM * 256));
+      if (WROWS) {
+#pragma unroll 1
+        for (int c = 0; c < p.bt; c += 16) {
+          float v[16];
+          tmem_ld16(tb + c, v);
+          float4* dst = base + static_cast<size_t>(c / 16) * 4 * BM + r_loc;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q * BM] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float v[32];
+          tmem_ld32(tb + c, v);
+          float4* dst = base + static_cast<size_t>(c / 32) * 8 * BM + r_loc;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q * BM] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+    };
+    // The owner's fix-up.  An owner item is the last item of its CTA, so the operand ring is
+    // idle: the contributors' partial slots come in through TMA, a column slab at a time,
+    // as many steps ahead as the ring holds (up to FIX_BUFS), and are added, in contributor
+    // order, to the owner's accumulator read from tensor memory; then the tile goes out as
+    // in the whole-tile epilogue.
+    auto owner_fixup = [&](const Item& it, uint32_t tb, int first, int last, int stride) {
+      const int nc = (last - first) / stride + 1;
+      const bool swig = p.mode == EPI_SWIGLU;
+      // token rows: 32-column chunks of 128 rows (16 KiB); weight rows: 16-token chunks of
+      // 128 features (8 KiB); SwiGLU token rows take the gate and the up chunk together
+      const int slab = WROWS ? 16 * BM * 4 : BM * 32 * 4;
+      const int per = nc * ((swig && !WROWS) ? 2 : 1);
+      const int ring_bytes = p.stages * p.stage_bytes;
+      const int steps = WROWS ? (min(p.bt, p.M - (it.tile % p.m_tiles) * p.bt) + 15) / 16 : (swig ? BN / 2 : BN) / 32;
+      const int depth = min(min(steps, FIX_BUFS), ring_bytes / (per * slab));
+      if (depth < 1) {  // the planner keeps contributors below this (uniform)
+        if (et == 0) set_status(p.status, ST_RANGE);
+        return;
+      }
+      auto issue = [&](int k, int buf) {
+        if (et != 0) return;
+        uint8_t* dst = ring + static_cast<size_t>(buf) * per * slab;
+        mbar_arrive_expect_tx(&fix_full[buf], static_cast<uint32_t>(per * slab));
+        int n = 0;
+        for (int q = first; q <= last; q += stride) {
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(p.partials + static_cast<size_t>(q) * (BM * 256));
+          bulk_load(dst + (n++) * slab, src + static_cast<size_t>(k) * slab, slab, &fix_full[buf]);
+          if (!WROWS && swig)
+            bulk_load(dst + (n++) * slab, src + static_cast<size_t>(k + BN / 64) * slab, slab, &fix_full[buf]);
+        }
+      };
+      if (et == 0) fence_proxy_async_global();
+      for (int k = 0; k < depth; ++k) issue(k, k);
+      const int sw = r_loc & 7;
+      for (int k = 0; k < steps; ++k) {
+        const int buf = k % depth;
+        mbar_wait_bounded(&fix_full[buf], static_cast<uint32_t>((k / depth) & 1), abort_flag);
+        const uint8_t* src = ring + static_cast<size_t>(buf) * per * slab;
+        if (WROWS) {
+          const int t0 = (it.tile % p.m_tiles) * p.bt, nt = min(p.bt, p.M - t0), wt = it.tile / p.m_tiles;
+          const int c = k * 16;
+          float v[16];
+          tmem_ld16(tb + c, v);
+          for (int n = 0; n < nc; ++n) {
+            const float4* sl = reinterpret_cast<const float4*>(src + n * slab) + r_loc;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 y = sl[q * BM];
+              v[4 * q] += y.x;
+              v[4 * q + 1] += y.y;
+              v[4 * q + 2] += y.z;
+              v[4 * q + 3] += y.w;
+            }
+          }
+          if (swig) {
+            float* xch = reinterpret_cast<float*>(smem + OFF_STG);  // [64][17]
+            if (quarter >= 2) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) xch[(r_loc - 64) * 17 + j] = v[j];
+            }
+            epi_bar();
+            if (quarter < 2) {
+              bf16* dst = static_cast<bf16*>(p.out) + static_cast<size_t>(t0 + c) * p.ldc + wt * (BM / 2) + r_loc;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c + j < nt)
+                  dst[static_cast<size_t>(j) * p.ldc] = __float2bfloat16_rn(silu_f(v[j]) * xch[r_loc * 17 + j]);
+            }
+          } else {
+            float* sbuf = reinterpret_cast<float*>(smem + OFF_STG) + (slab_par & 1) * (16 * BM);
+            if (et == 0) bulk_wait_read_all_but_1();
+            epi_bar();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sbuf[j * BM + r_loc] = v[j];
+            fence_proxy_async_smem();
+            epi_bar();
+            if (et == 0) {
+              if (p.mode == EPI_ADD_F32)
+                tma_reduce_add_2d(&tmC, sbuf, wt * BM, t0 + c);
+              else
+                tma_store_2d(&tmC, sbuf, wt * BM, t0 + c);
+              bulk_commit();
+            }
+            ++slab_par;
+          }
+        } else {
+          const int m0 = (it.tile % p.m_tiles) * BM, n0 = (it.tile / p.m_tiles) * BN;
+          const int c = k * 32;
+          float v[32];
+          tmem_ld32(tb + c, v);
+          auto add_slab = [&](float* x, const uint8_t* sl) {
+            const float4* row = reinterpret_cast<const float4*>(sl) + r_loc;
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) {
+              const float4 y = row[q8 * BM];
+              x[4 * q8] += y.x;
+              x[4 * q8 + 1] += y.y;
+              x[4 * q8 + 2] += y.z;
+              x[4 * q8 + 3] += y.w;
+            }
+          };
+          if (swig) {
+            float u[32];
+            tmem_ld32(tb + BN / 2 + c, u);
+            for (int n = 0; n < nc; ++n) {
+              add_slab(v, src + (2 * n) * slab);
+              add_slab(u, src + (2 * n + 1) * slab);
+            }
+            const int row = m0 + r_loc;
+            if (row < p.M) {
+              bf16* dst = static_cast<bf16*>(p.out) + static_cast<size_t>(row) * p.ldc + n0 / 2 + c;
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = silu_f(v[j + e]) * u[j + e];
+                store8(dst + j, f);
+              }
+            }
+          } else {
+            for (int n = 0; n < nc; ++n) add_slab(v, src + n * slab);
+            uint8_t* stg = smem + OFF_STG + (slab_par & 1) * 16384;
+            ++slab_par;
+            uint8_t* srow = stg + r_loc * 128;
+            if (et == 0) bulk_wait_read_all_but_1();
+            epi_bar();
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8)
+              *reinterpret_cast<float4*>(srow + ((q8 ^ sw) << 4)) =
+                  make_float4(v[4 * q8], v[4 * q8 + 1], v[4 * q8 + 2], v[4 * q8 + 3]);
+            fence_proxy_async_smem();
+            epi_bar();
+            if (et == 0) {
+              if (p.mode == EPI_ADD_F32)
+                tma_reduce_add_2d(&tmC, stg, n0 + c, m0);
+              else
+                tma_store_2d(&tmC, stg, n0 + c, m0);
+              bulk_commit();
+            }
+          }
+        }
+        epi_bar();  // every thread is done with this step's slabs before they are refilled
+        if (k + depth < steps) issue(k + depth, buf);
+      }
+    };
     Item it;
     for (int idx = 0; get_item(p, g, G, idx, it); ++idx) {
       const int b = idx & 1;
@@ -400,26 +572,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int n0 = (it.tile / p.m_tiles) * BN;
       const int row = m0 + r_loc;
       const uint32_t tbase = tmem + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      if (it.kind == ITEM_PARTIAL) {
-        // write the partial accumulator of this tile to this CTA's slot, then publish it
-        float* slot = p.partials + (static_cast<size_t>(g) * BM + r_loc) * BN;
-        const int ncols = WROWS ? ((p.bt + 31) & ~31) : BN;
-#pragma unroll 1
-        for (int c = 0; c < ncols; c += 32) {
-          float v[32];
-          tmem_ld32(tbase + c, v);
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) store8(slot + c + j, v + j);
-        }
-        __threadfence();
-        epi_bar();
-        if (et == 0) atomicExch(&p.flags[g], 1);
-      } else {
-        const int first = g + 1, last = it.kind == ITEM_OWNER ? it.last : g;
-        if (it.kind == ITEM_OWNER) {
-          // wait for the later contributors of this tile (bounded), in order
-          if (et == 0) {
-            for (int q = first; q <= last; ++q) {
+      if (it.kind != ITEM_FULL) {
+        // Stream-K: this CTA's accumulator -> its partial slot; the owner of the tile adds
+        // the slots to its own accumulator in a fixed order.
+        if (it.kind == ITEM_PARTIAL) {
+          write_slot(tbase, g);
+          __threadfence();  // every thread's slot stores before the flag
+          epi_bar();
+          if (et == 0) atomicExch(&p.flags[g], 1);
+        } else {
+          const int first = it.first, last = it.last, stride = it.stride;
+          if (et == 0) {  // the later contributors, in order (bounded)
+            for (int q = first; q <= last; q += stride) {
               const uint64_t t0 = global_ns();
               while (atomicAdd(&p.flags[q], 0) == 0) {
                 if (global_ns() - t0 > 2000000000ull || *abort_flag) {
@@ -431,8 +595,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             __threadfence();
           }
           epi_bar();
+          owner_fixup(it, tbase, first, last, stride);
+          if (et == 0)
+            for (int q = first; q <= last; q += stride) atomicExch(&p.flags[q], 0);
         }
-        auto add_partials = [&](float* v, int col) { add_partial_slots<32, BN>(p, v, first, last, r_loc, col); };
+      } else {
         if (WROWS) {
           // lanes = output features, columns = the tile's tokens t0 .. t0 + nt - 1
           const int t0 = (it.tile % p.m_tiles) * p.bt;
@@ -448,7 +615,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int c = 0; c < nt; c += 16) {
               float v[16];
               tmem_ld16(tbase + c, v);
-              add_partial_slots<16, BN>(p, v, first, last, r_loc, c);
               if (quarter >= 2) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) xch[(r_loc - 64) * 17 + j] = v[j];
@@ -469,11 +635,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int f0 = wt * BM;
             float* stg = reinterpret_cast<float*>(smem + OFF_STG);
 #pragma unroll 1
-            for (int c = 0; c < nt; c += 16, ++slab) {
+            for (int c = 0; c < nt; c += 16, ++slab_par) {
               float v[16];
               tmem_ld16(tbase + c, v);
-              add_partial_slots<16, BN>(p, v, first, last, r_loc, c);
-              float* sbuf = stg + (slab & 1) * (16 * BM);
+              float* sbuf = stg + (slab_par & 1) * (16 * BM);
               if (et == 0) bulk_wait_read_all_but_1();  // the store from this buffer two slabs ago
               epi_bar();
 #pragma unroll
@@ -492,16 +657,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else if (p.mode != EPI_SWIGLU) {
           // stage a 128-row x 32-column slab in shared memory (128-byte swizzle: 16-byte
           // chunk q of row r at chunk q ^ (r & 7), conflict-free), then one thread stores
-          // it; the staging buffer is reused once the previous store has read it
-          uint8_t* stg = smem + OFF_STG;
-          uint8_t* srow = stg + r_loc * 128;
+          // it; two staging buffers, each reused once its previous store has read it
           const int sw = r_loc & 7;
 #pragma unroll 1
-          for (int c = 0; c < BN; c += 32) {
+          for (int c = 0; c < BN; c += 32, ++slab_par) {
             float v[32];
             tmem_ld32(tbase + c, v);
-            add_partials(v, c);
-            if (et == 0) bulk_wait_read_all();
+            uint8_t* stg = smem + OFF_STG + (slab_par & 1) * 16384;
+            uint8_t* srow = stg + r_loc * 128;
+            if (et == 0) bulk_wait_read_all_but_1();
             epi_bar();
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -524,8 +688,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             float gv[32], uv[32];
             tmem_ld32(tbase + c, gv);
             tmem_ld32(tbase + BN / 2 + c, uv);
-            add_partials(gv, c);
-            add_partials(uv, BN / 2 + c);
             if (row < p.M) {
               bf16* dst = out + static_cast<size_t>(row) * p.ldc + n0 / 2 + c;
 #pragma unroll
@@ -537,11 +699,6 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           }
-        }
-        if (it.kind == ITEM_OWNER) {
-          epi_bar();  // every thread has read the partials
-          if (et == 0)
-            for (int q = first; q <= last; ++q) atomicExch(&p.flags[q], 0);
         }
       }
       // accumulator b may be overwritten once every epilogue warp has read it
@@ -651,7 +808,7 @@ static int sm_count() {
   return n;
 }
 
-// Scratch that lets every shape use its preferred schedule: the flags plus one 128 x 256
+// Scratch that lets every shape use its preferred schedule: the flags plus one 128 KiB
 // fp32 partial slot per SM.
 size_t gemm_scratch_bytes() {
   return tc::FLAG_BYTES + static_cast<size_t>(std::min(sm_count(), tc::MAX_CTAS)) * tc::BM * 256 * sizeof(float);
@@ -672,6 +829,7 @@ struct GemmPlan {
   int grid;
   int dp_tiles;
   long long sk_iters;
+  int sk_group;         // CTAs per stream-K group (1: plain stream-K)
   size_t scratch_used;  // bytes of scratch the stream-K split touches (0: data-parallel)
 };
 
@@ -690,7 +848,7 @@ struct GemmPlan {
 static double kblock_us(int n_cols) { return std::max(0.336 * n_cols / 256.0, 0.31 + 0.02 * n_cols / 256.0); }
 
 struct Sched {
-  int grid, dp_tiles;
+  int grid, dp_tiles, sk_group;
   long long sk_iters;
   size_t scratch;
   double us;
@@ -704,13 +862,14 @@ static Sched schedule(int tok_tiles, int w_tiles, int kb, double kb_us, double w
   const int tiles = tok_tiles * w_tiles;
   r.grid = std::min(sms, tiles);
   r.dp_tiles = tiles;
+  r.sk_group = 1;
   r.sk_iters = 0;
   r.scratch = 0;
   r.us = ((tiles + sms - 1) / sms) * kb * kb_us;
   if (2 * tiles <= sms) {
     const long long iters = static_cast<long long>(tiles) * kb;
-    // at most ~8 CTAs share one tile, one partial slot per CTA, at least 8 k-blocks each
-    const int g_sk = static_cast<int>(std::min<long long>(std::min(sms, 8 * tiles), slots));
+    // at most ~4 CTAs share one tile, one partial slot per CTA, at least 8 k-blocks each
+    const int g_sk = static_cast<int>(std::min<long long>(std::min(sms, 4 * tiles), slots));
     if (g_sk >= 2 * tiles && iters >= 8LL * g_sk) {
       r.grid = g_sk;
       r.dp_tiles = 0;
@@ -718,6 +877,29 @@ static Sched schedule(int tok_tiles, int w_tiles, int kb, double kb_us, double w
       r.scratch = tc::FLAG_BYTES + static_cast<size_t>(g_sk) * tc::BM * 256 * sizeof(float);
       // (+0.5 us per extra token tile: their CTAs no longer share the weight stream)
       r.us = std::max(((iters + g_sk - 1) / g_sk) * kb_us, weight_bytes * tok_tiles / 6.5e6) + 0.5 * (tok_tiles - 1);
+    }
+  }
+  // Grouped stream-K: groups of tok_tiles CTAs divide the (weight tile, k-block) iterations
+  // evenly; the members of a group take the token tiles of the same weight tile and k-range
+  // together, so weights are still streamed once, and every SM gets the same number of
+  // k-blocks (a few hundred tokens otherwise leave SMs idle or a wave ragged).  At most 4
+  // groups share one weight tile; +8 us for writing and summing the split tiles (measured
+  // on GB300 with one owner per tile: ~3 us to write a partial, ~6 us for the owner's
+  // eight 32-column steps), so it only pays off on long k ranges.
+  if (tok_tiles >= 2) {
+    const long long iters = static_cast<long long>(w_tiles) * kb;
+    const int ng = static_cast<int>(
+        std::min<long long>(std::min<long long>(sms / tok_tiles, slots / tok_tiles), 4LL * w_tiles));
+    if (ng >= 2 && iters >= 8LL * ng) {
+      const double us = ((iters + ng - 1) / ng) * kb_us + 8.0;
+      if (us < 0.9 * r.us) {
+        r.grid = ng * tok_tiles;
+        r.dp_tiles = 0;
+        r.sk_group = tok_tiles;
+        r.sk_iters = iters;
+        r.scratch = tc::FLAG_BYTES + static_cast<size_t>(r.grid) * tc::BM * 256 * sizeof(float);
+        r.us = us;
+      }
     }
   }
   return r;
@@ -766,6 +948,7 @@ static GemmPlan plan_gemm(int M, int N, int K, int split0, int split1, long long
   g.grid = c.grid;
   g.dp_tiles = c.dp_tiles;
   g.sk_iters = c.sk_iters;
+  g.sk_group = c.sk_group;
   g.scratch_used = c.scratch;
   return g;
 }
@@ -785,6 +968,7 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
   p.tiles = g.tiles;
   p.dp_tiles = g.dp_tiles;
   p.sk_iters = g.sk_iters;
+  p.sk_group = g.sk_group;
   p.bt = g.bt;
   p.stage_bytes = tc::A_STAGE + (WROWS ? g.bt : BN) * tc::BK * 2;
   p.stages = std::min(tc::MAX_STAGES, tc::RING_BYTES / p.stage_bytes);

@@ -23,9 +23,9 @@ def _build():
     built()
 
 
-# (M, N, K, epilogue): stream-K splits over 32 CTAs (4 output tiles), which fit the
+# (M, N, K, epilogue): stream-K splits over 16 CTAs (4 output tiles), which fit the
 # built-in array, and a data-parallel shape that needs no scratch at all
-SHAPES = [(64, 512, 28672, 1), (48, 512, 14336, 0), (64, 512, 8192, 2), (535, 4096, 4096, 1)]
+SHAPES = [(64, 512, 28672, 1), (48, 512, 14336, 0), (64, 512, 8192, 2), (1024, 4096, 4096, 1)]
 
 
 @pytest.mark.parametrize("M,N,K,epi", SHAPES)
