@@ -164,6 +164,7 @@ def run_ours(args, rank, world):
     from rag_non_prefix_gb300 import build as cbbuild
 
     cbbuild.build()
+    cb.cb_set_launch_overlap(args.launch_overlap)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     spec = hz.workload(args.workload)
@@ -359,7 +360,7 @@ def run_ours(args, rank, world):
                                f"({spec.n_cached(0)} cached); r={ratio} {args.schedule or spec.schedule}",
                    "ratio_schedule": [round(x, 4) for x in ratios], "tokens_per_step": T,
                    "l2": "512 MiB buffer written between timed steps; weights 14+ GB > L2",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "launch_overlap": bool(args.launch_overlap)},
         "ttft_ms": {"blend": round(blend_mean, 4), "full_prefill": round(full_mean, 4),
                     "blend_median": round(statistics.median(blend_ms), 4),
                     "full_median": round(statistics.median(full_ms), 4)},
@@ -506,6 +507,8 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="also time r in {0, 5, 10, 15, 20, 50, 100} %%")
     ap.add_argument("--staged", default=None, action=argparse.BooleanOptionalAction,
                     help="cached KV in pinned host memory, staged per layer (default: on for llama7b)")
+    ap.add_argument("--launch-overlap", default=True, action=argparse.BooleanOptionalAction,
+                    help="programmatic dependent launch of the layer kernels (default: on)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))

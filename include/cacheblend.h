@@ -175,6 +175,14 @@ size_t cb_gemm_scratch_size(void);
  * values: CB_ERR_INVALID_ARG. */
 cb_status cb_gemm_set_orientation(int orientation);
 
+/* Programmatic dependent launch of the blended-prefill kernels, process-wide (default
+ * 1): each kernel of a layer may start while the previous one drains, running the part
+ * of its prologue that touches only its own on-chip memory (barriers, tensor-memory
+ * allocation, tensor-map prefetch) before it waits for the previous kernel's results.
+ * 0 launches every kernel after the previous one has completed.  Results are identical
+ * either way. */
+cb_status cb_set_launch_overlap(int enabled);
+
 /* Allocation-free variant of cb_gemm (no counterpart on the pages: an addition for
  * callers that cannot allocate device memory, e.g. a process held to a fixed device
  * budget after start-up, or code inside a framework that owns every allocation).

@@ -27,7 +27,8 @@ EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_
             "cb_blend_prefill",
             "cb_full_prefill", "cb_blend_begin", "cb_fetch_kv", "cb_synchronize", "cb_prefill_layer",
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
-            "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_set_orientation")
+            "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_set_orientation",
+            "cb_set_launch_overlap")
 PHASES = ("begin", "staged_rot", "norm", "qkv", "rope", "deviation", "select", "scatter", "attention", "oproj",
           "gateup", "down", "finish")
 
@@ -95,6 +96,7 @@ def load_library(path: str = LIB_PATH):
         "cb_gemm": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_size_t, vp]),
         "cb_gemm_scratch_size": (C.c_size_t, []),
         "cb_gemm_set_orientation": (st, [C.c_int]),
+        "cb_set_launch_overlap": (st, [C.c_int]),
         "cb_gemm_noalloc": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp]),
         "cb_gemm_noalloc_error": (C.c_char_p, []),
         "cb_attention": (st, [vp, i32p, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp]),
@@ -230,6 +232,11 @@ def cb_gemm_set_orientation(orientation: int) -> None:
     """Process-wide tile orientation of the bf16 GEMMs: 0 by the library's time model,
     1 tokens as tile rows, 2 output features as tile rows (tuning and tests)."""
     _check(load_library().cb_gemm_set_orientation(int(orientation)))
+
+
+def cb_set_launch_overlap(enabled: bool) -> None:
+    """Programmatic dependent launch of the blended-prefill kernels (process-wide, default on)."""
+    _check(load_library().cb_set_launch_overlap(1 if enabled else 0))
 
 
 def cb_gemm_noalloc(A: torch.Tensor, B: torch.Tensor, C_out: torch.Tensor, epilogue: int = 0,

@@ -98,6 +98,8 @@ __host__ __device__ constexpr uint32_t idesc(bool b_mn) {
 //   pv_done[2]        PV_j accumulated into O                      (MMA commit)
 __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_constant__ Args a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  pdl_trigger();
+  pdl_wait();
   if (smem_u32(smem_raw) & 1023u) {  // uniform across the block
     if (threadIdx.x == 0) set_status(a.status, ST_RANGE);
     return;
@@ -546,7 +548,7 @@ static cudaError_t tc_launch(ta::Args& args, int n_tiles, cudaStream_t s) {
   if (n_tiles <= 0) return cudaSuccess;
   args.n_tiles = n_tiles;
   dim3 grid(n_tiles, args.Hkv);
-  ta::attn_tc_kernel<<<grid, ta::THREADS, ta::SMEM, s>>>(args);
+  launch_chain(ta::attn_tc_kernel, grid, dim3(ta::THREADS), ta::SMEM, s, args);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,7 @@
 // Host-resident chunk KV is staged layer by layer on a caller-provided copy stream into
 // the fused cache (cb_fetch_kv) and re-rotated in place just before the layer runs, so
 // loading layer i+1 overlaps recomputing layer i.
+#include <atomic>
 #include <chrono>
 #include <cmath>
 #include <cstdio>
@@ -824,6 +825,12 @@ cb_status finish_impl(cb_ctx* ctx, cudaStream_t s) {
 
 }  // namespace
 
+namespace cb {
+static std::atomic<bool> g_launch_overlap{true};
+bool launch_overlap_enabled() { return g_launch_overlap.load(std::memory_order_relaxed); }
+void set_launch_overlap(bool on) { g_launch_overlap.store(on); }
+}  // namespace cb
+
 // ============================================================================= C ABI
 extern "C" {
 
@@ -1051,6 +1058,11 @@ cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, 
 }
 
 size_t cb_gemm_scratch_size(void) { return gemm_scratch_bytes(); }
+
+cb_status cb_set_launch_overlap(int enabled) {
+  cb::set_launch_overlap(enabled != 0);
+  return CB_OK;
+}
 
 cb_status cb_gemm_set_orientation(int orientation) {
   const bool tile = orientation >= 16 && orientation <= 256 && orientation % 16 == 0;

@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const uint32_t stages = static_cast<uint32_t>(p.stages);
   uint8_t* ring = smem + OFF_RING;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -254,6 +255,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // (everything above touches only this CTA's shared and tensor memory: it overlaps the
+  // previous kernel's tail under programmatic dependent launch)
+  pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -976,7 +980,7 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
   p.partials = scratch ? reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + tc::FLAG_BYTES) : nullptr;
   // request only what the ring uses (+1 KiB to align the base)
   const int smem = tc::OFF_RING + p.stages * p.stage_bytes + 1024;
-  tc::gemm_bf16_tc<BN, WROWS><<<g.grid, tc::THREADS, smem, s>>>(a, b0, b1, b2, c, p);
+  launch_chain(tc::gemm_bf16_tc<BN, WROWS>, dim3(g.grid), dim3(tc::THREADS), smem, s, a, b0, b1, b2, c, p);
   return cudaGetLastError();
 }
 

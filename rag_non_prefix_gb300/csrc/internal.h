@@ -45,6 +45,29 @@ struct AttnTile {
   int pad;
 };
 
+// Launches of the blended-prefill chain go through launch_chain: with programmatic
+// dependent launch enabled (the default; cb_set_launch_overlap), a kernel may start while
+// the previous one drains, and runs its prologue up to its pdl_wait.  Every kernel
+// launched this way calls pdl_wait before it touches memory that earlier kernels write.
+bool launch_overlap_enabled();
+void set_launch_overlap(bool on);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                         Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = launch_overlap_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_embed(const void* embed, const int32_t* ids, int n_rows, int d, int vocab, cb_dtype dt, float* h,
                          int32_t* status, cudaStream_t s);
 cudaError_t launch_rerotate(const RerotSeg* segs, int n_segs, int max_rows, int n_kv_heads, int head_dim,

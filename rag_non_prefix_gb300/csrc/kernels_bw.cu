@@ -17,6 +17,8 @@ static inline int grid_for(long long work, int per_block, int cap = 152 * 16) {
 template <typename T>
 __global__ void embed_kernel(const T* __restrict__ E, const int32_t* __restrict__ ids, int d, int vocab,
                              float* __restrict__ h, int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x;
   int id = ids[row];
   if (id < 0 || id >= vocab) {  // out-of-range token id: flag it and read row 0 instead
@@ -36,9 +38,9 @@ cudaError_t launch_embed(const void* embed, const int32_t* ids, int n_rows, int 
                          int32_t* status, cudaStream_t s) {
   if (n_rows <= 0) return cudaSuccess;
   if (dt == CB_BF16)
-    embed_kernel<bf16><<<n_rows, 128, 0, s>>>(static_cast<const bf16*>(embed), ids, d, vocab, h, status);
+    launch_chain(embed_kernel<bf16>, dim3(n_rows), dim3(128), 0, s, static_cast<const bf16*>(embed), ids, d, vocab, h, status);
   else
-    embed_kernel<float><<<n_rows, 128, 0, s>>>(static_cast<const float*>(embed), ids, d, vocab, h, status);
+    launch_chain(embed_kernel<float>, dim3(n_rows), dim3(128), 0, s, static_cast<const float*>(embed), ids, d, vocab, h, status);
   return cudaGetLastError();
 }
 
@@ -82,6 +84,8 @@ __device__ __forceinline__ void rerotate_item(const T* __restrict__ ks, T* __res
 template <typename T>
 __global__ void rerotate_batched_kernel(const RerotSeg* __restrict__ segs, int n_kv_heads, int head_dim,
                                         const float2* __restrict__ table, int max_pos, int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const RerotSeg sg = segs[blockIdx.y];
   const int kvw = n_kv_heads * head_dim;
   if (sg.delta < 0 || sg.delta >= max_pos) {
@@ -119,9 +123,9 @@ cudaError_t launch_rerotate(const RerotSeg* segs, int n_segs, int max_rows, int 
   const int gx = grid_for(work, 256, 1 << 16);
   dim3 grid(gx, n_segs);
   if (dt == CB_BF16)
-    rerotate_batched_kernel<bf16><<<grid, 256, 0, s>>>(segs, n_kv_heads, head_dim, rope_table, max_pos, status);
+    launch_chain(rerotate_batched_kernel<bf16>, dim3(grid), dim3(256), 0, s, segs, n_kv_heads, head_dim, rope_table, max_pos, status);
   else
-    rerotate_batched_kernel<float><<<grid, 256, 0, s>>>(segs, n_kv_heads, head_dim, rope_table, max_pos, status);
+    launch_chain(rerotate_batched_kernel<float>, dim3(grid), dim3(256), 0, s, segs, n_kv_heads, head_dim, rope_table, max_pos, status);
   return cudaGetLastError();
 }
 
@@ -161,6 +165,8 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
 // are read twice.  Thread t always owns chunks t, t + 256, ... of 8 elements.
 template <typename T, bool IN_REGS>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ h, int d, float eps, T* __restrict__ x) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int CH = 4;
   __shared__ float red[32];
   const size_t row = blockIdx.x;
@@ -213,14 +219,14 @@ cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x
   const bool regs = d <= 256 * 8 * 4;
   if (dt == CB_BF16) {
     if (regs)
-      rmsnorm_kernel<bf16, true><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<bf16*>(x));
+      launch_chain(rmsnorm_kernel<bf16, true>, dim3(n_rows), dim3(256), 0, s, h, d, eps, static_cast<bf16*>(x));
     else
-      rmsnorm_kernel<bf16, false><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<bf16*>(x));
+      launch_chain(rmsnorm_kernel<bf16, false>, dim3(n_rows), dim3(256), 0, s, h, d, eps, static_cast<bf16*>(x));
   } else {
     if (regs)
-      rmsnorm_kernel<float, true><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<float*>(x));
+      launch_chain(rmsnorm_kernel<float, true>, dim3(n_rows), dim3(256), 0, s, h, d, eps, static_cast<float*>(x));
     else
-      rmsnorm_kernel<float, false><<<n_rows, 256, 0, s>>>(h, d, eps, static_cast<float*>(x));
+      launch_chain(rmsnorm_kernel<float, false>, dim3(n_rows), dim3(256), 0, s, h, d, eps, static_cast<float*>(x));
   }
   return cudaGetLastError();
 }
@@ -228,6 +234,8 @@ cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x
 // final norm of selected rows into fp32 (LM-head input)
 __global__ void last_rows_norm_kernel(const float* __restrict__ h, const int32_t* __restrict__ rows, int d, float eps,
                                       float* __restrict__ x) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const float* src = h + static_cast<size_t>(rows[blockIdx.x]) * d;
   float ss = 0.f;
@@ -252,7 +260,7 @@ __global__ void last_rows_norm_kernel(const float* __restrict__ h, const int32_t
 cudaError_t launch_last_rows_norm(const float* h, const int32_t* rows, int n, int d, float eps, float* x_out,
                                   cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  last_rows_norm_kernel<<<n, 256, 0, s>>>(h, rows, d, eps, x_out);
+  launch_chain(last_rows_norm_kernel, dim3(n), dim3(256), 0, s, h, rows, d, eps, x_out);
   return cudaGetLastError();
 }
 
@@ -307,6 +315,8 @@ __global__ void deviation_rows_kernel(const float* __restrict__ qkv, int n_rows,
                                       const int32_t* __restrict__ req, const ReqDev* __restrict__ reqs, int layer,
                                       int q_width, int kvw, int head_dim, int mode, const float2* __restrict__ table,
                                       int max_pos, float* __restrict__ dev, int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const int warps = blockDim.x >> 5;
   const int row = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -370,11 +380,11 @@ cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* p
   if (n_rows <= 0) return cudaSuccess;
   const int blocks = (n_rows + 7) / 8;
   if (dt == CB_BF16)
-    deviation_rows_kernel<bf16><<<blocks, 256, 0, s>>>(qkv, n_rows, pos, req, reqs, layer, n_heads * head_dim,
+    launch_chain(deviation_rows_kernel<bf16>, dim3(blocks), dim3(256), 0, s, qkv, n_rows, pos, req, reqs, layer, n_heads * head_dim,
                                                        n_kv_heads * head_dim, head_dim, mode, rope_table, max_pos,
                                                        dev, status);
   else
-    deviation_rows_kernel<float><<<blocks, 256, 0, s>>>(qkv, n_rows, pos, req, reqs, layer, n_heads * head_dim,
+    launch_chain(deviation_rows_kernel<float>, dim3(blocks), dim3(256), 0, s, qkv, n_rows, pos, req, reqs, layer, n_heads * head_dim,
                                                         n_kv_heads * head_dim, head_dim, mode, rope_table, max_pos,
                                                         dev, status);
   return cudaGetLastError();
@@ -418,6 +428,8 @@ __global__ void post_qkv_kernel(const float* __restrict__ qkv, const int32_t* __
                                 const ReqDev* __restrict__ reqs, int layer, int q_width, int kvw, int head_dim,
                                 const float2* __restrict__ table, int max_pos, T* __restrict__ q_out,
                                 const float* __restrict__ h_in, float* __restrict__ h_out, int d, int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int src = s_src ? s_src[t] : t;
   const int p = s_pos[t];
@@ -471,11 +483,11 @@ cudaError_t launch_post_qkv(const float* qkv, int n_s_rows, const int32_t* s_src
                             const float* h_in, float* h_out, int d, int32_t* status, cudaStream_t s) {
   if (n_s_rows <= 0) return cudaSuccess;
   if (dt == CB_BF16)
-    post_qkv_kernel<bf16><<<n_s_rows, 256, 0, s>>>(qkv, s_src, s_pos, s_req, reqs, layer, n_heads * head_dim,
+    launch_chain(post_qkv_kernel<bf16>, dim3(n_s_rows), dim3(256), 0, s, qkv, s_src, s_pos, s_req, reqs, layer, n_heads * head_dim,
                                                    n_kv_heads * head_dim, head_dim, rope_table, max_pos,
                                                    static_cast<bf16*>(q_out), h_in, h_out, d, status);
   else
-    post_qkv_kernel<float><<<n_s_rows, 256, 0, s>>>(qkv, s_src, s_pos, s_req, reqs, layer, n_heads * head_dim,
+    launch_chain(post_qkv_kernel<float>, dim3(n_s_rows), dim3(256), 0, s, qkv, s_src, s_pos, s_req, reqs, layer, n_heads * head_dim,
                                                     n_kv_heads * head_dim, head_dim, rope_table, max_pos,
                                                     static_cast<float*>(q_out), h_in, h_out, d, status);
   return cudaGetLastError();
@@ -484,6 +496,8 @@ cudaError_t launch_post_qkv(const float* qkv, int n_s_rows, const int32_t* s_src
 // ----------------------------------------------------------------------------- outputs
 __global__ void write_hidden_kernel(const float* __restrict__ h, const int32_t* __restrict__ s_pos, int row0, int d,
                                     float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int t = row0 + blockIdx.x;
   const float* src = h + static_cast<size_t>(t) * d;
   float* dst = out + static_cast<size_t>(s_pos[t]) * d;
@@ -497,7 +511,7 @@ __global__ void write_hidden_kernel(const float* __restrict__ h, const int32_t* 
 cudaError_t launch_write_hidden(const float* h, const int32_t* s_pos, int row0, int n, int d, float* out,
                                 cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  write_hidden_kernel<<<n, 256, 0, s>>>(h, s_pos, row0, d, out);
+  launch_chain(write_hidden_kernel, dim3(n), dim3(256), 0, s, h, s_pos, row0, d, out);
   return cudaGetLastError();
 }
 
@@ -507,6 +521,8 @@ constexpr int LM_MAX_REQ = 16;
 template <typename T>
 __global__ void lm_head_kernel(const float* __restrict__ x, int n_req, int d, const T* __restrict__ w, int vocab,
                                float* __restrict__ logits) {
+  pdl_trigger();
+  pdl_wait();
   const int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (v >= vocab) return;
   const int lane = threadIdx.x & 31;
@@ -543,10 +559,10 @@ cudaError_t launch_lm_head(const float* x, int n_req, int d, const void* w, int 
     const int nr = n_req - r0 < LM_MAX_REQ ? n_req - r0 : LM_MAX_REQ;
     const int blocks = (vocab + 7) / 8;
     if (dt == CB_BF16)
-      lm_head_kernel<bf16><<<blocks, 256, 0, s>>>(x + static_cast<size_t>(r0) * d, nr, d, static_cast<const bf16*>(w),
+      launch_chain(lm_head_kernel<bf16>, dim3(blocks), dim3(256), 0, s, x + static_cast<size_t>(r0) * d, nr, d, static_cast<const bf16*>(w),
                                                   vocab, logits + static_cast<size_t>(r0) * vocab);
     else
-      lm_head_kernel<float><<<blocks, 256, 0, s>>>(x + static_cast<size_t>(r0) * d, nr, d,
+      launch_chain(lm_head_kernel<float>, dim3(blocks), dim3(256), 0, s, x + static_cast<size_t>(r0) * d, nr, d,
                                                    static_cast<const float*>(w), vocab,
                                                    logits + static_cast<size_t>(r0) * vocab);
   }
@@ -556,6 +572,8 @@ cudaError_t launch_lm_head(const float* x, int n_req, int d, const void* w, int 
 // argmax per request; ties go to the lowest token id; NaN logits never win.
 __global__ void argmax_kernel(const float* __restrict__ logits, int vocab, int32_t* const* outs,
                               int32_t* __restrict__ out_dev) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sv[32];
   __shared__ int si[32];
   const float* l = logits + static_cast<size_t>(blockIdx.x) * vocab;
@@ -606,7 +624,7 @@ __global__ void argmax_kernel(const float* __restrict__ logits, int vocab, int32
 cudaError_t launch_argmax(const float* logits, int n_req, int vocab, int32_t* const* outs, int32_t* out_dev,
                           cudaStream_t s) {
   if (n_req <= 0) return cudaSuccess;
-  argmax_kernel<<<n_req, 1024, 0, s>>>(logits, vocab, outs, out_dev);
+  launch_chain(argmax_kernel, dim3(n_req), dim3(1024), 0, s, logits, vocab, outs, out_dev);
   return cudaGetLastError();
 }
 

@@ -184,6 +184,8 @@ __global__ void __launch_bounds__(SEL_THREADS) select_batched_kernel(const float
                                                                      int32_t* __restrict__ s_src,
                                                                      int32_t* __restrict__ s_pos,
                                                                      int32_t* __restrict__ s_req, int32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ SelShared sh;
   const int r = blockIdx.x;
   const PlanEntry pe = plan[r];
@@ -244,7 +246,7 @@ cudaError_t launch_select_batched(const float* dev, const int32_t* r_pos, const 
                                   const int32_t* forced, int n_req, int32_t* s_src, int32_t* s_pos, int32_t* s_req,
                                   int32_t* status, cudaStream_t s) {
   if (n_req <= 0) return cudaSuccess;
-  select_batched_kernel<<<n_req, SEL_THREADS, 0, s>>>(dev, r_pos, plan, reqs, forced, s_src, s_pos, s_req, status);
+  launch_chain(select_batched_kernel, dim3(n_req), dim3(SEL_THREADS), 0, s, dev, r_pos, plan, reqs, forced, s_src, s_pos, s_req, status);
   return cudaGetLastError();
 }
 
