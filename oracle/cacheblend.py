@@ -39,6 +39,10 @@ R7  Fresh K/V of candidates that are not selected are discarded.
 R9  RMSNorm weight 1, eps 1e-5; no biases; untied LM head; no BOS token.
 R14 Selection runs on the fp32-rounded deviations, so the CUDA selection can be
     compared bit for bit on the same fp32 array.
+R17 The cosine deviation is 1 - cos over the concatenated K and V rows; a zero row
+    against a zero row deviates by 0, against a non-zero row by 1.
+R18 Spatial seam repair recomputes the last R tokens of every cached chunk (each
+    ends at a boundary) plus the query, at every layer from layer 0 on.
 
 Parity pins (tests/test_oracle_*.py) tie every function here to something other
 than itself: closed forms, invariants, the pages' printed byte counts, library
@@ -210,14 +214,31 @@ def precompute_chunk(cfg, weights, ids: Sequence[int], storage: str):
 
 # --------------------------------------------------------------------------- HKVD
 def kv_deviation(k_new, v_new, k_fused, v_fused, mode: int = 0) -> np.ndarray:
-    """Squared KV deviation per token (reading R4).
+    """KV deviation per token (readings R4, R17).
 
     [P1] 技術的詳細 / HKVD トークン選定: Delta_KV^(i)[j] = || KV_cached^(i)[j] - KV_full^(i)[j] ||_2.
     The squared norm ranks tokens the same way.  mode 0: K and V together;
     mode 1: K only; mode 2: V only.
+
+    mode 3 is the cosine form of [P2] シーム修復戦略 / CacheBlendRecompute (a per-token
+    cosine-similarity deviation): 1 - cos(a, b) of the concatenated K and V rows a
+    (fresh) and b (fused cache).  Reading R17: two zero rows deviate by 0, a zero row
+    against a non-zero one by 1.
     """
     n = k_new.shape[0]
     width = int(np.prod(k_new.shape[1:]))
+    if mode == 3:
+        a = np.concatenate([np.asarray(k_new, np.float64).reshape(n, width),
+                            np.asarray(v_new, np.float64).reshape(n, width)], axis=1)
+        b = np.concatenate([np.asarray(k_fused, np.float64).reshape(n, width),
+                            np.asarray(v_fused, np.float64).reshape(n, width)], axis=1)
+        ab = np.sum(a * b, axis=1)
+        aa = np.sum(a * a, axis=1)
+        bb = np.sum(b * b, axis=1)
+        out = np.where((aa == 0) & (bb == 0), 0.0, 1.0)
+        both = (aa > 0) & (bb > 0)
+        out[both] = 1.0 - ab[both] / np.sqrt(aa[both] * bb[both])
+        return out
     dk = (np.asarray(k_new, np.float64) - np.asarray(k_fused, np.float64)).reshape(n, width)
     dv = (np.asarray(v_new, np.float64) - np.asarray(v_fused, np.float64)).reshape(n, width)
     sk = np.sum(dk * dk, axis=1)
@@ -389,6 +410,56 @@ def full_reuse(cfg, weights, segments, chunk_caches, storage: str = "f64"):
         attn = causal_attention(q, Q, Kf[i], Vf[i])
         h = output_and_mlp(cfg, W, h, attn)
     return {"hidden": h, "rows": Q, "first_token": first_token(cfg, weights, h[-1])}
+
+
+def seam_positions(segments, seam_tokens: int) -> np.ndarray:
+    """Tokens that spatial seam repair recomputes (reading R18).
+
+    [P2] シーム修復戦略 / SelectiveRecompute: the R tokens just before each chunk
+    boundary are encoded again with the whole context.  Every cached segment ends at a
+    boundary (with the next chunk, or with the query after the last one), so these are
+    the last min(R, n_c) tokens of every cached chunk c, in prompt positions, ascending.
+    """
+    offs, _, _ = _layout(segments)
+    out = []
+    for seg, off in zip(segments, offs):
+        if seg.chunk < 0:
+            continue
+        n = len(seg.ids)
+        r = min(int(seam_tokens), n)
+        out.extend(range(off + n - r, off + n))
+    return np.array(sorted(out), dtype=np.int64)
+
+
+def fixed_set_prefill(cfg, weights, segments, chunk_caches, S, storage: str = "f64"):
+    """Prefill over re-rotated chunk caches that recomputes one fixed token set S at every
+    layer, layer 0 included (no deviation is measured, so no layer needs other tokens).
+
+    Per layer: q, k, v of S; fresh K/V of S overwrite the fused cache; S attends causally
+    over the whole fused cache; output projection and MLP for S.
+    """
+    offs, ids, cached = _layout(segments)
+    N = len(ids)
+    Kf, Vf = init_fused_cache(cfg, segments, chunk_caches, storage)
+    S = np.asarray(S, dtype=np.int64)
+    h = weights.embed(ids[S]).astype(np.float64)
+    for i in range(cfg.n_layers):
+        W = weights.layer(i)
+        q, k, v = project_qkv(cfg, W, h, S)
+        Kf[i][S] = round_storage(k, storage)
+        Vf[i][S] = round_storage(v, storage)
+        attn = causal_attention(q, S, Kf[i], Vf[i])
+        h = output_and_mlp(cfg, W, h, attn)
+    return {"hidden": h, "rows": S, "k": Kf, "v": Vf, "first_token": first_token(cfg, weights, h[-1])}
+
+
+def seam_repair_prefill(cfg, weights, segments, chunk_caches, seam_tokens: int, storage: str = "f64"):
+    """Spatial seam repair ([P2] SelectiveRecompute): the query and the R tokens before every
+    chunk boundary are recomputed at every layer; all other tokens keep their re-rotated
+    cached K/V."""
+    offs, ids, cached = _layout(segments)
+    S = np.union1d(seam_positions(segments, seam_tokens), np.nonzero(~cached)[0]).astype(np.int64)
+    return fixed_set_prefill(cfg, weights, segments, chunk_caches, S, storage)
 
 
 def precompute_all(cfg, weights, spec, storage: str, chunk_indices=None):

@@ -64,6 +64,24 @@ def _mlp_no_residual(cfg, W, h, attn):
     return (ocb.silu(x @ W["wgate"].T) * (x @ W["wup"].T)) @ W["wdown"].T
 
 
+def _cosine_k_only(k_new, v_new, k_fused, v_fused, mode=0):
+    if mode != 3:
+        return _orig_dev(k_new, v_new, k_fused, v_fused, mode)
+    z = np.zeros_like(np.asarray(v_new, np.float64))
+    return _orig_dev(k_new, z, k_fused, z, 3)
+
+
+def _seam_after_boundary(segments, seam_tokens):
+    # the first R tokens after each chunk start instead of the last R before its end
+    out, off = [], 0
+    for seg in segments:
+        n = len(seg.ids)
+        if seg.chunk >= 0:
+            out.extend(range(off, off + min(int(seam_tokens), n)))
+        off += n
+    return np.array(sorted(out), dtype=np.int64)
+
+
 def _rms_no_eps_mean(x, eps):
     x = np.asarray(x, dtype=np.float64)
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
@@ -78,6 +96,8 @@ MUTATIONS = [
     ("select_hkvd", _select_ties_high_index, [pins.test_select_exhaustive_small_with_ties]),
     ("output_and_mlp", _mlp_no_residual, [lambda: pins.test_full_prefill_matches_torch_library_decoder(pins.TINY)]),
     ("rms_norm", _rms_no_eps_mean, [pins.test_rms_norm_properties]),
+    ("kv_deviation", _cosine_k_only, [pins.test_cosine_deviation_closed_forms]),
+    ("seam_positions", _seam_after_boundary, [pins.test_seam_positions_hand_examples]),
 ]
 
 

@@ -373,6 +373,81 @@ def test_deviation_closed_forms():
     assert np.all(orc.kv_deviation(kn, vn, kn, vn) == 0)
 
 
+def test_cosine_deviation_closed_forms():
+    """mode 3 = 1 - cos of the concatenated K and V rows: 0 for a positive multiple, 2 for
+    the negated row, 1 for an orthogonal one, scale-free, and on unit rows half the
+    squared L2 deviation of mode 0 (||a - b||^2 = 2 (1 - cos))."""
+    rng = _rng(15)
+    kn, vn, kf, vf = (rng.standard_normal((9, 2, 8)) for _ in range(4))
+    assert np.max(np.abs(orc.kv_deviation(3.0 * kf, 3.0 * vf, kf, vf, 3))) < 1e-14
+    assert np.allclose(orc.kv_deviation(-kf, -vf, kf, vf, 3), 2.0, rtol=0, atol=1e-14)
+    ek = np.zeros((2, 1, 4))
+    ev = np.zeros((2, 1, 4))
+    ek[0, 0, 0] = 1.0  # row 0: a = e0 (K part), b = e1 (V part): orthogonal
+    fk = np.zeros((2, 1, 4))
+    fv = np.zeros((2, 1, 4))
+    fv[0, 0, 1] = 2.0
+    ek[1, 0, 2], fk[1, 0, 2], fv[1, 0, 3] = 1.0, 1.0, 1.0  # row 1: cos = 1/sqrt(2)
+    assert np.allclose(orc.kv_deviation(ek, ev, fk, fv, 3), [1.0, 1.0 - 1.0 / math.sqrt(2.0)], rtol=0, atol=1e-15)
+    assert np.allclose(orc.kv_deviation(5.0 * kn, 5.0 * vn, 0.25 * kf, 0.25 * vf, 3),
+                       orc.kv_deviation(kn, vn, kf, vf, 3), rtol=1e-12)
+
+    def unit(k, v):
+        nrm = np.sqrt(np.sum(k.reshape(9, -1) ** 2, 1) + np.sum(v.reshape(9, -1) ** 2, 1))[:, None, None]
+        return k / nrm, v / nrm
+
+    ku, vu = unit(kn, vn)
+    kfu, vfu = unit(kf, vf)
+    assert np.allclose(orc.kv_deviation(ku, vu, kfu, vfu, 0), 2.0 * orc.kv_deviation(ku, vu, kfu, vfu, 3),
+                       rtol=1e-12)
+    z = np.zeros((2, 1, 4))
+    assert list(orc.kv_deviation(z, z, z, z, 3)) == [0.0, 0.0]
+    assert list(orc.kv_deviation(z, z, fk, fv, 3)) == [1.0, 1.0]
+
+
+def _seam_layout(lens, qlen):
+    segs = [hz.Segment(np.arange(n) % 7, i) for i, n in enumerate(lens)]
+    segs.append(hz.Segment(np.arange(qlen) % 5, -1))
+    return segs
+
+
+def test_seam_positions_hand_examples():
+    """[P2] SelectiveRecompute: the R tokens just before each chunk boundary; chunks of 5, 3
+    and 7 tokens sit at 0-4, 5-7 and 8-14, the query at 15-18."""
+    segs = _seam_layout([5, 3, 7], 4)
+    assert list(orc.seam_positions(segs, 2)) == [3, 4, 6, 7, 13, 14]
+    assert list(orc.seam_positions(segs, 4)) == [1, 2, 3, 4, 5, 6, 7, 11, 12, 13, 14]
+    assert list(orc.seam_positions(segs, 0)) == []
+    assert list(orc.seam_positions(segs, 99)) == list(range(15))
+    assert list(orc.seam_positions(_seam_layout([6], 2), 1)) == [5]
+
+
+def test_seam_repair_limits():
+    """R = 0 is full KV reuse; R covering every chunk recomputes everything (a full prefill);
+    a lone chunk at offset 0 is an exact prefix cache, so any R gives the full prefill."""
+    W = hz.HostWeights(TINY, 28)
+    segs, chunks = _prompt(TINY, 28, [9, 14, 7], 6)
+    caches = _caches(TINY, W, chunks, "f64")
+    s0 = orc.seam_repair_prefill(TINY, W, segs, caches, 0, "f64")
+    u = orc.full_reuse(TINY, W, segs, caches, "f64")
+    assert np.array_equal(s0["rows"], u["rows"])
+    assert np.max(np.abs(s0["hidden"] - u["hidden"])) < 1e-11
+    f = orc.full_prefill(TINY, W, _concat(segs), "f64")
+    s_all = orc.seam_repair_prefill(TINY, W, segs, caches, 14, "f64")
+    assert np.array_equal(s_all["rows"], np.arange(36))
+    assert np.max(np.abs(s_all["hidden"] - f["hidden"])) < 1e-11
+    assert np.max(np.abs(s_all["k"] - f["k"])) < 1e-11 and s_all["first_token"] == f["first_token"]
+    s4 = orc.seam_repair_prefill(TINY, W, segs, caches, 4, "f64")
+    assert len(s4["rows"]) == 12 + 6
+    assert np.max(np.abs(s4["hidden"][-6:] - f["hidden"][-6:])) > 1e-6  # still an approximation
+    segs1, chunks1 = _prompt(TINY, 29, [20], 6)
+    caches1 = _caches(TINY, W, chunks1, "f64")
+    f1 = orc.full_prefill(TINY, W, _concat(segs1), "f64")
+    for R in (1, 5):
+        s = orc.seam_repair_prefill(TINY, W, segs1, caches1, R, "f64")
+        assert np.max(np.abs(s["hidden"] - f1["hidden"][s["rows"]])) < 1e-11
+
+
 def test_ratio_schedule_and_k():
     assert orc.ratio_schedule(2, 0.15, "fixed") == [-1.0, 0.15]
     g = orc.ratio_schedule(32, 0.15, "gradual")
