@@ -200,8 +200,8 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # 512 MiB > L2
 
-    def blend_step(rat=None):
-        eng.blend_prefill(reqs, ratios if rat is None else rat, stream=stream, copy_stream=copy_stream)
+    def blend_step(rat=None, **kw):
+        eng.blend_prefill(reqs, ratios if rat is None else rat, stream=stream, copy_stream=copy_stream, **kw)
 
     def full_step():
         for ids in full_ids:
@@ -264,6 +264,19 @@ def run_ours(args, rank, world):
                 blend_step(rat)
             ts = timed(lambda: blend_step(rat), max(3, args.steps // 2), "sweep")
             sweep.append({"ratio": r, "ttft_ms": round(statistics.mean(ts), 4)})
+    # selection variants on the same prompt: cosine deviation (same schedule) and spatial
+    # seam repair (the 16 tokens before every chunk boundary, recomputed from layer 0 on)
+    variants = None
+    if args.variants:
+        variants = {}
+        n_var = max(3, min(args.steps, 5))
+        for tag, kw in (("cosine_deviation", {"dev_mode": 3}), ("seam_repair_r16", {"seam_tokens": 16})):
+            for _ in range(2):
+                blend_step(**kw)
+            ts = timed(lambda: blend_step(**kw), n_var, tag)
+            variants[tag] = {"ttft_ms": round(statistics.mean(ts), 4),
+                             "speedup_vs_full_prefill": round(statistics.mean(full_ms) / statistics.mean(ts), 3)}
+        eng.get_status()
     staging = None
     if staged:
         # T_load: host->device bandwidth of the chunk KV measured on the copy stream
@@ -379,6 +392,7 @@ def run_ours(args, rank, world):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(step_launches * args.steps),
         "sweep": sweep,
+        "variants": variants,
         "staging": staging,
         "clocks": clocks,
     }
@@ -507,6 +521,8 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="also time r in {0, 5, 10, 15, 20, 50, 100} %%")
     ap.add_argument("--staged", default=None, action=argparse.BooleanOptionalAction,
                     help="cached KV in pinned host memory, staged per layer (default: on for llama7b)")
+    ap.add_argument("--variants", default=True, action=argparse.BooleanOptionalAction,
+                    help="also time the cosine-deviation and seam-repair selection variants")
     ap.add_argument("--launch-overlap", default=True, action=argparse.BooleanOptionalAction,
                     help="programmatic dependent launch of the layer kernels (default: on)")
     args = ap.parse_args()

@@ -134,8 +134,9 @@ cb_status cb_rope_rerotate(const void* k_src, void* k_dst, const void* v_src, vo
  * [P1] 技術的詳細 / HKVD トークン選定: Delta_KV^(i)[j] = ||KV_cached^(i)[j] - KV_full^(i)[j]||_2
  * (squared: same ranking).  k_new, v_new: fp32 [n][kv_width] (fresh, after RoPE);
  * k_fus, v_fus: dtype [*][kv_width]; row j is compared with fused row idx[j]
- * (idx NULL: row j).  mode 0 = K and V, 1 = K only, 2 = V only.  dev_out fp32 [n];
- * accumulation in fp32. */
+ * (idx NULL: row j).  mode 0 = K and V, 1 = K only, 2 = V only (squared L2), 3 = 1 - cos
+ * of the concatenated K and V rows ([P2] シーム修復戦略 / CacheBlendRecompute).
+ * dev_out fp32 [n]; accumulation in fp32. */
 cb_status cb_kv_deviation(const float* k_new, const float* v_new, const void* k_fus, const void* v_fus,
                           const int32_t* idx, int n, int kv_width, int mode, cb_dtype dtype, float* dev_out,
                           void* stream);
@@ -216,16 +217,27 @@ cb_status cb_attention(const void* q, const int32_t* q_pos, int m, const void* k
  * "no check: keep the previous layer's set".  Layer 0 always runs on every token.
  * At a check layer k = ceil(r * Nc - 1e-9) cached tokens are kept (clamped to the
  * candidates that exist); query tokens are always kept.
- * dev_mode: 0 = K and V, 1 = K only, 2 = V only.
+ * dev_mode: 0 = squared L2 of K and V, 1 = K only, 2 = V only, 3 = 1 - cos of the
+ * concatenated K and V rows (the cosine deviation of [P2] シーム修復戦略 /
+ * CacheBlendRecompute; a zero row against a zero row gives 0, against a non-zero one 1).
  * forced_sel_host: NULL, or a host array [n_layers] of host int32 arrays: at a
  * check layer with a non-NULL entry the given sets replace the top-k (used to
  * separate numerics from selection).  Each entry lists, request after request,
- * a count c followed by c ascending cached token indices of that request. */
+ * a count c followed by c ascending cached token indices of that request.
+ * select_mode: CB_SELECT_HKVD (deviation-guided, above) or CB_SELECT_SEAM: spatial
+ * seam repair ([P2] シーム修復戦略 / SelectiveRecompute): the last seam_tokens tokens
+ * of every cached chunk (each ends at a chunk boundary) and the query are recomputed
+ * at every layer, layer 0 included; nothing else is recomputed and no deviation is
+ * measured (layer_ratio_host, dev_mode and forced_sel_host are ignored; the ratio
+ * array may be NULL). */
+enum { CB_SELECT_HKVD = 0, CB_SELECT_SEAM = 1 };
 typedef struct {
   int n_layers;
   const double* layer_ratio_host;
   int dev_mode;
   const int32_t* const* forced_sel_host;
+  int select_mode;
+  int seam_tokens;
 } cb_blend_params;
 
 /* One prompt: cached chunks (by registry id) in order, then the query tokens

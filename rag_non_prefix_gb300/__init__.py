@@ -51,9 +51,13 @@ class Weights(C.Structure):
         (n, C.POINTER(C.c_void_p)) for n in ("wq", "wk", "wv", "wo", "wgate", "wup", "wdown")]
 
 
+CB_SELECT_HKVD, CB_SELECT_SEAM = 0, 1
+
+
 class BlendParams(C.Structure):
     _fields_ = [("n_layers", C.c_int), ("layer_ratio_host", C.POINTER(C.c_double)), ("dev_mode", C.c_int),
-                ("forced_sel_host", C.POINTER(C.POINTER(C.c_int32)))]
+                ("forced_sel_host", C.POINTER(C.POINTER(C.c_int32))), ("select_mode", C.c_int),
+                ("seam_tokens", C.c_int)]
 
 
 class Request(C.Structure):
@@ -361,9 +365,10 @@ class Engine:
                              r["first_token"].data_ptr())
         return arr, keep
 
-    def _c_params(self, ratios, dev_mode=0, forced=None):
+    def _c_params(self, ratios, dev_mode=0, forced=None, seam_tokens=None):
+        """``seam_tokens`` (an int) selects spatial seam repair instead of the ratio schedule."""
         L = self.cfg.n_layers
-        rat = (C.c_double * L)(*[float(x) for x in ratios])
+        rat = (C.c_double * L)(*[float(x) for x in (ratios if ratios is not None else [-1.0] * L)])
         keep = [rat]
         fptr = None
         if forced is not None:
@@ -379,18 +384,20 @@ class Engine:
                 tbl[layer] = C.cast(a, C.POINTER(C.c_int32))
             keep.append(tbl)
             fptr = C.cast(tbl, C.POINTER(C.POINTER(C.c_int32)))
-        return BlendParams(L, C.cast(rat, C.POINTER(C.c_double)), dev_mode, fptr), keep
+        seam = seam_tokens is not None
+        return BlendParams(L, C.cast(rat, C.POINTER(C.c_double)), dev_mode, fptr,
+                           CB_SELECT_SEAM if seam else CB_SELECT_HKVD, int(seam_tokens) if seam else 0), keep
 
-    def blend_prefill(self, reqs, ratios, dev_mode=0, forced=None, stream=None, copy_stream=None):
+    def blend_prefill(self, reqs, ratios, dev_mode=0, forced=None, stream=None, copy_stream=None, seam_tokens=None):
         arr, k1 = self._c_requests(reqs)
-        params, k2 = self._c_params(ratios, dev_mode, forced)
+        params, k2 = self._c_params(ratios, dev_mode, forced, seam_tokens)
         _check(self.lib.cb_blend_prefill(self.ctx, arr, len(reqs), C.byref(params), _stream(stream),
                                          None if copy_stream is None else _stream(copy_stream)), self.ctx)
         return reqs
 
-    def blend_begin(self, reqs, ratios, dev_mode=0, forced=None, stream=None):
+    def blend_begin(self, reqs, ratios, dev_mode=0, forced=None, stream=None, seam_tokens=None):
         arr, k1 = self._c_requests(reqs)
-        params, k2 = self._c_params(ratios, dev_mode, forced)
+        params, k2 = self._c_params(ratios, dev_mode, forced, seam_tokens)
         _check(self.lib.cb_blend_begin(self.ctx, arr, len(reqs), C.byref(params), _stream(stream)), self.ctx)
 
     def fetch_kv(self, layer: int, copy_stream=None):

@@ -409,8 +409,11 @@ cb_status ensure_pinned(cb_ctx* ctx, size_t bytes) {
 }
 
 // Plans the batch, uploads metadata, gathers embeddings, re-rotates resident chunks.
+// seam_tokens < 0: deviation-guided selection (ratios per layer, layer 0 on every token);
+// seam_tokens >= 0: spatial seam repair, one fixed set (the last seam_tokens tokens of every
+// cached chunk, and the query) recomputed at every layer from layer 0 on, no check layers.
 cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, int dev_mode,
-                     const int32_t* const* forced, cudaStream_t s) {
+                     const int32_t* const* forced, int seam_tokens, cudaStream_t s) {
   const cb_model_cfg& c = ctx->cfg;
   Batch& b = ctx->b;
   if (b.active) return fail(ctx, CB_ERR_STATE, "a batch is already active (finish it first)");
@@ -452,6 +455,25 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
   }
   if (T > ctx->ws_tokens) return fail(ctx, CB_ERR_WORKSPACE, "prompt tokens exceed the workspace");
   b.T = T;
+  const bool seam = seam_tokens >= 0;
+  // layer-0 rows of each request: every token, or (seam repair) the seam tokens and the query
+  std::vector<std::vector<int32_t>> rows0(n_req);
+  int T0 = 0;
+  for (int r = 0; r < n_req; ++r) {
+    const ReqHost& rh = b.reqs[r];
+    std::vector<int32_t>& v = rows0[r];
+    if (seam) {
+      for (const SegHost& sg : rh.segs) {
+        const int keep = std::min(seam_tokens, sg.n);
+        for (int j = sg.n - keep; j < sg.n; ++j) v.push_back(sg.off + j);
+      }
+      for (int j = rh.Nc; j < rh.N; ++j) v.push_back(j);
+    } else {
+      v.resize(rh.N);
+      for (int j = 0; j < rh.N; ++j) v[j] = j;
+    }
+    T0 += static_cast<int>(v.size());
+  }
 
   // ---- per-layer plan (sizes are host-known)
   b.plan.resize(static_cast<size_t>(L) * n_req);
@@ -460,13 +482,12 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
   b.check.assign(L, 0);
   std::vector<int> rN(n_req), rC(n_req);  // rows of R, cached rows of R
   for (int r = 0; r < n_req; ++r) {
-    rN[r] = b.reqs[r].N;
-    rC[r] = b.reqs[r].Nc;
+    rN[r] = static_cast<int>(rows0[r].size());
+    rC[r] = rN[r] - b.reqs[r].n_query;
   }
-  std::vector<std::vector<int32_t>> forced_flat;  // per layer: concatenated forced lists
   std::vector<int32_t> forced_all;
   for (int i = 0; i < L; ++i) {
-    const bool chk = ratios && ratios[i] >= 0.0;
+    const bool chk = !seam && ratios && ratios[i] >= 0.0;
     b.check[i] = chk ? 1 : 0;
     int roff = 0, soff = 0;
     for (int r = 0; r < n_req; ++r) {
@@ -581,18 +602,18 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
 
   // ---- request descriptors, layer-0 rows, last rows, counts, first-token pointers
   std::vector<ReqDev> rd(n_req);
-  std::vector<int32_t> pos0(T), req0(T), lastrows(n_req), counts(static_cast<size_t>(L) * n_req);
+  std::vector<int32_t> pos0(T0), req0(T0), lastrows(n_req), counts(static_cast<size_t>(L) * n_req);
   std::vector<int32_t*> firsts(n_req);
   {
     int at = 0;
     for (int r = 0; r < n_req; ++r) {
       const ReqHost& rh = b.reqs[r];
       rd[r] = ReqDev{rh.fused_k, rh.fused_v, rh.layer_stride, rh.N, rh.Nc};
-      for (int j = 0; j < rh.N; ++j) {
-        pos0[at + j] = j;
+      for (size_t j = 0; j < rows0[r].size(); ++j) {
+        pos0[at + j] = rows0[r][j];
         req0[at + j] = r;
       }
-      at += rh.N;
+      at += static_cast<int>(rows0[r].size());
       const PlanEntry& last = b.plan[static_cast<size_t>(L - 1) * n_req + r];
       lastrows[r] = last.s_off + last.s_n - 1;
       firsts[r] = rh.out_first_token;
@@ -608,7 +629,7 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
   const size_t szForced = align_up(std::max<size_t>(1, forced_all.size()) * 4, 256);
   const size_t szSmall = align_up(lastrows.size() * 4, 256) + align_up(counts.size() * 4, 256) +
                          align_up(firsts.size() * sizeof(void*), 256) + align_up(n_req * 4, 256);
-  const size_t szRows = align_up(T * 4, 256) * 2;
+  const size_t szRows = align_up(T0 * 4, 256) * 2;
   const size_t total = szPlan + szReq + szTiles + szSegs + szForced + szSmall + szRows;
   if (total > ctx->meta_bytes) return fail(ctx, CB_ERR_WORKSPACE, "batch metadata exceeds the workspace");
   cb_status st = ensure_pinned(ctx, total);
@@ -631,28 +652,33 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
   ctx->d_counts = reinterpret_cast<int32_t*>(put(counts.data(), counts.size() * 4, align_up(counts.size() * 4, 256)));
   ctx->d_first_ptrs = reinterpret_cast<int32_t**>(put(firsts.data(), firsts.size() * sizeof(void*), align_up(firsts.size() * sizeof(void*), 256)));
   ctx->d_first = reinterpret_cast<int32_t*>(put(nullptr, 0, align_up(n_req * 4, 256)));
-  int32_t* d_pos0 = reinterpret_cast<int32_t*>(put(pos0.data(), T * 4, align_up(T * 4, 256)));
-  int32_t* d_req0 = reinterpret_cast<int32_t*>(put(req0.data(), T * 4, align_up(T * 4, 256)));
+  int32_t* d_pos0 = reinterpret_cast<int32_t*>(put(pos0.data(), T0 * 4, align_up(T0 * 4, 256)));
+  int32_t* d_req0 = reinterpret_cast<int32_t*>(put(req0.data(), T0 * 4, align_up(T0 * 4, 256)));
   CB_CUDA(ctx, cudaMemcpyAsync(ctx->meta, ctx->pinned, o, cudaMemcpyHostToDevice, s));
   CB_CUDA(ctx, cudaEventRecord(ctx->pinned_ev, s));
   ctx->pinned_pending = true;
-  CB_CUDA(ctx, cudaMemcpyAsync(ctx->pos[0], d_pos0, T * 4, cudaMemcpyDeviceToDevice, s));
-  CB_CUDA(ctx, cudaMemcpyAsync(ctx->req[0], d_req0, T * 4, cudaMemcpyDeviceToDevice, s));
+  CB_CUDA(ctx, cudaMemcpyAsync(ctx->pos[0], d_pos0, T0 * 4, cudaMemcpyDeviceToDevice, s));
+  CB_CUDA(ctx, cudaMemcpyAsync(ctx->req[0], d_req0, T0 * 4, cudaMemcpyDeviceToDevice, s));
 
-  // ---- token ids of every row (chunk ids from the registry, then the query), embeddings
+  // ---- token ids of every layer-0 row (chunk ids from the registry, then the query), embeddings
   {
     int at = 0;
     for (int r = 0; r < n_req; ++r) {
       const ReqHost& rh = b.reqs[r];
-      for (const SegHost& sg : rh.segs)
-        CB_CUDA(ctx, cudaMemcpyAsync(ctx->tok + at + sg.off, sg.chunk->ids, sg.n * 4, cudaMemcpyDeviceToDevice, s));
-      CB_CUDA(ctx, cudaMemcpyAsync(ctx->tok + at + rh.Nc, rh.query_ids, rh.n_query * 4, cudaMemcpyDeviceToDevice, s));
-      at += rh.N;
+      for (const SegHost& sg : rh.segs) {
+        const int keep = seam ? std::min(seam_tokens, sg.n) : sg.n;
+        if (keep > 0)
+          CB_CUDA(ctx, cudaMemcpyAsync(ctx->tok + at, sg.chunk->ids + (sg.n - keep), keep * 4,
+                                       cudaMemcpyDeviceToDevice, s));
+        at += keep;
+      }
+      CB_CUDA(ctx, cudaMemcpyAsync(ctx->tok + at, rh.query_ids, rh.n_query * 4, cudaMemcpyDeviceToDevice, s));
+      at += rh.n_query;
     }
   }
   {
     PhaseScope ps(ctx, CB_PH_BEGIN, s, 1 + (b.resident_segs > 0 ? 1 : 0));
-    CB_CUDA(ctx, launch_embed(ctx->embed, ctx->tok, T, c.d_model, c.vocab, c.dtype, ctx->h[0], ctx->status, s));
+    CB_CUDA(ctx, launch_embed(ctx->embed, ctx->tok, T0, c.d_model, c.vocab, c.dtype, ctx->h[0], ctx->status, s));
     if (b.resident_segs > 0)
       CB_CUDA(ctx, launch_rerotate(ctx->d_segs, b.resident_segs, b.resident_max_rows, c.n_kv_heads, c.head_dim,
                                    ctx->rope, c.max_positions, c.dtype, ctx->status, s));
@@ -1021,7 +1047,7 @@ cb_status cb_kv_deviation(const float* k_new, const float* v_new, const void* k_
   if (!k_new || !v_new || !k_fus || !v_fus || !dev_out) return fail(nullptr, CB_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_fus) || !aligned16(v_fus))
     return fail(nullptr, CB_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
-  if (n < 0 || kv_width < 8 || kv_width % 8 || mode < 0 || mode > 2) return fail(nullptr, CB_ERR_SHAPE, "bad sizes");
+  if (n < 0 || kv_width < 8 || kv_width % 8 || mode < 0 || mode > 3) return fail(nullptr, CB_ERR_SHAPE, "bad sizes");
   if (dtype != CB_F32 && dtype != CB_BF16) return fail(nullptr, CB_ERR_DTYPE, "unknown dtype");
   cudaError_t e = launch_deviation_plain(k_new, v_new, k_fus, v_fus, idx, n, kv_width, mode, dtype, dev_out,
                                          as_stream(stream));
@@ -1118,16 +1144,18 @@ static cb_status build_blend_requests(cb_ctx* ctx, const cb_request* reqs, int n
 
 cb_status cb_blend_begin(cb_ctx* ctx, const cb_request* reqs, int n_req, const cb_blend_params* params, void* stream) {
   if (!ctx || !reqs || !params) return fail(ctx, CB_ERR_INVALID_ARG, "null argument");
-  if (params->n_layers != ctx->cfg.n_layers || !params->layer_ratio_host)
+  if (params->select_mode != CB_SELECT_HKVD && params->select_mode != CB_SELECT_SEAM)
+    return fail(ctx, CB_ERR_INVALID_ARG, "bad select_mode");
+  const bool seam = params->select_mode == CB_SELECT_SEAM;
+  if (params->n_layers != ctx->cfg.n_layers || (!seam && !params->layer_ratio_host))
     return fail(ctx, CB_ERR_INVALID_ARG, "layer_ratio_host must have n_layers entries");
-  if (params->dev_mode < 0 || params->dev_mode > 2) return fail(ctx, CB_ERR_INVALID_ARG, "bad dev_mode");
-  for (int i = 1; i < params->n_layers; ++i) {
-    (void)i;  // any schedule is accepted; non-increasing ratios are the method's intent
-  }
+  if (params->dev_mode < 0 || params->dev_mode > 3) return fail(ctx, CB_ERR_INVALID_ARG, "bad dev_mode");
+  if (seam && params->seam_tokens < 0) return fail(ctx, CB_ERR_INVALID_ARG, "seam_tokens must be >= 0");
   std::vector<InReq> in;
   cb_status st = build_blend_requests(ctx, reqs, n_req, in);
   if (st != CB_OK) return st;
-  return begin_impl(ctx, in, params->layer_ratio_host, params->dev_mode, params->forced_sel_host, as_stream(stream));
+  return begin_impl(ctx, in, seam ? nullptr : params->layer_ratio_host, params->dev_mode,
+                    seam ? nullptr : params->forced_sel_host, seam ? params->seam_tokens : -1, as_stream(stream));
 }
 
 cb_status cb_fetch_kv(cb_ctx* ctx, int layer, void* copy_stream) {
@@ -1213,7 +1241,7 @@ cb_status cb_full_prefill(cb_ctx* ctx, const int32_t* ids, int n, void* k_out, v
   in[0].out_hidden = out_hidden;
   in[0].out_first_token = first_token;
   cudaStream_t s = as_stream(stream);
-  cb_status st = begin_impl(ctx, in, nullptr, 0, nullptr, s);
+  cb_status st = begin_impl(ctx, in, nullptr, 0, nullptr, -1, s);
   if (st != CB_OK) return st;
   for (int i = 0; i < ctx->b.L; ++i) {
     st = layer_impl(ctx, i, s);

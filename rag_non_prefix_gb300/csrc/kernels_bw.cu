@@ -279,32 +279,54 @@ __device__ __forceinline__ void rope8(const float* a, const float* b, const floa
 }
 
 // ----------------------------------------------------------------------------- KV deviation
+// mode 0: squared L2 of [k; v]_fresh - [k; v]_fused;  1: K part only;  2: V part only;
+// 3: 1 - cos([k; v]_fresh, [k; v]_fused) (zero against zero: 0, zero against non-zero: 1).
+// Sums run in fp32: `acc` holds the squared difference (modes 0-2) or the dot product (3),
+// `aa` and `bb` the squared norms of the two rows (mode 3).
+struct DevAcc {
+  float acc = 0.f, aa = 0.f, bb = 0.f;
+  __device__ __forceinline__ void add(float a, float b, bool cosine) {
+    if (cosine) {
+      acc = fmaf(a, b, acc);
+      aa = fmaf(a, a, aa);
+      bb = fmaf(b, b, bb);
+    } else {
+      const float e = a - b;
+      acc = fmaf(e, e, acc);
+    }
+  }
+  // warp-reduced result, valid in every lane
+  __device__ __forceinline__ float finish(bool cosine) {
+    const float s = warp_sum(acc);
+    if (!cosine) return s;
+    const float na = warp_sum(aa), nb = warp_sum(bb);
+    if (na == 0.f && nb == 0.f) return 0.f;
+    if (na == 0.f || nb == 0.f) return 1.f;
+    return 1.f - s / (sqrtf(na) * sqrtf(nb));
+  }
+};
+
 template <typename T>
 __device__ __forceinline__ float dev_row(const float* __restrict__ kn, const float* __restrict__ vn,
                                          const T* __restrict__ kf, const T* __restrict__ vf, int kvw, int mode) {
-  float acc = 0.f;
+  const bool cosine = mode == 3;
+  DevAcc d;
   for (int c = (threadIdx.x & 31) * 8; c < kvw; c += 256) {
     float a[8], b[8];
     if (mode != 2) {
       load8(kn + c, a);
       load8(kf + c, b);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float e = a[j] - b[j];
-        acc += e * e;
-      }
+      for (int j = 0; j < 8; ++j) d.add(a[j], b[j], cosine);
     }
     if (mode != 1) {
       load8(vn + c, a);
       load8(vf + c, b);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float e = a[j] - b[j];
-        acc += e * e;
-      }
+      for (int j = 0; j < 8; ++j) d.add(a[j], b[j], cosine);
     }
   }
-  return warp_sum(acc);
+  return d.finish(cosine);
 }
 
 // One warp per row of R; only cached rows (position < Nc of their request) are candidates.
@@ -339,7 +361,8 @@ __global__ void deviation_rows_kernel(const float* __restrict__ qkv, int n_rows,
   const T* vf = static_cast<const T*>(rq.v) + off;
   const int half = head_dim / 2, cpr = half / 8;
   const float2* cs = table + static_cast<size_t>(p) * half;
-  float acc = 0.f;
+  const bool cosine = mode == 3;
+  DevAcc acc;
   if (mode != 2) {
     for (int w = lane; w < kvw / 16; w += 32) {  // 8 rotation pairs per step
       const int head = w / cpr, j = (w - head * cpr) * 8;
@@ -352,8 +375,8 @@ __global__ void deviation_rows_kernel(const float* __restrict__ qkv, int n_rows,
       load8(kf + o + half, fb);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float x = ra[e] - fa[e], y = rb[e] - fb[e];
-        acc += x * x + y * y;
+        acc.add(ra[e], fa[e], cosine);
+        acc.add(rb[e], fb[e], cosine);
       }
     }
   }
@@ -363,14 +386,11 @@ __global__ void deviation_rows_kernel(const float* __restrict__ qkv, int n_rows,
       load8(vn + c, a);
       load8(vf + c, b);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float x = a[e] - b[e];
-        acc += x * x;
-      }
+      for (int e = 0; e < 8; ++e) acc.add(a[e], b[e], cosine);
     }
   }
-  acc = warp_sum(acc);
-  if (lane == 0) dev[row] = acc;
+  const float r = acc.finish(cosine);
+  if (lane == 0) dev[row] = r;
 }
 
 cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* pos, const int32_t* req,

@@ -60,10 +60,10 @@ class GpuWorkload:
             out.append(self.eng.make_request(chunks, hd.ids_tensor(q.ids)))
         return out
 
-    def blend(self, ratios, forced=None, copy_stream=None, dev_mode=0):
+    def blend(self, ratios, forced=None, copy_stream=None, dev_mode=0, seam_tokens=None):
         reqs = self.requests()
         self.eng.blend_prefill(reqs, ratios, dev_mode=dev_mode, forced=forced,
-                               copy_stream=copy_stream)
+                               copy_stream=copy_stream, seam_tokens=seam_tokens)
         self.eng.get_status()
         torch.cuda.synchronize()
         return reqs
@@ -82,6 +82,10 @@ class OracleWorkload:
     def blend(self, r: int, ratios, force_sel=None, dev_mode=0):
         return orc.blend_prefill(self.cfg, self.W, self.spec.requests[r], self.caches, ratios, self.storage,
                                  dev_mode=dev_mode, force_sel=force_sel)
+
+    def seam(self, r: int, seam_tokens: int):
+        return orc.seam_repair_prefill(self.cfg, self.W, self.spec.requests[r], self.caches, seam_tokens,
+                                       self.storage)
 
     def full(self, r: int):
         ids = np.concatenate([s.ids for s in self.spec.requests[r]])

@@ -54,7 +54,9 @@ def test_struct_layout_matches_c_compiler(tmp_path):
         'printf("%zu %zu %zu %zu %zu\\n", sizeof(cb_model_cfg), offsetof(cb_model_cfg, rope_theta),'
         " offsetof(cb_model_cfg, rms_eps), offsetof(cb_model_cfg, dtype), offsetof(cb_model_cfg, max_positions));\n"
         'printf("%zu %zu %zu\\n", sizeof(cb_request), offsetof(cb_request, n_query), offsetof(cb_request, out_first_token));\n'
-        'printf("%zu %zu %zu\\n", sizeof(cb_blend_params), offsetof(cb_blend_params, dev_mode), offsetof(cb_blend_params, forced_sel_host));\n'
+        'printf("%zu %zu %zu %zu %zu\\n", sizeof(cb_blend_params), offsetof(cb_blend_params, dev_mode),'
+        " offsetof(cb_blend_params, forced_sel_host), offsetof(cb_blend_params, select_mode),"
+        " offsetof(cb_blend_params, seam_tokens));\n"
         'printf("%zu\\n", sizeof(cb_weights));\nreturn 0;}\n')
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
@@ -65,7 +67,8 @@ def test_struct_layout_matches_c_compiler(tmp_path):
     r = cb.Request
     assert lines[1].split() == [str(v) for v in (C.sizeof(r), r.n_query.offset, r.out_first_token.offset)]
     p = cb.BlendParams
-    assert lines[2].split() == [str(v) for v in (C.sizeof(p), p.dev_mode.offset, p.forced_sel_host.offset)]
+    assert lines[2].split() == [str(v) for v in (C.sizeof(p), p.dev_mode.offset, p.forced_sel_host.offset,
+                                                 p.select_mode.offset, p.seam_tokens.offset)]
     assert lines[3].strip() == str(C.sizeof(cb.Weights))
 
 

@@ -140,6 +140,49 @@ def test_mha_bf16_blend_forced(tmp_path):
     assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 2e-2
 
 
+# ----------------------------------------------------------------------------- selection variants
+def test_cosine_deviation_blend(tiny):
+    """dev_mode 3 (cosine): the checked sets overlap the oracle's, and under the oracle's
+    sets the hidden states agree to fp32 rounding."""
+    spec, g, o = tiny
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    ref = o.blend(0, ratios, dev_mode=3)
+    req = g.blend(ratios, dev_mode=3)[0]
+    sets = _sets(req, cfg)
+    for i in range(cfg.n_layers):
+        assert len(sets[i]) == len(ref["sets"][i])
+        assert len(np.intersect1d(sets[i], ref["sets"][i])) / len(ref["sets"][i]) >= 0.97, i
+    l2 = o.blend(0, ratios, dev_mode=0)
+    assert not np.array_equal(l2["sets"][1], ref["sets"][1])  # the mode changes the choice
+    forced = forced_from_oracle(ref, ref["n_cached"], cfg.n_layers, ratios)
+    req = g.blend(ratios, forced=forced, dev_mode=3)[0]
+    assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 1e-4
+
+
+@pytest.mark.parametrize("name,R", [("tiny", 16), ("tiny", 0), ("small_bf16", 16), ("small_bf16", 200)])
+def test_seam_repair_matches_oracle(name, R):
+    """Spatial seam repair: the same fixed set at every layer (layer 0 included) as the
+    oracle's, and hidden states within the dtype's tolerance; R = 0 is full KV reuse and
+    an R above every chunk length recomputes everything."""
+    spec = hz.workload(name)
+    g, o = GpuWorkload(spec), OracleWorkload(spec)
+    cfg = spec.cfg
+    ref = o.seam(0, R)
+    req = g.blend(None, seam_tokens=R)[0]
+    sets = _sets(req, cfg)
+    for i in range(cfg.n_layers):
+        assert np.array_equal(sets[i], ref["rows"]), i
+    assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < tol(cfg)
+    if cfg.dtype == "f32":
+        assert int(req["first_token"].item()) == ref["first_token"]
+    N = spec.n_tokens(0)
+    if R == 0:
+        assert len(ref["rows"]) == N - spec.n_cached(0)
+    if R >= max(len(c) for c in spec.chunks):
+        assert len(ref["rows"]) == N
+
+
 # ----------------------------------------------------------------------------- special cases
 def test_full_recompute_equals_full_prefill_on_gpu(small_bf16):
     """r = 100 %: the blend recomputes everything, which is the GPU's own full prefill."""

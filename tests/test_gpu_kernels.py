@@ -99,6 +99,32 @@ def test_deviation_matches_oracle(dtype, mode):
     assert np.max(np.abs(dev.cpu().numpy() - ref) / ref) < 1e-5
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_cosine_deviation_matches_oracle(dtype):
+    """mode 3 (1 - cos of [k; v]) on rows far apart (dev ~ 1) and close together
+    (dev ~ 1e-3, where fp32 sums lose the most relative accuracy), plus zero rows."""
+    rng = np.random.default_rng(17)
+    n, N, kvw = 300, 520, 1024
+    kf = rng.standard_normal((N, kvw)).astype(np.float32)
+    vf = rng.standard_normal((N, kvw)).astype(np.float32)
+    idx = np.sort(rng.choice(N, n, replace=False)).astype(np.int32)
+    near = np.arange(n) % 2 == 0
+    kn = rng.standard_normal((n, kvw)).astype(np.float32)
+    vn = rng.standard_normal((n, kvw)).astype(np.float32)
+    kn[near] = kf[idx[near]] + 0.05 * kn[near]
+    vn[near] = vf[idx[near]] + 0.05 * vn[near]
+    kn[1], vn[1] = 0.0, 0.0  # a zero fresh row against a non-zero cached one: 1
+    mk = _bf16 if dtype == "bf16" else _f32
+    kft, vft = mk(kf), mk(vf)
+    dev = cb.cb_kv_deviation(_f32(kn), _f32(vn), kft, vft, torch.from_numpy(idx).cuda(), 3)
+    torch.cuda.synchronize()
+    ref = orc.kv_deviation(kn.astype(np.float64), vn.astype(np.float64), to_np(kft)[idx], to_np(vft)[idx], 3)
+    got = dev.cpu().numpy().astype(np.float64)
+    assert got[1] == 1.0 and ref[1] == 1.0
+    assert np.max(np.abs(got - ref)) < 4e-6, np.max(np.abs(got - ref))
+    assert np.max(ref[near]) < 5e-3 and np.min(ref[~near]) > 0.5
+
+
 # ----------------------------------------------------------------------------- selection (bit-exact)
 def _select_case(dev32, cand, k):
     d = torch.from_numpy(dev32).cuda()
