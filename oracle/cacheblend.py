@@ -43,6 +43,13 @@ R17 The cosine deviation is 1 - cos over the concatenated K and V rows; a zero r
     against a zero row deviates by 0, against a non-zero row by 1.
 R18 Spatial seam repair recomputes the last R tokens of every cached chunk (each
     ends at a boundary) plus the query, at every layer from layer 0 on.
+R19 A quantised key group is one channel of one KV head of one layer over all the
+    chunk's tokens ("per channel").
+R20 A quantised value group is one token's row of one KV head of one layer, head_dim
+    channels ("per token").
+R21 Quantisation is asymmetric min/max (as KIVI): scale = (max - min) / (2^b - 1), the
+    minimum kept as the zero point, codes rounded half to even and clamped; a group
+    whose values are all equal gets scale 0 and codes 0.
 
 Parity pins (tests/test_oracle_*.py) tie every function here to something other
 than itself: closed forms, invariants, the pages' printed byte counts, library
@@ -328,7 +335,7 @@ def init_fused_cache(cfg, segments, chunk_caches, storage: str):
         n = len(seg.ids)
         for i in range(cfg.n_layers):
             Kf[i, off:off + n] = round_storage(rerotate_keys(Kc[i], off, cfg.rope_theta), storage)
-            Vf[i, off:off + n] = Vc[i]
+            Vf[i, off:off + n] = round_storage(Vc[i], storage)
     return Kf, Vf
 
 
@@ -468,6 +475,51 @@ def precompute_all(cfg, weights, spec, storage: str, chunk_indices=None):
     if chunk_indices is not None:
         used = [c for c in used if c in chunk_indices]
     return {c: precompute_chunk(cfg, weights, spec.chunks[c], storage) for c in used}
+
+
+# --------------------------------------------------------------------------- KV codec
+def _minmax_codes(x32: np.ndarray, axis, bits: int):
+    """Asymmetric min/max quantisation of float32 values along ``axis`` (reading R21).
+
+    scale = (max - min) / (2**bits - 1), code = clamp(rint((x - min) / scale), 0, 2**bits - 1)
+    (code 0 where scale is 0).  Every step is one float32 operation, so the integer codes
+    are decided in the precision the kernel uses.
+    """
+    levels = np.float32(2 ** bits - 1)
+    mn = np.min(x32, axis=axis, keepdims=True)
+    mx = np.max(x32, axis=axis, keepdims=True)
+    scale = (mx - mn) / levels
+    diff = x32 - mn
+    q = np.zeros_like(x32)
+    np.divide(diff, np.broadcast_to(scale, diff.shape), out=q, where=np.broadcast_to(scale > 0, diff.shape))
+    codes = np.clip(np.rint(q), 0, float(levels)).astype(np.int64)
+    return codes, scale.astype(np.float32), mn.astype(np.float32)
+
+
+def kv_encode(K: np.ndarray, V: np.ndarray, bits: int) -> Dict[str, np.ndarray]:
+    """KIVI-style asymmetric quantisation of a chunk's KV cache ([P2] KV量子化とメモリ管理 /
+    非対称量子化: keys per channel, values per token; int8 or int4).
+
+    K, V: [L, n, Hkv, dh] as the cache stores them.  Readings R19, R20: a key channel
+    (layer, head, channel) is one group over the chunk's n tokens; a value group is one
+    (layer, token, head) row of dh channels.  Returns the integer codes and the float32
+    scale and minimum ("zero") of each group.
+    """
+    if bits not in (4, 8):
+        raise ValueError(bits)
+    K32 = np.asarray(K, dtype=np.float32)
+    V32 = np.asarray(V, dtype=np.float32)
+    kc, ks, kz = _minmax_codes(K32, 1, bits)   # over tokens: [L, 1, Hkv, dh]
+    vc, vs, vz = _minmax_codes(V32, 3, bits)   # over channels: [L, n, Hkv, 1]
+    return {"bits": bits, "k_codes": kc, "k_scale": ks[:, 0], "k_zero": kz[:, 0],
+            "v_codes": vc, "v_scale": vs[..., 0], "v_zero": vz[..., 0]}
+
+
+def kv_decode(enc: Dict[str, np.ndarray]):
+    """Dequantised K, V [L, n, Hkv, dh] in float64: zero + code * scale of each group."""
+    K = enc["k_zero"][:, None].astype(np.float64) + enc["k_codes"] * enc["k_scale"][:, None].astype(np.float64)
+    V = enc["v_zero"][..., None].astype(np.float64) + enc["v_codes"] * enc["v_scale"][..., None].astype(np.float64)
+    return K, V
 
 
 # --------------------------------------------------------------------------- cost model

@@ -82,6 +82,22 @@ def _seam_after_boundary(segments, seam_tokens):
     return np.array(sorted(out), dtype=np.int64)
 
 
+_orig_minmax = ocb._minmax_codes
+
+
+def _codec_keys_per_token(x32, axis, bits):
+    # groups along the other axis: keys per token instead of per channel
+    return _orig_minmax(x32, 3 if axis == 1 else axis, bits)
+
+
+def _codec_round_down(x32, axis, bits):
+    codes, scale, mn = _orig_minmax(x32, axis, bits)
+    q = np.zeros_like(x32)
+    d = x32 - mn
+    np.divide(d, np.broadcast_to(scale, d.shape), out=q, where=np.broadcast_to(scale > 0, d.shape))
+    return np.clip(np.floor(q), 0, 2 ** bits - 1).astype(np.int64), scale, mn
+
+
 def _rms_no_eps_mean(x, eps):
     x = np.asarray(x, dtype=np.float64)
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
@@ -98,6 +114,8 @@ MUTATIONS = [
     ("rms_norm", _rms_no_eps_mean, [pins.test_rms_norm_properties]),
     ("kv_deviation", _cosine_k_only, [pins.test_cosine_deviation_closed_forms]),
     ("seam_positions", _seam_after_boundary, [pins.test_seam_positions_hand_examples]),
+    ("_minmax_codes", _codec_keys_per_token, [pins.test_codec_hand_example_fixes_the_axes]),
+    ("_minmax_codes", _codec_round_down, [lambda: pins.test_codec_error_bound_and_extremes(8)]),
 ]
 
 

@@ -448,6 +448,57 @@ def test_seam_repair_limits():
         assert np.max(np.abs(s["hidden"] - f1["hidden"][s["rows"]])) < 1e-11
 
 
+# ----------------------------------------------------------------------------- KV codec
+def test_codec_hand_example_fixes_the_axes():
+    """Keys are grouped per channel over the tokens, values per token over the channels:
+    tokens x channels [[0, 10], [1, 20], [3, 40]] give key codes 0, 85, 255 down each channel
+    (int8) and value codes 0, 255 along each token."""
+    x = np.array([[0.0, 10.0], [1.0, 20.0], [3.0, 40.0]], dtype=np.float32)[None, :, None, :]  # [1, 3, 1, 2]
+    e8 = orc.kv_encode(x, x, 8)
+    assert e8["k_codes"][0, :, 0, :].tolist() == [[0, 0], [85, 85], [255, 255]]
+    assert e8["v_codes"][0, :, 0, :].tolist() == [[0, 255], [0, 255], [0, 255]]
+    assert e8["k_zero"][0, 0].tolist() == [0.0, 10.0] and e8["v_zero"][0, :, 0].tolist() == [0.0, 1.0, 3.0]
+    assert e8["k_scale"][0, 0].tolist() == [np.float32(3.0) / np.float32(255.0), np.float32(30.0) / np.float32(255.0)]
+    e4 = orc.kv_encode(x, x, 4)
+    assert e4["k_codes"][0, :, 0, :].tolist() == [[0, 0], [5, 5], [15, 15]]
+    assert e4["v_codes"][0, :, 0, :].tolist() == [[0, 15], [0, 15], [0, 15]]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_codec_error_bound_and_extremes(bits):
+    """Round trip within half a step of each group; every group's minimum maps to code 0
+    and its maximum to 2^b - 1."""
+    rng = _rng(31 + bits)
+    K = (rng.standard_normal((2, 37, 3, 16)) * rng.uniform(0.1, 5.0, (1, 1, 3, 16))).astype(np.float32)
+    V = (rng.standard_normal((2, 37, 3, 16)) * rng.uniform(0.1, 5.0, (1, 37, 1, 1))).astype(np.float32)
+    e = orc.kv_encode(K, V, bits)
+    Kh, Vh = orc.kv_decode(e)
+    lv = 2 ** bits - 1
+    assert e["k_scale"].shape == (2, 3, 16) and e["v_scale"].shape == (2, 37, 3)
+    assert np.all(np.abs(K - Kh) <= e["k_scale"][:, None] * 0.5 * (1 + 1e-5))
+    assert np.all(np.abs(V - Vh) <= e["v_scale"][..., None] * 0.5 * (1 + 1e-5))
+    assert np.all(e["k_codes"].min(axis=1) == 0) and np.all(e["k_codes"].max(axis=1) == lv)
+    assert np.all(e["v_codes"].min(axis=3) == 0) and np.all(e["v_codes"].max(axis=3) == lv)
+    # the error really is of the order of a step (the bound is not vacuous)
+    assert np.max(np.abs(K - Kh) / e["k_scale"][:, None]) > 0.4
+
+
+def test_codec_exact_on_grid_and_constant_groups():
+    """Values on a power-of-two grid spanning the levels come back exactly; a constant group
+    has scale 0, codes 0 and decodes exactly."""
+    rng = _rng(33)
+    q = rng.integers(0, 256, (1, 40, 2, 8)).astype(np.float32)
+    q[:, 0], q[:, 1] = 0.0, 255.0  # every channel spans the full range
+    K = (q * np.float32(2.0 ** -4) - np.float32(3.0)).astype(np.float32)
+    e = orc.kv_encode(K, K, 8)
+    assert np.array_equal(orc.kv_decode(e)[0], K.astype(np.float64))
+    C = np.full((1, 5, 2, 8), 1.25, dtype=np.float32)
+    e = orc.kv_encode(C, C, 4)
+    assert np.all(e["k_scale"] == 0) and np.all(e["k_codes"] == 0) and np.all(e["v_codes"] == 0)
+    Kd, Vd = orc.kv_decode(e)
+    assert np.all(Kd == 1.25) and np.all(Vd == 1.25)
+
+
 def test_ratio_schedule_and_k():
     assert orc.ratio_schedule(2, 0.15, "fixed") == [-1.0, 0.15]
     g = orc.ratio_schedule(32, 0.15, "gradual")
