@@ -310,6 +310,33 @@ def run_ours(args, rank, world):
         staging = {"h2d_gbs": round(h2d_gbs, 1), "staged_bytes": total_bytes, "t_load_ms": round(t_load, 3),
                    "t_recompute_ms": round(res_ms, 3), "max_load_recompute_ms": round(max(t_load, res_ms), 3),
                    "ttft_staged_ms": round(statistics.mean(blend_ms), 3)}
+        # the same chunks quantised (KIVI-style int8 / int4) in pinned host memory, staged
+        # through a two-slot ring and decoded + re-rotated per layer on the GPU
+        if args.codec:
+            for bits in (8, 4):
+                slot = 0
+                for c in used:
+                    ids, k, v = chunk_store[c]
+                    blob = cb.cb_kv_encode(k, v, bits)
+                    torch.cuda.synchronize()
+                    hb = blob.cpu().pin_memory()
+                    host_store[("q", bits, c)] = hb
+                    eng.register_chunk_codec(c, ids, hb, bits, on_host=True)
+                for req in spec.requests:
+                    slot = max(slot, sum(cb.cb_codec_layer_bytes(len(s_.ids), cfg.n_kv_heads, cfg.head_dim, bits)
+                                         for s_ in req if s_.chunk >= 0))
+                eng.set_staging(2 * slot)
+                for _ in range(2):
+                    blend_step()
+                ts = timed(blend_step, args.steps, f"codec{bits}")
+                qbytes = sum(host_store[("q", bits, c_)].numel() for req in spec.requests
+                             for c_ in [s_.chunk for s_ in req if s_.chunk >= 0])
+                staging[f"int{bits}"] = {"staged_bytes": qbytes, "t_load_ms": round(qbytes / (h2d_gbs * 1e9) * 1e3, 3),
+                                         "ttft_staged_ms": round(statistics.mean(ts), 3), "staging_slots": 2}
+            eng.get_status()
+            for c in used:
+                ids, kh_, vh_ = host_store[c]
+                eng.register_chunk(c, ids, kh_, vh_, on_host=True)
 
     # end to end through the public API with host buffers: query ids in, first token out
     pinned_q = [r["query_ids"].cpu().pin_memory() for r in reqs]
@@ -386,8 +413,9 @@ def run_ours(args, rank, world):
                      "algorithmic_bytes_per_launch": round(gemm_bytes / max(1, gemm_launches)),
                      "peak_source": f"{peaks['source']} bf16 sustained", "launches": gemm_launches,
                      "flops": sum(fl.values())},
-        "rerotate": {"bytes": rerot_bytes, "ms": phase_ms.get("begin"),
-                     "gbs": round(rerot_bytes / (phase_ms["begin"] * 1e-3) / 1e9, 1) if phase_ms.get("begin") else None},
+        "rerotate": None if staged else {
+            "bytes": rerot_bytes, "ms": phase_ms.get("begin"),
+            "gbs": round(rerot_bytes / (phase_ms["begin"] * 1e-3) / 1e9, 1) if phase_ms.get("begin") else None},
         "e2e": {"value": round(n_total / (e2e_mean * 1e-3), 1), "unit": "tok/s", "ms": round(e2e_mean, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(step_launches * args.steps),
@@ -521,6 +549,8 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="also time r in {0, 5, 10, 15, 20, 50, 100} %%")
     ap.add_argument("--staged", default=None, action=argparse.BooleanOptionalAction,
                     help="cached KV in pinned host memory, staged per layer (default: on for llama7b)")
+    ap.add_argument("--codec", default=True, action=argparse.BooleanOptionalAction,
+                    help="with staged chunks: also time int8 / int4 quantised staging")
     ap.add_argument("--variants", default=True, action=argparse.BooleanOptionalAction,
                     help="also time the cosine-deviation and seam-repair selection variants")
     ap.add_argument("--launch-overlap", default=True, action=argparse.BooleanOptionalAction,

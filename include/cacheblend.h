@@ -118,6 +118,49 @@ cb_status cb_register_chunk(cb_ctx* ctx, uint64_t chunk_id, const int32_t* ids, 
 cb_status cb_unregister_chunk(cb_ctx* ctx, uint64_t chunk_id);
 int cb_registered_chunks(const cb_ctx* ctx);
 
+/* --------------------------------------------------------------------- KV codec
+ * KIVI-style asymmetric quantisation of a chunk's KV cache ([P2] KV量子化とメモリ管理 /
+ * 非対称量子化: keys per channel, values per token, int8 or int4; about 2x / 4x fewer bytes
+ * to keep or to stage).  A key group is one channel of one KV head of one layer over the
+ * chunk's n tokens; a value group is one token's head_dim channels of one KV head.  Per group:
+ * scale = (max - min) / (2^bits - 1), code = clamp(rint((x - min) / scale), 0, 2^bits - 1)
+ * (0 when scale is 0), each step one IEEE float32 operation; decoding gives min + code * scale.
+ *
+ * A quantised chunk ("blob") is n_layers blocks of cb_codec_layer_bytes() bytes each.  With
+ * rows = n * Hkv and code_bytes = rows * head_dim * bits / 8, one block holds, each region
+ * starting at a multiple of 16 bytes (offsets rounded up) and the block padded to 256 bytes:
+ *   key codes   [n][Hkv][head_dim * bits / 8] uint8    at 0
+ *   value codes [n][Hkv][head_dim * bits / 8] uint8    at R16(code_bytes)
+ *   key scale   [Hkv][head_dim] float32                at 2 * R16(code_bytes)
+ *   key min     [Hkv][head_dim] float32                after the key scales (R16)
+ *   value scale [n][Hkv] float32                       after the key minima (R16)
+ *   value min   [n][Hkv] float32                       after the value scales (R16)
+ * int4 packs channel 2j in the low and channel 2j + 1 in the high nibble of byte j.
+ * head_dim must be 64 or 128. */
+size_t cb_codec_layer_bytes(int n_tok, int n_kv_heads, int head_dim, int bits);  /* 0 for bad sizes */
+/* Quantises k, v [n_layers][n_tok][n_kv_heads][head_dim] of dtype into blob (device, 16-byte
+ * aligned, n_layers * cb_codec_layer_bytes() bytes). */
+cb_status cb_kv_encode(const void* k, const void* v, int n_layers, int n_tok, int n_kv_heads, int head_dim,
+                       cb_dtype dtype, int bits, void* blob, void* stream);
+/* Dequantises a blob and re-rotates its keys by delta_pos positions (the rotation of
+ * cb_rope_rerotate) in one pass: k_out, v_out [n_layers][n_tok][n_kv_heads][head_dim] of dtype. */
+cb_status cb_kv_decode(const void* blob, int n_layers, int n_tok, int n_kv_heads, int head_dim, int bits,
+                       int delta_pos, double theta, cb_dtype dtype, void* k_out, void* v_out, void* stream);
+/* Registers a quantised chunk (a blob of cb_kv_encode) under chunk_id; ids as for
+ * cb_register_chunk.  on_host == 0: the blob is in device memory and is decoded straight into
+ * the fused caches when a batch begins.  on_host != 0: the blob is in page-locked host memory;
+ * cb_fetch_kv copies each layer's block into the staging ring (cb_set_staging) and
+ * cb_prefill_layer decodes it from there.  Borrowed, like cb_register_chunk. */
+cb_status cb_register_chunk_codec(cb_ctx* ctx, uint64_t chunk_id, const int32_t* ids, const void* blob, int n,
+                                  int bits, int on_host);
+/* Device buffer (caller-owned, 16-byte aligned) for the staging ring of host-resident quantised
+ * chunks.  A batch uses slots of S = the sum of cb_codec_layer_bytes() over the occurrences of
+ * its host-resident quantised chunks; layer i goes to slot i mod (bytes / S).  A batch that
+ * needs S > bytes fails at cb_blend_begin with CB_ERR_WORKSPACE.  With k slots, cb_fetch_kv of
+ * layer i is accepted only after cb_prefill_layer of layer i - k was enqueued (CB_ERR_STATE
+ * otherwise); cb_blend_prefill orders its calls that way.  NULL / 0 removes the buffer. */
+cb_status cb_set_staging(cb_ctx* ctx, void* buf, size_t bytes);
+
 /* --------------------------------------------------------------------- standalone kernels */
 
 /* RoPE re-rotation of cached keys by delta_pos positions; V is copied.

@@ -28,7 +28,8 @@ EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_
             "cb_full_prefill", "cb_blend_begin", "cb_fetch_kv", "cb_synchronize", "cb_prefill_layer",
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
             "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_set_orientation",
-            "cb_set_launch_overlap")
+            "cb_set_launch_overlap", "cb_codec_layer_bytes", "cb_kv_encode", "cb_kv_decode", "cb_register_chunk_codec",
+            "cb_set_staging")
 PHASES = ("begin", "staged_rot", "norm", "qkv", "rope", "deviation", "select", "scatter", "attention", "oproj",
           "gateup", "down", "finish")
 
@@ -104,6 +105,12 @@ def load_library(path: str = LIB_PATH):
         "cb_gemm_noalloc": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp]),
         "cb_gemm_noalloc_error": (C.c_char_p, []),
         "cb_attention": (st, [vp, i32p, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp]),
+        "cb_codec_layer_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
+        "cb_kv_encode": (st, [vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp]),
+        "cb_kv_decode": (st, [vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_double, C.c_int, vp, vp,
+                              vp]),
+        "cb_register_chunk_codec": (st, [vp, C.c_uint64, i32p, vp, C.c_int, C.c_int, C.c_int]),
+        "cb_set_staging": (st, [vp, vp, C.c_size_t]),
         "cb_blend_prefill": (st, [vp, C.POINTER(Request), C.c_int, C.POINTER(BlendParams), vp, vp]),
         "cb_full_prefill": (st, [vp, i32p, C.c_int, vp, vp, vp, i32p, vp]),
         "cb_blend_begin": (st, [vp, C.POINTER(Request), C.c_int, C.POINTER(BlendParams), vp]),
@@ -268,6 +275,34 @@ def cb_attention(q: torch.Tensor, q_pos: torch.Tensor, k: torch.Tensor, v: torch
     return out
 
 
+def cb_codec_layer_bytes(n_tok: int, n_kv_heads: int, head_dim: int, bits: int) -> int:
+    return int(load_library().cb_codec_layer_bytes(n_tok, n_kv_heads, head_dim, bits))
+
+
+def cb_kv_encode(k: torch.Tensor, v: torch.Tensor, bits: int, blob: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """Quantised chunk (uint8 blob) of k, v [L, n, Hkv, dh]: keys per channel, values per token."""
+    lib = load_library()
+    L, n, hkv, dh = k.shape
+    nbytes = L * cb_codec_layer_bytes(n, hkv, dh, bits)
+    blob = torch.empty(nbytes, dtype=torch.uint8, device=k.device) if blob is None else blob
+    _check(lib.cb_kv_encode(_ptr(k), _ptr(v), L, n, hkv, dh, _dtype_code(k.dtype), int(bits), _ptr(blob),
+                            _stream(stream)))
+    return blob
+
+
+def cb_kv_decode(blob: torch.Tensor, shape, bits: int, delta_pos: int, theta: float, dtype: torch.dtype,
+                 stream=None):
+    """Dequantised k, v [L, n, Hkv, dh] of a blob, keys re-rotated by ``delta_pos`` positions."""
+    lib = load_library()
+    L, n, hkv, dh = shape
+    k = torch.empty(shape, dtype=dtype, device=blob.device)
+    v = torch.empty_like(k)
+    _check(lib.cb_kv_decode(_ptr(blob), L, n, hkv, dh, int(bits), int(delta_pos), float(theta), _dtype_code(dtype),
+                            _ptr(k), _ptr(v), _stream(stream)))
+    return k, v
+
+
 # ----------------------------------------------------------------------------- model / engine
 class Engine:
     """A cb_ctx bound to one model's device weights and a workspace.
@@ -331,6 +366,18 @@ class Engine:
         _check(self.lib.cb_register_chunk(self.ctx, C.c_uint64(chunk_id), _ptr(ids), _ptr(k), _ptr(v), ids.numel(),
                                           int(on_host)), self.ctx)
         self._chunks[chunk_id] = (ids, k, v)
+
+    def register_chunk_codec(self, chunk_id: int, ids: torch.Tensor, blob: torch.Tensor, bits: int,
+                             on_host: bool = False):
+        """Registers a quantised chunk (a blob from cb_kv_encode; pinned host memory if on_host)."""
+        _check(self.lib.cb_register_chunk_codec(self.ctx, C.c_uint64(chunk_id), _ptr(ids), _ptr(blob), ids.numel(),
+                                                int(bits), int(on_host)), self.ctx)
+        self._chunks[chunk_id] = (ids, blob, None)
+
+    def set_staging(self, nbytes: int):
+        """Allocates (caller side) and binds the staging ring for host-resident quantised chunks."""
+        self.staging = torch.empty(max(1, nbytes), dtype=torch.uint8, device=self.device) if nbytes else None
+        _check(self.lib.cb_set_staging(self.ctx, _ptr(self.staging), nbytes if nbytes else 0), self.ctx)
 
     def unregister_chunk(self, chunk_id: int):
         _check(self.lib.cb_unregister_chunk(self.ctx, C.c_uint64(chunk_id)), self.ctx)

@@ -54,6 +54,9 @@ struct ChunkEntry {
   int n = 0;
   int on_host = 0;
   int state = 0;  // 0 empty, 1 live, 2 deleted
+  const uint8_t* blob = nullptr;  // quantised chunk (bits 8 or 4) instead of k / v
+  int bits = 0;
+  size_t layer_bytes = 0;  // bytes of one layer block of the blob
 };
 
 // Open addressing with linear probing, keyed by a 64-bit chunk id (e.g. a text hash).
@@ -153,6 +156,20 @@ struct Batch {
   int next_layer = 0;
   bool has_forced = false;
   int dev_mode = 0;
+  // quantised chunks: resident ones are decoded at begin (all layers); host ones are copied
+  // layer by layer into a ring of staging slots and decoded from there
+  int codec_res_segs = 0, codec_res_max = 0;
+  std::vector<int> codec_host_off, codec_host_n;  // per layer: range of host codec segments
+  int codec_host_max = 0;
+  int n_slots = 0;
+  size_t slot_bytes = 0;
+  struct StageCopy {
+    const uint8_t* src;  // host blob of the chunk (layer 0 block)
+    size_t layer_bytes;
+    size_t slot_off;     // offset of this occurrence inside a slot
+  };
+  std::vector<StageCopy> stage;
+  std::vector<char> slot_freed;  // per layer: the slot this layer used was released (decode enqueued)
   // tcgen05 attention: per request K/V tensor maps, sizes, and per layer the tile range of each request
   std::vector<CUtensorMap> kmaps, vmaps;
   std::vector<int> n_kv, one_layer;
@@ -211,6 +228,10 @@ struct cb_ctx {
   ReqDev* d_reqs = nullptr;
   AttnTile* d_tiles = nullptr;
   RerotSeg* d_segs = nullptr;  // resident segments first, then the host ones per layer
+  CodecSeg* d_csegs = nullptr;  // quantised chunks: resident segments first, then host ones per layer
+  uint8_t* staging = nullptr;   // caller's staging ring for host-resident quantised chunks
+  size_t staging_bytes = 0;
+  std::vector<cudaEvent_t> slot_ev;  // per slot: its last decode was enqueued after this event
   int32_t* d_forced = nullptr;
   int32_t* d_lastrows = nullptr;
   int32_t* d_counts = nullptr;
@@ -353,6 +374,7 @@ WsLayout ws_layout(const cb_model_cfg& c, int T, int R) {
   m += align_up(R * sizeof(ReqDev), 256);
   m += align_up(L * (Tz + R) * sizeof(AttnTile), 256);
   m += align_up(2 * L * (Tz / 1 + R) * sizeof(RerotSeg) / 1, 256);  // segments: at most one per chunk per layer
+  m += 256;                                                          // (the codec segments' own alignment)
   m += align_up(L * Tz * 4, 256);                                  // forced sets
   m += align_up(R * 4 + L * R * 4 + R * sizeof(void*) + R * 4, 256);
   m += align_up(2 * Tz * 4, 256);  // layer-0 positions and requests
@@ -573,7 +595,7 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
     for (int r = 0; r < n_req; ++r) {
       const ReqHost& rh = b.reqs[r];
       for (const SegHost& sg : rh.segs) {
-        if (!sg.chunk || sg.chunk->on_host) continue;
+        if (!sg.chunk || sg.chunk->on_host || sg.chunk->bits) continue;
         const size_t so = static_cast<size_t>(i) * sg.n * kvw * es;
         const size_t dof = (static_cast<size_t>(i) * rh.layer_stride + static_cast<size_t>(sg.off) * kvw) * es;
         segs.push_back(RerotSeg{static_cast<const uint8_t*>(sg.chunk->k) + so,
@@ -590,7 +612,7 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
     for (int r = 0; r < n_req; ++r) {
       const ReqHost& rh = b.reqs[r];
       for (const SegHost& sg : rh.segs) {
-        if (!sg.chunk || !sg.chunk->on_host || sg.off == 0) continue;  // offset 0: R(0) is the identity
+        if (!sg.chunk || !sg.chunk->on_host || sg.chunk->bits || sg.off == 0) continue;  // offset 0: R(0) = I
         const size_t dof = (static_cast<size_t>(i) * rh.layer_stride + static_cast<size_t>(sg.off) * kvw) * es;
         uint8_t* kd = static_cast<uint8_t*>(rh.fused_k) + dof;
         segs.push_back(RerotSeg{kd, nullptr, kd, nullptr, sg.n, sg.off});
@@ -598,6 +620,58 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
       }
     }
     b.host_seg_n[i] = static_cast<int>(segs.size()) - b.host_seg_off[i];
+  }
+
+  // ---- quantised chunks: resident blocks decoded at begin; host blocks staged per layer into
+  //      slot (layer mod n_slots) of the staging ring, one region per chunk occurrence
+  std::vector<CodecSeg> csegs;
+  for (int i = 0; i < L; ++i)
+    for (int r = 0; r < n_req; ++r) {
+      const ReqHost& rh = b.reqs[r];
+      for (const SegHost& sg : rh.segs) {
+        if (!sg.chunk || !sg.chunk->bits || sg.chunk->on_host) continue;
+        const size_t dof = (static_cast<size_t>(i) * rh.layer_stride + static_cast<size_t>(sg.off) * kvw) * es;
+        csegs.push_back(CodecSeg{sg.chunk->blob + static_cast<size_t>(i) * sg.chunk->layer_bytes,
+                                 static_cast<uint8_t*>(rh.fused_k) + dof, static_cast<uint8_t*>(rh.fused_v) + dof,
+                                 sg.n, sg.off, sg.chunk->bits, 0});
+        b.codec_res_max = std::max(b.codec_res_max, sg.n);
+      }
+    }
+  b.codec_res_segs = static_cast<int>(csegs.size());
+  std::vector<std::pair<int, const SegHost*>> staged_occ;  // (request, segment) of host codec chunks
+  for (int r = 0; r < n_req; ++r)
+    for (const SegHost& sg : b.reqs[r].segs)
+      if (sg.chunk && sg.chunk->bits && sg.chunk->on_host) {
+        b.stage.push_back(Batch::StageCopy{sg.chunk->blob, sg.chunk->layer_bytes, b.slot_bytes});
+        b.slot_bytes += sg.chunk->layer_bytes;
+        staged_occ.push_back({r, &sg});
+      }
+  b.codec_host_off.assign(L, 0);
+  b.codec_host_n.assign(L, 0);
+  b.slot_freed.assign(L, 0);
+  if (!b.stage.empty()) {
+    if (!ctx->staging || ctx->staging_bytes < b.slot_bytes)
+      return fail(ctx, CB_ERR_WORKSPACE, "the staging buffer (cb_set_staging) holds less than one layer of the "
+                                         "batch's host-resident quantised chunks");
+    b.n_slots = static_cast<int>(std::min<size_t>(L, ctx->staging_bytes / b.slot_bytes));
+    while (static_cast<int>(ctx->slot_ev.size()) < b.n_slots) {
+      cudaEvent_t e = nullptr;
+      CB_CUDA(ctx, cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+      ctx->slot_ev.push_back(e);
+    }
+    for (int i = 0; i < L; ++i) {
+      b.codec_host_off[i] = static_cast<int>(csegs.size());
+      const uint8_t* slot = ctx->staging + static_cast<size_t>(i % b.n_slots) * b.slot_bytes;
+      for (size_t k = 0; k < staged_occ.size(); ++k) {
+        const ReqHost& rh = b.reqs[staged_occ[k].first];
+        const SegHost& sg = *staged_occ[k].second;
+        const size_t dof = (static_cast<size_t>(i) * rh.layer_stride + static_cast<size_t>(sg.off) * kvw) * es;
+        csegs.push_back(CodecSeg{slot + b.stage[k].slot_off, static_cast<uint8_t*>(rh.fused_k) + dof,
+                                 static_cast<uint8_t*>(rh.fused_v) + dof, sg.n, sg.off, sg.chunk->bits, 0});
+        b.codec_host_max = std::max(b.codec_host_max, sg.n);
+      }
+      b.codec_host_n[i] = static_cast<int>(csegs.size()) - b.codec_host_off[i];
+    }
   }
 
   // ---- request descriptors, layer-0 rows, last rows, counts, first-token pointers
@@ -626,11 +700,12 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
   const size_t szReq = align_up(rd.size() * sizeof(ReqDev), 256);
   const size_t szTiles = align_up(std::max<size_t>(1, tiles.size()) * sizeof(AttnTile), 256);
   const size_t szSegs = align_up(std::max<size_t>(1, segs.size()) * sizeof(RerotSeg), 256);
+  const size_t szCsegs = align_up(std::max<size_t>(1, csegs.size()) * sizeof(CodecSeg), 256);
   const size_t szForced = align_up(std::max<size_t>(1, forced_all.size()) * 4, 256);
   const size_t szSmall = align_up(lastrows.size() * 4, 256) + align_up(counts.size() * 4, 256) +
                          align_up(firsts.size() * sizeof(void*), 256) + align_up(n_req * 4, 256);
   const size_t szRows = align_up(T0 * 4, 256) * 2;
-  const size_t total = szPlan + szReq + szTiles + szSegs + szForced + szSmall + szRows;
+  const size_t total = szPlan + szReq + szTiles + szSegs + szCsegs + szForced + szSmall + szRows;
   if (total > ctx->meta_bytes) return fail(ctx, CB_ERR_WORKSPACE, "batch metadata exceeds the workspace");
   cb_status st = ensure_pinned(ctx, total);
   if (st != CB_OK) return st;
@@ -647,6 +722,7 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
   ctx->d_reqs = reinterpret_cast<ReqDev*>(put(rd.data(), rd.size() * sizeof(ReqDev), szReq));
   ctx->d_tiles = reinterpret_cast<AttnTile*>(put(tiles.data(), tiles.size() * sizeof(AttnTile), szTiles));
   ctx->d_segs = reinterpret_cast<RerotSeg*>(put(segs.data(), segs.size() * sizeof(RerotSeg), szSegs));
+  ctx->d_csegs = reinterpret_cast<CodecSeg*>(put(csegs.data(), csegs.size() * sizeof(CodecSeg), szCsegs));
   ctx->d_forced = reinterpret_cast<int32_t*>(put(forced_all.data(), forced_all.size() * 4, szForced));
   ctx->d_lastrows = reinterpret_cast<int32_t*>(put(lastrows.data(), lastrows.size() * 4, align_up(lastrows.size() * 4, 256)));
   ctx->d_counts = reinterpret_cast<int32_t*>(put(counts.data(), counts.size() * 4, align_up(counts.size() * 4, 256)));
@@ -677,11 +753,14 @@ cb_status begin_impl(cb_ctx* ctx, std::vector<InReq>& in, const double* ratios, 
     }
   }
   {
-    PhaseScope ps(ctx, CB_PH_BEGIN, s, 1 + (b.resident_segs > 0 ? 1 : 0));
+    PhaseScope ps(ctx, CB_PH_BEGIN, s, 1 + (b.resident_segs > 0 ? 1 : 0) + (b.codec_res_segs > 0 ? 1 : 0));
     CB_CUDA(ctx, launch_embed(ctx->embed, ctx->tok, T0, c.d_model, c.vocab, c.dtype, ctx->h[0], ctx->status, s));
     if (b.resident_segs > 0)
       CB_CUDA(ctx, launch_rerotate(ctx->d_segs, b.resident_segs, b.resident_max_rows, c.n_kv_heads, c.head_dim,
                                    ctx->rope, c.max_positions, c.dtype, ctx->status, s));
+    if (b.codec_res_segs > 0)
+      CB_CUDA(ctx, launch_codec_decode(ctx->d_csegs, b.codec_res_segs, b.codec_res_max, c.n_kv_heads, c.head_dim,
+                                       ctx->rope, c.max_positions, c.dtype, ctx->status, s));
   }
   b.fetched.assign(L, 0);
   b.cur = 0;
@@ -697,9 +776,21 @@ cb_status fetch_impl(cb_ctx* ctx, int layer, cudaStream_t cs) {
   if (layer < 0 || layer >= b.L) return fail(ctx, CB_ERR_INVALID_ARG, "layer out of range");
   const size_t kvw = static_cast<size_t>(c.n_kv_heads) * c.head_dim;
   const size_t es = dtype_bytes(c.dtype);
+  if (!b.stage.empty()) {
+    const int slot = layer % b.n_slots;
+    if (layer >= b.n_slots) {
+      if (!b.slot_freed[layer - b.n_slots])
+        return fail(ctx, CB_ERR_STATE, "staging slot still in use: enqueue cb_prefill_layer of layer - n_slots first");
+      CB_CUDA(ctx, cudaStreamWaitEvent(cs, ctx->slot_ev[slot], 0));
+    }
+    uint8_t* dst = ctx->staging + static_cast<size_t>(slot) * b.slot_bytes;
+    for (const Batch::StageCopy& sc : b.stage)
+      CB_CUDA(ctx, cudaMemcpyAsync(dst + sc.slot_off, sc.src + static_cast<size_t>(layer) * sc.layer_bytes,
+                                   sc.layer_bytes, cudaMemcpyHostToDevice, cs));
+  }
   for (const ReqHost& rh : b.reqs)
     for (const SegHost& sg : rh.segs) {
-      if (!sg.chunk || !sg.chunk->on_host) continue;
+      if (!sg.chunk || !sg.chunk->on_host || sg.chunk->bits) continue;
       const size_t bytes = static_cast<size_t>(sg.n) * kvw * es;
       const size_t so = static_cast<size_t>(layer) * bytes;
       const size_t dof = (static_cast<size_t>(layer) * rh.layer_stride + static_cast<size_t>(sg.off) * kvw) * es;
@@ -725,6 +816,13 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
       PhaseScope ps(ctx, CB_PH_STAGED_ROT, s, 1);
       CB_CUDA(ctx, launch_rerotate(ctx->d_segs + b.host_seg_off[i], b.host_seg_n[i], b.host_max_rows, c.n_kv_heads,
                                    c.head_dim, ctx->rope, c.max_positions, c.dtype, ctx->status, s));
+    }
+    if (b.codec_host_n[i] > 0) {
+      PhaseScope ps(ctx, CB_PH_STAGED_ROT, s, 1);
+      CB_CUDA(ctx, launch_codec_decode(ctx->d_csegs + b.codec_host_off[i], b.codec_host_n[i], b.codec_host_max,
+                                       c.n_kv_heads, c.head_dim, ctx->rope, c.max_positions, c.dtype, ctx->status, s));
+      CB_CUDA(ctx, cudaEventRecord(ctx->slot_ev[i % b.n_slots], s));  // the slot may be refilled after this
+      b.slot_freed[i] = 1;
     }
   }
   const int H = c.n_heads, Hkv = c.n_kv_heads, dh = c.head_dim, d = c.d_model;
@@ -926,6 +1024,8 @@ cb_status cb_destroy(cb_ctx* ctx) {
   if (ctx->pinned_pending) cudaEventSynchronize(ctx->pinned_ev);
   for (cudaEvent_t e : ctx->fetch_ev)
     if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : ctx->slot_ev)
+    if (e) cudaEventDestroy(e);
   if (ctx->pinned_ev) cudaEventDestroy(ctx->pinned_ev);
   if (ctx->status_ev) cudaEventDestroy(ctx->status_ev);
   if (ctx->pinned) cudaFreeHost(ctx->pinned);
@@ -1011,6 +1111,74 @@ cb_status cb_register_chunk(cb_ctx* ctx, uint64_t chunk_id, const int32_t* ids, 
   e.on_host = on_host ? 1 : 0;
   ctx->reg.put(e);
   return CB_OK;
+}
+
+cb_status cb_register_chunk_codec(cb_ctx* ctx, uint64_t chunk_id, const int32_t* ids, const void* blob, int n,
+                                  int bits, int on_host) {
+  if (!ctx || !ids || !blob || n < 1) return fail(ctx, CB_ERR_INVALID_ARG, "bad chunk arguments");
+  if (bits != 8 && bits != 4) return fail(ctx, CB_ERR_INVALID_ARG, "bits must be 8 or 4");
+  if (!aligned16(blob)) return fail(ctx, CB_ERR_INVALID_ARG, "the quantised chunk must be 16-byte aligned");
+  if (ctx->cfg.head_dim != 64 && ctx->cfg.head_dim != 128)
+    return fail(ctx, CB_ERR_SHAPE, "the KV codec needs head_dim 64 or 128");
+  if (n >= ctx->cfg.max_positions) return fail(ctx, CB_ERR_SHAPE, "chunk longer than max_positions");
+  if (ctx->b.active) return fail(ctx, CB_ERR_STATE, "cannot change the registry during a batch");
+  ChunkEntry e;
+  e.id = chunk_id;
+  e.ids = ids;
+  e.n = n;
+  e.on_host = on_host ? 1 : 0;
+  e.blob = static_cast<const uint8_t*>(blob);
+  e.bits = bits;
+  e.layer_bytes = codec_layout(n, ctx->cfg.n_kv_heads, ctx->cfg.head_dim, bits).bytes;
+  ctx->reg.put(e);
+  return CB_OK;
+}
+
+cb_status cb_set_staging(cb_ctx* ctx, void* buf, size_t bytes) {
+  if (!ctx || (bytes && !buf)) return fail(ctx, CB_ERR_INVALID_ARG, "bad staging buffer");
+  if (buf && !aligned16(buf)) return fail(ctx, CB_ERR_INVALID_ARG, "the staging buffer must be 16-byte aligned");
+  if (ctx->b.active) return fail(ctx, CB_ERR_STATE, "cannot change the staging buffer during a batch");
+  ctx->staging = static_cast<uint8_t*>(buf);
+  ctx->staging_bytes = buf ? bytes : 0;
+  return CB_OK;
+}
+
+size_t cb_codec_layer_bytes(int n_tok, int n_kv_heads, int head_dim, int bits) {
+  if (n_tok < 1 || n_kv_heads < 1 || (head_dim != 64 && head_dim != 128) || (bits != 8 && bits != 4)) return 0;
+  return codec_layout(n_tok, n_kv_heads, head_dim, bits).bytes;
+}
+
+cb_status cb_kv_encode(const void* k, const void* v, int n_layers, int n_tok, int n_kv_heads, int head_dim,
+                       cb_dtype dtype, int bits, void* blob, void* stream) {
+  if (!k || !v || !blob) return fail(nullptr, CB_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(blob)) return fail(nullptr, CB_ERR_INVALID_ARG, "blob must be 16-byte aligned");
+  if (n_layers < 1 || n_tok < 1 || n_kv_heads < 1 || (head_dim != 64 && head_dim != 128))
+    return fail(nullptr, CB_ERR_SHAPE, "bad codec sizes (head_dim 64 or 128)");
+  if (bits != 8 && bits != 4) return fail(nullptr, CB_ERR_INVALID_ARG, "bits must be 8 or 4");
+  if (dtype != CB_F32 && dtype != CB_BF16) return fail(nullptr, CB_ERR_DTYPE, "unknown dtype");
+  cudaError_t e = launch_kv_encode(k, v, n_layers, n_tok, n_kv_heads, head_dim, bits, dtype, blob, as_stream(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(nullptr, e, "cb_kv_encode");
+}
+
+cb_status cb_kv_decode(const void* blob, int n_layers, int n_tok, int n_kv_heads, int head_dim, int bits,
+                       int delta_pos, double theta, cb_dtype dtype, void* k_out, void* v_out, void* stream) {
+  if (!blob || !k_out || !v_out) return fail(nullptr, CB_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(blob) || !aligned16(k_out) || !aligned16(v_out))
+    return fail(nullptr, CB_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  if (n_layers < 1 || n_tok < 1 || n_kv_heads < 1 || (head_dim != 64 && head_dim != 128) || delta_pos < 0 ||
+      !(theta > 0))
+    return fail(nullptr, CB_ERR_SHAPE, "bad codec sizes (head_dim 64 or 128)");
+  if (bits != 8 && bits != 4) return fail(nullptr, CB_ERR_INVALID_ARG, "bits must be 8 or 4");
+  if (dtype != CB_F32 && dtype != CB_BF16) return fail(nullptr, CB_ERR_DTYPE, "unknown dtype");
+  float cs[128];
+  for (int i = 0; i < head_dim / 2; ++i) {
+    const double a = static_cast<double>(delta_pos) * std::pow(theta, -2.0 * i / head_dim);
+    cs[2 * i] = static_cast<float>(std::cos(a));
+    cs[2 * i + 1] = static_cast<float>(std::sin(a));
+  }
+  cudaError_t e = launch_codec_decode_blob(blob, n_layers, n_tok, n_kv_heads, head_dim, bits, cs, dtype, k_out, v_out,
+                                           as_stream(stream));
+  return e == cudaSuccess ? CB_OK : cuda_fail(nullptr, e, "cb_kv_decode");
 }
 
 cb_status cb_unregister_chunk(cb_ctx* ctx, uint64_t chunk_id) {
@@ -1196,21 +1364,23 @@ cb_status cb_blend_prefill(cb_ctx* ctx, const cb_request* reqs, int n_req, const
   cb_status st = cb_blend_begin(ctx, reqs, n_req, params, stream);
   if (st != CB_OK) return st;
   Batch& b = ctx->b;
-  if (b.any_host) {
-    if (!copy_stream) {
+  // fetches run ahead of the layers by `window` layers: all of them for plain host chunks
+  // (each layer has its own destination), the staging ring's slot count for quantised ones
+  const int window = b.any_host ? (b.stage.empty() ? b.L : b.n_slots) : 0;
+  if (b.any_host && !copy_stream) {
+    b.active = false;
+    return fail(ctx, CB_ERR_INVALID_ARG, "host-resident chunks need a copy stream");
+  }
+  for (int i = 0; i < std::min(window, b.L); ++i) {
+    st = fetch_impl(ctx, i, as_stream(copy_stream));
+    if (st != CB_OK) {
       b.active = false;
-      return fail(ctx, CB_ERR_INVALID_ARG, "host-resident chunks need a copy stream");
-    }
-    for (int i = 0; i < b.L; ++i) {
-      st = fetch_impl(ctx, i, as_stream(copy_stream));
-      if (st != CB_OK) {
-        b.active = false;
-        return st;
-      }
+      return st;
     }
   }
   for (int i = 0; i < b.L; ++i) {
     st = layer_impl(ctx, i, as_stream(stream));
+    if (st == CB_OK && window > 0 && i + window < b.L) st = fetch_impl(ctx, i + window, as_stream(copy_stream));
     if (st != CB_OK) {
       b.active = false;
       return st;

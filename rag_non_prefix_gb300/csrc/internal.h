@@ -18,6 +18,41 @@ struct RerotSeg {
   int delta;
 };
 
+// Byte offsets inside one layer block of a quantised chunk (the layout cacheblend.h
+// documents at cb_codec_layer_bytes): key codes, value codes, key scales and minima per
+// channel, value scales and minima per (token, head) row; regions 16-byte aligned, the
+// block padded to 256 bytes.
+struct CodecLayout {
+  size_t kc, vc, ks, kz, vs, vz, bytes;
+};
+__host__ __device__ inline size_t codec_align(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline CodecLayout codec_layout(int n, int n_kv_heads, int head_dim, int bits) {
+  const size_t rows = static_cast<size_t>(n) * n_kv_heads;
+  const size_t codes = codec_align(rows * head_dim * bits / 8, 16);
+  const size_t chan = codec_align(static_cast<size_t>(n_kv_heads) * head_dim * 4, 16);
+  const size_t per_row = codec_align(rows * 4, 16);
+  CodecLayout l;
+  l.kc = 0;
+  l.vc = codes;
+  l.ks = 2 * codes;
+  l.kz = l.ks + chan;
+  l.vs = l.kz + chan;
+  l.vz = l.vs + per_row;
+  l.bytes = codec_align(l.vz + per_row, 256);
+  return l;
+}
+
+// One quantised chunk-layer block decoded into its fused-cache rows, keys turned by delta.
+struct CodecSeg {
+  const uint8_t* block;
+  void* k_dst;
+  void* v_dst;
+  int n;
+  int delta;
+  int bits;  // 8 or 4
+  int pad;
+};
+
 // Per request, per layer: where its rows sit in the batched R and S row lists.
 struct PlanEntry {
   int r_off, r_n;   // rows of R_i (layer input) of this request
@@ -74,6 +109,13 @@ cudaError_t launch_rerotate(const RerotSeg* segs, int n_segs, int max_rows, int 
                             const float2* rope_table, int max_pos, cb_dtype dt, int32_t* status, cudaStream_t s);
 cudaError_t launch_rerotate_single(const void* k_src, void* k_dst, const void* v_src, void* v_dst, int n_rows,
                                    int n_kv_heads, int head_dim, const float* cs_host, cb_dtype dt, cudaStream_t s);
+cudaError_t launch_kv_encode(const void* k, const void* v, int L, int n, int n_kv_heads, int head_dim, int bits,
+                             cb_dtype dt, void* blob, cudaStream_t s);
+cudaError_t launch_codec_decode(const CodecSeg* segs, int n_segs, int max_n, int n_kv_heads, int head_dim,
+                                const float2* rope_table, int max_pos, cb_dtype dt, int32_t* status, cudaStream_t s);
+// cs_host: head_dim/2 (cos, sin) pairs of the rotation
+cudaError_t launch_codec_decode_blob(const void* blob, int L, int n, int n_kv_heads, int head_dim, int bits,
+                                     const float* cs_host, cb_dtype dt, void* k_out, void* v_out, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x, cb_dtype dt, cudaStream_t s);
 // (both rotate the fresh q / k of the fp32 projection output at each row's position)
 cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* pos, const int32_t* req,

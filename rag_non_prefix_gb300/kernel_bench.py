@@ -5,6 +5,7 @@
     python -m rag_non_prefix_gb300.kernel_bench rerotate --rows 100352 --hkv 8
     python -m rag_non_prefix_gb300.kernel_bench select --n 3136 --k 471
     python -m rag_non_prefix_gb300.kernel_bench deviation --n 3200 --kvw 1024
+    python -m rag_non_prefix_gb300.kernel_bench codec --n 3136 --hkv 8 --bits 8
 
 Operands are random device tensors sized like one layer of the Mistral-7B-shaped
 workload; weight operands exceed the 129 MB L2 where the shape allows, and a 512 MiB
@@ -47,7 +48,7 @@ def _time(fn, iters, warmup=3, flush=None, batch=1):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemm", "attention", "rerotate", "select", "deviation"])
+    ap.add_argument("kernel", choices=["gemm", "attention", "rerotate", "select", "deviation", "codec"])
     ap.add_argument("--M", type=int, default=535)
     ap.add_argument("--N", type=int, default=28672)
     ap.add_argument("--K", type=int, default=4096)
@@ -60,6 +61,8 @@ def main():
     ap.add_argument("--n", type=int, default=3136)
     ap.add_argument("--k", type=int, default=471)
     ap.add_argument("--kvw", type=int, default=1024)
+    ap.add_argument("--bits", type=int, default=8)
+    ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-flush", action="store_true")
@@ -128,6 +131,22 @@ def main():
         avg, best = _time(fn, a.iters, a.warmup, flush, a.batch)
         by = a.n * a.kvw * (4 + 2) * 2
         out.update(n=a.n, ms=avg, best_ms=best, gbs=by / (avg * 1e-3) / 1e9, bytes=by)
+    elif a.kernel == "codec":
+        # decode + re-rotation of a quantised chunk of n tokens, all layers in one launch
+        shape = (a.layers, a.n, a.hkv, 128)
+        k = torch.randn(shape, device=dev).to(torch.bfloat16)
+        v = torch.randn(shape, device=dev).to(torch.bfloat16)
+        blob = cb.cb_kv_encode(k, v, a.bits)
+        kd, vd = torch.empty_like(k), torch.empty_like(v)
+        lib = cb.load_library()
+        fn = lambda: cb._check(lib.cb_kv_decode(cb._ptr(blob), *shape, a.bits, 1234, 1e4, cb.CB_BF16,  # noqa: E731
+                                                cb._ptr(kd), cb._ptr(vd), cb._stream(None)))
+        avg, best = _time(fn, a.iters, a.warmup, flush, a.batch)
+        by = blob.numel() + 2 * k.numel() * 2  # blob read, K and V written
+        enc = lambda: cb.cb_kv_encode(k, v, a.bits, blob)  # noqa: E731
+        eavg, _ = _time(enc, max(3, a.iters // 4), 1, flush, 1)
+        out.update(shape=list(shape), bits=a.bits, ms=avg, best_ms=best, gbs=by / (avg * 1e-3) / 1e9, bytes=by,
+                   blob_bytes=blob.numel(), encode_ms=eavg)
     torch.cuda.synchronize()
     print(json.dumps(out))
 

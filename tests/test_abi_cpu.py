@@ -89,3 +89,14 @@ def test_library_fails_loudly_when_missing(tmp_path):
             cb.load_library(str(tmp_path / "nope.so"))
         finally:
             cb._lib = None
+
+
+def test_codec_layer_bytes_follow_the_documented_layout():
+    """cb_codec_layer_bytes (a host-side size query) against the byte layout the header documents."""
+    from tests.codec_layout import layer_layout
+
+    lib = cb.load_library()
+    for n, hkv, dh, bits in [(1, 1, 64, 8), (1, 1, 64, 4), (37, 2, 64, 4), (512, 8, 128, 8), (512, 32, 128, 4),
+                             (129, 4, 128, 8), (3, 3, 64, 4)]:
+        assert lib.cb_codec_layer_bytes(n, hkv, dh, bits) == layer_layout(n, hkv, dh, bits)[1]
+    assert lib.cb_codec_layer_bytes(10, 2, 96, 8) == 0 and lib.cb_codec_layer_bytes(10, 2, 128, 2) == 0
