@@ -47,6 +47,12 @@ R19 A quantised key group is one channel of one KV head of one layer over all th
     chunk's tokens ("per channel").
 R20 A quantised value group is one token's row of one KV head of one layer, head_dim
     channels ("per token").
+R22 The "text hash" that keys the chunk store is FNV-1a 64 over the chunk's token ids
+    (little-endian int32 bytes): content only, independent of the chunk's position.
+R23 Per chunk: device-resident -> use; host-resident -> load when bytes / bandwidth +
+    latency is below n x prefill time per token, else recompute; missing -> recompute.
+R24 The ratio chosen is the largest whose recompute time (fixed + r x T_prefill) fits
+    under T_load, clamped to [r_min, r_max]; r_min when nothing is loaded.
 R21 Quantisation is asymmetric min/max (as KIVI): scale = (max - min) / (2^b - 1), the
     minimum kept as the zero point, codes rounded half to even and clamped; a group
     whose values are all equal gets scale 0 and codes 0.
@@ -547,3 +553,72 @@ def pipelined_latency(t_load_layers: Sequence[float], t_rec_layers: Sequence[flo
 def break_even_bandwidth(kv_bytes_token: float, prefill_s_per_token: float) -> float:
     """[P4] §5: loading beats recomputing above BW* = KV bytes per token / prefill time per token."""
     return kv_bytes_token / prefill_s_per_token
+
+
+# --------------------------------------------------------------------------- loading controller
+FNV64_OFFSET = 0xCBF29CE484222325
+FNV64_PRIME = 0x100000001B3
+
+
+def fnv1a64(data: bytes) -> int:
+    """FNV-1a, 64-bit (Fowler, Noll, Vo): h = offset basis; per byte h = (h xor byte) * prime mod 2^64."""
+    h = FNV64_OFFSET
+    for b in data:
+        h ^= b
+        h = (h * FNV64_PRIME) & 0xFFFFFFFFFFFFFFFF
+    return h
+
+
+def chunk_hash(ids: Sequence[int]) -> int:
+    """Content key of a chunk (reading R22): FNV-1a 64 of its token ids as little-endian int32 bytes.
+
+    [P3] loading controller: the cache manager finds a chunk's KV by a hash of its text; [P1]
+    vLLMとの統合: the hash table lives in CPU memory.  Content only, so the key does not depend
+    on where the chunk sits in a prompt.
+    """
+    return fnv1a64(np.asarray(ids, dtype="<i4").tobytes())
+
+
+TIER_MISSING, TIER_DEVICE, TIER_HOST = -1, 0, 1
+ACT_USE, ACT_LOAD, ACT_RECOMPUTE = 0, 1, 2
+
+
+def chunk_action(tier: int, n_tokens: int, nbytes: float, link_bytes_per_s: float, link_latency_s: float,
+                 prefill_s_per_token: float) -> int:
+    """Use, load or recompute one chunk (reading R23).
+
+    [P4] §5 損益分岐: loading n tokens costs n x (KV bytes per token) / bandwidth + a fixed
+    latency, recomputing them costs n x (prefill time per token); load only when that is
+    cheaper.  A chunk already in device memory is used as it is; a missing one is recomputed.
+    """
+    if tier == TIER_DEVICE:
+        return ACT_USE
+    if tier == TIER_MISSING:
+        return ACT_RECOMPUTE
+    t_load = nbytes / link_bytes_per_s + link_latency_s
+    return ACT_LOAD if t_load < n_tokens * prefill_s_per_token else ACT_RECOMPUTE
+
+
+def plan_loading(model: Dict[str, float], chunks: Sequence[Dict[str, float]], n_query: int):
+    """Loading plan of one prompt and the recompute ratio that hides under the load (reading R24).
+
+    [P1] パイプライン化の設計: T_recompute = r% x T_prefill and T_load = KV bytes / storage
+    throughput overlap, so a layer costs max(T_load, T_recompute) ([P3] "로딩과 재계산의 시간을
+    겹친다").  [P1] 閾値チューニング: raise r on slow storage (the extra recompute hides under the
+    load), lower it on fast storage, within the quality bounds [r_min, r_max].  Here
+    T_recompute(r) = fixed + r x T_prefill with T_prefill = N x prefill time per token; the
+    chosen r is the largest whose recompute still fits under T_load:
+    r = clamp((T_load - fixed) / T_prefill, r_min, r_max), r_min when nothing is loaded.
+    Returns (actions, r, T_load, T_recompute(r)).
+    """
+    actions = [chunk_action(c["tier"], c["n_tokens"], c["bytes"], model["link_bytes_per_s"],
+                            model["link_latency_s"], model["prefill_s_per_token"]) for c in chunks]
+    t_load = sum(c["bytes"] / model["link_bytes_per_s"] + model["link_latency_s"]
+                 for c, a in zip(chunks, actions) if a == ACT_LOAD)
+    n_total = sum(c["n_tokens"] for c in chunks) + n_query
+    t_prefill = n_total * model["prefill_s_per_token"]
+    if t_load <= 0 or t_prefill <= 0:
+        r = model["r_min"]
+    else:
+        r = min(model["r_max"], max(model["r_min"], (t_load - model["recompute_fixed_s"]) / t_prefill))
+    return actions, r, t_load, model["recompute_fixed_s"] + r * t_prefill

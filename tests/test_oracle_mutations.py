@@ -98,6 +98,24 @@ def _codec_round_down(x32, axis, bits):
     return np.clip(np.floor(q), 0, 2 ** bits - 1).astype(np.int64), scale, mn
 
 
+def _fnv1_order(data):
+    # FNV-1 (multiply, then xor) instead of FNV-1a
+    h = ocb.FNV64_OFFSET
+    for b in data:
+        h = (h * ocb.FNV64_PRIME) & 0xFFFFFFFFFFFFFFFF
+        h ^= b
+    return h
+
+
+_orig_plan = ocb.plan_loading
+
+
+def _ratio_inverted(model, chunks, n_query):
+    acts, r, t_load, t_rec = _orig_plan(model, chunks, n_query)
+    r2 = model["r_max"] + model["r_min"] - r  # lower r on slow storage
+    return acts, r2, t_load, model["recompute_fixed_s"] + r2 * (t_rec - model["recompute_fixed_s"]) / max(r, 1e-30)
+
+
 def _rms_no_eps_mean(x, eps):
     x = np.asarray(x, dtype=np.float64)
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
@@ -116,6 +134,8 @@ MUTATIONS = [
     ("seam_positions", _seam_after_boundary, [pins.test_seam_positions_hand_examples]),
     ("_minmax_codes", _codec_keys_per_token, [pins.test_codec_hand_example_fixes_the_axes]),
     ("_minmax_codes", _codec_round_down, [lambda: pins.test_codec_error_bound_and_extremes(8)]),
+    ("fnv1a64", _fnv1_order, [pins.test_fnv1a64_published_vectors_and_chunk_key]),
+    ("plan_loading", _ratio_inverted, [pins.test_ratio_rule_hides_recompute_under_the_load]),
 ]
 
 

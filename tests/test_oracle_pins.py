@@ -530,3 +530,72 @@ def test_kv_bytes_and_cost_model_match_printed_numbers():
     assert abs(t * 1e3 - ll["printed_ms"]) / ll["printed_ms"] < ll["rel_tol"]
     assert orc.pipelined_latency([1, 5, 2], [3, 3, 3]) == 11
     assert orc.t_recompute(0.15, 100.0) == pytest.approx(15.0)
+
+
+# ----------------------------------------------------------------------------- loading controller
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def test_fnv1a64_published_vectors_and_chunk_key():
+    g = _golden("loading_controller.json")["fnv1a64_vectors"]
+    for text, hexval in g.items():
+        if text.startswith("_"):
+            continue
+        assert orc.fnv1a64(text.encode()) == int(hexval, 16), text
+    ids = [1, 258, -1, 70000]
+    raw = b"".join(int(x).to_bytes(4, "little", signed=True) for x in ids)
+    assert orc.chunk_hash(ids) == orc.fnv1a64(raw)
+    assert orc.chunk_hash(np.array(ids, dtype=np.int64)) == orc.chunk_hash(ids)
+    keys = {orc.chunk_hash(hz.gen_token_ids(hz.stream_key(7, i), 64, 32000, "zipf")) for i in range(200)}
+    assert len(keys) == 200
+    assert orc.chunk_hash([1, 2]) != orc.chunk_hash([2, 1])
+
+
+def test_load_or_recompute_follows_the_printed_break_even():
+    """[P4] §5: 6,414 tokens (0.12 ms each), 28,672 B per token: load over 13.4 GB/s, recompute
+    over 104 MB/s (about 1.8 s of transfer against 0.77 s of prefill)."""
+    g = _golden("loading_controller.json")["break_even_cases"]
+    n, t_tok = g["n_tokens"], g["prefill_s"] / g["n_tokens"]
+    nbytes = n * g["bytes_per_token"]
+    act = {"load": orc.ACT_LOAD, "recompute": orc.ACT_RECOMPUTE}
+    assert orc.chunk_action(orc.TIER_HOST, n, nbytes, g["fast_link_bytes_per_s"], 0.0, t_tok) == act[g["fast_action"]]
+    assert orc.chunk_action(orc.TIER_HOST, n, nbytes, g["slow_link_bytes_per_s"], 0.0, t_tok) == act[g["slow_action"]]
+    assert abs(nbytes / g["slow_link_bytes_per_s"] - g["slow_load_s"]) < g["slow_load_tol"]
+    # the threshold is the break-even bandwidth of the same section
+    bw = orc.break_even_bandwidth(g["bytes_per_token"], t_tok)
+    assert orc.chunk_action(orc.TIER_HOST, n, nbytes, bw * 1.01, 0.0, t_tok) == orc.ACT_LOAD
+    assert orc.chunk_action(orc.TIER_HOST, n, nbytes, bw * 0.99, 0.0, t_tok) == orc.ACT_RECOMPUTE
+    assert orc.chunk_action(orc.TIER_DEVICE, n, nbytes, 1.0, 0.0, t_tok) == orc.ACT_USE
+    assert orc.chunk_action(orc.TIER_MISSING, n, nbytes, 1e12, 0.0, t_tok) == orc.ACT_RECOMPUTE
+
+
+def test_ratio_rule_hides_recompute_under_the_load():
+    """[P1] 閾値チューニング: slower storage raises r (up to r_max), faster storage lowers it (down
+    to r_min, also when nothing is loaded); between the bounds the chosen r makes T_recompute
+    equal T_load exactly.  A link so slow that recomputing beats loading loads nothing."""
+    g = _golden("loading_controller.json")["ratio_rule"]
+    base = {"link_latency_s": 0.0, "prefill_s_per_token": 1e-5, "recompute_fixed_s": 0.0,
+            "r_min": g["r_min"], "r_max": g["r_max"]}
+    chunks = [{"tier": orc.TIER_HOST, "n_tokens": 512, "bytes": 512 * 131072.0} for _ in range(8)]
+    n_q = 32
+    t_prefill = (8 * 512 + n_q) * 1e-5
+    rs = []
+    inside = 0
+    for bw in (2e10, 7e10, 1.31e11, 2e11, 1e12):  # per-token load 6.6 .. 0.13 us < 10 us of prefill
+        acts, r, t_load, t_rec = orc.plan_loading(dict(base, link_bytes_per_s=bw), chunks, n_q)
+        assert all(a == orc.ACT_LOAD for a in acts)
+        rs.append(r)
+        if g["r_min"] < r < g["r_max"]:
+            inside += 1
+            assert abs(t_rec - t_load) < 1e-12 and abs(t_rec - r * t_prefill) < 1e-12
+    assert rs[0] == g["r_max"] and rs[-1] == g["r_min"] and inside == 3
+    assert all(a > b for a, b in zip(rs, rs[1:]))
+    acts, r, t_load, _ = orc.plan_loading(dict(base, link_bytes_per_s=1e9), chunks, n_q)  # 131 us per token
+    assert all(a == orc.ACT_RECOMPUTE for a in acts) and t_load == 0 and r == g["r_min"]
+    fixed = dict(base, link_bytes_per_s=1.31e11, recompute_fixed_s=0.001)
+    _, r_f, t_load_f, t_rec_f = orc.plan_loading(fixed, chunks, n_q)
+    assert abs(t_rec_f - t_load_f) < 1e-12 and r_f < rs[2]  # a fixed recompute cost leaves less room
+    assert orc.plan_loading(dict(base, link_bytes_per_s=1e9), [{"tier": orc.TIER_DEVICE, "n_tokens": 9, "bytes": 1.0}],
+                            3)[1] == g["r_min"]
