@@ -310,6 +310,36 @@ def run_ours(args, rank, world):
         staging = {"h2d_gbs": round(h2d_gbs, 1), "staged_bytes": total_bytes, "t_load_ms": round(t_load, 3),
                    "t_recompute_ms": round(res_ms, 3), "max_load_recompute_ms": round(max(t_load, res_ms), 3),
                    "ttft_staged_ms": round(statistics.mean(blend_ms), 3)}
+        # loading controller: the plan and the ratio it picks from the measured costs (link
+        # bandwidth, full-prefill time per token, the blend's fixed recompute time at r = 0),
+        # then the staged blend timed at that ratio against the plan's prediction
+        for c in used:
+            ids, k, v = chunk_store[c]
+            eng.register_chunk(c, ids, k, v)
+        copy_stream = None
+        r0 = cb.ratio_schedule(cfg.n_layers, 0.0, args.schedule or spec.schedule)
+        for _ in range(2):
+            blend_step(r0)
+        fixed_ms = statistics.mean(timed(lambda: blend_step(r0), max(3, args.steps // 2), "r0"))
+        copy_stream = cs_saved
+        for c in used:
+            ids, kh_, vh_ = host_store[c]
+            eng.register_chunk(c, ids, kh_, vh_, on_host=True)
+        model = {"link_bytes_per_s": h2d_gbs * 1e9, "link_latency_s": 0.0,
+                 "prefill_s_per_token": statistics.mean(full_ms) * 1e-3 / T, "recompute_fixed_s": fixed_ms * 1e-3,
+                 "r_min": 0.05, "r_max": 0.20}
+        req0 = spec.requests[0]
+        infos = [eng.chunk_info(s_.chunk) for s_ in req0 if s_.chunk >= 0]
+        acts, r_star, t_load_p, t_rec_p = cb.cb_plan_loading(model, infos, n_tok[0] - spec.n_cached(0))
+        rat_star = cb.ratio_schedule(cfg.n_layers, r_star, args.schedule or spec.schedule)
+        for _ in range(2):
+            blend_step(rat_star)
+        ts = timed(lambda: blend_step(rat_star), args.steps, "controller")
+        staging["controller"] = {"model": {k_: round(v_, 9) for k_, v_ in model.items()},
+                                 "actions": acts, "ratio": round(r_star, 4), "t_load_pred_ms": round(t_load_p * 1e3, 3),
+                                 "t_recompute_pred_ms": round(t_rec_p * 1e3, 3),
+                                 "ttft_pred_ms": round(max(t_load_p, t_rec_p) * 1e3, 3),
+                                 "ttft_measured_ms": round(statistics.mean(ts), 3), "fixed_ms_at_r0": round(fixed_ms, 3)}
         # the same chunks quantised (KIVI-style int8 / int4) in pinned host memory, staged
         # through a two-slot ring and decoded + re-rotated per layer on the GPU
         if args.codec:

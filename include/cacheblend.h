@@ -118,6 +118,49 @@ cb_status cb_register_chunk(cb_ctx* ctx, uint64_t chunk_id, const int32_t* ids, 
 cb_status cb_unregister_chunk(cb_ctx* ctx, uint64_t chunk_id);
 int cb_registered_chunks(const cb_ctx* ctx);
 
+/* --------------------------------------------------------------------- loading controller
+ * [P3] loading controller: it checks whether the chunks a retriever chose have caches and
+ * where they are stored, and coordinates loading with recompute; the cache manager finds a
+ * cache by a hash of its text ([P1] vLLMとの統合: a hash table in CPU memory).  The key used
+ * here is the chunk's content only, so a chunk is found wherever it sits in a prompt. */
+
+/* FNV-1a 64 (Fowler, Noll, Vo) of the token ids as little-endian int32 bytes (host array).
+ * Intended as the chunk_id of cb_register_chunk / cb_request. */
+uint64_t cb_chunk_hash(const int32_t* ids_host, int n);
+
+enum { CB_TIER_MISSING = -1, CB_TIER_DEVICE = 0, CB_TIER_HOST = 1 };
+enum { CB_ACT_USE = 0, CB_ACT_LOAD = 1, CB_ACT_RECOMPUTE = 2 };
+typedef struct {
+  int n_tokens;
+  int tier;      /* CB_TIER_* */
+  double bytes;  /* bytes a load moves (the chunk's KV, or its quantised blob) */
+} cb_chunk_info;
+/* What the registry holds under chunk_id: tier, tokens and bytes (CB_TIER_MISSING, 0, 0 if
+ * it is not registered; the call still returns CB_OK). */
+cb_status cb_chunk_info_of(const cb_ctx* ctx, uint64_t chunk_id, cb_chunk_info* out);
+
+/* Costs the plan weighs, measured on the machine: the host->device link of the staging tier,
+ * the full-prefill time per token, and the part of the blend's recompute time that does not
+ * scale with the ratio (layer 0, the query, launch overheads). */
+typedef struct {
+  double link_bytes_per_s;
+  double link_latency_s;       /* per chunk loaded */
+  double prefill_s_per_token;
+  double recompute_fixed_s;
+  double r_min, r_max;         /* quality bounds of the ratio ([P1]: 5 % latency first ... 20 % quality first) */
+} cb_cost_model;
+/* Plan of one prompt (host arrays).  Per chunk ([P4] §5 損益分岐): a device-resident chunk is
+ * used (CB_ACT_USE); a host-resident one is loaded when bytes / link + latency is below
+ * n_tokens x prefill time per token, else recomputed; a missing one is recomputed (the caller
+ * prefills it, e.g. with cb_precompute_chunk, and registers it).  The ratio ([P1] パイプライン化の設計,
+ * 閾値チューニング): T_load = the summed load times, T_prefill = N x prefill time per token (N = all
+ * chunk tokens + n_query), T_recompute(r) = recompute_fixed_s + r x T_prefill, and
+ * *ratio_out = clamp((T_load - recompute_fixed_s) / T_prefill, r_min, r_max): the largest ratio
+ * whose recompute still hides under the load (r_min when nothing is loaded).  t_load_out and
+ * t_recompute_out (T_recompute at the chosen ratio) may be NULL.  Host-only; no GPU needed. */
+cb_status cb_plan_loading(const cb_cost_model* model, const cb_chunk_info* chunks_host, int n_chunks, int n_query,
+                          int32_t* actions_host, double* ratio_out, double* t_load_out, double* t_recompute_out);
+
 /* --------------------------------------------------------------------- KV codec
  * KIVI-style asymmetric quantisation of a chunk's KV cache ([P2] KV量子化とメモリ管理 /
  * 非対称量子化: keys per channel, values per token, int8 or int4; about 2x / 4x fewer bytes

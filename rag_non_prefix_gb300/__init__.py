@@ -29,7 +29,7 @@ EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
             "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_set_orientation",
             "cb_set_launch_overlap", "cb_codec_layer_bytes", "cb_kv_encode", "cb_kv_decode", "cb_register_chunk_codec",
-            "cb_set_staging")
+            "cb_set_staging", "cb_chunk_hash", "cb_chunk_info_of", "cb_plan_loading")
 PHASES = ("begin", "staged_rot", "norm", "qkv", "rope", "deviation", "select", "scatter", "attention", "oproj",
           "gateup", "down", "finish")
 
@@ -65,6 +65,20 @@ class Request(C.Structure):
     _fields_ = [("n_chunks", C.c_int), ("chunk_ids_host", C.POINTER(C.c_uint64)), ("query_ids", C.c_void_p),
                 ("n_query", C.c_int), ("fused_k", C.c_void_p), ("fused_v", C.c_void_p), ("out_hidden", C.c_void_p),
                 ("out_sel", C.c_void_p), ("out_sel_count", C.c_void_p), ("out_first_token", C.c_void_p)]
+
+
+class ChunkInfo(C.Structure):
+    _fields_ = [("n_tokens", C.c_int), ("tier", C.c_int), ("bytes", C.c_double)]
+
+
+class CostModel(C.Structure):
+    _fields_ = [("link_bytes_per_s", C.c_double), ("link_latency_s", C.c_double),
+                ("prefill_s_per_token", C.c_double), ("recompute_fixed_s", C.c_double),
+                ("r_min", C.c_double), ("r_max", C.c_double)]
+
+
+TIER_MISSING, TIER_DEVICE, TIER_HOST = -1, 0, 1
+ACT_USE, ACT_LOAD, ACT_RECOMPUTE = 0, 1, 2
 
 
 class Profile(C.Structure):
@@ -111,6 +125,10 @@ def load_library(path: str = LIB_PATH):
                               vp]),
         "cb_register_chunk_codec": (st, [vp, C.c_uint64, i32p, vp, C.c_int, C.c_int, C.c_int]),
         "cb_set_staging": (st, [vp, vp, C.c_size_t]),
+        "cb_chunk_hash": (C.c_uint64, [C.POINTER(C.c_int32), C.c_int]),
+        "cb_chunk_info_of": (st, [vp, C.c_uint64, C.POINTER(ChunkInfo)]),
+        "cb_plan_loading": (st, [C.POINTER(CostModel), C.POINTER(ChunkInfo), C.c_int, C.c_int, C.POINTER(C.c_int32),
+                                 C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(C.c_double)]),
         "cb_blend_prefill": (st, [vp, C.POINTER(Request), C.c_int, C.POINTER(BlendParams), vp, vp]),
         "cb_full_prefill": (st, [vp, i32p, C.c_int, vp, vp, vp, i32p, vp]),
         "cb_blend_begin": (st, [vp, C.POINTER(Request), C.c_int, C.POINTER(BlendParams), vp]),
@@ -275,6 +293,27 @@ def cb_attention(q: torch.Tensor, q_pos: torch.Tensor, k: torch.Tensor, v: torch
     return out
 
 
+def cb_chunk_hash(ids) -> int:
+    """Content key of a chunk: FNV-1a 64 of its token ids (host sequence or tensor)."""
+    if isinstance(ids, torch.Tensor):
+        ids = ids.detach().to("cpu", torch.int32).tolist()
+    arr = (C.c_int32 * max(1, len(ids)))(*[int(x) for x in ids])
+    return int(load_library().cb_chunk_hash(arr, len(ids)))
+
+
+def cb_plan_loading(model: Dict[str, float], chunks: Sequence[Dict[str, float]], n_query: int):
+    """(actions, ratio, T_load, T_recompute) of one prompt; see cb_plan_loading in the header."""
+    lib = load_library()
+    m = CostModel(model["link_bytes_per_s"], model["link_latency_s"], model["prefill_s_per_token"],
+                  model["recompute_fixed_s"], model["r_min"], model["r_max"])
+    n = len(chunks)
+    arr = (ChunkInfo * max(1, n))(*[ChunkInfo(int(c["n_tokens"]), int(c["tier"]), float(c["bytes"])) for c in chunks])
+    acts = (C.c_int32 * max(1, n))()
+    r, tl, tr = C.c_double(), C.c_double(), C.c_double()
+    _check(lib.cb_plan_loading(C.byref(m), arr, n, int(n_query), acts, C.byref(r), C.byref(tl), C.byref(tr)))
+    return [int(acts[i]) for i in range(n)], r.value, tl.value, tr.value
+
+
 def cb_codec_layer_bytes(n_tok: int, n_kv_heads: int, head_dim: int, bits: int) -> int:
     return int(load_library().cb_codec_layer_bytes(n_tok, n_kv_heads, head_dim, bits))
 
@@ -378,6 +417,12 @@ class Engine:
         """Allocates (caller side) and binds the staging ring for host-resident quantised chunks."""
         self.staging = torch.empty(max(1, nbytes), dtype=torch.uint8, device=self.device) if nbytes else None
         _check(self.lib.cb_set_staging(self.ctx, _ptr(self.staging), nbytes if nbytes else 0), self.ctx)
+
+    def chunk_info(self, chunk_id: int) -> Dict[str, float]:
+        """Tier, tokens and load bytes of a registered chunk (tier -1 when missing)."""
+        info = ChunkInfo()
+        _check(self.lib.cb_chunk_info_of(self.ctx, C.c_uint64(chunk_id), C.byref(info)), self.ctx)
+        return {"n_tokens": info.n_tokens, "tier": info.tier, "bytes": info.bytes}
 
     def unregister_chunk(self, chunk_id: int):
         _check(self.lib.cb_unregister_chunk(self.ctx, C.c_uint64(chunk_id)), self.ctx)

@@ -24,7 +24,7 @@ FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", 
 LIBS = {
     os.path.join(PKG, "libcacheblend.so"): {
         "srcs": [os.path.join(PKG, "csrc", f) for f in ("kernels_bw.cu", "select.cu", "gemm.cu", "gemm_noalloc.cu", "attention.cu",
-                                                               "codec.cu", "engine.cu")],
+                                                               "codec.cu", "engine.cu", "controller.cpp")],
         "deps": [os.path.join(PKG, "csrc", f) for f in ("common.cuh", "internal.h")] + [os.path.join(INCLUDE, "cacheblend.h")],
         "build": os.path.join(PKG, "_build"),
     },
@@ -65,7 +65,7 @@ def build(verbose: bool = False) -> list:
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         for lib, spec in LIBS.items():
             os.makedirs(spec["build"], exist_ok=True)
-            objs = [os.path.join(spec["build"], os.path.basename(s)[:-3] + ".o") for s in spec["srcs"]]
+            objs = [os.path.join(spec["build"], os.path.splitext(os.path.basename(s))[0] + ".o") for s in spec["srcs"]]
             list(ex.map(lambda so: _compile(so[0], so[1], spec["deps"]), zip(spec["srcs"], objs)))
             if _stale(lib, objs):
                 cmd = [nvcc(), *ARCH, "-shared", "-o", lib, *objs]

@@ -1134,6 +1134,19 @@ cb_status cb_register_chunk_codec(cb_ctx* ctx, uint64_t chunk_id, const int32_t*
   return CB_OK;
 }
 
+cb_status cb_chunk_info_of(const cb_ctx* ctx, uint64_t chunk_id, cb_chunk_info* out) {
+  if (!ctx || !out) return fail(nullptr, CB_ERR_INVALID_ARG, "null argument");
+  *out = cb_chunk_info{0, CB_TIER_MISSING, 0.0};
+  const ChunkEntry* e = const_cast<cb_ctx*>(ctx)->reg.find(chunk_id);
+  if (!e) return CB_OK;
+  const cb_model_cfg& c = ctx->cfg;
+  out->n_tokens = e->n;
+  out->tier = e->on_host ? CB_TIER_HOST : CB_TIER_DEVICE;
+  out->bytes = e->bits ? static_cast<double>(e->layer_bytes) * c.n_layers
+                       : 2.0 * c.n_layers * e->n * c.n_kv_heads * c.head_dim * dtype_bytes(c.dtype);
+  return CB_OK;
+}
+
 cb_status cb_set_staging(cb_ctx* ctx, void* buf, size_t bytes) {
   if (!ctx || (bytes && !buf)) return fail(ctx, CB_ERR_INVALID_ARG, "bad staging buffer");
   if (buf && !aligned16(buf)) return fail(ctx, CB_ERR_INVALID_ARG, "the staging buffer must be 16-byte aligned");

@@ -193,3 +193,37 @@ def test_staging_ring_rules(small_bf16_spec):
     with pytest.raises(cb.CacheBlendError) as e:
         host.g.blend(ratios, copy_stream=cs)
     assert e.value.name == "CB_ERR_WORKSPACE"
+
+
+# ----------------------------------------------------------------------------- loading controller
+def test_chunk_info_and_plan_over_the_registry(small_bf16_spec):
+    """cb_chunk_info_of reports each registered chunk's tier and load bytes (bf16 KV, or the
+    quantised blob), missing ids as missing; keyed by cb_chunk_hash, the registry finds a
+    chunk by its content, and the plan over those infos is the oracle's."""
+    spec = small_bf16_spec
+    cfg = spec.cfg
+    g = GpuWorkload(spec)
+    eng = g.eng
+    ids0, k0, v0 = g.chunk_kv[0]
+    key = cb.cb_chunk_hash(spec.chunks[0])
+    assert key == orc.chunk_hash(spec.chunks[0])
+    eng.register_chunk(key, ids0, k0.cpu().pin_memory(), v0.cpu().pin_memory(), on_host=True)
+    info = eng.chunk_info(key)
+    n0 = len(spec.chunks[0])
+    assert info == {"n_tokens": n0, "tier": cb.TIER_HOST,
+                    "bytes": float(2 * cfg.n_layers * n0 * cfg.n_kv_heads * cfg.head_dim * 2)}
+    assert eng.chunk_info(1)["tier"] == cb.TIER_DEVICE
+    assert eng.chunk_info(0xDEADBEEF) == {"n_tokens": 0, "tier": cb.TIER_MISSING, "bytes": 0.0}
+    ids1, k1, v1 = g.chunk_kv[1]
+    blob = cb.cb_kv_encode(k1, v1, 4)
+    torch.cuda.synchronize()
+    eng.register_chunk_codec(77, ids1, blob, 4)
+    n1 = len(spec.chunks[1])
+    assert eng.chunk_info(77)["bytes"] == cfg.n_layers * cb.cb_codec_layer_bytes(n1, cfg.n_kv_heads, cfg.head_dim, 4)
+    infos = [eng.chunk_info(c) for c in (key, 1, 77, 0xDEADBEEF)]
+    model = {"link_bytes_per_s": 2e11, "link_latency_s": 1e-5, "prefill_s_per_token": 2e-6,
+             "recompute_fixed_s": 1e-4, "r_min": 0.05, "r_max": 0.2}
+    got = cb.cb_plan_loading(model, infos, 40)
+    ref = orc.plan_loading(model, infos, 40)
+    assert got[0] == ref[0] and got[0][1:] == [cb.ACT_USE, cb.ACT_USE, cb.ACT_RECOMPUTE]
+    assert got[1] == pytest.approx(ref[1], rel=1e-12)
