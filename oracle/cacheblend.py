@@ -475,6 +475,39 @@ def seam_repair_prefill(cfg, weights, segments, chunk_caches, seam_tokens: int, 
     return fixed_set_prefill(cfg, weights, segments, chunk_caches, S, storage)
 
 
+def decode_step(cfg, weights, Kf: np.ndarray, Vf: np.ndarray, n_past: int, token: int, storage: str = "f64"):
+    """One greedy decoding step on a fused KV cache ([P3] flow: the response is generated
+    from the fused KV; [P1] 実験結果 / スループット: decoding follows the blended prefill).
+
+    The token ``token`` enters at position ``n_past``: per layer its q, k, v are computed
+    (RoPE at n_past), its K/V are written to row n_past of the cache (rounded to the storage
+    type), its query attends to rows 0..n_past, then output projection and MLP.  Kf, Vf
+    [L, capacity, Hkv, dh] are updated in place.  Returns the final hidden state and the
+    argmax of the LM head (the next token).
+    """
+    h = weights.embed(np.asarray([token])).astype(np.float64)
+    pos = [int(n_past)]
+    for i in range(cfg.n_layers):
+        W = weights.layer(i)
+        q, k, v = project_qkv(cfg, W, h, pos)
+        Kf[i][n_past] = round_storage(k[0], storage)
+        Vf[i][n_past] = round_storage(v[0], storage)
+        attn = causal_attention(q, pos, Kf[i], Vf[i])
+        h = output_and_mlp(cfg, W, h, attn)
+    return {"hidden": h[0], "token": first_token(cfg, weights, h[0])}
+
+
+def greedy_decode(cfg, weights, Kf: np.ndarray, Vf: np.ndarray, n_past: int, token: int, steps: int,
+                  storage: str = "f64"):
+    """``steps`` decode steps, each feeding the previous step's argmax; returns the tokens."""
+    out = []
+    for t in range(steps):
+        r = decode_step(cfg, weights, Kf, Vf, n_past + t, token, storage)
+        token = r["token"]
+        out.append(token)
+    return out
+
+
 def precompute_all(cfg, weights, spec, storage: str, chunk_indices=None):
     """Chunk caches for every chunk a workload's requests use."""
     used = sorted({s.chunk for req in spec.requests for s in req if s.chunk >= 0})

@@ -116,6 +116,21 @@ def _ratio_inverted(model, chunks, n_query):
     return acts, r2, t_load, model["recompute_fixed_s"] + r2 * (t_rec - model["recompute_fixed_s"]) / max(r, 1e-30)
 
 
+_orig_decode = ocb.decode_step
+
+
+def _decode_position_off_by_one(cfg, weights, Kf, Vf, n_past, token, storage="f64"):
+    # RoPE and the causal bound at n_past + 1 while the K/V row still goes to n_past
+    h = weights.embed(np.asarray([token])).astype(np.float64)
+    for i in range(cfg.n_layers):
+        W = weights.layer(i)
+        q, k, v = ocb.project_qkv(cfg, W, h, [n_past + 1])
+        Kf[i][n_past] = ocb.round_storage(k[0], storage)
+        Vf[i][n_past] = ocb.round_storage(v[0], storage)
+        h = ocb.output_and_mlp(cfg, W, h, ocb.causal_attention(q, [n_past], Kf[i], Vf[i]))
+    return {"hidden": h[0], "token": ocb.first_token(cfg, weights, h[0])}
+
+
 def _rms_no_eps_mean(x, eps):
     x = np.asarray(x, dtype=np.float64)
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
@@ -136,6 +151,7 @@ MUTATIONS = [
     ("_minmax_codes", _codec_round_down, [lambda: pins.test_codec_error_bound_and_extremes(8)]),
     ("fnv1a64", _fnv1_order, [pins.test_fnv1a64_published_vectors_and_chunk_key]),
     ("plan_loading", _ratio_inverted, [pins.test_ratio_rule_hides_recompute_under_the_load]),
+    ("decode_step", _decode_position_off_by_one, [pins.test_decode_after_prefill_equals_a_longer_prefill]),
 ]
 
 

@@ -599,3 +599,28 @@ def test_ratio_rule_hides_recompute_under_the_load():
     assert abs(t_rec_f - t_load_f) < 1e-12 and r_f < rs[2]  # a fixed recompute cost leaves less room
     assert orc.plan_loading(dict(base, link_bytes_per_s=1e9), [{"tier": orc.TIER_DEVICE, "n_tokens": 9, "bytes": 1.0}],
                             3)[1] == g["r_min"]
+
+
+# ----------------------------------------------------------------------------- decode
+def test_decode_after_prefill_equals_a_longer_prefill():
+    """A decode step on the KV of a full prefill of ids[:-1], fed ids[-1], is the last row of a
+    full prefill of ids; two steps extend it by the greedy token."""
+    W = hz.HostWeights(TINY, 51)
+    ids = hz.gen_token_ids(hz.stream_key(51, 1), 23, TINY.vocab, "uniform")
+    f_short = orc.full_prefill(TINY, W, ids[:-1], "f64")
+    cap = 30
+    K = np.zeros((TINY.n_layers, cap, TINY.n_kv_heads, TINY.head_dim))
+    V = np.zeros_like(K)
+    K[:, :22], V[:, :22] = f_short["k"], f_short["v"]
+    st = orc.decode_step(TINY, W, K, V, 22, int(ids[-1]), "f64")
+    f_full = orc.full_prefill(TINY, W, ids, "f64")
+    assert np.max(np.abs(st["hidden"] - f_full["hidden"][-1])) < 1e-11
+    assert st["token"] == f_full["first_token"]
+    assert np.max(np.abs(K[:, :23] - f_full["k"])) < 1e-11
+    st2 = orc.decode_step(TINY, W, K, V, 23, st["token"], "f64")
+    f2 = orc.full_prefill(TINY, W, np.append(ids, st["token"]), "f64")
+    assert np.max(np.abs(st2["hidden"] - f2["hidden"][-1])) < 1e-11
+    K2 = np.zeros_like(K)
+    V2 = np.zeros_like(V)
+    K2[:, :22], V2[:, :22] = f_short["k"], f_short["v"]
+    assert orc.greedy_decode(TINY, W, K2, V2, 22, int(ids[-1]), 2, "f64") == [st["token"], st2["token"]]
