@@ -174,8 +174,9 @@ def run_ours(args, rank, world):
     W = hd.device_weights(cfg, spec.seed)
     n_tok = [spec.n_tokens(r) for r in range(len(spec.requests))]
     T = sum(n_tok)
+    dec_room = args.decode_steps + 8 if args.decode_steps else 0
     eng = cb.Engine(cfg, W, max_tokens=max(T, max(len(c) for c in spec.chunks)), max_requests=len(spec.requests),
-                    max_positions=max(n_tok) + 1)
+                    max_positions=max(n_tok) + 1 + dec_room)
     used = sorted({s.chunk for req in spec.requests for s in req if s.chunk >= 0})
     staged = args.staged if args.staged is not None else spec.name == "llama7b"
     chunk_store = {}
@@ -264,6 +265,54 @@ def run_ours(args, rank, world):
                 blend_step(rat)
             ts = timed(lambda: blend_step(rat), max(3, args.steps // 2), "sweep")
             sweep.append({"ratio": r, "ttft_ms": round(statistics.mean(ts), 4)})
+    # decode after the blend: greedy steps of every request on its fused cache (one token per
+    # request per step), each step timed; the step streams every weight once, so its bound is HBM
+    decode = None
+    if args.decode_steps:
+        dreqs = []
+        for req in spec.requests:
+            q = [s_ for s_ in req if s_.chunk < 0][0]
+            dreqs.append(eng.make_request([s_.chunk for s_ in req if s_.chunk >= 0], hd.ids_tensor(q.ids),
+                                          want_hidden=False, want_sel=False, decode_room=dec_room))
+        cs_saved_d = copy_stream
+        eng.blend_prefill(dreqs, ratios, stream=stream, copy_stream=copy_stream)
+        eng.get_status()
+        tok0 = torch.cat([r["first_token"] for r in dreqs]).to(torch.int32)
+        tok = tok0.clone()
+        for _ in range(4):
+            tok = eng.decode_step(dreqs, tok)
+        torch.cuda.synchronize()
+        ts = []
+        eng.get_profile()
+        for _ in range(args.decode_steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            tok = eng.decode_step(dreqs, tok)
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        dprof = eng.get_profile()
+        eng.get_status()
+        ms = statistics.mean(ts)
+        n_seq = len(dreqs)
+        params_layer = cfg.params_per_layer() if callable(cfg.params_per_layer) else cfg.params_per_layer
+        es_ = 2 if cfg.dtype == "bf16" else 4
+        ctx_len = statistics.mean(r["n_tokens"] + r["decoded"] for r in dreqs)  # mid-run context
+        wbytes = (cfg.n_layers * params_layer + cfg.vocab * cfg.d_model) * es_
+        kvbytes = n_seq * cfg.n_layers * ctx_len * 2 * cfg.kv_width * es_
+        by = wbytes + kvbytes
+        peaks_d = _peaks()
+        gbs = by / (ms * 1e-3) / 1e9
+        decode = {"steps": args.decode_steps, "sequences": n_seq, "ms_per_step": round(ms, 4),
+                  "tok_s": round(n_seq / (ms * 1e-3), 1), "context_tokens": round(ctx_len, 1),
+                  "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks_d["hbm_gbs"], "unit": "GB/s",
+                               "frac": round(gbs / peaks_d["hbm_gbs"], 4), "bytes_per_step": int(by),
+                               "weight_bytes": int(wbytes), "kv_bytes": int(kvbytes),
+                               "peak_source": f"{peaks_d['source']} HBM copy"},
+                  "launches_per_step": sum(v["launches"] for v in dprof.values()) / args.decode_steps}
+        copy_stream = cs_saved_d
+
     # selection variants on the same prompt: cosine deviation (same schedule) and spatial
     # seam repair (the 16 tokens before every chunk boundary, recomputed from layer 0 on)
     variants = None
@@ -450,6 +499,7 @@ def run_ours(args, rank, world):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(step_launches * args.steps),
         "sweep": sweep,
+        "decode": decode,
         "variants": variants,
         "staging": staging,
         "clocks": clocks,
@@ -579,6 +629,7 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="also time r in {0, 5, 10, 15, 20, 50, 100} %%")
     ap.add_argument("--staged", default=None, action=argparse.BooleanOptionalAction,
                     help="cached KV in pinned host memory, staged per layer (default: on for llama7b)")
+    ap.add_argument("--decode-steps", type=int, default=32, help="timed greedy decode steps after the blend (0: none)")
     ap.add_argument("--codec", default=True, action=argparse.BooleanOptionalAction,
                     help="with staged chunks: also time int8 / int4 quantised staging")
     ap.add_argument("--variants", default=True, action=argparse.BooleanOptionalAction,

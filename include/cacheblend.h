@@ -329,13 +329,15 @@ typedef struct {
 /* One prompt: cached chunks (by registry id) in order, then the query tokens
  * (uncached, always recomputed).  A system prefix is simply the first chunk.
  *   query_ids: device int32 [n_query] (n_query >= 1)
- *   fused_k, fused_v: caller-owned [n_layers][N][n_kv_heads][head_dim] (N = all
- *     prompt tokens): the blended cache, written by the call
+ *   fused_k, fused_v: caller-owned [n_layers][kv_capacity][n_kv_heads][head_dim] (N = all
+ *     prompt tokens <= kv_capacity): the blended cache, rows 0..N-1 written by the call
  *   out_hidden: NULL or fp32 [N][d_model]; rows of the final recomputed set are
  *     written (other rows untouched)
  *   out_sel: NULL or int32 [n_layers][N]: per layer the recomputed token indices,
  *     ascending; out_sel_count: NULL or int32 [n_layers] (device)
- *   out_first_token: NULL or int32 [1]: argmax of the LM head at the last token */
+ *   out_first_token: NULL or int32 [1]: argmax of the LM head at the last token
+ *   kv_capacity: rows per layer of fused_k / fused_v (0: exactly N); a capacity above N leaves
+ *     room to decode after the blend (cb_decode_step) */
 typedef struct {
   int n_chunks;
   const uint64_t* chunk_ids_host;
@@ -347,6 +349,7 @@ typedef struct {
   int32_t* out_sel;
   int32_t* out_sel_count;
   int32_t* out_first_token;
+  int kv_capacity;
 } cb_request;
 
 /* Whole blended prefill of n_req prompts (batched: the projections of all
@@ -362,6 +365,30 @@ cb_status cb_blend_prefill(cb_ctx* ctx, const cb_request* reqs, int n_req, const
  * first_token: NULL or int32 [1]. */
 cb_status cb_full_prefill(cb_ctx* ctx, const int32_t* ids, int n, void* k_out, void* v_out, float* out_hidden,
                           int32_t* first_token, void* stream);
+
+/* --------------------------------------------------------------------- decode
+ * Generation after the blend: the response is produced from the fused KV ([P3] flow: "융합한 KV로
+ * 응답 생성"; [P1] 実験結果 reports the decoding throughput that follows).  One step feeds one token
+ * per sequence at position n_past: per layer its q, k, v are computed (RoPE at n_past), its K/V
+ * are written to row n_past of the sequence's cache, its query attends causally to rows
+ * 0..n_past (split over the keys across the GPU, then merged), then output projection and MLP;
+ * the LM head's argmax (ties to the lowest id) is the next token.
+ *   fused_k, fused_v: [n_layers][kv_capacity][n_kv_heads][head_dim] (a blend's fused cache made
+ *     with kv_capacity >= the prompt length + the tokens to generate); rows 0..n_past-1 hold
+ *     the context; n_past + 1 <= kv_capacity.
+ *   out_hidden: NULL or fp32 [d_model]: the token's final hidden state (before the last norm). */
+typedef struct {
+  void* fused_k;
+  void* fused_v;
+  int kv_capacity;
+  int n_past;
+  float* out_hidden;
+} cb_decode_seq;
+/* One decode step of n_seq sequences (n_seq <= the workspace's max_requests and max_tokens;
+ * at most 16 query heads per KV head; head_dim 64 or 128).  tokens: device int32 [n_seq];
+ * out_tokens: device int32 [n_seq] (may be the same array as tokens).  No batch may be active. */
+cb_status cb_decode_step(cb_ctx* ctx, const cb_decode_seq* seqs_host, int n_seq, const int32_t* tokens,
+                         int32_t* out_tokens, void* stream);
 
 /* --------------------------------------------------------------------- per-layer API
  * The pages' three calls ([P1] vLLMとの統合): fetch_kv(text, layer_id) loads a layer's

@@ -29,7 +29,7 @@ EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
             "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_set_orientation",
             "cb_set_launch_overlap", "cb_codec_layer_bytes", "cb_kv_encode", "cb_kv_decode", "cb_register_chunk_codec",
-            "cb_set_staging", "cb_chunk_hash", "cb_chunk_info_of", "cb_plan_loading")
+            "cb_set_staging", "cb_chunk_hash", "cb_chunk_info_of", "cb_plan_loading", "cb_decode_step")
 PHASES = ("begin", "staged_rot", "norm", "qkv", "rope", "deviation", "select", "scatter", "attention", "oproj",
           "gateup", "down", "finish")
 
@@ -64,7 +64,13 @@ class BlendParams(C.Structure):
 class Request(C.Structure):
     _fields_ = [("n_chunks", C.c_int), ("chunk_ids_host", C.POINTER(C.c_uint64)), ("query_ids", C.c_void_p),
                 ("n_query", C.c_int), ("fused_k", C.c_void_p), ("fused_v", C.c_void_p), ("out_hidden", C.c_void_p),
-                ("out_sel", C.c_void_p), ("out_sel_count", C.c_void_p), ("out_first_token", C.c_void_p)]
+                ("out_sel", C.c_void_p), ("out_sel_count", C.c_void_p), ("out_first_token", C.c_void_p),
+                ("kv_capacity", C.c_int)]
+
+
+class DecodeSeq(C.Structure):
+    _fields_ = [("fused_k", C.c_void_p), ("fused_v", C.c_void_p), ("kv_capacity", C.c_int), ("n_past", C.c_int),
+                ("out_hidden", C.c_void_p)]
 
 
 class ChunkInfo(C.Structure):
@@ -126,6 +132,7 @@ def load_library(path: str = LIB_PATH):
         "cb_register_chunk_codec": (st, [vp, C.c_uint64, i32p, vp, C.c_int, C.c_int, C.c_int]),
         "cb_set_staging": (st, [vp, vp, C.c_size_t]),
         "cb_chunk_hash": (C.c_uint64, [C.POINTER(C.c_int32), C.c_int]),
+        "cb_decode_step": (st, [vp, C.POINTER(DecodeSeq), C.c_int, vp, vp, vp]),
         "cb_chunk_info_of": (st, [vp, C.c_uint64, C.POINTER(ChunkInfo)]),
         "cb_plan_loading": (st, [C.POINTER(CostModel), C.POINTER(ChunkInfo), C.c_int, C.c_int, C.POINTER(C.c_int32),
                                  C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(C.c_double)]),
@@ -429,12 +436,15 @@ class Engine:
         self._chunks.pop(chunk_id, None)
 
     # -- requests
-    def make_request(self, chunk_ids: Sequence[int], query_ids: torch.Tensor, want_hidden=True, want_sel=True):
+    def make_request(self, chunk_ids: Sequence[int], query_ids: torch.Tensor, want_hidden=True, want_sel=True,
+                     decode_room: int = 0):
+        """Buffers of one blend request; ``decode_room`` extra cache rows per layer leave room to
+        decode that many tokens after the blend (cb_decode_step)."""
         n = sum(self._chunks[c][0].numel() for c in chunk_ids) + query_ids.numel()
         L, d = self.cfg.n_layers, self.cfg.d_model
         r = {
-            "chunk_ids": list(chunk_ids), "query_ids": query_ids, "n_tokens": n,
-            "fused_k": torch.empty(self.kv_shape(n), dtype=self.dtype, device=self.device),
+            "chunk_ids": list(chunk_ids), "query_ids": query_ids, "n_tokens": n, "kv_capacity": n + int(decode_room),
+            "fused_k": torch.empty(self.kv_shape(n + int(decode_room)), dtype=self.dtype, device=self.device),
             "first_token": torch.full((1,), -1, dtype=torch.int32, device=self.device),
         }
         r["fused_v"] = torch.empty_like(r["fused_k"])
@@ -454,7 +464,7 @@ class Engine:
                              None if r["hidden"] is None else r["hidden"].data_ptr(),
                              None if r["sel"] is None else r["sel"].data_ptr(),
                              None if r["sel_count"] is None else r["sel_count"].data_ptr(),
-                             r["first_token"].data_ptr())
+                             r["first_token"].data_ptr(), int(r.get("kv_capacity", 0)))
         return arr, keep
 
     def _c_params(self, ratios, dev_mode=0, forced=None, seam_tokens=None):
@@ -517,6 +527,24 @@ class Engine:
         _check(self.lib.cb_full_prefill(self.ctx, _ptr(ids), n, _ptr(out.get("k")), _ptr(out.get("v")),
                                         _ptr(out["hidden"]), _ptr(out["first_token"]), _stream(stream)), self.ctx)
         return out
+
+    def decode_step(self, reqs, tokens: torch.Tensor, out_tokens: Optional[torch.Tensor] = None, n_past=None,
+                    out_hidden=None, stream=None) -> torch.Tensor:
+        """One greedy decode step of the blended requests ``reqs`` (made with decode_room):
+        tokens [n] enter at positions n_past[i] (default: each request's prompt length plus the
+        steps it already decoded); returns the next tokens [n]."""
+        n = len(reqs)
+        out_tokens = torch.empty(n, dtype=torch.int32, device=self.device) if out_tokens is None else out_tokens
+        arr = (DecodeSeq * n)()
+        for i, r in enumerate(reqs):
+            past = r["n_tokens"] + r.setdefault("decoded", 0) if n_past is None else int(n_past[i])
+            arr[i] = DecodeSeq(r["fused_k"].data_ptr(), r["fused_v"].data_ptr(), int(r["kv_capacity"]), past,
+                               None if out_hidden is None else out_hidden[i].data_ptr())
+        _check(self.lib.cb_decode_step(self.ctx, arr, n, _ptr(tokens), _ptr(out_tokens), _stream(stream)), self.ctx)
+        if n_past is None:
+            for r in reqs:
+                r["decoded"] += 1
+        return out_tokens
 
     def get_status(self, stream=None, timeout_ms: int = 60000):
         _check(self.lib.cb_get_status(self.ctx, _stream(stream), timeout_ms), self.ctx)

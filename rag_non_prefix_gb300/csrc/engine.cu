@@ -208,6 +208,8 @@ struct cb_ctx {
   void* tmp_v = nullptr;
   float* logits = nullptr;
   float* xlast = nullptr;
+  float* dec_o = nullptr;
+  float2* dec_ml = nullptr;
   void* gemm_scratch = nullptr;
   size_t gemm_scratch_bytes = 0;
   uint8_t* meta = nullptr;  // plan, requests, tiles, segments, row ids ... (uploaded per batch)
@@ -332,7 +334,7 @@ bool valid_cfg(const cb_model_cfg& c, std::string* why) {
 
 struct WsLayout {
   size_t status, rope, tok, pos0, pos1, req0, req1, src, dev, h0, h1, x, qkv, q, attn, act, tmpk, tmpv, logits,
-      xlast, gemm, meta, total, meta_bytes;
+      xlast, gemm, dec_o, dec_ml, meta, total, meta_bytes;
 };
 
 WsLayout ws_layout(const cb_model_cfg& c, int T, int R) {
@@ -367,6 +369,10 @@ WsLayout ws_layout(const cb_model_cfg& c, int T, int R) {
   w.logits = take(static_cast<size_t>(R) * c.vocab * 4);
   w.xlast = take(static_cast<size_t>(R) * c.d_model * 4);
   w.gemm = take(gemm_scratch_bytes());
+  // decode attention: per (sequence, head, key range) partial outputs and (max, sum)
+  const size_t dec_rows = static_cast<size_t>(R) * c.n_heads * DECODE_MAX_SPLITS;
+  w.dec_o = take(dec_rows * c.head_dim * 4);
+  w.dec_ml = take(dec_rows * sizeof(float2));
   // metadata: plan, requests, tiles, segments, forced sets, last rows, counts, first-token pointers
   const size_t L = c.n_layers;
   size_t m = 0;
@@ -1078,6 +1084,8 @@ cb_status cb_set_workspace(cb_ctx* ctx, void* ws, size_t bytes, int max_tokens, 
   ctx->xlast = reinterpret_cast<float*>(base + w.xlast);
   ctx->gemm_scratch = base + w.gemm;
   ctx->gemm_scratch_bytes = gemm_scratch_bytes();
+  ctx->dec_o = reinterpret_cast<float*>(base + w.dec_o);
+  ctx->dec_ml = reinterpret_cast<float2*>(base + w.dec_ml);
   ctx->meta = base + w.meta;
   ctx->meta_bytes = w.meta_bytes;
   // rotary table: (cos, sin) of p * theta^(-2i/dh), evaluated in double on the host
@@ -1310,11 +1318,13 @@ static cb_status build_blend_requests(cb_ctx* ctx, const cb_request* reqs, int n
     }
     N += q.n_query;
     if (N > c.max_positions) return fail(ctx, CB_ERR_SHAPE, "prompt longer than max_positions");
+    if (q.kv_capacity != 0 && q.kv_capacity < N) return fail(ctx, CB_ERR_SHAPE, "kv_capacity below the prompt length");
+    const int cap = q.kv_capacity ? q.kv_capacity : N;
     in[r].query_ids = q.query_ids;
     in[r].n_query = q.n_query;
     in[r].fused_k = q.fused_k;
     in[r].fused_v = q.fused_v;
-    in[r].layer_stride = static_cast<long long>(N) * c.n_kv_heads * c.head_dim;
+    in[r].layer_stride = static_cast<long long>(cap) * c.n_kv_heads * c.head_dim;
     in[r].out_hidden = q.out_hidden;
     in[r].out_sel = q.out_sel;
     in[r].out_sel_count = q.out_sel_count;
@@ -1400,6 +1410,110 @@ cb_status cb_blend_prefill(cb_ctx* ctx, const cb_request* reqs, int n_req, const
     }
   }
   return finish_impl(ctx, as_stream(stream));
+}
+
+// ----------------------------------------------------------------------------- decode
+cb_status cb_decode_step(cb_ctx* ctx, const cb_decode_seq* seqs, int n_seq, const int32_t* tokens,
+                         int32_t* out_tokens, void* stream) {
+  if (!ctx || !seqs || !tokens || !out_tokens || n_seq < 1) return fail(ctx, CB_ERR_INVALID_ARG, "bad decode arguments");
+  if (!ctx->ws) return fail(ctx, CB_ERR_WORKSPACE, "no workspace bound");
+  if (ctx->b.active) return fail(ctx, CB_ERR_STATE, "a blend batch is active (finish it first)");
+  if (n_seq > ctx->ws_reqs || n_seq > ctx->ws_tokens)
+    return fail(ctx, CB_ERR_WORKSPACE, "more sequences than the workspace's max_requests / max_tokens");
+  const cb_model_cfg& c = ctx->cfg;
+  if (c.n_heads / c.n_kv_heads > 16) return fail(ctx, CB_ERR_SHAPE, "decode supports at most 16 query heads per KV head");
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(ctx, CB_ERR_SHAPE, "decode needs head_dim 64 or 128");
+  const int H = c.n_heads, Hkv = c.n_kv_heads, dh = c.head_dim, d = c.d_model;
+  const int qw = H * dh, kvw = Hkv * dh;
+  cudaStream_t s = as_stream(stream);
+  std::vector<ReqDev> rd(n_seq);
+  std::vector<int32_t> pos(n_seq), req(n_seq);
+  int max_keys = 1;
+  for (int i = 0; i < n_seq; ++i) {
+    const cb_decode_seq& q = seqs[i];
+    if (!q.fused_k || !q.fused_v || !aligned16(q.fused_k) || !aligned16(q.fused_v))
+      return fail(ctx, CB_ERR_INVALID_ARG, "bad fused cache of a decode sequence");
+    if (q.n_past < 0 || q.kv_capacity < q.n_past + 1) return fail(ctx, CB_ERR_SHAPE, "no room in the cache for the new token");
+    if (q.n_past + 1 > c.max_positions) return fail(ctx, CB_ERR_SHAPE, "position beyond max_positions");
+    rd[i] = ReqDev{q.fused_k, q.fused_v, static_cast<long long>(q.kv_capacity) * kvw, q.n_past + 1, q.n_past};
+    pos[i] = q.n_past;
+    req[i] = i;
+    max_keys = std::max(max_keys, q.n_past + 1);
+  }
+  int split_len = 0, n_splits = 0;
+  decode_split_plan(n_seq, Hkv, max_keys, &split_len, &n_splits);
+  // metadata: request descriptors, positions, request indices, last rows (= 0..n-1)
+  const size_t szReq = align_up(n_seq * sizeof(ReqDev), 256), szI = align_up(n_seq * 4, 256);
+  const size_t total = szReq + 3 * szI;
+  if (total > ctx->meta_bytes) return fail(ctx, CB_ERR_WORKSPACE, "decode metadata exceeds the workspace");
+  cb_status st = ensure_pinned(ctx, total);
+  if (st != CB_OK) return st;
+  std::memcpy(ctx->pinned, rd.data(), n_seq * sizeof(ReqDev));
+  std::memcpy(ctx->pinned + szReq, pos.data(), n_seq * 4);
+  std::memcpy(ctx->pinned + szReq + szI, req.data(), n_seq * 4);
+  std::memcpy(ctx->pinned + szReq + 2 * szI, req.data(), n_seq * 4);  // last rows: row i of sequence i
+  CB_CUDA(ctx, cudaMemcpyAsync(ctx->meta, ctx->pinned, total, cudaMemcpyHostToDevice, s));
+  CB_CUDA(ctx, cudaEventRecord(ctx->pinned_ev, s));
+  ctx->pinned_pending = true;
+  const ReqDev* d_rd = reinterpret_cast<const ReqDev*>(ctx->meta);
+  const int32_t* d_pos = reinterpret_cast<const int32_t*>(ctx->meta + szReq);
+  const int32_t* d_req = reinterpret_cast<const int32_t*>(ctx->meta + szReq + szI);
+  const int32_t* d_rows = reinterpret_cast<const int32_t*>(ctx->meta + szReq + 2 * szI);
+  float* h = ctx->h[0];
+  {
+    PhaseScope ps(ctx, CB_PH_BEGIN, s, 1);
+    CB_CUDA(ctx, launch_embed(ctx->embed, tokens, n_seq, d, c.vocab, c.dtype, h, ctx->status, s));
+  }
+  for (int i = 0; i < c.n_layers; ++i) {
+    {
+      PhaseScope ps(ctx, CB_PH_NORM, s, 1);
+      CB_CUDA(ctx, launch_rmsnorm(h, n_seq, d, c.rms_eps, ctx->x, c.dtype, s));
+    }
+    {
+      PhaseScope ps(ctx, CB_PH_QKV, s, 1);
+      CB_CUDA(ctx, launch_gemm(ctx->x, ctx->wq[i], ctx->wk[i], ctx->wv[i], qw, qw + kvw, ctx->qkv, n_seq, qw + 2 * kvw,
+                               d, qw + 2 * kvw, 0, c.dtype, ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
+    }
+    {
+      PhaseScope ps(ctx, CB_PH_SCATTER, s, 1);  // RoPE of q and k, the new K/V row appended to the cache
+      CB_CUDA(ctx, launch_post_qkv(ctx->qkv, n_seq, nullptr, d_pos, d_req, d_rd, i, H, Hkv, dh, ctx->rope,
+                                   c.max_positions, c.dtype, ctx->q, h, h, d, ctx->status, s));
+    }
+    {
+      PhaseScope ps(ctx, CB_PH_ATTENTION, s, n_splits > 1 ? 2 : 1);
+      CB_CUDA(ctx, launch_decode_attention(ctx->q, d_pos, d_rd, n_seq, i, H, Hkv, dh, split_len, n_splits, ctx->dec_o,
+                                           ctx->dec_ml, ctx->attn, c.dtype, ctx->status, s));
+    }
+    {
+      PhaseScope ps(ctx, CB_PH_OPROJ, s, 1);
+      CB_CUDA(ctx, launch_gemm(ctx->attn, ctx->wo[i], nullptr, nullptr, d, d, h, n_seq, d, qw, d, 1, c.dtype,
+                               ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
+    }
+    {
+      PhaseScope ps(ctx, CB_PH_NORM, s, 1);
+      CB_CUDA(ctx, launch_rmsnorm(h, n_seq, d, c.rms_eps, ctx->x, c.dtype, s));
+    }
+    {
+      PhaseScope ps(ctx, CB_PH_GATEUP, s, 1);
+      CB_CUDA(ctx, launch_gemm(ctx->x, ctx->wg[i], ctx->wu[i], nullptr, 0, 0, ctx->act, n_seq, 2 * c.ffn_dim, d,
+                               c.ffn_dim, 2, c.dtype, ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
+    }
+    {
+      PhaseScope ps(ctx, CB_PH_DOWN, s, 1);
+      CB_CUDA(ctx, launch_gemm(ctx->act, ctx->wd[i], nullptr, nullptr, d, d, h, n_seq, d, c.ffn_dim, d, 1, c.dtype,
+                               ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
+    }
+  }
+  {
+    PhaseScope ps(ctx, CB_PH_FINISH, s, 2 + (n_seq + 15) / 16);
+    CB_CUDA(ctx, launch_last_rows_norm(h, d_rows, n_seq, d, c.rms_eps, ctx->xlast, s));
+    CB_CUDA(ctx, launch_lm_head(ctx->xlast, n_seq, d, ctx->lm, c.vocab, c.dtype, ctx->logits, s));
+    CB_CUDA(ctx, launch_argmax(ctx->logits, n_seq, c.vocab, nullptr, out_tokens, s));
+  }
+  for (int i = 0; i < n_seq; ++i)
+    if (seqs[i].out_hidden)
+      CB_CUDA(ctx, cudaMemcpyAsync(seqs[i].out_hidden, h + static_cast<size_t>(i) * d, d * 4, cudaMemcpyDeviceToDevice, s));
+  return CB_OK;
 }
 
 cb_status cb_full_prefill(cb_ctx* ctx, const int32_t* ids, int n, void* k_out, void* v_out, float* out_hidden,

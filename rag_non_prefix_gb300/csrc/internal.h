@@ -116,6 +116,15 @@ cudaError_t launch_codec_decode(const CodecSeg* segs, int n_segs, int max_n, int
 // cs_host: head_dim/2 (cos, sin) pairs of the rotation
 cudaError_t launch_codec_decode_blob(const void* blob, int L, int n, int n_kv_heads, int head_dim, int bits,
                                      const float* cs_host, cb_dtype dt, void* k_out, void* v_out, cudaStream_t s);
+// decode attention (one query per sequence over its cache rows 0..pos): key ranges of
+// split_len keys, n_splits of them (decode_split_plan picks both); the partial buffers hold
+// n_seq * n_heads * n_splits rows of head_dim floats and (max, sum) pairs.
+constexpr int DECODE_MAX_SPLITS = 32;
+void decode_split_plan(int n_seq, int n_kv_heads, int max_keys, int* split_len, int* n_splits);
+cudaError_t launch_decode_attention(const void* q, const int32_t* pos, const ReqDev* reqs, int n_seq, int layer,
+                                    int n_heads, int n_kv_heads, int head_dim, int split_len, int n_splits,
+                                    float* part_o, float2* part_ml, void* out, cb_dtype dt, int32_t* status,
+                                    cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x, cb_dtype dt, cudaStream_t s);
 // (both rotate the fresh q / k of the fp32 projection output at each row's position)
 cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* pos, const int32_t* req,

@@ -32,7 +32,7 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 class GpuWorkload:
     """A workload on the GPU: weights, an engine, every chunk precomputed and registered."""
 
-    def __init__(self, spec: hz.PromptSpec, on_host: bool = False, max_tokens=None):
+    def __init__(self, spec: hz.PromptSpec, on_host: bool = False, max_tokens=None, extra_positions: int = 0):
         built()
         self.spec = spec
         self.cfg = spec.cfg
@@ -40,7 +40,7 @@ class GpuWorkload:
         total = sum(spec.n_tokens(r) for r in range(len(spec.requests)))
         longest = max(max(len(c) for c in spec.chunks), max(spec.n_tokens(r) for r in range(len(spec.requests))))
         self.eng = cb.Engine(self.cfg, self.W, max_tokens=max_tokens or max(total, longest),
-                             max_requests=len(spec.requests), max_positions=longest + 1)
+                             max_requests=len(spec.requests), max_positions=longest + 1 + extra_positions)
         self.chunk_kv = {}
         used = sorted({s.chunk for req in spec.requests for s in req if s.chunk >= 0})
         for c in used:

@@ -53,7 +53,8 @@ def test_struct_layout_matches_c_compiler(tmp_path):
         "int main(void){\n"
         'printf("%zu %zu %zu %zu %zu\\n", sizeof(cb_model_cfg), offsetof(cb_model_cfg, rope_theta),'
         " offsetof(cb_model_cfg, rms_eps), offsetof(cb_model_cfg, dtype), offsetof(cb_model_cfg, max_positions));\n"
-        'printf("%zu %zu %zu\\n", sizeof(cb_request), offsetof(cb_request, n_query), offsetof(cb_request, out_first_token));\n'
+        'printf("%zu %zu %zu %zu\\n", sizeof(cb_request), offsetof(cb_request, n_query), offsetof(cb_request, out_first_token), offsetof(cb_request, kv_capacity));\n'
+        'printf("%zu %zu %zu\\n", sizeof(cb_decode_seq), offsetof(cb_decode_seq, n_past), offsetof(cb_decode_seq, out_hidden));\n'
         'printf("%zu %zu %zu %zu %zu\\n", sizeof(cb_blend_params), offsetof(cb_blend_params, dev_mode),'
         " offsetof(cb_blend_params, forced_sel_host), offsetof(cb_blend_params, select_mode),"
         " offsetof(cb_blend_params, seam_tokens));\n"
@@ -65,11 +66,14 @@ def test_struct_layout_matches_c_compiler(tmp_path):
     assert lines[0].split() == [str(v) for v in (C.sizeof(m), m.rope_theta.offset, m.rms_eps.offset, m.dtype.offset,
                                                  m.max_positions.offset)]
     r = cb.Request
-    assert lines[1].split() == [str(v) for v in (C.sizeof(r), r.n_query.offset, r.out_first_token.offset)]
+    assert lines[1].split() == [str(v) for v in (C.sizeof(r), r.n_query.offset, r.out_first_token.offset,
+                                                 r.kv_capacity.offset)]
+    ds = cb.DecodeSeq
+    assert lines[2].split() == [str(v) for v in (C.sizeof(ds), ds.n_past.offset, ds.out_hidden.offset)]
     p = cb.BlendParams
-    assert lines[2].split() == [str(v) for v in (C.sizeof(p), p.dev_mode.offset, p.forced_sel_host.offset,
+    assert lines[3].split() == [str(v) for v in (C.sizeof(p), p.dev_mode.offset, p.forced_sel_host.offset,
                                                  p.select_mode.offset, p.seam_tokens.offset)]
-    assert lines[3].strip() == str(C.sizeof(cb.Weights))
+    assert lines[4].strip() == str(C.sizeof(cb.Weights))
 
 
 @pytest.mark.parametrize("L,r,sched", [(2, 0.15, "fixed"), (32, 0.15, "gradual"), (60, 0.15, "gradual"),
