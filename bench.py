@@ -293,6 +293,11 @@ def run_ours(args, rank, world):
             b.synchronize()
             ts.append(a.elapsed_time(b))
         dprof = eng.get_profile()
+        eng.set_profiling(True)
+        tok = eng.decode_step(dreqs, tok)
+        torch.cuda.synchronize()
+        dph = eng.get_profile()
+        eng.set_profiling(False)
         eng.get_status()
         ms = statistics.mean(ts)
         n_seq = len(dreqs)
@@ -310,7 +315,8 @@ def run_ours(args, rank, world):
                                "frac": round(gbs / peaks_d["hbm_gbs"], 4), "bytes_per_step": int(by),
                                "weight_bytes": int(wbytes), "kv_bytes": int(kvbytes),
                                "peak_source": f"{peaks_d['source']} HBM copy"},
-                  "launches_per_step": sum(v["launches"] for v in dprof.values()) / args.decode_steps}
+                  "launches_per_step": sum(v["launches"] for v in dprof.values()) / args.decode_steps,
+                  "phase_ms": {k_: round(v_["ms"], 4) for k_, v_ in dph.items() if v_["calls"]}}
         copy_stream = cs_saved_d
 
     # selection variants on the same prompt: cosine deviation (same schedule) and spatial

@@ -385,7 +385,7 @@ typedef struct {
   float* out_hidden;
 } cb_decode_seq;
 /* One decode step of n_seq sequences (n_seq <= the workspace's max_requests and max_tokens;
- * at most 16 query heads per KV head; head_dim 64 or 128).  tokens: device int32 [n_seq];
+ * 1, 2, 4, 7, 8 or 16 query heads per KV head; head_dim 64 or 128).  tokens: device int32 [n_seq];
  * out_tokens: device int32 [n_seq] (may be the same array as tokens).  No batch may be active. */
 cb_status cb_decode_step(cb_ctx* ctx, const cb_decode_seq* seqs_host, int n_seq, const int32_t* tokens,
                          int32_t* out_tokens, void* stream);

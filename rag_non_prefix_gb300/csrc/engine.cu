@@ -370,7 +370,7 @@ WsLayout ws_layout(const cb_model_cfg& c, int T, int R) {
   w.xlast = take(static_cast<size_t>(R) * c.d_model * 4);
   w.gemm = take(gemm_scratch_bytes());
   // decode attention: per (sequence, head, key range) partial outputs and (max, sum)
-  const size_t dec_rows = static_cast<size_t>(R) * c.n_heads * DECODE_MAX_SPLITS;
+  const size_t dec_rows = static_cast<size_t>(R) * c.n_heads * decode_splits(c.max_positions);
   w.dec_o = take(dec_rows * c.head_dim * 4);
   w.dec_ml = take(dec_rows * sizeof(float2));
   // metadata: plan, requests, tiles, segments, forced sets, last rows, counts, first-token pointers
@@ -1421,7 +1421,11 @@ cb_status cb_decode_step(cb_ctx* ctx, const cb_decode_seq* seqs, int n_seq, cons
   if (n_seq > ctx->ws_reqs || n_seq > ctx->ws_tokens)
     return fail(ctx, CB_ERR_WORKSPACE, "more sequences than the workspace's max_requests / max_tokens");
   const cb_model_cfg& c = ctx->cfg;
-  if (c.n_heads / c.n_kv_heads > 16) return fail(ctx, CB_ERR_SHAPE, "decode supports at most 16 query heads per KV head");
+  {
+    const int g = c.n_heads / c.n_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 7 && g != 8 && g != 16)
+      return fail(ctx, CB_ERR_SHAPE, "decode supports 1, 2, 4, 7, 8 or 16 query heads per KV head");
+  }
   if (c.head_dim != 64 && c.head_dim != 128) return fail(ctx, CB_ERR_SHAPE, "decode needs head_dim 64 or 128");
   const int H = c.n_heads, Hkv = c.n_kv_heads, dh = c.head_dim, d = c.d_model;
   const int qw = H * dh, kvw = Hkv * dh;
@@ -1440,8 +1444,7 @@ cb_status cb_decode_step(cb_ctx* ctx, const cb_decode_seq* seqs, int n_seq, cons
     req[i] = i;
     max_keys = std::max(max_keys, q.n_past + 1);
   }
-  int split_len = 0, n_splits = 0;
-  decode_split_plan(n_seq, Hkv, max_keys, &split_len, &n_splits);
+  const int n_splits = decode_splits(max_keys);
   // metadata: request descriptors, positions, request indices, last rows (= 0..n-1)
   const size_t szReq = align_up(n_seq * sizeof(ReqDev), 256), szI = align_up(n_seq * 4, 256);
   const size_t total = szReq + 3 * szI;
@@ -1481,8 +1484,8 @@ cb_status cb_decode_step(cb_ctx* ctx, const cb_decode_seq* seqs, int n_seq, cons
     }
     {
       PhaseScope ps(ctx, CB_PH_ATTENTION, s, n_splits > 1 ? 2 : 1);
-      CB_CUDA(ctx, launch_decode_attention(ctx->q, d_pos, d_rd, n_seq, i, H, Hkv, dh, split_len, n_splits, ctx->dec_o,
-                                           ctx->dec_ml, ctx->attn, c.dtype, ctx->status, s));
+      CB_CUDA(ctx, launch_decode_attention(ctx->q, d_pos, d_rd, n_seq, i, H, Hkv, dh, n_splits, ctx->dec_o, ctx->dec_ml,
+                                           ctx->attn, c.dtype, ctx->status, s));
     }
     {
       PhaseScope ps(ctx, CB_PH_OPROJ, s, 1);

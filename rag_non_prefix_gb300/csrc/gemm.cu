@@ -1000,6 +1000,8 @@ cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const voi
                         int M, int N, int K, int ldc, int mode, cb_dtype dt, int32_t* status, void* scratch,
                         size_t scratch_bytes, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
+  if (gemv_applies(M, K, dt, A, B0, B1, B2))
+    return launch_gemv(A, B0, B1, B2, split0, split1, C, M, N, K, ldc, mode, dt, s);
   if (dt == CB_F32) {
     if (mode == EPI_SWIGLU) {
       dim3 grid((M + simt::TM - 1) / simt::TM, (N / 2 + simt::TN - 1) / simt::TN);

@@ -117,14 +117,13 @@ cudaError_t launch_codec_decode(const CodecSeg* segs, int n_segs, int max_n, int
 cudaError_t launch_codec_decode_blob(const void* blob, int L, int n, int n_kv_heads, int head_dim, int bits,
                                      const float* cs_host, cb_dtype dt, void* k_out, void* v_out, cudaStream_t s);
 // decode attention (one query per sequence over its cache rows 0..pos): key ranges of
-// split_len keys, n_splits of them (decode_split_plan picks both); the partial buffers hold
-// n_seq * n_heads * n_splits rows of head_dim floats and (max, sum) pairs.
-constexpr int DECODE_MAX_SPLITS = 32;
-void decode_split_plan(int n_seq, int n_kv_heads, int max_keys, int* split_len, int* n_splits);
+// DECODE_KEYS keys, decode_splits() of them for the longest sequence; the partial buffers
+// hold n_seq * n_heads * n_splits rows of head_dim floats and (max, sum) pairs.
+constexpr int DECODE_KEYS = 128;
+int decode_splits(int max_keys);
 cudaError_t launch_decode_attention(const void* q, const int32_t* pos, const ReqDev* reqs, int n_seq, int layer,
-                                    int n_heads, int n_kv_heads, int head_dim, int split_len, int n_splits,
-                                    float* part_o, float2* part_ml, void* out, cb_dtype dt, int32_t* status,
-                                    cudaStream_t s);
+                                    int n_heads, int n_kv_heads, int head_dim, int n_splits, float* part_o,
+                                    float2* part_ml, void* out, cb_dtype dt, int32_t* status, cudaStream_t s);
 cudaError_t launch_rmsnorm(const float* h, int n_rows, int d, float eps, void* x, cb_dtype dt, cudaStream_t s);
 // (both rotate the fresh q / k of the fp32 projection output at each row's position)
 cudaError_t launch_deviation_rows(const float* qkv, int n_rows, const int32_t* pos, const int32_t* req,
@@ -146,6 +145,15 @@ cudaError_t launch_post_qkv(const float* qkv, int n_s_rows, const int32_t* s_src
 cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, void* C,
                         int M, int N, int K, int ldc, int mode, cb_dtype dt, int32_t* status, void* scratch,
                         size_t scratch_bytes, cudaStream_t s);
+// Projections of at most GEMV_MAX_ROWS token rows stream the weights with a warp-per-feature
+// kernel (launch_gemm takes that path by itself when gemv_applies).
+constexpr int GEMV_MAX_ROWS = 2;  // measured: from 3-4 rows on the tensor-core tiles stream faster
+bool gemv_applies(int M, int K, cb_dtype dt, const void* A, const void* B0, const void* B1, const void* B2);
+cudaError_t launch_gemv(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, void* C,
+                        int M, int N, int K, int ldc, int mode, cb_dtype dt, cudaStream_t s);
+// logits fp32 [M][vocab] = x fp32 [M][d] . W^T for M <= GEMV_MAX_ROWS (d % 8 == 0)
+cudaError_t launch_gemv_f32a(const float* x, const void* W, int M, int vocab, int d, float* logits, cb_dtype dt,
+                             cudaStream_t s);
 // bytes of GEMM scratch (stream-K partial tiles + flags) that enable every schedule
 size_t gemm_scratch_bytes();
 void gemm_set_orientation(int o);  // 0 model, 1 token rows, 2 weight rows

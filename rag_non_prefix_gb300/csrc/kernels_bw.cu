@@ -575,6 +575,10 @@ __global__ void lm_head_kernel(const float* __restrict__ x, int n_req, int d, co
 cudaError_t launch_lm_head(const float* x, int n_req, int d, const void* w, int vocab, cb_dtype dt, float* logits,
                            cudaStream_t s) {
   if (n_req <= 0) return cudaSuccess;
+  // a row or two (the decode step, a single blended request): the weight-streaming GEMV
+  if (n_req <= GEMV_MAX_ROWS && d % 8 == 0 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0 &&
+      (reinterpret_cast<uintptr_t>(x) & 15u) == 0)
+    return launch_gemv_f32a(x, w, n_req, vocab, d, logits, dt, s);
   for (int r0 = 0; r0 < n_req; r0 += LM_MAX_REQ) {
     const int nr = n_req - r0 < LM_MAX_REQ ? n_req - r0 : LM_MAX_REQ;
     const int blocks = (vocab + 7) / 8;

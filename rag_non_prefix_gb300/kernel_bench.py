@@ -6,6 +6,11 @@
     python -m rag_non_prefix_gb300.kernel_bench select --n 3136 --k 471
     python -m rag_non_prefix_gb300.kernel_bench deviation --n 3200 --kvw 1024
     python -m rag_non_prefix_gb300.kernel_bench codec --n 3136 --hkv 8 --bits 8
+    python -m rag_non_prefix_gb300.kernel_bench decode --layers 32 --steps 2
+
+(`decode` builds the Mistral-7B-shaped model with --layers layers, blends the configuration-2
+prompt, decodes 4 warm-up steps, then --steps steps inside the NVTX range "decode_prof" that
+profilers can filter on.)
 
 Operands are random device tensors sized like one layer of the Mistral-7B-shaped
 workload; weight operands exceed the 129 MB L2 where the shape allows, and a 512 MiB
@@ -48,7 +53,8 @@ def _time(fn, iters, warmup=3, flush=None, batch=1):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("kernel", choices=["gemm", "attention", "rerotate", "select", "deviation", "codec"])
+    ap.add_argument("kernel", choices=["gemm", "attention", "rerotate", "select", "deviation", "codec", "decode"])
+    ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--M", type=int, default=535)
     ap.add_argument("--N", type=int, default=28672)
     ap.add_argument("--K", type=int, default=4096)
@@ -147,6 +153,41 @@ def main():
         eavg, _ = _time(enc, max(3, a.iters // 4), 1, flush, 1)
         out.update(shape=list(shape), bits=a.bits, ms=avg, best_ms=best, gbs=by / (avg * 1e-3) / 1e9, bytes=by,
                    blob_bytes=blob.numel(), encode_ms=eavg)
+    elif a.kernel == "decode":
+        import harness as hz
+        import harness.device as hd
+
+        base = hz.MODELS["mistral7b"]
+        cfg = hz.ModelConfig(f"mistral7b_{a.layers}l", a.layers, base.d_model, base.n_heads, base.n_kv_heads,
+                             base.head_dim, base.ffn_dim, base.vocab, base.rope_theta, base.rms_eps, base.dtype)
+        hz.MODELS[cfg.name] = cfg
+        spec = hz.make_prompt(cfg.name, 2, [512] * 6, 64, 0.15, "gradual", "zipf", prefix_len=64)
+        W = hd.device_weights(cfg, spec.seed)
+        n = spec.n_tokens(0)
+        eng = cb.Engine(cfg, W, max_tokens=n, max_requests=1, max_positions=n + a.steps + 16)
+        for sg in spec.requests[0]:
+            if sg.chunk >= 0:
+                ids = hd.ids_tensor(sg.ids)
+                k, v = eng.precompute_chunk(ids)
+                eng.register_chunk(sg.chunk, ids, k, v)
+        qseg = [sg for sg in spec.requests[0] if sg.chunk < 0][0]
+        req = eng.make_request([sg.chunk for sg in spec.requests[0] if sg.chunk >= 0], hd.ids_tensor(qseg.ids),
+                               want_hidden=False, want_sel=False, decode_room=a.steps + 8)
+        eng.blend_prefill([req], cb.ratio_schedule(cfg.n_layers, 0.15, "gradual"))
+        tok = req["first_token"].clone()
+        for _ in range(4):
+            tok = eng.decode_step([req], tok)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda.nvtx.range_push("decode_prof")
+        ev[0].record()
+        for _ in range(a.steps):
+            tok = eng.decode_step([req], tok)
+        ev[1].record()
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
+        eng.get_status()
+        out.update(layers=a.layers, context=n, steps=a.steps, ms_per_step=ev[0].elapsed_time(ev[1]) / a.steps)
     torch.cuda.synchronize()
     print(json.dumps(out))
 

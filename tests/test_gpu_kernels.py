@@ -181,7 +181,7 @@ def orientation(request):
 
 
 @pytest.mark.parametrize("sk", [False, True], ids=["whole-tiles", "stream-k"])
-@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (71, 256, 512), (128, 384, 256), (300, 768, 1024), (535, 1024, 4096),
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (2, 6144, 4096), (3, 6144, 4096), (8, 1024, 14336), (71, 256, 512), (128, 384, 256), (300, 768, 1024), (535, 1024, 4096),
                                    (1000, 512, 320), (535, 4096, 4096), (535, 4096, 14336), (3000, 6144, 512),
                                    (128, 4096, 14336), (256, 4096, 4096), (200, 2560, 8192), (64, 1024, 28672)])
 def test_gemm_bf16_store_and_add(M, N, K, sk, orientation):
@@ -204,7 +204,7 @@ def test_gemm_bf16_store_and_add(M, N, K, sk, orientation):
 
 
 @pytest.mark.parametrize("sk", [False, True], ids=["whole-tiles", "stream-k"])
-@pytest.mark.parametrize("M,F,K", [(5, 64, 128), (130, 128, 256), (535, 384, 512), (535, 14336, 4096), (96, 2048, 4096),
+@pytest.mark.parametrize("M,F,K", [(1, 14336, 4096), (2, 2048, 1024), (5, 64, 128), (8, 2048, 1024), (130, 128, 256), (535, 384, 512), (535, 14336, 4096), (96, 2048, 4096),
                                    (3200, 1024, 256), (1005, 3584, 1024)])
 def test_gemm_bf16_swiglu(M, F, K, sk, orientation):
     rng = np.random.default_rng(M + F)
@@ -250,7 +250,7 @@ def test_gemm_stream_k_is_deterministic():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 64, 8), (77, 200, 96), (288, 1024, 256)])
+@pytest.mark.parametrize("M,N,K", [(1, 64, 8), (2, 100, 36), (4, 100, 36), (8, 256, 1024), (77, 200, 96), (288, 1024, 256)])
 def test_gemm_f32_all_epilogues(M, N, K):
     rng = np.random.default_rng(M * 3 + N)
     A = _f32(rng.standard_normal((M, K)))
