@@ -154,6 +154,25 @@ def plan_rows(cfg, n_tokens, n_cached, n_query, ratios):
     return rows_R, rows_S
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(values, world: int, device=None):
+    """Element-wise maximum of per-rank scalars over all ranks (the slowest rank's times):
+    replicas share no data, only this reduction and the barriers around the timed region."""
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time (weak scaling)."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world):
     import torch
@@ -442,11 +461,8 @@ def run_ours(args, rank, world):
     d2h = 4 * len(reqs)
 
     # max over ranks
-    vals = torch.tensor([statistics.mean(blend_ms), statistics.mean(full_ms), statistics.mean(e2e), wall],
-                        dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
-    blend_mean, full_mean, e2e_mean, wall = [float(x) for x in vals.cpu()]
+    blend_mean, full_mean, e2e_mean, wall = max_over_ranks(
+        [statistics.mean(blend_ms), statistics.mean(full_ms), statistics.mean(e2e), wall], world, dev)
 
     # roofline of the dominant kernel: the tcgen05 projection GEMM (all four phases)
     rows = [plan_rows(cfg, n_tok[r], spec.n_cached(r), n_tok[r] - spec.n_cached(r), ratios) for r in range(len(reqs))]
@@ -469,7 +485,7 @@ def run_ours(args, rank, world):
     ttft = blend_mean
     out = {
         "metric": METRIC,
-        "value": round(n_total / (ttft * 1e-3), 1),
+        "value": round(job_throughput(T, world, ttft), 1),
         "unit": "tok/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -490,7 +506,7 @@ def run_ours(args, rank, world):
                     "blend_median": round(statistics.median(blend_ms), 4),
                     "full_median": round(statistics.median(full_ms), 4)},
         "speedup_vs_full_prefill": round(full_mean / blend_mean, 3),
-        "full_prefill_tok_s": round(n_total / (full_mean * 1e-3), 1),
+        "full_prefill_tok_s": round(job_throughput(T, world, full_mean), 1),
         "phase_ms": phase_ms,
         "roofline": {"kernel": "gemm_bf16_tc (tcgen05 projections: qkv, o, gate/up, down)", "bound": "tensor",
                      "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "TFLOP/s",
@@ -501,7 +517,7 @@ def run_ours(args, rank, world):
         "rerotate": None if staged else {
             "bytes": rerot_bytes, "ms": phase_ms.get("begin"),
             "gbs": round(rerot_bytes / (phase_ms["begin"] * 1e-3) / 1e9, 1) if phase_ms.get("begin") else None},
-        "e2e": {"value": round(n_total / (e2e_mean * 1e-3), 1), "unit": "tok/s", "ms": round(e2e_mean, 4),
+        "e2e": {"value": round(job_throughput(T, world, e2e_mean), 1), "unit": "tok/s", "ms": round(e2e_mean, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(step_launches * args.steps),
         "sweep": sweep,
