@@ -38,7 +38,8 @@ class GpuWorkload:
         self.cfg = spec.cfg
         self.W = hd.device_weights(self.cfg, spec.seed)
         total = sum(spec.n_tokens(r) for r in range(len(spec.requests)))
-        longest = max(max(len(c) for c in spec.chunks), max(spec.n_tokens(r) for r in range(len(spec.requests))))
+        longest = max(max((len(c) for c in spec.chunks), default=0),
+                      max(spec.n_tokens(r) for r in range(len(spec.requests))))
         self.eng = cb.Engine(self.cfg, self.W, max_tokens=max_tokens or max(total, longest),
                              max_requests=len(spec.requests), max_positions=longest + 1 + extra_positions)
         self.chunk_kv = {}

@@ -295,3 +295,69 @@ def test_synchronize_deadline_on_a_stalled_copy_stream(small_bf16):
     gh.eng.blend_finish()
     gh.eng.get_status()
     torch.cuda.synchronize()
+
+
+# ----------------------------------------------------------------------------- degenerate prompts
+def _custom(model, seed, lens, qlen, ratio=0.2, schedule="gradual"):
+    return hz.make_prompt(model, seed, lens, qlen, ratio, schedule, "uniform", name=f"edge{seed}")
+
+
+@pytest.mark.parametrize("model", ["tiny", "small_bf16"])
+def test_prompt_without_chunks_is_a_full_prefill(model):
+    """No cached chunk: every token is query, recomputed at every layer; the blend is the
+    full prefill of the query (the oracle's blend with Nc = 0 is checked too)."""
+    spec = _custom(model, 41, [], 37)
+    g, o = GpuWorkload(spec), OracleWorkload(spec)
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, 0.2, "gradual")
+    req = g.blend(ratios)[0]
+    ref = o.blend(0, ratios)
+    full = o.full(0)
+    assert np.array_equal(ref["rows"], np.arange(37))
+    assert np.max(np.abs(ref["hidden"] - full["hidden"])) < 1e-9 * max(1.0, np.max(np.abs(full["hidden"])))
+    assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < tol(cfg)
+    sel, cnt = req["sel"].cpu().numpy(), req["sel_count"].cpu().numpy()
+    assert all(cnt[i] == 37 and np.array_equal(sel[i, :37], np.arange(37)) for i in range(cfg.n_layers))
+
+
+@pytest.mark.parametrize("model", ["tiny", "small_bf16"])
+def test_one_token_chunks_and_a_one_token_query(model):
+    """Chunks of one token (re-rotation rows of one, deviation of single rows) and a query of
+    one token: the sets and hidden states follow the oracle."""
+    spec = _custom(model, 42, [1, 1, 5, 1, 130], 1, ratio=0.5)
+    g, o = GpuWorkload(spec), OracleWorkload(spec)
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, 0.5, "gradual")
+    ref = o.blend(0, ratios)
+    forced = forced_from_oracle(ref, ref["n_cached"], cfg.n_layers, ratios)
+    req = g.blend(ratios, forced=forced)[0]
+    assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < tol(cfg)
+    if cfg.dtype == "f32":
+        free = g.blend(ratios)[0]
+        sel, cnt = free["sel"].cpu().numpy(), free["sel_count"].cpu().numpy()
+        for i in range(cfg.n_layers):
+            assert np.array_equal(sel[i, : cnt[i]], ref["sets"][i]), i
+
+
+def test_prompt_at_max_positions():
+    """The longest prompt the rotary table allows (N = max_positions) blends; one more token is
+    refused before anything runs."""
+    import rag_non_prefix_gb300 as cb_
+
+    spec = _custom("small_bf16", 43, [200, 111], 9)
+    N = spec.n_tokens(0)
+    g = GpuWorkload(spec, max_tokens=N)
+    # GpuWorkload sizes max_positions to N + 1: an engine with max_positions = N exactly
+    eng = cb_.Engine(spec.cfg, g.W, max_tokens=N, max_requests=1, max_positions=N)
+    for c, (ids, k, v) in g.chunk_kv.items():
+        eng.register_chunk(c, ids, k, v)
+    q = hd.ids_tensor(spec.requests[0][-1].ids)
+    r = eng.make_request([0, 1], q)
+    eng.blend_prefill([r], orc.ratio_schedule(spec.cfg.n_layers, 0.2, "gradual"))
+    eng.get_status()
+    torch.cuda.synchronize()
+    assert int(r["first_token"].item()) >= 0
+    longer = eng.make_request([0, 1], hd.ids_tensor(np.concatenate([spec.requests[0][-1].ids, [3]])))
+    with pytest.raises(cb_.CacheBlendError) as e:
+        eng.blend_prefill([longer], orc.ratio_schedule(spec.cfg.n_layers, 0.2, "gradual"))
+    assert e.value.name in ("CB_ERR_SHAPE", "CB_ERR_WORKSPACE")
