@@ -132,6 +132,7 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int bn) {
 // depth is what fits (at most MAX_STAGES): the deeper the ring, the more weight bytes are
 // in flight per SM, which is what bounds a launch whose tiles stream weights from DRAM.
 constexpr int MAX_STAGES = 12;
+constexpr int L2_AHEAD = 6;   // k-blocks of weights prefetched into L2 beyond the ring
 constexpr int FIX_BUFS = 16;  // stream-K fix-up: slab steps in flight
 constexpr int OFF_BAR = 0;
 constexpr int OFF_STG = 1024;          // epilogue staging: two 16 KiB buffers
@@ -286,11 +287,26 @@ __global__ void __launch_bounds__(THREADS, 1)
           brow = n0 - p.split0;
         }
       }
+      // When several token tiles share a weight tile, the first of them pulls the weights into
+      // L2 L2_AHEAD k-blocks ahead of its ring, so that the weight tile's DRAM latency is not
+      // paid once per ring's worth of stages (measured on GB300, 535 tokens: the down projection
+      // 76.5 -> 68.7 us).  A weight tile with one token tile gets no prefetch: there it only
+      // added copy-unit traffic (seam repair, 176 tokens: 7.49 -> 7.73 ms per blend).
+      const bool lead = p.m_tiles >= 2 && (it.tile % p.m_tiles) == 0;
       for (int kb = it.kb0; kb < it.kb1; ++kb) {
         if (lane == 0) ok = mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
+          const int kp = kb + L2_AHEAD;
+          if (lead && kp < it.kb1) {
+            if (p.mode == EPI_SWIGLU) {
+              tma_prefetch_l2_2d(&tmB0, kp * BK, n0 / 2);
+              tma_prefetch_l2_2d(&tmB1, kp * BK, n0 / 2);
+            } else {
+              tma_prefetch_l2_2d(mb, kp * BK, brow);
+            }
+          }
           uint8_t* sa = ring + s * stage_bytes;
           uint8_t* sb = sa + A_STAGE;
           uint8_t* sw_dst = WROWS ? sa : sb;  // weights
