@@ -854,10 +854,12 @@ struct GemmPlan {
 };
 
 // Time model used to pick the orientation, the token tile and the schedule.  A tile takes
-// K/64 k-blocks.  Measured on GB300 (one CTA per SM): the four MMAs of a k-block take
-// ~0.31 us whatever N below 256 (0.336 us at N = 256, the bf16 peak), so narrow tiles buy
-// no MMA time; the stage copies alone take ~0.24 us per k-block and are hidden behind
-// the MMAs.  A k-block therefore costs about max(0.336 * N / 256, 0.31) us (with a slight
+// K/64 k-blocks.  Measured on GB300 (one CTA per SM, this kernel): a k-block takes ~0.31 us
+// for any N below 256 and 0.336 us at N = 256.  The MMAs alone would take 128 cycles per
+// N = 256 instruction and proportionally less for narrower ones; what sets the k-block time
+// here is the stage landing in time and the shared-memory bandwidth that the copies and the
+// MMA operand reads share, so narrow tiles buy little.  A k-block therefore costs about
+// max(0.336 * N / 256, 0.31) us (with a slight
 // slope below the floor, so that of two plans with as many waves the one spreading the
 // tokens over more SMs wins), and the choice is about padding and filling the SMs.
 // Data-parallel: tiles go round-robin over at most one CTA per SM, ceil(tiles / SMs) tile

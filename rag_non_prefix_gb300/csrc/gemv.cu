@@ -1,7 +1,8 @@
 // Projections of a few token rows (M <= GEMV_MAX_ROWS: decoding): C = A . B^T streamed straight
 // from the weights.  With so few rows every weight is used M times only, so the product is
-// bound by reading the weights once from HBM; a tensor-core tile would be 1/16 to 1/128 full
-// and its per-k-block issue cost caps the weight stream per SM.  Instead a CTA owns four
+// bound by reading the weights once from HBM; a tensor-core tile would be 1/16 to 1/128 full,
+// and measured on GB300 the tiles stream the weights slower than this kernel for one or two
+// rows (faster from three or four on, where the GEMM takes over).  A CTA owns four
 // weight rows (SwiGLU: the gate and up rows of two features) and its 256 threads split the
 // k range in 16-byte pieces (two pieces of each row in flight per thread), so that even
 // 4096 output features give a thousand CTAs and every SM keeps enough loads in flight to
