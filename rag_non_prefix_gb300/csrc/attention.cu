@@ -296,7 +296,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       if (ok && lane == 0) ok = mbar_wait_bounded(b, ph, abort_flag);
       ok = __shfl_sync(0xffffffffu, ok, 0);
     };
-    auto sm_bar = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };  // the eight softmax warps
+    // The two warps that hold the same 32 rows (one per column half) exchange row maxima and
+    // sums through shared memory: a named barrier per such pair (ids 1-4, 64 threads), so a
+    // warp never waits for the other six.
+    const uint32_t pair_bar = 1u + static_cast<uint32_t>(quarter);
+    auto sm_bar = [pair_bar]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
     for (int j = 0; j < n_blk; ++j) {
       const int st = j & 1;
       wait(&s_full[st], (j >> 1) & 1);
