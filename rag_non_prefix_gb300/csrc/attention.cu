@@ -55,6 +55,32 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed fp32 pairs (sm_100 family): one instruction for two lanes of fp32 arithmetic, each
+// rounded as its scalar counterpart.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 struct Args {
   CUtensorMap kmap[MAXREQ];
   CUtensorMap vmap[MAXREQ];
@@ -318,20 +344,24 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[st]);
       const int k0 = j * BKV + half * 64;
-      const bool full = k0 + 63 <= pos;
+      // the unmasked path only when every row of the warp sees the whole block (a warp-uniform
+      // branch: rows of sparse tiles sit at scattered positions)
+      const bool full = __all_sync(0xffffffffu, k0 + 63 <= pos);
       // row max of this half: eight independent chains, then a tree
       float pm[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-      if (full) {
+      if (full) {  // three-input max: 32 instructions for the 64 columns
 #pragma unroll
-        for (int e = 0; e < 64; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(sv[e]));
+        for (int e = 0; e < 64; e += 16)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) pm[u] = max3(pm[u], __uint_as_float(sv[e + u]), __uint_as_float(sv[e + 8 + u]));
       } else {
 #pragma unroll
         for (int e = 0; e < 64; ++e)
           if (k0 + e <= pos) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(sv[e]));
       }
-      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      float mx = max3(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
       mx *= a.scale_log2;  // scale > 0: the max commutes with it
       // row max over both halves (slots by block parity: a slot is rewritten two blocks later,
       // after the barrier of the next block, so the partner has read it)
@@ -366,23 +396,50 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       if (j >= 2) wait(&pv_done[st], ((j - 2) >> 1) & 1);
       if (ok) {
         uint8_t* pb = smem + OFF_P + st * 2 * ATOM + half * ATOM;
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial row sums
+        if (full) {
+          // every key visible: (s * scale - m) for two columns per packed FMA, the row sum in
+          // two packed accumulators
+          const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-m, -m);
+          uint64_t acc0 = f2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int c = 0; c < 64; c += 8) {
-          uint32_t pk[4];
+          for (int c = 0; c < 64; c += 8) {
+            uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const int x = c + e;
-            const float p0 = (full || k0 + x <= pos) ? ex2(fmaf(__uint_as_float(sv[x]), a.scale_log2, -m)) : 0.f;
-            const float p1 =
-                (full || k0 + x + 1 <= pos) ? ex2(fmaf(__uint_as_float(sv[x + 1]), a.scale_log2, -m)) : 0.f;
-            ls[e >> 1] += p0 + p1;
-            pk[e >> 1] = pack_bf16x2(p0, p1);
+            for (int e = 0; e < 8; e += 2) {
+              float t0, t1;
+              f2_split(fma2(f2(__uint_as_float(sv[c + e]), __uint_as_float(sv[c + e + 1])), sc2, nm2), t0, t1);
+              const float p0 = ex2(t0), p1 = ex2(t1);
+              if (e & 2)
+                acc1 = add2(acc1, f2(p0, p1));
+              else
+                acc0 = add2(acc0, f2(p0, p1));
+              pk[e >> 1] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(pb + r * 128 + (((c >> 3) ^ (r & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
-          *reinterpret_cast<uint4*>(pb + r * 128 + (((c >> 3) ^ (r & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          float a0, a1, b0, b1;
+          f2_split(acc0, a0, a1);
+          f2_split(acc1, b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        } else {
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial row sums
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const int x = c + e;
+              const float p0 = k0 + x <= pos ? ex2(fmaf(__uint_as_float(sv[x]), a.scale_log2, -m)) : 0.f;
+              const float p1 = k0 + x + 1 <= pos ? ex2(fmaf(__uint_as_float(sv[x + 1]), a.scale_log2, -m)) : 0.f;
+              ls[e >> 1] += p0 + p1;
+              pk[e >> 1] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(pb + r * 128 + (((c >> 3) ^ (r & 7)) << 4)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         fence_proxy_async_smem();
         tc_fence_before();
       }
