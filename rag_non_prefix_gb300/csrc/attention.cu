@@ -144,8 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   uint64_t* v_empty = bar + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* s_maxpos = reinterpret_cast<int*>(tmem_slot + 2);
-  int* rowpos = reinterpret_cast<int*>(bar + 20);  // [128] (bar + 18: slot, abort flag, max position)
+  int* rowpos = reinterpret_cast<int*>(bar + 20);  // [128] (bar + 18: slot, abort flag)
   float* xmax = reinterpret_cast<float*>(rowpos + ROWS);  // [2][2][128]: per block parity, per half
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -179,12 +178,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
     *abort_flag = 0;
     fence_mbar_init();
   }
+  int* wmaxpos = reinterpret_cast<int*>(smem + OFF_BAR + 2720);  // [4] per-warp maxima of rowpos
   if (threadIdx.x >= 64 && threadIdx.x < 64 + ROWS) {  // row positions (-1: no query in this row)
     const int r = threadIdx.x - 64;
     const int qi = r / G;
     int p = -1;
     if (qi < t.count && r < QT * G) p = min(a.s_pos[t.row0 + qi], n_kv - 1);
     rowpos[r] = p;
+    const int wm = __reduce_max_sync(0xffffffffu, p);
+    if ((r & 31) == 0) wmaxpos[r >> 5] = wm;
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -193,14 +195,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (threadIdx.x == 0) {
-    int mp = -1;
-    for (int r = 0; r < ROWS; ++r) mp = max(mp, rowpos[r]);
-    *s_maxpos = mp;
-  }
-  __syncthreads();
   const uint32_t tmem = *tmem_slot;
-  const int n_blk = *s_maxpos < 0 ? 0 : *s_maxpos / BKV + 1;
+  const int maxpos = max(max(wmaxpos[0], wmaxpos[1]), max(wmaxpos[2], wmaxpos[3]));
+  const int n_blk = maxpos < 0 ? 0 : maxpos / BKV + 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
