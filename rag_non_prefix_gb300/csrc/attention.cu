@@ -96,6 +96,11 @@ struct Args {
   bf16* out;
   float scale_log2;
   int32_t* status;
+  // key-range splits (null: one CTA per tile): two CTAs per tile, unit = (tile_base + tile) * Hkv + head
+  float* part_o;       // [unit][2][128][128] unnormalised O
+  float2* part_ml;     // [unit][2][128] (reference max, row sum)
+  int* part_cnt;       // [unit] CTAs of the unit done (reset to 0 by the second)
+  int tile_base;
 };
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {  // K-major, 128-byte swizzle
@@ -148,13 +153,20 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   float* xmax = reinterpret_cast<float*>(rowpos + ROWS);  // [2][2][128]: per block parity, per half
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kvh = blockIdx.y;
+  // One-dimensional grid, KV head fastest, then the two key ranges of a split tile, then the
+  // tiles, longest first: CTAs start in that order, so the longest work of every head goes
+  // first and the shorter tiles fill the SMs that free up.
+  const bool split_mode = a.part_o != nullptr;
+  const int kvh = static_cast<int>(blockIdx.x % a.Hkv);
+  const int rest = static_cast<int>(blockIdx.x / a.Hkv);
+  const int tix = split_mode ? (rest >> 1) : rest;
+  const int part = split_mode ? (rest & 1) : 0;
   AttnTile t;
   if (a.tiles) {
-    t = a.tiles[a.n_tiles - 1 - blockIdx.x];  // longest tiles first
+    t = a.tiles[a.n_tiles - 1 - tix];  // longest tiles first
     t.req -= a.req_base;
   } else {
-    const int b = a.n_tiles - 1 - blockIdx.x;
+    const int b = a.n_tiles - 1 - tix;
     t.req = 0;
     t.row0 = b * a.QT;
     t.count = min(a.QT, a.direct_m - t.row0);
@@ -198,6 +210,22 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
   const int maxpos = max(max(wmaxpos[0], wmaxpos[1]), max(wmaxpos[2], wmaxpos[3]));
   const int n_blk = maxpos < 0 ? 0 : maxpos / BKV + 1;
+  // Key blocks [b0, b1) of this CTA: a long tile's two CTAs take one half each; the second CTA
+  // of a short tile has nothing to do.
+  const bool split = split_mode && n_blk >= ATTN_SPLIT_MIN_BLOCKS;
+  if (split_mode && !split && part == 1) {  // uniform across the block
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
+    return;
+  }
+  const int b_half = (n_blk + 1) / 2;
+  const int b0 = (split && part == 1) ? b_half : 0;
+  const int nb = split ? (part == 0 ? b_half : n_blk - b_half) : n_blk;  // blocks of this CTA
+  const int unit = (a.tile_base + a.n_tiles - 1 - tix) * a.Hkv + kvh;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -211,17 +239,17 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       uint64_t* full = is_v ? v_full : k_full;
       const int lc = a.layer_coord[t.req];
       int issued = 0;
-      for (int j = 0; j < n_blk; ++j) {
+      for (int j = 0; j < nb; ++j) {  // local block j = key block b0 + j
         const int st = j & 1;
         const uint32_t ph = ((j >> 1) & 1) ^ 1;
         uint8_t* dst = smem + OFF_KV + st * STAGE + (is_v ? 2 * ATOM : 0);
         if (!mbar_wait_bounded(&empty[st], ph, abort_flag)) break;
         mbar_arrive_expect_tx(&full[st], 2 * ATOM);
-        tma_load_4d(dst, map, &full[st], 0, kvh, j * BKV, lc);
-        tma_load_4d(dst + ATOM, map, &full[st], 64, kvh, j * BKV, lc);
+        tma_load_4d(dst, map, &full[st], 0, kvh, (b0 + j) * BKV, lc);
+        tma_load_4d(dst + ATOM, map, &full[st], 64, kvh, (b0 + j) * BKV, lc);
         issued = j + 1;
       }
-      if (issued < n_blk && !*abort_flag) {
+      if (issued < nb && !*abort_flag) {
         *abort_flag = 1;
         set_status(a.status, ST_WAIT_TIMEOUT);
       }
@@ -257,7 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       __syncwarp();
     };
     wait(q_full, 0);
-    for (int j = 0; ok && j < n_blk; ++j) {
+    for (int j = 0; ok && j < nb; ++j) {
       const int st = j & 1;
       if (!wait(&k_full[st], (j >> 1) & 1) || !wait(&s_empty[st], ((j >> 1) & 1) ^ 1)) break;
       tc_fence_after();
@@ -275,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       __syncwarp();
       if (j >= 1) issue_pv(j - 1);
     }
-    if (ok && n_blk > 0) issue_pv(n_blk - 1);
+    if (ok && nb > 0) issue_pv(nb - 1);
     if (!ok && lane == 0) {
       *abort_flag = 1;
       set_status(a.status, ST_WAIT_TIMEOUT);
@@ -324,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
     // warp never waits for the other six.
     const uint32_t pair_bar = 1u + static_cast<uint32_t>(quarter);
     auto sm_bar = [pair_bar]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
-    for (int j = 0; j < n_blk; ++j) {
+    for (int j = 0; j < nb; ++j) {  // local block j = key block b0 + j
       const int st = j & 1;
       wait(&s_full[st], (j >> 1) & 1);
       uint32_t sv[64];
@@ -340,7 +368,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[st]);
-      const int k0 = j * BKV + half * 64;
+      const int k0 = (b0 + j) * BKV + half * 64;
       // the unmasked path only when every row of the warp sees the whole block (a warp-uniform
       // branch: rows of sparse tiles sit at scattered positions)
       const bool full = __all_sync(0xffffffffu, k0 + 63 <= pos);
@@ -444,16 +472,71 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&p_full[st]);
     }
     // O = PV_0 + ... + PV_{n-1} (at the reference max) / (row sum of both halves); the sums go
-    // to the exchange slots of parity n_blk, last read before the previous block's barrier
-    float* xsum = xmax + (n_blk & 1) * 2 * ROWS;
+    // to the exchange slots of parity nb, last read before the previous block's barrier
+    float* xsum = xmax + (nb & 1) * 2 * ROWS;
     xsum[half * ROWS + r] = l;
-    if (n_blk > 0) wait(&pv_done[(n_blk - 1) & 1], ((n_blk - 1) >> 1) & 1);
+    if (nb > 0) wait(&pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1);
     sm_bar();
     const float l_all = xsum[r] + xsum[ROWS + r];  // same order in both halves
-    if (ok && n_blk > 0) {
+    bf16* dst = a.out + (static_cast<size_t>(t.row0 + (valid ? qi : 0)) * H + kvh * G + g) * DH + half * 64;
+    if (split) {
+      // This CTA's key range: O unnormalised (at the reference max m) and (m, row sum) of every
+      // row go to its partial slot; the CTA of the tile that finishes second adds the two
+      // ranges (each scaled to the larger max), normalises and stores.
+      const size_t mine = static_cast<size_t>(unit) * 2 + part, other = static_cast<size_t>(unit) * 2 + (part ^ 1);
+      uint32_t ov[64];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) tmem_ld16_nowait(tmem + O_COL + col0 + lane_off + c, ov + c);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) ov[e] = 0u;
+      }
+      float4* po = reinterpret_cast<float4*>(a.part_o + (mine * ROWS + r) * DH + half * 64);
+#pragma unroll
+      for (int c = 0; c < 64; c += 4)
+        po[c / 4] = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]), __uint_as_float(ov[c + 2]),
+                                __uint_as_float(ov[c + 3]));
+      if (half == 0) a.part_ml[mine * ROWS + r] = make_float2(m, l_all);
+      __threadfence();  // this thread's partial before the counter below
+      asm volatile("bar.sync 5, 256;" ::: "memory");  // the eight softmax warps
+      volatile int* second = wmaxpos + 4;
+      if (threadIdx.x == 64) *second = atomicAdd(&a.part_cnt[unit], 1) == 1;
+      asm volatile("bar.sync 5, 256;" ::: "memory");
+      if (*second) {
+        // part 0 and part 1 combined in that order whichever CTA merges, so results do not
+        // depend on which finished first
+        __threadfence();
+        const float2 oml = __ldcg(&a.part_ml[other * ROWS + r]);
+        const float m0 = part == 0 ? m : oml.x, m1 = part == 0 ? oml.x : m;
+        const float l0 = part == 0 ? l_all : oml.y, l1 = part == 0 ? oml.y : l_all;
+        const float mm = fmaxf(m0, m1);
+        const float w0 = ex2(m0 - mm), w1 = ex2(m1 - mm);
+        const float ls = __fmaf_rn(l1, w1, __fmul_rn(l0, w0));
+        const float inv = ls > 0.f ? 1.f / ls : 0.f;
+        const float4* qo = reinterpret_cast<const float4*>(a.part_o + (other * ROWS + r) * DH + half * 64);
+        if (valid) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            const float4 x0 = __ldcg(qo + c / 4), x1 = __ldcg(qo + c / 4 + 1);
+            const float xo[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float o0 = part == 0 ? __uint_as_float(ov[c + e]) : xo[e];
+              const float o1 = part == 0 ? xo[e] : __uint_as_float(ov[c + e]);
+              f[e] = __fmul_rn(__fmaf_rn(o1, w1, __fmul_rn(o0, w0)), inv);
+            }
+            store8(dst + c, f);
+          }
+        }
+        if (threadIdx.x == 64) a.part_cnt[unit] = 0;  // for the next launch
+      }
+    } else if (ok && nb > 0) {
       tc_fence_after();
       const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
-      bf16* dst = a.out + (static_cast<size_t>(t.row0 + (valid ? qi : 0)) * H + kvh * G + g) * DH + half * 64;
 #pragma unroll
       for (int c = 0; c < 64; c += 16) {
         uint32_t ov[16];
@@ -605,7 +688,7 @@ static cudaError_t tc_launch(ta::Args& args, int n_tiles, cudaStream_t s) {
   }
   if (n_tiles <= 0) return cudaSuccess;
   args.n_tiles = n_tiles;
-  dim3 grid(n_tiles, args.Hkv);
+  dim3 grid((args.part_o ? 2 : 1) * n_tiles * args.Hkv);
   launch_chain(ta::attn_tc_kernel, grid, dim3(ta::THREADS), ta::SMEM, s, args);
   return cudaGetLastError();
 }
@@ -615,8 +698,23 @@ static cudaError_t tc_launch(ta::Args& args, int n_tiles, cudaStream_t s) {
 cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const AttnTile* tiles, const int* tile_off,
                                   const CUtensorMap* kmaps, const CUtensorMap* vmaps, const int* n_kv,
                                   const int* one_layer, int n_req, int layer, int n_heads, int n_kv_heads, void* out,
-                                  int32_t* status, cudaStream_t s) {
+                                  int32_t* status, float* part_o, float2* part_ml, int* part_cnt, cudaStream_t s) {
   ta::Args a;
+  // Key-range splits only where the two CTAs of every (tile, head) unit still fit one wave:
+  // measured on GB300, splitting 136 units (535 queries of 3200, 272 CTAs on 152 SMs) made the
+  // layer's attention slower (1.68 -> 1.91 ms per blend: the extra CTAs' fixed cost and a second
+  // wave), splitting 48 units (seam repair, 176 rows) faster (7.38 -> 7.21 ms per blend).
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0) n_sm = 148;
+  }
+  const long long units = static_cast<long long>(tile_off[n_req]) * n_kv_heads;
+  const bool split = part_o && part_ml && part_cnt && units <= ATTN_SPLIT_UNITS && 2 * units <= n_sm;
+  a.part_o = split ? part_o : nullptr;
+  a.part_ml = part_ml;
+  a.part_cnt = part_cnt;
   a.q = static_cast<const bf16*>(q);
   a.s_pos = s_pos;
   a.H = n_heads;
@@ -636,6 +734,7 @@ cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const Att
       a.layer_coord[r - r0] = one_layer[r] ? 0 : layer;
     }
     a.req_base = r0;
+    a.tile_base = tile_off[r0];
     a.tiles = tiles + tile_off[r0];
     cudaError_t e = tc_launch(a, tile_off[r1] - tile_off[r0], s);
     if (e != cudaSuccess) return e;
@@ -682,6 +781,10 @@ cudaError_t launch_attention_direct(const void* q, const int32_t* q_pos, int m, 
     a.s_pos = q_pos;
     a.tiles = nullptr;
     a.req_base = 0;
+    a.tile_base = 0;
+    a.part_o = nullptr;  // one CTA per tile
+    a.part_ml = nullptr;
+    a.part_cnt = nullptr;
     a.direct_m = m;
     a.H = n_heads;
     a.Hkv = n_kv_heads;

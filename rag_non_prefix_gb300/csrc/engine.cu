@@ -209,6 +209,9 @@ struct cb_ctx {
   float* logits = nullptr;
   float* xlast = nullptr;
   float* dec_o = nullptr;
+  float* att_o = nullptr;     // attention key-range split partials (see launch_attention_bf16)
+  float2* att_ml = nullptr;
+  int* att_cnt = nullptr;
   float2* dec_ml = nullptr;
   void* gemm_scratch = nullptr;
   size_t gemm_scratch_bytes = 0;
@@ -334,7 +337,7 @@ bool valid_cfg(const cb_model_cfg& c, std::string* why) {
 
 struct WsLayout {
   size_t status, rope, tok, pos0, pos1, req0, req1, src, dev, h0, h1, x, qkv, q, attn, act, tmpk, tmpv, logits,
-      xlast, gemm, dec_o, dec_ml, meta, total, meta_bytes;
+      xlast, gemm, dec_o, dec_ml, att_o, att_ml, att_cnt, meta, total, meta_bytes;
 };
 
 WsLayout ws_layout(const cb_model_cfg& c, int T, int R) {
@@ -373,6 +376,10 @@ WsLayout ws_layout(const cb_model_cfg& c, int T, int R) {
   const size_t dec_rows = static_cast<size_t>(R) * c.n_heads * decode_splits(c.max_positions);
   w.dec_o = take(dec_rows * c.head_dim * 4);
   w.dec_ml = take(dec_rows * sizeof(float2));
+  // attention key-range splits of the sparse layers: partial outputs, (max, sum), counters
+  w.att_o = take(static_cast<size_t>(ATTN_SPLIT_UNITS) * 2 * 128 * 128 * 4);
+  w.att_ml = take(static_cast<size_t>(ATTN_SPLIT_UNITS) * 2 * 128 * sizeof(float2));
+  w.att_cnt = take(static_cast<size_t>(ATTN_SPLIT_UNITS) * 4);
   // metadata: plan, requests, tiles, segments, forced sets, last rows, counts, first-token pointers
   const size_t L = c.n_layers;
   size_t m = 0;
@@ -887,7 +894,8 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
       CB_CUDA(ctx, launch_attention_bf16(ctx->q, posS, ctx->d_tiles + b.tile_off[i],
                                          b.req_tile_off.data() + static_cast<size_t>(i) * (b.n_req + 1),
                                          b.kmaps.data(), b.vmaps.data(), b.n_kv.data(), b.one_layer.data(), b.n_req,
-                                         i, H, Hkv, ctx->attn, ctx->status, s));
+                                         i, H, Hkv, ctx->attn, ctx->status, ctx->att_o, ctx->att_ml, ctx->att_cnt,
+                                         s));
     else
       CB_CUDA(ctx, launch_attention(ctx->q, posS, reqS, ctx->d_reqs, nullptr, Sn, i, H, Hkv, dh, ctx->attn, c.dtype,
                                     s));
@@ -1086,6 +1094,9 @@ cb_status cb_set_workspace(cb_ctx* ctx, void* ws, size_t bytes, int max_tokens, 
   ctx->gemm_scratch_bytes = gemm_scratch_bytes();
   ctx->dec_o = reinterpret_cast<float*>(base + w.dec_o);
   ctx->dec_ml = reinterpret_cast<float2*>(base + w.dec_ml);
+  ctx->att_o = reinterpret_cast<float*>(base + w.att_o);
+  ctx->att_ml = reinterpret_cast<float2*>(base + w.att_ml);
+  ctx->att_cnt = reinterpret_cast<int*>(base + w.att_cnt);
   ctx->meta = base + w.meta;
   ctx->meta_bytes = w.meta_bytes;
   // rotary table: (cos, sin) of p * theta^(-2i/dh), evaluated in double on the host
@@ -1101,6 +1112,7 @@ cb_status cb_set_workspace(cb_ctx* ctx, void* ws, size_t bytes, int max_tokens, 
   CB_CUDA(ctx, cudaMemcpy(ctx->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
   CB_CUDA(ctx, cudaMemset(ctx->status, 0, 256));
   CB_CUDA(ctx, cudaMemset(ctx->gemm_scratch, 0, ctx->gemm_scratch_bytes));
+  CB_CUDA(ctx, cudaMemset(ctx->att_cnt, 0, static_cast<size_t>(ATTN_SPLIT_UNITS) * 4));
   return CB_OK;
 }
 

@@ -163,11 +163,18 @@ cudaError_t launch_attention(const void* q, const int32_t* s_pos, const int32_t*
                              const AttnTile* tiles, int n_tiles, int layer, int n_heads, int n_kv_heads, int head_dim,
                              void* out, cb_dtype dt, cudaStream_t s);
 int attention_tile_rows(int n_heads, int n_kv_heads, cb_dtype dt);
-// tcgen05 attention (bf16, head_dim 128): tiles of request r are tiles[tile_off[r] .. tile_off[r+1])
+// tcgen05 attention (bf16, head_dim 128): tiles of request r are tiles[tile_off[r] .. tile_off[r+1]).
+// When a layer's (tile, KV head) units fit twice into one wave (and ATTN_SPLIT_UNITS) and part_o is
+// given, every tile gets two CTAs and a tile of at least ATTN_SPLIT_MIN_BLOCKS 128-key blocks (known
+// on the device only) is split into two key ranges, merged by whichever CTA finishes second: part_o holds
+// ATTN_SPLIT_UNITS * 2 * 128 * 128 floats, part_ml as many * 128 (max, sum) pairs, part_cnt
+// ATTN_SPLIT_UNITS counters that must be zero before the first launch (each launch leaves them zero).
+constexpr int ATTN_SPLIT_UNITS = 256;
+constexpr int ATTN_SPLIT_MIN_BLOCKS = 12;
 cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const AttnTile* tiles, const int* tile_off,
                                   const CUtensorMap* kmaps, const CUtensorMap* vmaps, const int* n_kv,
                                   const int* one_layer, int n_req, int layer, int n_heads, int n_kv_heads, void* out,
-                                  int32_t* status, cudaStream_t s);
+                                  int32_t* status, float* part_o, float2* part_ml, int* part_cnt, cudaStream_t s);
 // 4-D tensor map over a bf16 KV cache [L][N][Hkv][128] (layer_stride_elems 0: one layer)
 bool encode_kv_map(CUtensorMap* map, const void* base, int n_layers, int n_tokens, int n_kv_heads,
                    long long layer_stride_elems);

@@ -112,6 +112,29 @@ def _forced_bf16(small_bf16):
     assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 2e-2
 
 
+def test_bf16_blend_long_context_matches_oracle_and_repeats():
+    """A 2176-token prompt on the reduced bf16 model: tiles reach 17 key blocks, so the
+    attention of every layer splits its long tiles into two key ranges merged on the device.
+    The GPU follows the oracle's sets and agrees with its hidden rows, and two runs agree bit
+    for bit (the merge adds the two ranges in a fixed order)."""
+    spec = hz.make_prompt("small_bf16", 31, [512] * 4, 32, 0.15, "gradual", "zipf", prefix_len=64, name="long")
+    g, o = GpuWorkload(spec), OracleWorkload(spec)
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    ref = o.blend(0, ratios)
+    forced = forced_from_oracle(ref, ref["n_cached"], cfg.n_layers, ratios)
+    outs = []
+    for _ in range(2):
+        req = g.blend(ratios, forced=forced)[0]
+        torch.cuda.synchronize()
+        sets = _sets(req, cfg)
+        for i in range(cfg.n_layers):
+            assert np.array_equal(sets[i], ref["sets"][i])
+        outs.append(to_np(req["hidden"])[ref["rows"]].copy())
+    assert max_rel_err(outs[0], ref["hidden"]) < 2e-2
+    assert np.array_equal(outs[0], outs[1])
+
+
 def test_bf16_blend_selection_overlap(small_bf16):
     """Free-running selection: >= 99 % overlap of every checked set with the oracle's."""
     spec, g, o = small_bf16
