@@ -96,11 +96,12 @@ struct Args {
   bf16* out;
   float scale_log2;
   int32_t* status;
-  // key-range splits (null: one CTA per tile): two CTAs per tile, unit = (tile_base + tile) * Hkv + head
+  // key-range splits: the n_paired longest tiles get two CTAs (unit = tile * Hkv + head, tile in
+  // longest-first order), the others one (n_paired 0 or part_o null: one CTA per tile)
   float* part_o;       // [unit][2][128][128] unnormalised O
   float2* part_ml;     // [unit][2][128] (reference max, row sum)
   int* part_cnt;       // [unit] CTAs of the unit done (reset to 0 by the second)
-  int tile_base;
+  int n_paired;
 };
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {  // K-major, 128-byte swizzle
@@ -153,14 +154,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   float* xmax = reinterpret_cast<float*>(rowpos + ROWS);  // [2][2][128]: per block parity, per half
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // One-dimensional grid, KV head fastest, then the two key ranges of a split tile, then the
+  // One-dimensional grid, KV head fastest, then the two key ranges of a paired tile, then the
   // tiles, longest first: CTAs start in that order, so the longest work of every head goes
   // first and the shorter tiles fill the SMs that free up.
-  const bool split_mode = a.part_o != nullptr;
+  const int n_paired = a.part_o != nullptr ? a.n_paired : 0;
   const int kvh = static_cast<int>(blockIdx.x % a.Hkv);
   const int rest = static_cast<int>(blockIdx.x / a.Hkv);
-  const int tix = split_mode ? (rest >> 1) : rest;
-  const int part = split_mode ? (rest & 1) : 0;
+  const bool paired = rest < 2 * n_paired;
+  const int tix = paired ? (rest >> 1) : rest - n_paired;
+  const int part = paired ? (rest & 1) : 0;
   AttnTile t;
   if (a.tiles) {
     t = a.tiles[a.n_tiles - 1 - tix];  // longest tiles first
@@ -210,10 +212,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
   const int maxpos = max(max(wmaxpos[0], wmaxpos[1]), max(wmaxpos[2], wmaxpos[3]));
   const int n_blk = maxpos < 0 ? 0 : maxpos / BKV + 1;
-  // Key blocks [b0, b1) of this CTA: a long tile's two CTAs take one half each; the second CTA
-  // of a short tile has nothing to do.
-  const bool split = split_mode && n_blk >= ATTN_SPLIT_MIN_BLOCKS;
-  if (split_mode && !split && part == 1) {  // uniform across the block
+  // Key blocks [b0, b1) of this CTA: a long paired tile's two CTAs take one half each; the
+  // second CTA of a short one has nothing to do.
+  const bool split = paired && n_blk >= ATTN_SPLIT_MIN_BLOCKS;
+  if (paired && !split && part == 1) {  // uniform across the block
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -225,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
   const int b_half = (n_blk + 1) / 2;
   const int b0 = (split && part == 1) ? b_half : 0;
   const int nb = split ? (part == 0 ? b_half : n_blk - b_half) : n_blk;  // blocks of this CTA
-  const int unit = (a.tile_base + a.n_tiles - 1 - tix) * a.Hkv + kvh;
+  const int unit = tix * a.Hkv + kvh;  // (paired tiles only: tix < n_paired)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -688,7 +690,9 @@ static cudaError_t tc_launch(ta::Args& args, int n_tiles, cudaStream_t s) {
   }
   if (n_tiles <= 0) return cudaSuccess;
   args.n_tiles = n_tiles;
-  dim3 grid((args.part_o ? 2 : 1) * n_tiles * args.Hkv);
+  const int paired = args.part_o ? std::min(args.n_paired, n_tiles) : 0;
+  args.n_paired = paired;
+  dim3 grid((n_tiles + paired) * args.Hkv);
   launch_chain(ta::attn_tc_kernel, grid, dim3(ta::THREADS), ta::SMEM, s, args);
   return cudaGetLastError();
 }
@@ -700,10 +704,11 @@ cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const Att
                                   const int* one_layer, int n_req, int layer, int n_heads, int n_kv_heads, void* out,
                                   int32_t* status, float* part_o, float2* part_ml, int* part_cnt, cudaStream_t s) {
   ta::Args a;
-  // Key-range splits only where the two CTAs of every (tile, head) unit still fit one wave:
-  // measured on GB300, splitting 136 units (535 queries of 3200, 272 CTAs on 152 SMs) made the
-  // layer's attention slower (1.68 -> 1.91 ms per blend: the extra CTAs' fixed cost and a second
-  // wave), splitting 48 units (seam repair, 176 rows) faster (7.38 -> 7.21 ms per blend).
+  // Key-range splits use only the SMs that one CTA per (tile, head) unit leaves idle: the
+  // longest tiles get a second CTA while (units + pairs) <= SMs, in one launch per layer.
+  // Measured on GB300: seam repair (176 rows, 48 units, every tile paired) 7.38 -> 7.19 ms per
+  // blend; pairing every tile at 535 selected rows (136 units, 272 CTAs on 152 SMs) made the
+  // attention slower (1.68 -> 1.91 ms per blend: the extra CTAs' fixed cost and a second wave).
   static int n_sm = 0;
   if (n_sm == 0) {
     int dev = 0;
@@ -711,8 +716,13 @@ cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const Att
     if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0) n_sm = 148;
   }
   const long long units = static_cast<long long>(tile_off[n_req]) * n_kv_heads;
-  const bool split = part_o && part_ml && part_cnt && units <= ATTN_SPLIT_UNITS && 2 * units <= n_sm;
+  const int n_paired = (n_req <= ta::MAXREQ && units < n_sm)
+                           ? static_cast<int>(std::min<long long>(tile_off[n_req], (n_sm - units) / n_kv_heads))
+                           : 0;
+  const bool split = part_o && part_ml && part_cnt && n_paired > 0 &&
+                     static_cast<long long>(n_paired) * n_kv_heads <= ATTN_SPLIT_UNITS;
   a.part_o = split ? part_o : nullptr;
+  a.n_paired = split ? n_paired : 0;
   a.part_ml = part_ml;
   a.part_cnt = part_cnt;
   a.q = static_cast<const bf16*>(q);
@@ -734,7 +744,6 @@ cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const Att
       a.layer_coord[r - r0] = one_layer[r] ? 0 : layer;
     }
     a.req_base = r0;
-    a.tile_base = tile_off[r0];
     a.tiles = tiles + tile_off[r0];
     cudaError_t e = tc_launch(a, tile_off[r1] - tile_off[r0], s);
     if (e != cudaSuccess) return e;
@@ -781,7 +790,7 @@ cudaError_t launch_attention_direct(const void* q, const int32_t* q_pos, int m, 
     a.s_pos = q_pos;
     a.tiles = nullptr;
     a.req_base = 0;
-    a.tile_base = 0;
+    a.n_paired = 0;
     a.part_o = nullptr;  // one CTA per tile
     a.part_ml = nullptr;
     a.part_cnt = nullptr;
