@@ -164,22 +164,42 @@ __global__ void __launch_bounds__(DH) decode_merge_kernel(const float* __restric
                                                           T* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ float2 mls[];  // [n_splits]
+  extern __shared__ float2 mls[];  // [n_splits] (max, sum), then [n_splits] weights
+  float* wts = reinterpret_cast<float*>(mls + n_splits);
+  __shared__ float inv_l;
   const size_t row = blockIdx.x;   // seq * H + head
   for (int s = threadIdx.x; s < n_splits; s += DH) mls[s] = part_ml[row * n_splits + s];
   __syncthreads();
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, mls[s].x);
-  float L = 0.f, acc = 0.f;
-  const float* po = part_o + row * n_splits * DH + threadIdx.x;
-#pragma unroll 4
-  for (int s = 0; s < n_splits; ++s) {
-    const float2 ml = mls[s];
-    const float wgt = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-    L = fmaf(ml.y, wgt, L);
-    acc = fmaf(po[static_cast<size_t>(s) * DH], wgt, acc);
+  // one warp: the largest max, each range's weight 2^(m_s - M) and the total sum, once per row
+  if (threadIdx.x < 32) {
+    float M = -INFINITY;
+    for (int s = threadIdx.x; s < n_splits; s += 32) M = fmaxf(M, mls[s].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    for (int s = threadIdx.x; s < n_splits; s += 32) {
+      const float2 ml = mls[s];
+      const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+      wts[s] = w;
+      L = fmaf(ml.y, w, L);
+    }
+    L = warp_sum(L);
+    if (threadIdx.x == 0) inv_l = L > 0.f ? 1.f / L : 0.f;
   }
-  out[row * DH + threadIdx.x] = from_f<T>(acc / L);
+  __syncthreads();
+  // each thread: one output element, the ranges' partial values loaded eight at a time
+  const float* po = part_o + row * n_splits * DH + threadIdx.x;
+  float acc = 0.f;
+  int s = 0;
+  for (; s + 8 <= n_splits; s += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = po[static_cast<size_t>(s + u) * DH];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc = fmaf(v[u], wts[s + u], acc);
+  }
+  for (; s < n_splits; ++s) acc = fmaf(po[static_cast<size_t>(s) * DH], wts[s], acc);
+  out[row * DH + threadIdx.x] = from_f<T>(acc * inv_l);
 }
 
 template <typename T, int DH, int G>
@@ -196,7 +216,7 @@ cudaError_t launch_dec(const void* q, const int32_t* pos, const ReqDev* reqs, in
   launch_chain(decode_attn_kernel<T, DH, G>, dim3(n_seq * Hkv, n_splits), dim3(DH), smem, s, static_cast<const T*>(q),
                pos, reqs, layer, H, Hkv, n_splits, scale_log2, part_o, part_ml, static_cast<T*>(out), status);
   if (n_splits > 1)
-    launch_chain(decode_merge_kernel<T, DH>, dim3(n_seq * H), dim3(DH), n_splits * sizeof(float2), s,
+    launch_chain(decode_merge_kernel<T, DH>, dim3(n_seq * H), dim3(DH), n_splits * (sizeof(float2) + sizeof(float)), s,
                  static_cast<const float*>(part_o), static_cast<const float2*>(part_ml), n_splits, static_cast<T*>(out));
   return cudaGetLastError();
 }
