@@ -12,6 +12,11 @@
 //           (ex2.approx), and write P_j (bf16) to one of two shared-memory buffers.  P is taken
 //           relative to a reference max that moves only when a row's max grows by more
 //           than 2^8; then the row of O in TMEM is rescaled (rarely).  Finally O / l -> bf16.
+// The grid is one-dimensional, KV head fastest and the longest tiles first.  When a layer's
+// (tile, head) units leave SMs idle, its longest tiles get a second CTA: a tile of at least
+// ATTN_SPLIT_MIN_BLOCKS key blocks then splits its key range in two, each CTA writes its
+// unnormalised O and per-row (max, sum) to a partial slot, and the CTA that finishes second
+// (an atomic ticket) combines the two halves in a fixed order and writes the rows.
 // Every mbarrier wait is bounded: on timeout the CTA records ST_WAIT_TIMEOUT and leaves.
 //
 // fp32 (any head_dim multiple of 32 up to 128): one warp per (query, head); lanes split
