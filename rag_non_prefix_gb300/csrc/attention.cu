@@ -709,11 +709,13 @@ cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const Att
                                   const int* one_layer, int n_req, int layer, int n_heads, int n_kv_heads, void* out,
                                   int32_t* status, float* part_o, float2* part_ml, int* part_cnt, cudaStream_t s) {
   ta::Args a;
-  // Key-range splits use only the SMs that one CTA per (tile, head) unit leaves idle: the
-  // longest tiles get a second CTA while (units + pairs) <= SMs, in one launch per layer.
-  // Measured on GB300: seam repair (176 rows, 48 units, every tile paired) 7.38 -> 7.19 ms per
-  // blend; pairing every tile at 535 selected rows (136 units, 272 CTAs on 152 SMs) made the
-  // attention slower (1.68 -> 1.91 ms per blend: the extra CTAs' fixed cost and a second wave).
+  // Key-range splits: when one CTA per (tile, head) unit leaves SMs idle, the longest tiles get a
+  // second CTA -- as many tiles as the idle SMs hold, plus two per KV head: the CTAs past one wave
+  // are then the shortest tiles', which start as soon as the first short tiles finish.  One launch
+  // per layer.  Measured on GB300 (535 selected rows of 3200, 136 units on 152 SMs), attention
+  // phase per blend: no pairs 1.68 ms, the idle SMs' 2 tiles per head 1.63, 4 tiles 1.47, 6 tiles
+  // 1.71, every tile 1.91 (the extra CTAs' fixed cost and a second wave); seam repair (176 rows,
+  // 48 units, every tile paired) 7.38 -> 7.20 ms per blend.
   static int n_sm = 0;
   if (n_sm == 0) {
     int dev = 0;
@@ -722,7 +724,7 @@ cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const Att
   }
   const long long units = static_cast<long long>(tile_off[n_req]) * n_kv_heads;
   const int n_paired = (n_req <= ta::MAXREQ && units < n_sm)
-                           ? static_cast<int>(std::min<long long>(tile_off[n_req], (n_sm - units) / n_kv_heads))
+                           ? static_cast<int>(std::min<long long>(tile_off[n_req], (n_sm - units) / n_kv_heads + 2))
                            : 0;
   const bool split = part_o && part_ml && part_cnt && n_paired > 0 &&
                      static_cast<long long>(n_paired) * n_kv_heads <= ATTN_SPLIT_UNITS;

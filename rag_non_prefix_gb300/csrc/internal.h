@@ -165,7 +165,8 @@ cudaError_t launch_attention(const void* q, const int32_t* s_pos, const int32_t*
 int attention_tile_rows(int n_heads, int n_kv_heads, cb_dtype dt);
 // tcgen05 attention (bf16, head_dim 128): tiles of request r are tiles[tile_off[r] .. tile_off[r+1]).
 // When a layer's (tile, KV head) units leave SMs idle (one launch per layer) and part_o is given,
-// the longest tiles get a second CTA while the CTAs fit the SMs, and such a tile of at least
+// the longest tiles get a second CTA (as many as the idle SMs hold, plus two per KV head), and such
+// a tile of at least
 // ATTN_SPLIT_MIN_BLOCKS 128-key blocks (known on the device only) is split into two key ranges,
 // merged by whichever CTA finishes second: part_o holds
 // ATTN_SPLIT_UNITS * 2 * 128 * 128 floats, part_ml as many * 128 (max, sum) pairs, part_cnt
