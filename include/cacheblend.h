@@ -417,7 +417,9 @@ cb_status cb_blend_layer(cb_ctx* ctx, int layer, void* stream);
 cb_status cb_blend_finish(cb_ctx* ctx, void* stream);
 
 /* Waits (deadline timeout_ms) for the work enqueued so far on `stream` and reports
- * the device status word: CB_OK, CB_ERR_NAN or CB_ERR_DEVICE.  Clears it. */
+ * the device status word: CB_OK, CB_ERR_NAN or CB_ERR_DEVICE.  Clears it; when it was
+ * not zero, also clears (on `stream`) the workspace counters that a kernel which gave up
+ * may have left set, so that later calls start from a clean state. */
 cb_status cb_get_status(cb_ctx* ctx, void* stream, int timeout_ms);
 
 /* --------------------------------------------------------------------- profiling

@@ -1579,6 +1579,13 @@ cb_status cb_get_status(cb_ctx* ctx, void* stream, int timeout_ms) {
   cb_status st = wait_event_deadline(ctx, ctx->status_ev, timeout_ms);
   if (st != CB_OK) return st;
   const int32_t v = *ctx->status_host;
+  if (v) {
+    // A kernel that gave up (a bounded wait ran out) may have left the counters that later
+    // launches expect at zero -- the stream-K flags of the GEMM scratch, the attention's
+    // key-range tickets: clear them before anything else runs on the stream.
+    CB_CUDA(ctx, cudaMemsetAsync(ctx->gemm_scratch, 0, ctx->gemm_scratch_bytes, s));
+    CB_CUDA(ctx, cudaMemsetAsync(ctx->att_cnt, 0, static_cast<size_t>(ATTN_SPLIT_UNITS) * 4, s));
+  }
   if (v & ST_NAN) return fail(ctx, CB_ERR_NAN, "a deviation was NaN");
   if (v) return fail(ctx, CB_ERR_DEVICE, "device status word " + std::to_string(v));
   return CB_OK;
