@@ -248,7 +248,10 @@ cb_status cb_select_hkvd(const float* dev, const int32_t* cand, int n, int k, in
  * ragged; the sums of split tiles are formed in a fixed order, so results repeat
  * exactly): 1 KiB of flags, then one 128 KiB fp32 partial slot per CTA of the split (a smaller
  * scratch narrows the split).  cb_gemm_scratch_size() bytes allow every split.  The
- * call leaves the flags zeroed.  Calls sharing one scratch must not overlap on the GPU. */
+ * call leaves the flags zeroed.  Calls sharing one scratch must not overlap on the GPU.
+ * Device-side problems (a stream-K wait for a partial tile that gave up after 2 s) are
+ * recorded in the standalone GEMM status word that cb_gemm_get_status() reads; after such
+ * a report the output is not valid and the scratch's flags must be zeroed again. */
 cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, int N, int K, int ldc, int epilogue,
                   cb_dtype dtype, void* scratch, size_t scratch_bytes, void* stream);
 size_t cb_gemm_scratch_size(void);
@@ -275,17 +278,34 @@ cb_status cb_set_launch_overlap(int enabled);
  * budget after start-up, or code inside a framework that owns every allocation).
  * Same arguments and results as cb_gemm without the scratch arguments: its stream-K
  * scratch is a built-in device array of CB_GEMM_STATIC_SCRATCH_BYTES (4 MiB + 1 KiB:
- * the flags and the partial slots of a 32-CTA split) that every GPU loading the library holds until the
- * process exits.  Shapes whose stream-K split needs more return CB_ERR_WORKSPACE
- * (cb_gemm_noalloc_error() has the reason); data-parallel shapes need none.  The call
- * allocates nothing; its first call on a device looks up the array's device address
- * (make that first call before any stream capture), and each call that uses the array
- * zeroes its flags first.  All calls share the array, so calls that overlap on the
- * GPU (other streams, other threads) race: order them on one stream. */
+ * the flags and 32 partial slots) that every GPU loading the library holds until the
+ * process exits.  The schedule narrows its stream-K split to those 32 slots, as cb_gemm
+ * does with a small scratch, so every shape cb_gemm accepts runs; the few-row GEMV and
+ * data-parallel shapes use no scratch.  A schedule asking for more than the array would
+ * be refused with CB_ERR_WORKSPACE.  Every non-OK return leaves its reason in
+ * cb_gemm_noalloc_error() (an empty string after CB_OK).  The call allocates nothing;
+ * its first call on a device looks up the array's device address (make that first call
+ * before any stream capture), and each call that uses the array zeroes its flags first.
+ * All calls share the array, so calls that overlap on the GPU (other streams, other
+ * threads) race: order them on one stream.  Device-side problems go to the standalone
+ * GEMM status word (cb_gemm_get_status). */
 #define CB_GEMM_STATIC_SCRATCH_BYTES ((size_t)(4u << 20) + 1024u)
 cb_status cb_gemm_noalloc(const void* A, const void* B, const void* B2, void* C, int M, int N, int K, int ldc,
                           int epilogue, cb_dtype dtype, void* stream);
 const char* cb_gemm_noalloc_error(void);
+/* Bytes of the built-in array that cb_gemm_noalloc uses for this shape on the current
+ * device with 16-byte aligned operands (0: the few-row GEMV or whole output tiles, no
+ * scratch; never more than CB_GEMM_STATIC_SCRATCH_BYTES).  Host-side planning only. */
+size_t cb_gemm_noalloc_scratch_used(int M, int N, int K, int epilogue, cb_dtype dtype);
+
+/* Status of the standalone GEMM calls (cb_gemm, cb_gemm_noalloc) on the current device:
+ * waits up to timeout_ms (< 0: no limit) for the work enqueued on `stream`, then reads
+ * and clears a device status word that those calls' kernels set when a bounded wait for
+ * a stream-K partial tile gave up (their output is then not valid).  CB_OK, CB_ERR_DEVICE
+ * (the word was set), CB_ERR_TIMEOUT (the stream did not finish in time; the word is not
+ * read) or CB_ERR_CUDA.  The reason is in cb_gemm_noalloc_error().  One word per device
+ * is shared by every caller: read it after the GEMMs that matter, on their stream. */
+cb_status cb_gemm_get_status(void* stream, int timeout_ms);
 
 /* Causal attention of sparse queries over one KV cache ([P3] "어떤 토큰을 다시 계산하는가":
  * selected queries attend under the causal mask to all available K/V).
@@ -317,6 +337,23 @@ cb_status cb_attention(const void* q, const int32_t* q_pos, int m, const void* k
  * measured (layer_ratio_host, dev_mode and forced_sel_host are ignored; the ratio
  * array may be NULL). */
 enum { CB_SELECT_HKVD = 0, CB_SELECT_SEAM = 1 };
+
+/* The layer_ratio array of gradual filtering ([P1] 段階的フィルタリングスキーム: the
+ * deviation is measured at an early layer over many tokens, and later layers keep a
+ * narrower share of the earlier set).  out_host [n_layers] gets: layer 0 -1 (no check:
+ * layer 0 runs on every token, which gives every cached token a layer-1 input); layer 1
+ * r1; layers 2 .. 1 + n_narrow r1 + (r - r1) * j / n_narrow for j = 1 .. n_narrow (the
+ * last of them is r); later layers -1 (the last checked set is kept).
+ * CB_SCHEDULE_FIXED checks once, at layer 1, with r.  CB_SCHEDULE_GRADUAL takes r1 < 0
+ * as min(1, 2 r).  Needs 0 <= r <= r1 <= 1 and n_narrow >= 0, else CB_ERR_INVALID_ARG.
+ * Host-only. */
+enum { CB_SCHEDULE_FIXED = 0, CB_SCHEDULE_GRADUAL = 1 };
+cb_status cb_ratio_schedule(int n_layers, double r, int schedule, double r1, int n_narrow, double* out_host);
+
+/* Cached tokens kept at a check layer of ratio r: ceil(r * n_cached - 1e-9) (0 when
+ * r <= 0).  The 1e-9 keeps r * Nc that rounds just above an integer on that integer.
+ * Host-only; the blend uses the same rule. */
+int cb_k_for_ratio(double r, int n_cached);
 typedef struct {
   int n_layers;
   const double* layer_ratio_host;

@@ -8,7 +8,6 @@ shared library has not been built (``python -m rag_non_prefix_gb300.build``).
 from __future__ import annotations
 
 import ctypes as C
-import math
 import os
 from typing import Dict, List, Optional, Sequence
 
@@ -27,9 +26,10 @@ EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_
             "cb_blend_prefill",
             "cb_full_prefill", "cb_blend_begin", "cb_fetch_kv", "cb_synchronize", "cb_prefill_layer",
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
-            "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_set_orientation",
+            "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_noalloc_scratch_used", "cb_gemm_get_status", "cb_gemm_set_orientation",
             "cb_set_launch_overlap", "cb_codec_layer_bytes", "cb_kv_encode", "cb_kv_decode", "cb_register_chunk_codec",
-            "cb_set_staging", "cb_chunk_hash", "cb_chunk_info_of", "cb_plan_loading", "cb_decode_step")
+            "cb_set_staging", "cb_chunk_hash", "cb_chunk_info_of", "cb_plan_loading", "cb_decode_step",
+            "cb_ratio_schedule", "cb_k_for_ratio")
 PHASES = ("begin", "staged_rot", "norm", "qkv", "rope", "deviation", "select", "scatter", "attention", "oproj",
           "gateup", "down", "finish")
 
@@ -124,6 +124,8 @@ def load_library(path: str = LIB_PATH):
         "cb_set_launch_overlap": (st, [C.c_int]),
         "cb_gemm_noalloc": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp]),
         "cb_gemm_noalloc_error": (C.c_char_p, []),
+        "cb_gemm_get_status": (st, [vp, C.c_int]),
+        "cb_gemm_noalloc_scratch_used": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int]),
         "cb_attention": (st, [vp, i32p, C.c_int, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, vp, C.c_int, vp]),
         "cb_codec_layer_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int]),
         "cb_kv_encode": (st, [vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp]),
@@ -132,6 +134,8 @@ def load_library(path: str = LIB_PATH):
         "cb_register_chunk_codec": (st, [vp, C.c_uint64, i32p, vp, C.c_int, C.c_int, C.c_int]),
         "cb_set_staging": (st, [vp, vp, C.c_size_t]),
         "cb_chunk_hash": (C.c_uint64, [C.POINTER(C.c_int32), C.c_int]),
+        "cb_ratio_schedule": (st, [C.c_int, C.c_double, C.c_int, C.c_double, C.c_int, C.POINTER(C.c_double)]),
+        "cb_k_for_ratio": (C.c_int, [C.c_double, C.c_int]),
         "cb_decode_step": (st, [vp, C.POINTER(DecodeSeq), C.c_int, vp, vp, vp]),
         "cb_chunk_info_of": (st, [vp, C.c_uint64, C.POINTER(ChunkInfo)]),
         "cb_plan_loading": (st, [C.POINTER(CostModel), C.POINTER(ChunkInfo), C.c_int, C.c_int, C.POINTER(C.c_int32),
@@ -184,29 +188,20 @@ def _dtype_code(t: torch.dtype) -> int:
 
 # ----------------------------------------------------------------------------- host logic
 def k_for_ratio(r: float, n_cached: int) -> int:
-    """Cached tokens kept at a check layer: ceil(r * Nc), guarded against float noise."""
-    return 0 if r <= 0 else int(math.ceil(r * n_cached - 1e-9))
+    """Cached tokens kept at a check layer (cb_k_for_ratio)."""
+    return int(load_library().cb_k_for_ratio(float(r), int(n_cached)))
 
 
 def ratio_schedule(n_layers: int, r: float, schedule: str = "gradual", r1: Optional[float] = None,
                    n_narrow: int = 3) -> List[float]:
-    """Per-layer ratios of gradual filtering: layer 0 none (all tokens), layer 1 r1,
-    layers 2..1+n_narrow linear from r1 down to r, later layers none (keep the set).
-    ``fixed`` checks once at layer 1 with r; ``gradual`` starts at r1 = min(1, 2r)."""
-    out = [-1.0] * n_layers
-    if n_layers < 2:
-        return out
-    if schedule == "fixed":
-        out[1] = float(r)
-        return out
-    if schedule != "gradual":
+    """Per-layer ratios of gradual filtering (cb_ratio_schedule)."""
+    sched = {"fixed": 0, "gradual": 1}.get(schedule)
+    if sched is None:
         raise ValueError(schedule)
-    r1 = min(1.0, 2.0 * r) if r1 is None else r1
-    out[1] = float(r1)
-    for j in range(1, n_narrow + 1):
-        if 1 + j < n_layers:
-            out[1 + j] = float(r1 + (r - r1) * j / n_narrow)
-    return out
+    out = (C.c_double * max(1, n_layers))()
+    _check(load_library().cb_ratio_schedule(int(n_layers), float(r), sched, -1.0 if r1 is None else float(r1),
+                                            int(n_narrow), out))
+    return [float(out[i]) for i in range(n_layers)]
 
 
 # ----------------------------------------------------------------------------- standalone kernels
@@ -287,6 +282,15 @@ def cb_gemm_noalloc(A: torch.Tensor, B: torch.Tensor, C_out: torch.Tensor, epilo
     if st != 0:
         raise CacheBlendError(st, lib.cb_gemm_noalloc_error().decode())
     return C_out
+
+
+def cb_gemm_get_status(stream=None, timeout_ms: int = 10000) -> None:
+    """Waits for ``stream`` and reads (and clears) the status word of the standalone GEMM
+    calls on the current device; raises when a device-side wait gave up."""
+    lib = load_library()
+    st = lib.cb_gemm_get_status(_stream(stream), int(timeout_ms))
+    if st != 0:
+        raise CacheBlendError(st, lib.cb_gemm_noalloc_error().decode())
 
 
 def cb_attention(q: torch.Tensor, q_pos: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -687,12 +687,9 @@ bool encode_kv_map(CUtensorMap* map, const void* base, int n_layers, int n_token
 }
 
 static cudaError_t tc_launch(ta::Args& args, int n_tiles, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(ta::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ta::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static DeviceOnce configured;
+  cudaError_t e = max_dynamic_smem_once(reinterpret_cast<const void*>(ta::attn_tc_kernel), ta::SMEM, configured);
+  if (e != cudaSuccess) return e;
   if (n_tiles <= 0) return cudaSuccess;
   args.n_tiles = n_tiles;
   const int paired = args.part_o ? std::min(args.n_paired, n_tiles) : 0;

@@ -14,6 +14,32 @@
 
 extern "C" {
 
+int cb_k_for_ratio(double r, int n_cached) {
+  // k = ceil(r * Nc), guarded against the rounding of r * Nc just above an integer
+  if (!(r > 0) || n_cached <= 0) return 0;
+  return static_cast<int>(std::ceil(r * n_cached - 1e-9));
+}
+
+cb_status cb_ratio_schedule(int n_layers, double r, int schedule, double r1, int n_narrow, double* out_host) {
+  // Gradual filtering ([P1] 段階的フィルタリングスキーム): layer 0 runs on every token (no
+  // check), layer 1 measures the deviation of all cached tokens and keeps r1 of them, the
+  // next n_narrow layers narrow linearly from r1 down to r, later layers keep the set.
+  if (n_layers < 0 || !(r >= 0) || r > 1 || (n_layers > 0 && !out_host) || n_narrow < 0)
+    return CB_ERR_INVALID_ARG;
+  if (schedule != CB_SCHEDULE_FIXED && schedule != CB_SCHEDULE_GRADUAL) return CB_ERR_INVALID_ARG;
+  for (int i = 0; i < n_layers; ++i) out_host[i] = -1.0;
+  if (n_layers < 2) return CB_OK;
+  if (schedule == CB_SCHEDULE_FIXED) {
+    out_host[1] = r;
+    return CB_OK;
+  }
+  if (r1 < 0) r1 = std::fmin(1.0, 2.0 * r);
+  if (r1 > 1 || r1 < r) return CB_ERR_INVALID_ARG;
+  out_host[1] = r1;
+  for (int j = 1; j <= n_narrow && 1 + j < n_layers; ++j) out_host[1 + j] = r1 + (r - r1) * j / n_narrow;
+  return CB_OK;
+}
+
 uint64_t cb_chunk_hash(const int32_t* ids_host, int n) {
   // FNV-1a, 64 bit (Fowler, Noll, Vo) over the ids as little-endian 32-bit integers
   uint64_t h = 0xCBF29CE484222325ull;

@@ -207,12 +207,9 @@ cudaError_t launch_dec(const void* q, const int32_t* pos, const ReqDev* reqs, in
                        int n_splits, float* part_o, float2* part_ml, void* out, int32_t* status, cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(DH));
   const int smem = 2 * DECODE_KEYS * (DH * static_cast<int>(sizeof(T)) + 16);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<T, DH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static DeviceOnce configured;
+  cudaError_t e = max_dynamic_smem_once(reinterpret_cast<const void*>(decode_attn_kernel<T, DH, G>), smem, configured);
+  if (e != cudaSuccess) return e;
   launch_chain(decode_attn_kernel<T, DH, G>, dim3(n_seq * Hkv, n_splits), dim3(DH), smem, s, static_cast<const T*>(q),
                pos, reqs, layer, H, Hkv, n_splits, scale_log2, part_o, part_ml, static_cast<T*>(out), status);
   if (n_splits > 1)

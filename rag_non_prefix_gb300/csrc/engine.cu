@@ -40,10 +40,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline size_t dtype_bytes(cb_dtype d) { return d == CB_BF16 ? 2 : 4; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int k_for_ratio(double r, int n_cached) {
-  if (r <= 0) return 0;
-  return static_cast<int>(std::ceil(r * n_cached - 1e-9));
-}
+int k_for_ratio(double r, int n_cached) { return cb_k_for_ratio(r, n_cached); }
 
 // ----------------------------------------------------------------------------- chunk registry
 struct ChunkEntry {
@@ -1279,8 +1276,11 @@ cb_status cb_gemm(const void* A, const void* B, const void* B2, void* C, int M, 
     return fail(nullptr, CB_ERR_DTYPE, "unknown dtype");
   }
   if (epilogue == 2 ? ldc < N / 2 : ldc < N) return fail(nullptr, CB_ERR_SHAPE, "ldc too small");
-  cudaError_t e = launch_gemm(A, B, epilogue == 2 ? B2 : nullptr, nullptr, N, N, C, M, N, K, ldc, epilogue, dtype,
-                              nullptr, scratch, scratch ? scratch_bytes : 0, as_stream(stream));
+  int32_t* status = nullptr;  // device-side problems go to the standalone GEMM status word
+  cudaError_t e = standalone_gemm_status(&status);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "cb_gemm");
+  e = launch_gemm(A, B, epilogue == 2 ? B2 : nullptr, nullptr, N, N, C, M, N, K, ldc, epilogue, dtype, status, scratch,
+                  scratch ? scratch_bytes : 0, as_stream(stream));
   return e == cudaSuccess ? CB_OK : cuda_fail(nullptr, e, "cb_gemm");
 }
 

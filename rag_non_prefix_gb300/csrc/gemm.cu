@@ -978,13 +978,10 @@ static GemmPlan plan_gemm(int M, int N, int K, int split0, int split1, long long
 template <int BN, bool WROWS>
 static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
                              const CUtensorMap& c, tc::Params p, const GemmPlan& g, void* scratch, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc::gemm_bf16_tc<BN, WROWS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tc::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static DeviceOnce configured;
+  cudaError_t e = max_dynamic_smem_once(reinterpret_cast<const void*>(tc::gemm_bf16_tc<BN, WROWS>), tc::SMEM_ALLOC,
+                                        configured);
+  if (e != cudaSuccess) return e;
   p.m_tiles = g.tok_tiles;
   p.kb_per_tile = p.K / tc::BK;
   p.tiles = g.tiles;
@@ -1002,11 +999,29 @@ static cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const 
   return cudaGetLastError();
 }
 
+// Stream-K partial slots that scratch_bytes of scratch holds (after the flags).
+static long long scratch_slots(const void* scratch, size_t scratch_bytes) {
+  const size_t slot_bytes = static_cast<size_t>(tc::BM) * 256 * sizeof(float);
+  return scratch && scratch_bytes > static_cast<size_t>(tc::FLAG_BYTES)
+             ? static_cast<long long>((scratch_bytes - tc::FLAG_BYTES) / slot_bytes)
+             : 0;
+}
+
 // Scratch bytes the schedule of launch_gemm would use for a single-tensor B of N output
 // columns with unlimited scratch (0 when the shape runs data-parallel).
 size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt) {
   if (dt != CB_BF16 || M <= 0) return 0;
   return plan_gemm(M, N, K, N, N, 1LL << 40).scratch_used;
+}
+
+// Scratch bytes launch_gemm uses for these operands when it is given scratch_bytes of
+// scratch: 0 on the paths that take none (no rows, the few-row GEMV, fp32), otherwise
+// what the schedule narrowed to the slots that scratch holds uses (never more than it).
+size_t gemm_scratch_used(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, int M,
+                         int N, int K, cb_dtype dt, size_t scratch_bytes) {
+  if (M <= 0 || dt != CB_BF16 || gemv_applies(M, K, dt, A, B0, B1, B2)) return 0;
+  return plan_gemm(M, N, K, split0, split1, scratch_slots(reinterpret_cast<const void*>(1), scratch_bytes))
+      .scratch_used;
 }
 
 // mode: EPI_STORE_F32 / EPI_ADD_F32 (C fp32 [M][ldc]) or EPI_SWIGLU (C dtype [M][ldc], N/2 columns).
@@ -1035,11 +1050,7 @@ cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const voi
     return cudaGetLastError();
   }
   // bf16 on tcgen05
-  const size_t slot_bytes = static_cast<size_t>(tc::BM) * 256 * sizeof(float);
-  const long long slots = scratch && scratch_bytes > static_cast<size_t>(tc::FLAG_BYTES)
-                              ? static_cast<long long>((scratch_bytes - tc::FLAG_BYTES) / slot_bytes)
-                              : 0;
-  const GemmPlan g = plan_gemm(M, N, K, split0, split1, slots);
+  const GemmPlan g = plan_gemm(M, N, K, split0, split1, scratch_slots(scratch, scratch_bytes));
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   // token rows: A box 128 rows, weight box BN rows (SwiGLU BN/2 + BN/2);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "cacheblend.h"
 
 namespace cb {
@@ -87,6 +89,24 @@ struct AttnTile {
 bool launch_overlap_enabled();
 void set_launch_overlap(bool on);
 
+// cudaFuncSetAttribute applies to the current device only: kernels that need more than
+// the default dynamic shared memory set it once per device (bit d of `done` for device d;
+// devices past 63 set it on every launch).  Threads racing on the first launch both set
+// it, which is harmless.
+struct DeviceOnce {
+  std::atomic<uint64_t> done{0};
+};
+inline cudaError_t max_dynamic_smem_once(const void* kernel, int bytes, DeviceOnce& once) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (once.done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) once.done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_chain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                          Args&&... args) {
@@ -159,6 +179,12 @@ size_t gemm_scratch_bytes();
 void gemm_set_orientation(int o);  // 0 model, 1 token rows, 2 weight rows
 // scratch the schedule of one single-B GEMM uses when scratch is unlimited (0: none)
 size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt);
+// scratch launch_gemm uses for these operands given scratch_bytes of it (<= scratch_bytes)
+size_t gemm_scratch_used(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, int M,
+                         int N, int K, cb_dtype dt, size_t scratch_bytes);
+// Device address of the status word that the standalone GEMM calls (cb_gemm,
+// cb_gemm_noalloc) report device-side problems into, on the current device.
+cudaError_t standalone_gemm_status(int32_t** out);
 cudaError_t launch_attention(const void* q, const int32_t* s_pos, const int32_t* s_req, const ReqDev* reqs,
                              const AttnTile* tiles, int n_tiles, int layer, int n_heads, int n_kv_heads, int head_dim,
                              void* out, cb_dtype dt, cudaStream_t s);

@@ -79,11 +79,28 @@ def test_struct_layout_matches_c_compiler(tmp_path):
 @pytest.mark.parametrize("L,r,sched", [(2, 0.15, "fixed"), (32, 0.15, "gradual"), (60, 0.15, "gradual"),
                                        (80, 0.1, "gradual"), (80, 0.2, "gradual"), (4, 0.5, "gradual"),
                                        (32, 0.0, "gradual"), (32, 1.0, "fixed")])
-def test_host_schedule_matches_oracle(L, r, sched):
-    assert cb.ratio_schedule(L, r, sched) == pytest.approx(orc.ratio_schedule(L, r, sched))
+def test_host_schedule_matches_oracle(lib, L, r, sched):
+    """cb_ratio_schedule / cb_k_for_ratio (C) against the oracle's reading R3 / R5, value for value."""
+    assert cb.ratio_schedule(L, r, sched) == orc.ratio_schedule(L, r, sched)
     for nc in (1, 255, 256, 3136, 4096, 8192):
         for x in cb.ratio_schedule(L, r, sched):
             assert cb.k_for_ratio(x, nc) == orc.k_for_ratio(x, nc)
+
+
+@pytest.mark.parametrize("L,r,r1,n", [(32, 0.15, 0.6, 5), (6, 0.1, 0.1, 3), (3, 0.2, None, 4), (60, 0.05, 1.0, 0)])
+def test_host_schedule_options_match_oracle(lib, L, r, r1, n):
+    assert cb.ratio_schedule(L, r, "gradual", r1=r1, n_narrow=n) == orc.ratio_schedule(L, r, "gradual", r1=r1,
+                                                                                        n_narrow=n)
+
+
+def test_host_schedule_rejects_bad_ratios(lib):
+    for args in ((8, -0.1, "gradual"), (8, 1.5, "fixed")):
+        with pytest.raises(cb.CacheBlendError):
+            cb.ratio_schedule(*args)
+    with pytest.raises(cb.CacheBlendError):  # r1 below r
+        cb.ratio_schedule(8, 0.3, "gradual", r1=0.2)
+    with pytest.raises(ValueError):
+        cb.ratio_schedule(8, 0.3, "linear")
 
 
 def test_library_fails_loudly_when_missing(tmp_path):
