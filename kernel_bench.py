@@ -1,12 +1,12 @@
 """Per-kernel timing of the library's hot kernels through the C ABI (CUDA events).
 
-    python -m rag_non_prefix_gb300.kernel_bench gemm --M 535 --N 28672 --K 4096 --mode swiglu
-    python -m rag_non_prefix_gb300.kernel_bench attention --H 32 --Hkv 8 --N 3200 --m 535
-    python -m rag_non_prefix_gb300.kernel_bench rerotate --rows 100352 --hkv 8
-    python -m rag_non_prefix_gb300.kernel_bench select --n 3136 --k 471
-    python -m rag_non_prefix_gb300.kernel_bench deviation --n 3200 --kvw 1024
-    python -m rag_non_prefix_gb300.kernel_bench codec --n 3136 --hkv 8 --bits 8
-    python -m rag_non_prefix_gb300.kernel_bench decode --layers 32 --steps 2
+    python kernel_bench.py gemm --M 535 --N 28672 --K 4096 --mode swiglu
+    python kernel_bench.py attention --H 32 --Hkv 8 --N 3200 --m 535
+    python kernel_bench.py rerotate --rows 100352 --hkv 8
+    python kernel_bench.py select --n 3136 --k 471
+    python kernel_bench.py deviation --n 3200 --kvw 1024
+    python kernel_bench.py codec --n 3136 --hkv 8 --bits 8
+    python kernel_bench.py decode --layers 32 --steps 2
 
 (`decode` builds the Mistral-7B-shaped model with --layers layers, blends the configuration-2
 prompt, decodes 4 warm-up steps, then --steps steps inside the NVTX range "decode_prof" that

@@ -1,14 +1,16 @@
 """Summarise an ncu launch list (``ncu --csv --log-file``) of the blended prefill.
 
-    python -m rag_non_prefix_gb300.ncu_summary launches.csv --steps 2 \\
+    python ncu_summary.py launches.csv --steps 2 \\
         --markdown out.md --traffic-json profiles/gemm_traffic.json --command "<the ncu command>"
 
 Per kernel: launches, total device time, share of the listed time and, when the capture
 has ``dram__bytes_read.sum`` / ``dram__bytes_write.sum``, the average DRAM bytes per
-launch.  ``--traffic-json`` records the projection GEMM's average bytes per launch with a
-hash of its sources, which ``bench.py`` reports as ``roofline.traffic`` only while the
-kernel source is unchanged.  Durations under ncu are serialised and cold-cache: compare
-shares, not absolute times.
+launch.  A launch list over a full-size workload carries ``gpu__time_duration.sum`` only;
+DRAM counters come from single-kernel captures of a small case (``-k``, ``-c 1..3``).
+``--traffic-json`` records, from such a capture, the projection GEMM's DRAM bytes per
+launch with a hash of its sources, which ``bench.py`` reports as ``roofline.traffic`` only
+while the kernel source is unchanged.  Durations under ncu are serialised and cold-cache:
+compare shares, not absolute times.
 """
 from __future__ import annotations
 
