@@ -32,8 +32,10 @@ decoders shaped like Mistral-7B, Llama-7B, Yi-34B and Llama-70B.
 """
 from __future__ import annotations
 
+import ctypes
 import dataclasses
 import math
+import os
 from typing import Dict, List, Optional, Sequence
 
 import numpy as np
@@ -78,14 +80,53 @@ def weight_scale(std: float = WEIGHT_STD) -> np.float32:
     return np.float32(std * math.sqrt(3.0) / float(1 << 22))
 
 
-def gen_weight_fp32(key: int, start: int, count: int, std: float = WEIGHT_STD) -> np.ndarray:
-    """fp32 weights for flat indices [start, start + count) of the stream ``key``."""
+def gen_weight_fp32_numpy(key: int, start: int, count: int, std: float = WEIGHT_STD) -> np.ndarray:
+    """fp32 weights for flat indices [start, start + count) of the stream ``key`` (numpy)."""
     e = np.arange(start, start + count, dtype=np.uint64)
     w0 = draw(key, e * np.uint64(2))
     w1 = draw(key, e * np.uint64(2) + np.uint64(1))
     s = (w0 & _MASK22) + ((w0 >> np.uint64(22)) & _MASK22) + (w1 & _MASK22) + ((w1 >> np.uint64(22)) & _MASK22)
     z = s.astype(np.int64) - ((1 << 23) - 2)
     return z.astype(np.float32) * weight_scale(std)
+
+
+_HOST_LIB_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "harness",
+                              "libsynth_host.so")
+_HOST_LIB = None
+
+
+def host_generator():
+    """The C twin of the generator (``harness/libsynth_host.so``), or None when it is not built."""
+    global _HOST_LIB
+    if _HOST_LIB is None:
+        if not os.path.exists(_HOST_LIB_PATH):
+            return None
+        lib = ctypes.CDLL(_HOST_LIB_PATH)
+        lib.synth_weights_host.restype = ctypes.c_int
+        lib.synth_weights_host.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_float,
+                                           ctypes.c_int, ctypes.c_void_p]
+        _HOST_LIB = lib
+    return _HOST_LIB
+
+
+def gen_weight_fp32_c(key: int, start: int, count: int, std: float = WEIGHT_STD, as_bf16: bool = False) -> np.ndarray:
+    """The same elements from the C generator (threads over the range); ``as_bf16`` rounds
+    each to bf16 (nearest, ties to even) and returns the fp32 value of the bf16."""
+    lib = host_generator()
+    if lib is None:
+        raise RuntimeError(f"{_HOST_LIB_PATH} is missing: run `python -m rag_non_prefix_gb300.build`")
+    out = np.empty(count, dtype=np.float32)
+    lib.synth_weights_host(key & 0xFFFFFFFFFFFFFFFF, start, count, float(weight_scale(std)), int(as_bf16),
+                           out.ctypes.data)
+    return out
+
+
+def gen_weight_fp32(key: int, start: int, count: int, std: float = WEIGHT_STD) -> np.ndarray:
+    """fp32 weights for flat indices [start, start + count) of the stream ``key``: the C
+    generator for large ranges when it is built, numpy otherwise (identical bits)."""
+    if count >= 1 << 16 and host_generator() is not None:
+        return gen_weight_fp32_c(key, start, count, std)
+    return gen_weight_fp32_numpy(key, start, count, std)
 
 
 def fp32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -162,6 +203,8 @@ def gen_matrix(cfg: ModelConfig, seed: int, layer: int, mat: int, rows: Optional
     """One weight matrix (or a subset of its rows) as float32 values of the model dtype."""
     out_f, in_f = cfg.mat_shape(mat) if layer < GLOBAL_LM_LAYER else (cfg.vocab, cfg.d_model)
     key = layer_weight_key(seed, layer, mat)
+    if rows is None and host_generator() is not None:
+        return gen_weight_fp32_c(key, 0, out_f * in_f, as_bf16=cfg.dtype == "bf16").reshape(out_f, in_f)
     if rows is None:
         w = gen_weight_fp32(key, 0, out_f * in_f).reshape(out_f, in_f)
     else:
@@ -256,10 +299,14 @@ class PromptSpec:
     chunks: List[np.ndarray]  # the pool of independently cached chunks (token ids)
     requests: List[List[Segment]]  # per request: [prefix chunk?][chunks...][query]
     id_dist: str
+    depth: Optional[int] = None  # when set: only the model's first ``depth`` layers (same weights)
 
     @property
     def cfg(self) -> ModelConfig:
-        return MODELS[self.model]
+        c = MODELS[self.model]
+        if self.depth is None:
+            return c
+        return dataclasses.replace(c, n_layers=self.depth, name=f"{c.name}@{self.depth}")
 
     def n_tokens(self, r: int = 0) -> int:
         return sum(len(s.ids) for s in self.requests[r])
@@ -323,6 +370,15 @@ def workload(name: str) -> PromptSpec:
     if name == "small_gqa_f32":
         return make_prompt("small_gqa_f32", 13, [64, 80, 72], 20, 0.2, "gradual", "uniform", prefix_len=16, name=name)
     raise KeyError(name)
+
+
+def with_depth(spec: PromptSpec, depth: int) -> PromptSpec:
+    """The same prompts on the first ``depth`` layers of the model: every width, head count,
+    FFN size, rotary base, token count and batch unchanged; layer i keeps its weights (they
+    are keyed by (seed, layer, matrix)), as do the embedding and the LM head."""
+    if not 1 <= depth <= MODELS[spec.model].n_layers:
+        raise ValueError(depth)
+    return dataclasses.replace(spec, depth=depth, name=f"{spec.name}@{depth}")
 
 
 def ratio_for_k(k: int, n_cached: int) -> float:

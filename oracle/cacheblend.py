@@ -183,11 +183,15 @@ def output_and_mlp(cfg, W: Dict[str, np.ndarray], h: np.ndarray, attn: np.ndarra
     return h + (silu(g) * u) @ W["wdown"].astype(np.float64).T
 
 
+def lm_logits(cfg, weights, h_last: np.ndarray) -> np.ndarray:
+    """Logits of the untied LM head over RMSNorm(h) of one hidden row (reading R9)."""
+    x = rms_norm(np.asarray(h_last, dtype=np.float64)[None, :], cfg.rms_eps)[0]
+    return weights.lm_head().astype(np.float64) @ x
+
+
 def first_token(cfg, weights, h_last: np.ndarray) -> int:
     """argmax of the LM head over RMSNorm(h) of the last prompt token; ties -> lowest id."""
-    x = rms_norm(np.asarray(h_last, dtype=np.float64)[None, :], cfg.rms_eps)[0]
-    logits = weights.lm_head().astype(np.float64) @ x
-    return int(np.argmax(logits))
+    return int(np.argmax(lm_logits(cfg, weights, h_last)))
 
 
 # --------------------------------------------------------------------------- full prefill

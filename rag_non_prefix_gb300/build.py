@@ -3,6 +3,8 @@
 * ``rag_non_prefix_gb300/libcacheblend.so``: the blended-prefill kernels and runtime
   behind include/cacheblend.h.
 * ``harness/libsynth.so``: the harness's device-side input generator.
+* ``harness/libsynth_host.so``: the same generator on the host (gcc, OpenMP), so that
+  CPU-side inputs of billion-parameter shapes take seconds instead of minutes.
 
 Objects are compiled in parallel into ``_build/`` and relinked only when a source or
 header is newer than the library.
@@ -35,6 +37,30 @@ LIBS = {
         "build": os.path.join(ROOT, "harness", "_build"),
     },
 }
+
+
+# plain C libraries (gcc; they run on the host of whichever machine builds them)
+HOST_LIBS = {
+    os.path.join(ROOT, "harness", "libsynth_host.so"): [os.path.join(ROOT, "harness", "csrc", "synth_host.c")],
+}
+
+
+def gcc() -> str:
+    p = shutil.which("gcc") or shutil.which("cc")
+    if not p:
+        raise RuntimeError("gcc not found: needed for the host-side libraries")
+    return p
+
+
+def _build_host(lib: str, srcs) -> None:
+    if not _stale(lib, srcs):
+        return
+    base = [gcc(), "-O2", "-shared", "-fPIC", "-ffp-contract=off", "-o", lib, *srcs]
+    r = subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True, text=True)
+    if r.returncode != 0:  # no OpenMP runtime: single-threaded build of the same code
+        r = subprocess.run(base, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"gcc failed for {lib}:\n{r.stdout}\n{r.stderr}")
 
 
 def nvcc() -> str:
@@ -76,6 +102,11 @@ def build(verbose: bool = False) -> list:
             if verbose:
                 print("built", lib, file=sys.stderr)
             out.append(lib)
+    for lib, srcs in HOST_LIBS.items():
+        _build_host(lib, srcs)
+        if verbose:
+            print("built", lib, file=sys.stderr)
+        out.append(lib)
     return out
 
 
