@@ -135,7 +135,8 @@ def silu(x: np.ndarray) -> np.ndarray:
     return x / (1.0 + np.exp(-x))
 
 
-def causal_attention(q: np.ndarray, q_pos: Sequence[int], k: np.ndarray, v: np.ndarray) -> np.ndarray:
+def causal_attention(q: np.ndarray, q_pos: Sequence[int], k: np.ndarray, v: np.ndarray,
+                     block: int = 256) -> np.ndarray:
     """Causal scaled-dot-product attention of sparse queries over a KV cache.
 
     q[m, H, dh] are queries at global positions q_pos[m]; k, v[N, Hkv, dh] hold the
@@ -143,22 +144,30 @@ def causal_attention(q: np.ndarray, q_pos: Sequence[int], k: np.ndarray, v: np.n
     reads KV head floor(h * Hkv / H) (grouped-query attention).  [P3] "어떤 토큰을
     다시 계산하는가": selected queries attend, under the causal mask, to all available
     K/V -- cached rows included.
+
+    Written as softmax(q K^T / sqrt(dh) + M) V with M[t, j] = -inf for keys j after
+    q_pos[t] (0 otherwise).  Query rows are independent; taking them ``block`` at a time
+    only bounds the memory of the score matrix.
     """
     m, H, dh = q.shape
     Hkv = k.shape[1]
     G = H // Hkv
     out = np.zeros((m, H, dh), dtype=np.float64)
     scale = 1.0 / math.sqrt(dh)
-    for t in range(m):
-        p = int(q_pos[t])
-        kk = k[: p + 1].transpose(1, 2, 0)  # [Hkv, dh, p+1]
-        vv = v[: p + 1].transpose(1, 0, 2)  # [Hkv, p+1, dh]
-        qg = q[t].reshape(Hkv, G, dh)
-        s = np.matmul(qg, kk) * scale  # [Hkv, G, p+1]
-        s = s - s.max(axis=-1, keepdims=True)
-        w = np.exp(s)
-        w = w / w.sum(axis=-1, keepdims=True)
-        out[t] = np.matmul(w, vv).reshape(H, dh)
+    q_pos = np.asarray(q_pos, dtype=np.int64).reshape(m)
+    for t0 in range(0, m, block):
+        t1 = min(m, t0 + block)
+        b = t1 - t0
+        n = int(q_pos[t0:t1].max()) + 1  # keys any query of the block may see
+        after = np.arange(n)[None, :] > q_pos[t0:t1, None]  # [b, n]: the causal mask
+        for g in range(Hkv):  # query heads g*G .. g*G + G - 1 read KV head g
+            qg = q[t0:t1, g * G:(g + 1) * G, :].reshape(b * G, dh)
+            s = (qg @ k[:n, g, :].T).reshape(b, G, n) * scale
+            s = np.where(after[:, None, :], -np.inf, s)
+            s = s - s.max(axis=-1, keepdims=True)
+            w = np.exp(s)
+            w = w / w.sum(axis=-1, keepdims=True)
+            out[t0:t1, g * G:(g + 1) * G, :] = (w.reshape(b * G, n) @ v[:n, g, :]).reshape(b, G, dh)
     return out
 
 

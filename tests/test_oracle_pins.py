@@ -133,6 +133,24 @@ def test_attention_matches_torch_sdpa_with_sparse_queries():
     assert np.max(np.abs(out - ref)) < 1e-12
 
 
+def test_attention_across_query_blocks_matches_torch_sdpa():
+    """Unsorted query positions spread over several query blocks (block = 4) of the oracle."""
+    rng = _rng(12)
+    N, H, Hkv, dh = 50, 8, 2, 16
+    k = rng.standard_normal((N, Hkv, dh))
+    v = rng.standard_normal((N, Hkv, dh))
+    qpos = rng.permutation(N)[:19]
+    q = rng.standard_normal((len(qpos), H, dh))
+    out = orc.causal_attention(q, qpos, k, v, block=4)
+    G = H // Hkv
+    kt = torch.from_numpy(k).repeat_interleave(G, dim=1).permute(1, 0, 2)
+    vt = torch.from_numpy(v).repeat_interleave(G, dim=1).permute(1, 0, 2)
+    qt = torch.from_numpy(q).permute(1, 0, 2)
+    mask = torch.from_numpy(np.arange(N)[None, :] <= qpos[:, None])
+    ref = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask).permute(1, 0, 2).numpy()
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
 def test_attention_textbook_loops_and_edge_cases():
     rng = _rng(10)
     N, H, dh = 6, 2, 4
