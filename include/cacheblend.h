@@ -484,9 +484,18 @@ typedef struct {
   int launches[CB_N_PHASES]; /* kernels launched per phase */
   int calls[CB_N_PHASES];    /* timed phase instances */
 } cb_profile;
+/* enable: 0 off, 1 per-phase events, 2 per-phase events and per-layer events (below). */
 cb_status cb_set_profiling(cb_ctx* ctx, int enable);
 /* Waits for the recorded events, fills *out and resets the counters. */
 cb_status cb_get_profile(cb_ctx* ctx, cb_profile* out);
+/* Per-layer device times of the batches run at profiling level 2 since the last call,
+ * for the overlap of loading and recompute ([P1] パイプライン化の設計: per layer
+ * T ~ max(T_load, T_recompute)).  load_ms_host[i]: the copy stream's staging of layer
+ * i's host-resident chunk KV, from its first copy to its last (0 when nothing of layer i
+ * was staged).  compute_ms_host[i]: layer i on the compute stream, from after its wait
+ * for the staged KV to its last kernel (the begin and finish steps are not a layer).
+ * Host arrays [n_layers]; waits for the recorded events and releases them. */
+cb_status cb_get_layer_profile(cb_ctx* ctx, int n_layers, float* load_ms_host, float* compute_ms_host);
 
 /* A context runs one batch at a time and reuses its workspace for the next one:
  * issue consecutive batches on one stream (or synchronize between them). */

@@ -26,7 +26,7 @@ EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_
             "cb_blend_prefill",
             "cb_full_prefill", "cb_blend_begin", "cb_fetch_kv", "cb_synchronize", "cb_prefill_layer",
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
-            "cb_get_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_noalloc_scratch_used", "cb_gemm_get_status", "cb_gemm_set_orientation",
+            "cb_get_profile", "cb_get_layer_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_noalloc_scratch_used", "cb_gemm_get_status", "cb_gemm_set_orientation",
             "cb_set_launch_overlap", "cb_codec_layer_bytes", "cb_kv_encode", "cb_kv_decode", "cb_register_chunk_codec",
             "cb_set_staging", "cb_chunk_hash", "cb_chunk_info_of", "cb_plan_loading", "cb_decode_step",
             "cb_ratio_schedule", "cb_k_for_ratio")
@@ -152,6 +152,7 @@ def load_library(path: str = LIB_PATH):
         "cb_plan_counts": (st, [vp, C.c_int, C.POINTER(C.c_int32)]),
         "cb_set_profiling": (st, [vp, C.c_int]),
         "cb_get_profile": (st, [vp, C.POINTER(Profile)]),
+        "cb_get_layer_profile": (st, [vp, C.c_int, C.POINTER(C.c_float), C.POINTER(C.c_float)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -553,8 +554,16 @@ class Engine:
     def get_status(self, stream=None, timeout_ms: int = 60000):
         _check(self.lib.cb_get_status(self.ctx, _stream(stream), timeout_ms), self.ctx)
 
-    def set_profiling(self, enable: bool):
+    def set_profiling(self, enable):
+        """0 / False off, 1 / True per-phase events, 2 per-phase and per-layer events."""
         _check(self.lib.cb_set_profiling(self.ctx, int(enable)), self.ctx)
+
+    def get_layer_profile(self) -> Dict[str, List[float]]:
+        """Per-layer staging (copy stream) and compute (compute stream) ms since the last call."""
+        L = self.cfg.n_layers
+        load, comp = (C.c_float * L)(), (C.c_float * L)()
+        _check(self.lib.cb_get_layer_profile(self.ctx, L, load, comp), self.ctx)
+        return {"load_ms": list(load), "compute_ms": list(comp)}
 
     def get_profile(self) -> Dict[str, Dict[str, float]]:
         """Per-phase device ms, launches and timed calls since the last call (waits for the events)."""

@@ -242,14 +242,21 @@ struct cb_ctx {
 
   Batch b;
 
-  // profiling: events around phases (when enabled) and launch counts (always)
-  bool prof = false;
+  // profiling: events around phases (level >= 1), around each layer's staging copies and
+  // compute (level 2), and launch counts (always)
+  int prof = 0;
   std::vector<cudaEvent_t> ev_pool;
   struct Mark {
     int phase;
     cudaEvent_t a, b;
   };
   std::vector<Mark> marks;
+  struct LayerMark {
+    int layer;
+    int load;  // 1: staging copies (copy stream), 0: the layer's compute (compute stream)
+    cudaEvent_t a, b;
+  };
+  std::vector<LayerMark> layer_marks;
   int launches[CB_N_PHASES] = {};
   cudaEvent_t get_event() {
     if (!ev_pool.empty()) {
@@ -786,6 +793,7 @@ cb_status fetch_impl(cb_ctx* ctx, int layer, cudaStream_t cs) {
   if (layer < 0 || layer >= b.L) return fail(ctx, CB_ERR_INVALID_ARG, "layer out of range");
   const size_t kvw = static_cast<size_t>(c.n_kv_heads) * c.head_dim;
   const size_t es = dtype_bytes(c.dtype);
+  cudaEvent_t load_a = nullptr;  // per-layer profiling: from the first copy of the layer
   if (!b.stage.empty()) {
     const int slot = layer % b.n_slots;
     if (layer >= b.n_slots) {
@@ -794,6 +802,10 @@ cb_status fetch_impl(cb_ctx* ctx, int layer, cudaStream_t cs) {
       CB_CUDA(ctx, cudaStreamWaitEvent(cs, ctx->slot_ev[slot], 0));
     }
     uint8_t* dst = ctx->staging + static_cast<size_t>(slot) * b.slot_bytes;
+    if (ctx->prof >= 2 && !load_a) {
+      load_a = ctx->get_event();
+      CB_CUDA(ctx, cudaEventRecord(load_a, cs));
+    }
     for (const Batch::StageCopy& sc : b.stage)
       CB_CUDA(ctx, cudaMemcpyAsync(dst + sc.slot_off, sc.src + static_cast<size_t>(layer) * sc.layer_bytes,
                                    sc.layer_bytes, cudaMemcpyHostToDevice, cs));
@@ -804,15 +816,46 @@ cb_status fetch_impl(cb_ctx* ctx, int layer, cudaStream_t cs) {
       const size_t bytes = static_cast<size_t>(sg.n) * kvw * es;
       const size_t so = static_cast<size_t>(layer) * bytes;
       const size_t dof = (static_cast<size_t>(layer) * rh.layer_stride + static_cast<size_t>(sg.off) * kvw) * es;
+      if (ctx->prof >= 2 && !load_a) {
+        load_a = ctx->get_event();
+        CB_CUDA(ctx, cudaEventRecord(load_a, cs));
+      }
       CB_CUDA(ctx, cudaMemcpyAsync(static_cast<uint8_t*>(rh.fused_k) + dof,
                                    static_cast<const uint8_t*>(sg.chunk->k) + so, bytes, cudaMemcpyHostToDevice, cs));
       CB_CUDA(ctx, cudaMemcpyAsync(static_cast<uint8_t*>(rh.fused_v) + dof,
                                    static_cast<const uint8_t*>(sg.chunk->v) + so, bytes, cudaMemcpyHostToDevice, cs));
     }
+  if (load_a) {
+    cudaEvent_t load_b = ctx->get_event();
+    CB_CUDA(ctx, cudaEventRecord(load_b, cs));
+    ctx->layer_marks.push_back(cb_ctx::LayerMark{layer, 1, load_a, load_b});
+  }
   CB_CUDA(ctx, cudaEventRecord(ctx->fetch_ev[layer], cs));
   b.fetched[layer] = 1;
   return CB_OK;
 }
+
+// Per-layer profiling (level 2): events around one layer's work on the compute stream,
+// from after its wait for staged KV to its last kernel.
+struct LayerScope {
+  cb_ctx* ctx;
+  int layer;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  LayerScope(cb_ctx* c, int i, cudaStream_t st) : ctx(c), layer(i), s(st) {
+    if (ctx->prof >= 2) {
+      a = ctx->get_event();
+      cudaEventRecord(a, s);
+    }
+  }
+  ~LayerScope() {
+    if (a) {
+      cudaEvent_t b = ctx->get_event();
+      cudaEventRecord(b, s);
+      ctx->layer_marks.push_back(cb_ctx::LayerMark{layer, 0, a, b});
+    }
+  }
+};
 
 cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   Batch& b = ctx->b;
@@ -822,6 +865,9 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   if (b.any_host) {
     if (!b.fetched[i]) return fail(ctx, CB_ERR_STATE, "cb_fetch_kv was not called for this layer");
     CB_CUDA(ctx, cudaStreamWaitEvent(s, ctx->fetch_ev[i], 0));
+  }
+  LayerScope layer_scope(ctx, i, s);
+  if (b.any_host) {
     if (b.host_seg_n[i] > 0) {
       PhaseScope ps(ctx, CB_PH_STAGED_ROT, s, 1);
       CB_CUDA(ctx, launch_rerotate(ctx->d_segs + b.host_seg_off[i], b.host_seg_n[i], b.host_max_rows, c.n_kv_heads,
@@ -1593,8 +1639,26 @@ cb_status cb_get_status(cb_ctx* ctx, void* stream, int timeout_ms) {
 
 cb_status cb_set_profiling(cb_ctx* ctx, int enable) {
   if (!ctx) return fail(ctx, CB_ERR_INVALID_ARG, "null context");
-  ctx->prof = enable != 0;
+  ctx->prof = enable <= 0 ? 0 : (enable >= 2 ? 2 : 1);
   return CB_OK;
+}
+
+cb_status cb_get_layer_profile(cb_ctx* ctx, int n_layers, float* load_ms_host, float* compute_ms_host) {
+  if (!ctx || n_layers < 0 || (n_layers > 0 && (!load_ms_host || !compute_ms_host)))
+    return fail(ctx, CB_ERR_INVALID_ARG, "bad arguments");
+  for (int i = 0; i < n_layers; ++i) load_ms_host[i] = compute_ms_host[i] = 0.f;
+  cb_status st = CB_OK;
+  for (const cb_ctx::LayerMark& m : ctx->layer_marks) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(m.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, m.a, m.b);
+    if (e != cudaSuccess && st == CB_OK) st = cuda_fail(ctx, e, "cb_get_layer_profile");
+    if (m.layer >= 0 && m.layer < n_layers) (m.load ? load_ms_host : compute_ms_host)[m.layer] += ms;
+    ctx->ev_pool.push_back(m.a);
+    ctx->ev_pool.push_back(m.b);
+  }
+  ctx->layer_marks.clear();
+  return st;
 }
 
 cb_status cb_get_profile(cb_ctx* ctx, cb_profile* out) {

@@ -43,19 +43,22 @@ def test_device_generator_matches_host_bits(dtype):
 
 # ----------------------------------------------------------------------------- re-rotation
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("n,hkv,dh,delta", [(1, 1, 64, 3), (37, 4, 64, 128), (512, 8, 128, 3136), (333, 2, 128, 8191),
-                                            (64, 8, 128, 0)])
-def test_rerotate_matches_oracle(dtype, n, hkv, dh, delta):
+@pytest.mark.parametrize("n,hkv,dh,delta,theta", [(1, 1, 64, 3, 1e4), (37, 4, 64, 128, 1e4), (512, 8, 128, 3136, 1e4),
+                                                  (333, 2, 128, 8191, 1e4), (64, 8, 128, 0, 1e4),
+                                                  # the Yi-34B shape's rotary base, chunks up to its last offset
+                                                  (512, 8, 128, 7680, 5e6), (128, 8, 128, 8320, 5e6),
+                                                  (512, 8, 128, 512, 5e6)])
+def test_rerotate_matches_oracle(dtype, n, hkv, dh, delta, theta):
     rng = np.random.default_rng(n + delta)
     k = rng.standard_normal((n, hkv, dh)).astype(np.float32)
     v = rng.standard_normal((n, hkv, dh)).astype(np.float32)
     mk = _bf16 if dtype == "bf16" else _f32
     ks, vs = mk(k), mk(v)
     kd, vd = torch.empty_like(ks), torch.empty_like(vs)
-    cb.cb_rope_rerotate(ks, kd, vs, vd, delta, 1e4)
+    cb.cb_rope_rerotate(ks, kd, vs, vd, delta, theta)
     torch.cuda.synchronize()
     kin = to_np(ks)
-    ref = orc.rerotate_keys(kin, delta, 1e4)
+    ref = orc.rerotate_keys(kin, delta, theta)
     got = to_np(kd)
     if dtype == "bf16":
         ref = orc.round_storage(ref, "bf16")
@@ -281,7 +284,10 @@ def test_attention_bf16_matches_oracle(H, Hkv, N, m):
     sample = np.arange(m) if m <= 80 else np.unique(np.concatenate([np.arange(8), rng.choice(m, 40), [m - 1]]))
     ref = orc.causal_attention(to_np(q)[sample], pos[sample], to_np(k), to_np(v))
     got = to_np(out)[sample]
-    assert np.max(np.abs(got - ref)) < 2e-2 * np.max(np.abs(ref))
+    # per query row and head: ||g - o||_inf / ||o||_inf (bf16 probabilities and output:
+    # a few 2^-9 relative errors per element)
+    err = np.max(np.abs(got - ref), axis=2) / np.maximum(np.max(np.abs(ref), axis=2), 1e-30)
+    assert np.max(err) < 2e-2, float(np.max(err))
 
 
 @pytest.mark.parametrize("H,Hkv,dh,N,m", [(4, 4, 64, 288, 71), (8, 2, 64, 252, 40), (2, 1, 128, 100, 100)])
