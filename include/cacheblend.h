@@ -265,6 +265,15 @@ size_t cb_gemm_scratch_size(void);
  * values: CB_ERR_INVALID_ARG. */
 cb_status cb_gemm_set_orientation(int orientation);
 
+/* Query tiles per CTA of the bf16 attention, process-wide (a tuning and test hook;
+ * default 0).  0: two 128-row tiles of one KV head per CTA when a launch's tile pairs
+ * times the KV heads fill the SMs (the tensor core then works for one tile while the
+ * other's softmax runs, and each K/V block is loaded once for both), else one tile per
+ * CTA with the longest tiles' key ranges split over two CTAs; 1 or 2: that many tiles
+ * per CTA.  Results agree to the rounding of the same sums.  Other values:
+ * CB_ERR_INVALID_ARG. */
+cb_status cb_attention_set_tiles(int tiles);
+
 /* Programmatic dependent launch of the blended-prefill kernels, process-wide (default
  * 1): each kernel of a layer may start while the previous one drains, running the part
  * of its prologue that touches only its own on-chip memory (barriers, tensor-memory

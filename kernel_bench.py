@@ -1,7 +1,7 @@
 """Per-kernel timing of the library's hot kernels through the C ABI (CUDA events).
 
     python kernel_bench.py gemm --M 535 --N 28672 --K 4096 --mode swiglu
-    python kernel_bench.py attention --H 32 --Hkv 8 --N 3200 --m 535
+    python kernel_bench.py attention --H 32 --Hkv 8 --N 3200 --m 535 [--tiles 1|2] [--causal]
     python kernel_bench.py rerotate --rows 100352 --hkv 8
     python kernel_bench.py select --n 3136 --k 471
     python kernel_bench.py deviation --n 3200 --kvw 1024
@@ -71,6 +71,8 @@ def main():
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--iters", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--tiles", type=int, default=0, help="attention: query tiles per CTA (0 by size, 1, 2)")
+    ap.add_argument("--causal", action="store_true", help="attention: every position a query (full prefill)")
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--batch", type=int, default=1, help="launches per timed region")
     ap.add_argument("--no-stream-k", action="store_true", help="GEMM without scratch: whole tiles per CTA")
@@ -108,10 +110,17 @@ def main():
         k = torch.randn(N, Hkv, 128, device=dev).to(torch.bfloat16)
         v = torch.randn(N, Hkv, 128, device=dev).to(torch.bfloat16)
         o = torch.empty_like(q)
+        if a.causal:  # every position a query: the attention of a full prefill
+            pos = torch.arange(N, device=dev, dtype=torch.int32)
+            q = torch.randn(N, H, 128, device=dev).to(torch.bfloat16)
+            o = torch.empty_like(q)
+        cb.cb_attention_set_tiles(a.tiles)
         fn = lambda: cb.cb_attention(q, pos, k, v, o)  # noqa: E731
         avg, best = _time(fn, a.iters, a.warmup, flush, a.batch)
+        cb.cb_attention_set_tiles(0)
         fl = 4.0 * H * 128 * float((pos.to(torch.float64) + 1).sum())
-        out.update(shape=[H, Hkv, N, m], ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12)
+        out.update(shape=[H, Hkv, N, int(pos.numel())], tiles=a.tiles, ms=avg, best_ms=best,
+                   tflops=fl / (avg * 1e-3) / 1e12)
     elif a.kernel == "rerotate":
         k = torch.randn(a.rows, a.hkv, 128, device=dev).to(torch.bfloat16)
         v = torch.randn(a.rows, a.hkv, 128, device=dev).to(torch.bfloat16)

@@ -22,6 +22,7 @@
 // fp32 (any head_dim multiple of 32 up to 128): one warp per (query, head); lanes split
 // 32 keys at a time for the scores and head_dim for the output; expf softmax.
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -107,6 +108,11 @@ struct Args {
   float2* part_ml;     // [unit][2][128] (reference max, row sum)
   int* part_cnt;       // [unit] CTAs of the unit done (reset to 0 by the second)
   int n_paired;
+  // two query tiles per CTA (attn_tc2_kernel): request r's tiles are tiles[tile_off[r] ..
+  // tile_off[r + 1]) of this launch and its tile pairs pair_off[r] .. pair_off[r + 1]
+  int tile_off[MAXREQ + 1];
+  int pair_off[MAXREQ + 1];
+  int n_pairs;
 };
 
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {  // K-major, 128-byte swizzle
@@ -573,6 +579,430 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
 
 }  // namespace ta
 
+// ----------------------------------------------------------------------------- two tiles per CTA
+// attn_tc2_kernel: the same attention with two query tiles of one KV head per CTA, so that
+// the tensor core works for one tile while the other tile's softmax runs, and every K/V
+// block is loaded once for both.  Per tile, S is single-buffered in tensor memory: the
+// softmax reads S_j into registers and releases it at once, so S_{j+1} is computed while
+// the softmax of block j still runs; P is single-buffered in shared memory and written
+// (and O rescaled) only after PV_{j-1} is done, the P values waiting in registers.  K and V
+// blocks share a three-slot ring loaded in the order K0, K1, V0, K2, V1, ..., K_{n-1},
+// V_{n-2}, V_{n-1}, the order the MMA issuer consumes them (S_{j+1} before PV_j): each K
+// block arrives two iterations ahead of its use, each V block one.
+//   warp 0: TMA producer (lane 0)            warp 1: TMEM owner + MMA issuer (lane 0)
+//   warps 2-9: softmax of tile 0             warps 10-17: softmax of tile 1
+// (in each group, as in attn_tc_kernel: two column halves x four lane quarters).
+// Tiles are paired within a request (tiles 2i and 2i + 1); pairs run longest first.  No
+// key-range split here: the launcher takes this kernel when the pairs fill the SMs.
+namespace tp {
+
+using namespace ta;
+constexpr int THREADS2 = 18 * 32;
+constexpr int OFF_Q2 = 0;                       // Q[2 tiles]: 2 atom columns each
+constexpr int OFF_P2 = OFF_Q2 + 4 * ATOM;       // P[2 tiles]: 2 atom columns each
+constexpr int OFF_RING = OFF_P2 + 4 * ATOM;     // 3 slots of one K or V block (2 atom columns)
+constexpr int SLOTS = 3;
+constexpr int SLOT = 2 * ATOM;
+constexpr int OFF_BAR2 = OFF_RING + SLOTS * SLOT;
+constexpr int SMEM2 = OFF_BAR2 + 3072;          // the 227 KiB limit, as attn_tc_kernel
+constexpr uint32_t S_COL = 0;                   // S of tile t at column 128 t
+constexpr uint32_t O_COL2 = 256;                // O of tile t at column 256 + 128 t
+
+// Position of K_j / V_j in the load order K0, K1, V0, K2, V1, ..., K_{n-1}, V_{n-2}, V_{n-1}
+__device__ __forceinline__ int k_item(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int v_item(int j, int nb) { return min(2 * j + 2, 2 * nb - 1); }
+
+struct PairTiles {
+  AttnTile t[2];
+  int n;  // tiles in the pair: 1 or 2
+};
+
+__device__ __forceinline__ PairTiles pair_of(const Args& a, int p) {
+  PairTiles pt;
+  if (a.tiles) {
+    int r = 0;
+    while (r + 1 < MAXREQ && p >= a.pair_off[r + 1]) ++r;
+    const int i0 = a.tile_off[r] + 2 * (p - a.pair_off[r]);
+    pt.n = i0 + 1 < a.tile_off[r + 1] ? 2 : 1;
+    for (int u = 0; u < 2; ++u) {
+      if (u < pt.n) {
+        pt.t[u] = a.tiles[i0 + u];
+        pt.t[u].req -= a.req_base;
+      } else {
+        pt.t[u] = AttnTile{pt.t[0].req, 0, 0, 0};
+      }
+    }
+  } else {
+    for (int u = 0; u < 2; ++u) {
+      const int row0 = (2 * p + u) * a.QT;
+      pt.t[u] = AttnTile{0, row0, max(0, min(a.QT, a.direct_m - row0)), 0};
+    }
+    pt.n = pt.t[1].count > 0 ? 2 : 1;
+  }
+  return pt;
+}
+
+// Barriers (per tile t, phase of block j is j & 1):
+//   q_full[t]   softmax warps of tile t stored Q_t      (8 arrivals)
+//   s_full[t]   S_t(j) in TMEM                          (MMA commit)
+//   s_empty[t]  S_t(j) read into registers              (8 arrivals)
+//   p_full[t]   P_t(j) in shared memory, O_t rescaled   (8 arrivals)
+//   pv_done[t]  PV_t(j) accumulated into O_t            (MMA commit)
+//   full[3]     ring slot loaded (TMA bytes); empty[3] ring slot consumed (MMA commit)
+__global__ void __launch_bounds__(THREADS2, 1) attn_tc2_kernel(const __grid_constant__ Args a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  pdl_trigger();
+  pdl_wait();
+  if (smem_u32(smem_raw) & 1023u) {  // uniform across the block
+    if (threadIdx.x == 0) set_status(a.status, ST_RANGE);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + OFF_BAR2);
+  uint64_t* q_full = bar;        // [2]
+  uint64_t* s_full = bar + 2;    // [2]
+  uint64_t* s_empty = bar + 4;   // [2]
+  uint64_t* p_full = bar + 6;    // [2]
+  uint64_t* pv_done = bar + 8;   // [2]
+  uint64_t* full = bar + 10;     // [3]
+  uint64_t* empty = bar + 13;    // [3]
+  uint64_t* drain = bar + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR2 + 144);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR2 + 148);
+  int* wmaxpos = reinterpret_cast<int*>(smem + OFF_BAR2 + 152);     // [2 tiles][4 quarters]
+  float* xch = reinterpret_cast<float*>(smem + OFF_BAR2 + 256);     // [2 tiles][2 halves][128]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = static_cast<int>(blockIdx.x % a.Hkv);
+  const int pix = a.n_pairs - 1 - static_cast<int>(blockIdx.x / a.Hkv);  // longest pairs first
+  const PairTiles pt = pair_of(a, pix);
+  const int G = a.G, QT = a.QT, H = a.H;
+  const int n_kv = a.n_kv[pt.t[0].req];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 8);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 8);
+      mbar_init(&p_full[i], 8);
+      mbar_init(&pv_done[i], 1);
+    }
+    for (int i = 0; i < SLOTS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // softmax thread: tile, column half, TMEM lane quarter, row
+  const int sw = warp - 2;
+  const int tl = sw >> 3;
+  const int half = (sw >> 2) & 1;
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;
+  const int qi = r / G, g = r - qi * G;
+  const AttnTile mt = tl == 1 ? pt.t[1] : pt.t[0];
+  const bool valid = warp >= 2 && qi < mt.count && r < QT * G;
+  const int pos = valid ? min(a.s_pos[mt.row0 + qi], n_kv - 1) : -1;
+  if (warp >= 2 && half == 0) {
+    const int wm = __reduce_max_sync(0xffffffffu, pos);
+    if (lane == 0) wmaxpos[tl * 4 + quarter] = wm;
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  int nbt[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int mp = max(max(wmaxpos[u * 4], wmaxpos[u * 4 + 1]), max(wmaxpos[u * 4 + 2], wmaxpos[u * 4 + 3]));
+    nbt[u] = mp < 0 ? 0 : mp / BKV + 1;
+  }
+  const int nb = max(nbt[0], nbt[1]);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const CUtensorMap* kmap = &a.kmap[pt.t[0].req];
+      const CUtensorMap* vmap = &a.vmap[pt.t[0].req];
+      const int lc = a.layer_coord[pt.t[0].req];
+      int issued = 0;
+      for (int x = 0; x < 2 * nb; ++x) {
+        const bool is_v = x == 2 * nb - 1 || (x > 0 && (x & 1) == 0);
+        const int j = x == 2 * nb - 1 ? nb - 1 : (x & 1) ? (x + 1) >> 1 : is_v ? (x - 2) >> 1 : 0;
+        const int st = x % SLOTS;
+        if (!mbar_wait_bounded(&empty[st], ((x / SLOTS) & 1) ^ 1, abort_flag)) break;
+        uint8_t* dst = smem + OFF_RING + st * SLOT;
+        mbar_arrive_expect_tx(&full[st], 2 * ATOM);
+        tma_load_4d(dst, is_v ? vmap : kmap, &full[st], 0, kvh, j * BKV, lc);
+        tma_load_4d(dst + ATOM, is_v ? vmap : kmap, &full[st], 64, kvh, j * BKV, lc);
+        issued = x + 1;
+      }
+      if (issued < 2 * nb && !*abort_flag) {
+        *abort_flag = 1;
+        set_status(a.status, ST_WAIT_TIMEOUT);
+      }
+      // copies issued into slots that nobody consumed must land before the block exits
+      for (int x = max(0, issued - SLOTS); x < issued; ++x) mbar_wait_bounded(&full[x % SLOTS], (x / SLOTS) & 1, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    bool ok = true;
+    auto wait = [&](uint64_t* b, uint32_t ph) {
+      if (ok && lane == 0) ok = mbar_wait_bounded(b, ph, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      return ok;
+    };
+    auto item_wait = [&](int x) { return wait(&full[x % SLOTS], (x / SLOTS) & 1); };
+    auto issue_s = [&](int u, int j) {  // S_u = Q_u K_j^T
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sq = smem_u32(smem + OFF_Q2 + u * 2 * ATOM);
+        const uint32_t sk = smem_u32(smem + OFF_RING + (k_item(j) % SLOTS) * SLOT);
+#pragma unroll
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint64_t da = desc_kmajor(sq + (kk >> 2) * ATOM) + 2 * (kk & 3);
+          const uint64_t db = desc_kmajor(sk + (kk >> 2) * ATOM) + 2 * (kk & 3);
+          tc_mma_f16(tmem + S_COL + u * 128, da, db, idesc(false), kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[u]);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int u, int j) {  // O_u (+)= P_u V_j
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sp = smem_u32(smem + OFF_P2 + u * 2 * ATOM);
+        const uint32_t sv = smem_u32(smem + OFF_RING + (v_item(j, nb) % SLOTS) * SLOT);
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk) {
+          const uint64_t da = desc_kmajor(sp + (kk >> 2) * ATOM) + 2 * (kk & 3);
+          const uint64_t db = desc_mnmajor(sv + kk * 16 * 128, ATOM);
+          tc_mma_f16(tmem + O_COL2 + u * 128, da, db, idesc(true), (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      }
+      __syncwarp();
+    };
+    for (int u = 0; u < 2; ++u)
+      if (nbt[u] > 0) wait(&q_full[u], 0);
+    if (nb > 0 && item_wait(k_item(0))) {
+      for (int u = 0; u < 2; ++u)
+        if (nbt[u] > 0) issue_s(u, 0);
+      if (lane == 0) tc_commit(&empty[k_item(0) % SLOTS]);
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < nb; ++j) {
+      // S_{j+1} of each tile as soon as its softmax has read S_j (and K_{j+1} landed) ...
+      const bool k_next = j + 1 < nb;
+      if (k_next && item_wait(k_item(j + 1))) {
+        for (int u = 0; u < 2 && ok; ++u) {
+          if (j + 1 >= nbt[u]) continue;
+          if (!wait(&s_empty[u], j & 1)) break;
+          issue_s(u, j + 1);
+        }
+        if (lane == 0 && ok) tc_commit(&empty[k_item(j + 1) % SLOTS]);
+        __syncwarp();
+      }
+      // ... then PV_j of each tile once its P_j is in shared memory
+      if (!ok || !item_wait(v_item(j, nb))) break;
+      for (int u = 0; u < 2 && ok; ++u) {
+        if (j >= nbt[u]) continue;
+        if (!wait(&p_full[u], j & 1)) break;
+        issue_pv(u, j);
+        if (lane == 0) tc_commit(&pv_done[u]);
+        __syncwarp();
+      }
+      if (lane == 0 && ok) tc_commit(&empty[v_item(j, nb) % SLOTS]);
+      __syncwarp();
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      set_status(a.status, ST_WAIT_TIMEOUT);
+    }
+    if (lane == 0) {  // no MMA may run when the tensor memory is released
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0u, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax / output (warps 2..17)
+    const int nbu = tl == 1 ? nbt[1] : nbt[0];
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(half * 64);
+    const uint32_t s_base = tmem + S_COL + tl * 128 + col0 + lane_off;
+    const uint32_t o_base = tmem + O_COL2 + tl * 128 + col0 + lane_off;
+    float* xs = xch + tl * 2 * ROWS;
+    bool ok = true;
+    auto wait = [&](uint64_t* b, uint32_t ph) {  // every lane polls: no divergent branch
+      if (ok) ok = mbar_wait_bounded(b, ph, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+    };
+    const uint32_t pair_bar = 1u + static_cast<uint32_t>(tl * 4 + quarter);
+    auto sm_bar = [pair_bar]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+    if (nbu > 0) {
+      {  // Q_tl: half h stores head_dim atom h of its rows
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + (static_cast<size_t>(mt.row0 + (valid ? qi : 0)) * H + kvh * G + g) * DH + half * 64);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = valid ? src[c] : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(smem + OFF_Q2 + tl * 2 * ATOM + half * ATOM + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_full[tl]);
+      }
+      float m = -1e30f, l = 0.f;
+      for (int j = 0; j < nbu; ++j) {
+        wait(&s_full[tl], j & 1);
+        uint32_t sv[64];
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) tmem_ld16_nowait(s_base + c, sv + c);
+          tmem_wait_ld();
+          tc_fence_before();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) sv[e] = 0u;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[tl]);  // S_{j+1} may now overwrite S_j
+        const int k0 = j * BKV + half * 64;
+        const bool fullblk = __all_sync(0xffffffffu, k0 + 63 <= pos);
+        float pm[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+        if (fullblk) {
+#pragma unroll
+          for (int e = 0; e < 64; e += 16)
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              pm[u] = max3(pm[u], __uint_as_float(sv[e + u]), __uint_as_float(sv[e + 8 + u]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (k0 + e <= pos) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(sv[e]));
+        }
+        float mx = max3(max3(pm[0], pm[1], pm[2]), max3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+        mx *= a.scale_log2;
+        // row max over both halves through one slot per (tile, half, row): the second barrier
+        // keeps either thread from rewriting its slot before the partner has read it
+        xs[half * ROWS + r] = mx;
+        sm_bar();
+        mx = fmaxf(mx, xs[(half ^ 1) * ROWS + r]);
+        sm_bar();
+        const bool need = mx > m + RESCALE_LOG2;
+        const float m_new = need ? mx : m;
+        const float alpha = ex2(m - m_new);
+        l *= alpha;
+        m = m_new;
+        // P_j in registers (bf16 pairs), then into this tile's buffer once PV_{j-1} is done
+        uint32_t pk[32];
+        if (fullblk) {
+          const uint64_t sc2 = f2(a.scale_log2, a.scale_log2), nm2 = f2(-m, -m);
+          uint64_t acc0 = f2(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float t0, t1;
+            f2_split(fma2(f2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sc2, nm2), t0, t1);
+            const float p0 = ex2(t0), p1 = ex2(t1);
+            if (e & 2)
+              acc1 = add2(acc1, f2(p0, p1));
+            else
+              acc0 = add2(acc0, f2(p0, p1));
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          float a0, a1, b0, b1;
+          f2_split(acc0, a0, a1);
+          f2_split(acc1, b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        } else {
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            const float p0 = k0 + e <= pos ? ex2(fmaf(__uint_as_float(sv[e]), a.scale_log2, -m)) : 0.f;
+            const float p1 = k0 + e + 1 <= pos ? ex2(fmaf(__uint_as_float(sv[e + 1]), a.scale_log2, -m)) : 0.f;
+            ls[(e >> 1) & 3] += p0 + p1;
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        }
+        if (j > 0) wait(&pv_done[tl], (j - 1) & 1);  // PV_{j-1} read P and wrote O
+        if (ok) {
+          tc_fence_after();
+          uint8_t* pb = smem + OFF_P2 + tl * 2 * ATOM + half * ATOM;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(pb + r * 128 + ((c ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          fence_proxy_async_smem();
+        }
+        if (__any_sync(0xffffffffu, need) && j > 0 && ok) {
+          // lazy rescale, after P (the S values are no longer live): O_tl holds PV_0 ..
+          // PV_{j-1}, complete (waited above); PV_j waits for this block's P
+#pragma unroll
+          for (int c = 0; c < 64; c += 16) {
+            uint32_t ov[16];
+            tmem_ld16_nowait(o_base + c, ov);
+            tmem_wait_ld();
+            float f[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(ov[e]) * alpha;
+            tmem_st16(o_base + c, f);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[tl]);
+      }
+      // O / (row sum of both halves)
+      sm_bar();
+      xs[half * ROWS + r] = l;
+      wait(&pv_done[tl], (nbu - 1) & 1);  // the last PV of this tile
+      sm_bar();
+      const float l_all = xs[r] + xs[ROWS + r];  // same order in both halves
+      if (ok) {
+        tc_fence_after();
+        bf16* dst = a.out + (static_cast<size_t>(mt.row0 + (valid ? qi : 0)) * H + kvh * G + g) * DH + half * 64;
+        const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t ov[16];
+          tmem_ld16_nowait(o_base + c, ov);
+          tmem_wait_ld();
+          if (valid) {
+            float f[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(ov[e]) * inv;
+            store8(dst + c, f);
+            store8(dst + c + 8, f + 8);
+          }
+        }
+      }
+      if (!ok && lane == 0) {
+        *abort_flag = 1;
+        set_status(a.status, ST_WAIT_TIMEOUT);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace tp
+
 // ----------------------------------------------------------------------------- fp32
 struct AttnArgsF32 {
   const float* q;
@@ -686,6 +1116,46 @@ bool encode_kv_map(CUtensorMap* map, const void* base, int n_layers, int n_token
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tiles per CTA of the bf16 attention, process-wide: 0 chosen per launch (two when the
+// tile pairs of a launch fill the SMs), 1 or 2 forced (tests, tuning).
+static std::atomic<int> g_attn_tiles{0};
+
+void attention_set_tiles(int tiles) { g_attn_tiles.store(tiles); }
+
+// Two tiles per CTA when the waves of pair units finish sooner than the waves of single
+// tiles: a pair unit takes ~1.75x a single tile's time (measured on GB300: full causal
+// 8320 tokens, 56/8 heads 1.360 -> 1.222 ms in 25 -> 13 waves; 1357 of 8320 queries 0.232
+// -> 0.208 ms), so the pairs win only where they also save a wave or more (884 of 8256
+// queries, 64/8 heads: 3 -> 2 waves, 0.167 -> 0.194 ms).  MHA (one head per KV head) was
+// slower with pairs at every size measured.
+static bool use_pairs(long long tiles, long long pairs, int n_heads, int n_kv_heads, int n_sm) {
+  const int mode = g_attn_tiles.load();
+  if (mode != 0) return mode == 2;
+  if (n_heads == n_kv_heads) return false;
+  const long long w1 = (tiles * n_kv_heads + n_sm - 1) / n_sm;
+  const long long w2 = (pairs * n_kv_heads + n_sm - 1) / n_sm;
+  return 1.75 * static_cast<double>(w2) < 0.97 * static_cast<double>(w1);
+}
+
+static int sm_count_cached() {
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    n_sm = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 148;
+  }
+  return n_sm;
+}
+
+static cudaError_t tc2_launch(ta::Args& args, cudaStream_t s) {
+  static DeviceOnce configured;
+  cudaError_t e = max_dynamic_smem_once(reinterpret_cast<const void*>(tp::attn_tc2_kernel), tp::SMEM2, configured);
+  if (e != cudaSuccess) return e;
+  if (args.n_pairs <= 0) return cudaSuccess;
+  launch_chain(tp::attn_tc2_kernel, dim3(args.n_pairs * args.Hkv), dim3(tp::THREADS2), tp::SMEM2, s, args);
+  return cudaGetLastError();
+}
+
 static cudaError_t tc_launch(ta::Args& args, int n_tiles, cudaStream_t s) {
   static DeviceOnce configured;
   cudaError_t e = max_dynamic_smem_once(reinterpret_cast<const void*>(ta::attn_tc_kernel), ta::SMEM, configured);
@@ -713,12 +1183,10 @@ cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const Att
   // phase per blend: no pairs 1.68 ms, the idle SMs' 2 tiles per head 1.63, 4 tiles 1.47, 6 tiles
   // 1.71, every tile 1.91 (the extra CTAs' fixed cost and a second wave); seam repair (176 rows,
   // 48 units, every tile paired) 7.38 -> 7.20 ms per blend.
-  static int n_sm = 0;
-  if (n_sm == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0) n_sm = 148;
-  }
+  const int n_sm = sm_count_cached();
+  long long pairs = 0;
+  for (int r = 0; r < n_req; ++r) pairs += (tile_off[r + 1] - tile_off[r] + 1) / 2;
+  const bool two = use_pairs(tile_off[n_req], pairs, n_heads, n_kv_heads, n_sm);
   const long long units = static_cast<long long>(tile_off[n_req]) * n_kv_heads;
   const int n_paired = (n_req <= ta::MAXREQ && units < n_sm)
                            ? static_cast<int>(std::min<long long>(tile_off[n_req], (n_sm - units) / n_kv_heads + 2))
@@ -749,7 +1217,22 @@ cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const Att
     }
     a.req_base = r0;
     a.tiles = tiles + tile_off[r0];
-    cudaError_t e = tc_launch(a, tile_off[r1] - tile_off[r0], s);
+    cudaError_t e;
+    if (two) {
+      int np = 0;
+      for (int r = r0; r <= r0 + ta::MAXREQ - 1; ++r) {
+        const int rr = std::min(r, r1);  // entries past the group repeat its end
+        a.tile_off[r - r0] = tile_off[rr] - tile_off[r0];
+        a.pair_off[r - r0] = np;
+        if (r < r1) np += (tile_off[r + 1] - tile_off[r] + 1) / 2;
+      }
+      a.tile_off[ta::MAXREQ] = tile_off[r1] - tile_off[r0];
+      a.pair_off[ta::MAXREQ] = np;
+      a.n_pairs = np;
+      e = tc2_launch(a, s);
+    } else {
+      e = tc_launch(a, tile_off[r1] - tile_off[r0], s);
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -806,7 +1289,12 @@ cudaError_t launch_attention_direct(const void* q, const int32_t* q_pos, int m, 
     a.out = static_cast<bf16*>(out);
     a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(head_dim));
     a.status = nullptr;
-    return tc_launch(a, (m + a.QT - 1) / a.QT, s);
+    const int n_tiles = (m + a.QT - 1) / a.QT;
+    if (use_pairs(n_tiles, (n_tiles + 1) / 2, n_heads, n_kv_heads, sm_count_cached())) {
+      a.n_pairs = (n_tiles + 1) / 2;
+      return tc2_launch(a, s);
+    }
+    return tc_launch(a, n_tiles, s);
   }
   AttnArgsF32 a{};
   a.q = static_cast<const float*>(q);

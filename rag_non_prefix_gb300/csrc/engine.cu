@@ -1337,6 +1337,12 @@ cb_status cb_set_launch_overlap(int enabled) {
   return CB_OK;
 }
 
+cb_status cb_attention_set_tiles(int tiles) {
+  if (tiles < 0 || tiles > 2) return fail(nullptr, CB_ERR_INVALID_ARG, "tiles must be 0, 1 or 2");
+  attention_set_tiles(tiles);
+  return CB_OK;
+}
+
 cb_status cb_gemm_set_orientation(int orientation) {
   const bool tile = orientation >= 16 && orientation <= 256 && orientation % 16 == 0;
   if ((orientation < 0 || orientation > 2) && !tile)

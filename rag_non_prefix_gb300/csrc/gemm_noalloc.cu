@@ -142,7 +142,8 @@ extern "C" cb_status cb_gemm_get_status(void* stream, int timeout_ms) {
   const auto t0 = std::chrono::steady_clock::now();
   while (e == cudaSuccess) {  // bounded wait for the stream's earlier work
     e = cudaEventQuery(ev);
-    if (e != cudaErrorNotReady) break;
+    if (e != cudaErrorNotReady) break;  // done (cudaSuccess) or a real error
+    e = cudaSuccess;
     if (timeout_ms >= 0 &&
         std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(timeout_ms)) {
       cudaEventDestroy(ev);
@@ -165,5 +166,6 @@ extern "C" cb_status cb_gemm_get_status(void* stream, int timeout_ms) {
              static_cast<int>(v), (v & ST_WAIT_TIMEOUT) ? "a stream-K wait gave up" : "index out of range");
     return CB_ERR_DEVICE;
   }
+  g_noalloc_msg[0] = '\0';
   return CB_OK;
 }

@@ -198,6 +198,7 @@ int attention_tile_rows(int n_heads, int n_kv_heads, cb_dtype dt);
 // ATTN_SPLIT_UNITS * 2 * 128 * 128 floats, part_ml as many * 128 (max, sum) pairs, part_cnt
 // ATTN_SPLIT_UNITS counters that must be zero before the first launch (each launch leaves them zero).
 constexpr int ATTN_SPLIT_UNITS = 256;
+void attention_set_tiles(int tiles);  // 0 by the launch's size, 1 or 2 query tiles per CTA
 constexpr int ATTN_SPLIT_MIN_BLOCKS = 12;
 cudaError_t launch_attention_bf16(const void* q, const int32_t* s_pos, const AttnTile* tiles, const int* tile_off,
                                   const CUtensorMap* kmaps, const CUtensorMap* vmaps, const int* n_kv,

@@ -108,3 +108,56 @@ def forced_from_oracle(res, n_cached: int, n_layers: int, ratios):
             S = res["sets"][i]
             out[i] = [[int(x) for x in S if x < n_cached]]
     return out
+
+
+def bf16_operand_full_prefill(cfg, W, ids: np.ndarray) -> torch.Tensor:
+    """A plain-PyTorch full prefill on the GPU that rounds to bf16 exactly the operands a bf16
+    tensor-core path must round, and computes everything else in fp32 (TF32 off): the
+    normalised rows x entering each projection, q / k / v after RoPE (the cache's K and V),
+    the softmax probabilities P entering P.V (the row sum taken before rounding), the
+    attention output entering the output projection, and the SwiGLU output entering the down
+    projection; the residual stream stays fp32.
+
+    It shares no code with the library or the oracle (library routines: matmul, rms_norm,
+    silu).  Its distance to the oracle's fp64 prefill is the rounding floor of bf16 operands
+    for the model's depth, against which the library's own error is judged.  Returns the
+    hidden states [N, d] (fp32)."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        bf = lambda t: t.to(torch.bfloat16).to(torch.float32)  # noqa: E731
+        dev = W["embed"].device
+        t_ids = torch.from_numpy(np.asarray(ids, dtype=np.int64)).to(dev)
+        N, d, H, Hkv, dh = len(ids), cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+        G, half = H // Hkv, dh // 2
+        h = W["embed"][t_ids].float()
+        inv = torch.pow(torch.tensor(float(cfg.rope_theta), dtype=torch.float64),
+                        -2.0 * torch.arange(half, dtype=torch.float64) / dh)
+        ang = torch.arange(N, dtype=torch.float64)[:, None] * inv[None, :]
+        cos, sin = ang.cos().float().to(dev)[:, None, :], ang.sin().float().to(dev)[:, None, :]
+
+        def rope(x):
+            a, b = x[..., :half], x[..., half:]
+            return torch.cat([a * cos - b * sin, b * cos + a * sin], dim=-1)
+
+        later = torch.ones(N, N, dtype=torch.bool, device=dev).triu(1)  # key after query
+        scale = 1.0 / float(np.sqrt(dh))
+        for lw in W["layers"][: cfg.n_layers]:
+            x = bf(torch.nn.functional.rms_norm(h, (d,), eps=cfg.rms_eps))
+            q = bf(rope((x @ lw["wq"].float().T).view(N, H, dh)))
+            k = bf(rope((x @ lw["wk"].float().T).view(N, Hkv, dh)))
+            v = bf((x @ lw["wv"].float().T).view(N, Hkv, dh))
+            att = torch.empty(N, H, dh, device=dev)
+            for g in range(Hkv):
+                s = torch.einsum("ngd,md->gnm", q[:, g * G:(g + 1) * G, :], k[:, g, :]) * scale
+                s = s.masked_fill(later, float("-inf"))
+                p = torch.exp(s - s.amax(dim=-1, keepdim=True))
+                o = (bf(p) @ v[:, g, :]) / p.sum(dim=-1, keepdim=True)
+                att[:, g * G:(g + 1) * G, :] = o.transpose(0, 1)
+            h = h + bf(att.reshape(N, H * dh)) @ lw["wo"].float().T
+            x2 = bf(torch.nn.functional.rms_norm(h, (d,), eps=cfg.rms_eps))
+            act = bf(torch.nn.functional.silu(x2 @ lw["wgate"].float().T) * (x2 @ lw["wup"].float().T))
+            h = h + act @ lw["wdown"].float().T
+        return h
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev

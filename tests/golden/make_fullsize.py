@@ -22,6 +22,11 @@ for the four-request batch), the 16 largest LM-head logits at the last position 
 token ids (the first token is the first id), and the oracle's wall time.
 
     python tests/golden/make_fullsize.py mistral7b llama7b yi34b llama70b
+    python tests/golden/make_fullsize.py --full-prefill mistral7b
+
+The second form stores the oracle's plain full prefill of the Mistral-7B-shaped prompt
+(same model, all 32 layers), against which the GPU's own full prefill and a plain-PyTorch
+bf16 witness are compared to measure the rounding floor of bf16 operands at full depth.
 """
 from __future__ import annotations
 
@@ -111,6 +116,40 @@ def make(name: str) -> str:
     return path_of(name)
 
 
+def full_path_of(name: str) -> str:
+    return os.path.join(HERE, f"fullsize_{name}_full_prefill.npz")
+
+
+def make_full(name: str, n_rows: int = 32) -> str:
+    """The oracle's plain full prefill of the workload's first prompt (the full-recompute
+    baseline): hidden rows of the last ``n_rows`` // 2 tokens and of as many earlier tokens
+    drawn with a fixed seed, the top logits at the last token, and the wall time."""
+    spec = spec_of(name)
+    cfg = spec.cfg
+    storage = "bf16" if cfg.dtype == "bf16" else "f32"
+    W = hz.HostWeights(cfg, spec.seed)
+    ids = np.concatenate([s.ids for s in spec.requests[0]])
+    n = len(ids)
+    t = time.perf_counter()
+    res = orc.full_prefill(cfg, W, ids, storage)
+    secs = time.perf_counter() - t
+    tail = np.arange(n - n_rows // 2, n)
+    early = np.sort(np.random.default_rng(7 * spec.seed).choice(n - n_rows // 2, n_rows // 2, replace=False))
+    rows = np.concatenate([early, tail]).astype(np.int64)
+    logits = orc.lm_logits(cfg, W, res["hidden"][-1])
+    top = np.lexsort((np.arange(len(logits)), -logits))[:TOP_LOGITS]
+    np.savez_compressed(full_path_of(name), n_layers=np.int32(cfg.n_layers), rows=rows.astype(np.int32),
+                        hidden=res["hidden"][rows].astype(np.float32), top_ids=top.astype(np.int32),
+                        top_logits=logits[top], full_prefill_s=np.float64(secs))
+    print(f"{name}: full prefill of {n} tokens in {secs:.0f} s, first token {res['first_token']}", flush=True)
+    return full_path_of(name)
+
+
 if __name__ == "__main__":
-    for n in sys.argv[1:] or list(CASES):
-        print("wrote", make(n), flush=True)
+    args = sys.argv[1:] or list(CASES)
+    if args[0] == "--full-prefill":
+        for n in args[1:]:
+            print("wrote", make_full(n), flush=True)
+    else:
+        for n in args:
+            print("wrote", make(n), flush=True)

@@ -99,6 +99,16 @@ def test_bf16_blend_forced_selection_matches_oracle(small_bf16, orientation):
         cb.cb_gemm_set_orientation(0)
 
 
+@pytest.mark.parametrize("tiles", [1, 2], ids=["one-tile", "two-tiles"])
+def test_bf16_blend_attention_kernels_match_oracle(small_bf16, tiles):
+    """Numerics with each attention kernel forced (one or two query tiles per CTA)."""
+    cb.cb_attention_set_tiles(tiles)
+    try:
+        _forced_bf16(small_bf16)
+    finally:
+        cb.cb_attention_set_tiles(0)
+
+
 def _forced_bf16(small_bf16):
     spec, g, o = small_bf16
     cfg = spec.cfg

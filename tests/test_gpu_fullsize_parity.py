@@ -16,6 +16,13 @@ The expected values are the oracle's, written once by ``tests/golden/make_fullsi
   the first token is the oracle's, or a token whose oracle logit is within 2 % of the top
   logit when the oracle's own margin is that small;
 * free-running selection: every checked set overlaps the oracle's by >= 99 %.
+
+At full depth (32 layers) the bf16 rounding of the tensor-core operands alone moves the
+hidden rows by ~3 % from the fp64 oracle.  There the GPU's own full prefill and a plain-
+PyTorch witness that rounds the same operands to bf16 (and computes the rest in fp32) are
+both compared with the oracle's full prefill first; the blend's bound at that depth is then
+max(2e-2, 1.25 x the witness's distance): the library may not lose more than a quarter
+above the rounding floor of its operand type.
 """
 from __future__ import annotations
 
@@ -27,7 +34,8 @@ import numpy as np
 import pytest
 import torch
 
-from tests._gpu import GpuWorkload, max_rel_err, to_np
+import harness.device as hd
+from tests._gpu import GpuWorkload, bf16_operand_full_prefill, max_rel_err, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -72,16 +80,56 @@ def _sets(req, n_layers):
     return {i: sel[i, : cnt[i]] for i in range(n_layers)}
 
 
-# both modes of one workload run back to back, so each model is built once
-RUNS = [(name, r, mode) for name, r in CASES for mode in ("forced", "free")]
+FLOOR_MARGIN = 1.25
+FLOOR = {}  # workload -> the bf16-operand witness's distance to the oracle's full prefill
+
+
+def tolerance(name: str) -> float:
+    return max(TOL, FLOOR_MARGIN * FLOOR[name]) if name in FLOOR else TOL
+
+
+# every mode of one workload runs back to back, so each model is built once; the full
+# prefill (where the oracle stored one) runs first and measures the rounding floor
+RUNS = []
+for _name in MF.CASES:
+    if os.path.exists(MF.full_path_of(_name)):
+        RUNS.append((_name, 0.0, "full"))
+    RUNS += [(_name, _r, _m) for _r in MF.CASES[_name]["ratios"] for _m in ("forced", "free")]
 
 
 @pytest.mark.parametrize("name,r,mode", RUNS, ids=[f"{n}-r{int(r * 100)}-{m}" for n, r, m in RUNS])
 def test_fullsize_blend_matches_oracle(name, r, mode):
-    if mode == "forced":
+    if mode == "full":
+        _full(name)
+    elif mode == "forced":
         _forced(name, r)
     else:
         _free(name, r)
+
+
+def _full(name):
+    """The GPU's full prefill and the bf16-operand witness against the oracle's full prefill."""
+    with np.load(MF.full_path_of(name)) as d:
+        gold = {k: d[k] for k in d.files}
+    g, _ = gpu(name)
+    spec, cfg = g.spec, g.cfg
+    assert int(gold["n_layers"]) == cfg.n_layers
+    ids = np.concatenate([s.ids for s in spec.requests[0]])
+    rows, ref = gold["rows"], gold["hidden"].astype(np.float64)
+    out = g.eng.full_prefill(hd.ids_tensor(ids))
+    wit = bf16_operand_full_prefill(cfg, g.W, ids)
+    torch.cuda.synchronize()
+    err_ours = max_rel_err(to_np(out["hidden"])[rows], ref)
+    err_wit = max_rel_err(to_np(wit)[rows], ref)
+    FLOOR[name] = err_wit
+    print(f"{name} full prefill: library {err_ours:.4f}, bf16-operand witness {err_wit:.4f} "
+          f"(max over rows of ||g - o||_inf / ||o||_inf)")
+    assert err_ours <= max(TOL, FLOOR_MARGIN * err_wit), (err_ours, err_wit)
+    tok = int(out["first_token"].item())
+    ids_top, logits = gold["top_ids"], gold["top_logits"]
+    if tok != int(ids_top[0]):
+        assert tok in set(int(x) for x in ids_top), (tok, ids_top[:4])
+        assert logits[list(ids_top).index(tok)] >= logits[0] - TOL * abs(logits[0]), tok
 
 
 def _forced(name, r):
@@ -106,7 +154,7 @@ def _forced(name, r):
         rows = gold[f"{tag}_q{q}_rows"]
         got = to_np(req["hidden"])[rows]
         err = max_rel_err(got, gold[f"{tag}_q{q}_hidden"].astype(np.float64))
-        assert err < TOL, (q, err)
+        assert err < tolerance(name), (q, err, tolerance(name))
         tok = int(req["first_token"].item())
         ids, logits = gold[f"{tag}_q{q}_top_ids"], gold[f"{tag}_q{q}_top_logits"]
         if tok != int(ids[0]):

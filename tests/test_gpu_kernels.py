@@ -271,16 +271,23 @@ def test_gemm_f32_all_epilogues(M, N, K):
 
 
 # ----------------------------------------------------------------------------- attention
+@pytest.mark.parametrize("tiles", [1, 2], ids=["one-tile", "two-tiles"])
 @pytest.mark.parametrize("H,Hkv,N,m", [(8, 2, 300, 70), (4, 4, 200, 130), (32, 8, 3200, 535), (56, 8, 700, 50),
-                                       (64, 8, 260, 33), (8, 8, 64, 64)])
-def test_attention_bf16_matches_oracle(H, Hkv, N, m):
+                                       (64, 8, 260, 33), (8, 8, 64, 64), (56, 8, 8320, 1357), (32, 8, 1000, 96)])
+def test_attention_bf16_matches_oracle(H, Hkv, N, m, tiles):
+    """Both kernels: one query tile per CTA, and two tiles of one KV head per CTA (odd and
+    even tile counts, tiles of different lengths, the Yi-34B shape at its kept-layer size)."""
     rng = np.random.default_rng(H * N + m)
     pos = np.sort(rng.choice(N, m, replace=False)).astype(np.int32)
     q = _bf16(rng.standard_normal((m, H, 128)))
     k = _bf16(rng.standard_normal((N, Hkv, 128)))
     v = _bf16(rng.standard_normal((N, Hkv, 128)))
-    out = cb.cb_attention(q, torch.from_numpy(pos).cuda(), k, v)
-    torch.cuda.synchronize()
+    cb.cb_attention_set_tiles(tiles)
+    try:
+        out = cb.cb_attention(q, torch.from_numpy(pos).cuda(), k, v)
+        torch.cuda.synchronize()
+    finally:
+        cb.cb_attention_set_tiles(0)
     sample = np.arange(m) if m <= 80 else np.unique(np.concatenate([np.arange(8), rng.choice(m, 40), [m - 1]]))
     ref = orc.causal_attention(to_np(q)[sample], pos[sample], to_np(k), to_np(v))
     got = to_np(out)[sample]
