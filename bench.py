@@ -349,7 +349,7 @@ class Workload:
         fn()
         self.torch.cuda.synchronize()
         phases = self.eng.get_profile()
-        layers = self.eng.get_layer_profile() if level >= 2 else None
+        layers = self.eng.get_layer_profile() if level & 2 else None
         self.eng.set_profiling(0)
         return phases, layers
 
@@ -564,9 +564,11 @@ def measure_staging(wl, ratios, schedule, blend_staged_ms, full_ms, steps, peaks
     total_bytes = sum(2 * wl.host_store[s.chunk][1].numel() * wl.host_store[s.chunk][1].element_size()
                       for r in wl.req_idx for s in wl.spec.requests[r] if s.chunk >= 0)
     t_load = total_bytes / (h2d_gbs * 1e9) * 1e3
-    # per-layer events of one staged blend: staging copies (copy stream), compute (after
-    # the wait for the staged KV); begin and finish are outside the layers
-    ph_s, lay = wl.profiled(lambda: wl.blend_step(ratios), level=2)
+    # per-layer events of one staged blend (no phase events in that run): staging copies
+    # (copy stream), compute (after the wait for the staged KV); begin and finish, which are
+    # outside the layers, from a run with phase events
+    _, lay = wl.profiled(lambda: wl.blend_step(ratios), level=2)
+    ph_s, _ = wl.profiled(lambda: wl.blend_step(ratios), level=1)
     load_l, comp_l = lay["load_ms"], lay["compute_ms"]
     edge = ph_s.get("begin", {"ms": 0.0})["ms"] + ph_s.get("finish", {"ms": 0.0})["ms"]
     sum_max = sum(max(a, b) for a, b in zip(load_l, comp_l)) + edge

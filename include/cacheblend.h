@@ -493,11 +493,12 @@ typedef struct {
   int launches[CB_N_PHASES]; /* kernels launched per phase */
   int calls[CB_N_PHASES];    /* timed phase instances */
 } cb_profile;
-/* enable: 0 off, 1 per-phase events, 2 per-phase events and per-layer events (below). */
+/* enable: 0 off, 1 per-phase events, 2 per-layer events only (below), 3 both.  Events cost
+ * a few microseconds each, so per-layer times are taken without the phase events. */
 cb_status cb_set_profiling(cb_ctx* ctx, int enable);
 /* Waits for the recorded events, fills *out and resets the counters. */
 cb_status cb_get_profile(cb_ctx* ctx, cb_profile* out);
-/* Per-layer device times of the batches run at profiling level 2 since the last call,
+/* Per-layer device times of the batches run at profiling level 2 or 3 since the last call,
  * for the overlap of loading and recompute ([P1] パイプライン化の設計: per layer
  * T ~ max(T_load, T_recompute)).  load_ms_host[i]: the copy stream's staging of layer
  * i's host-resident chunk KV, from its first copy to its last (0 when nothing of layer i

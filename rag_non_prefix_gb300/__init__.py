@@ -562,7 +562,7 @@ class Engine:
         _check(self.lib.cb_get_status(self.ctx, _stream(stream), timeout_ms), self.ctx)
 
     def set_profiling(self, enable):
-        """0 / False off, 1 / True per-phase events, 2 per-phase and per-layer events."""
+        """0 / False off, 1 / True per-phase events, 2 per-layer events, 3 both."""
         _check(self.lib.cb_set_profiling(self.ctx, int(enable)), self.ctx)
 
     def get_layer_profile(self) -> Dict[str, List[float]]:

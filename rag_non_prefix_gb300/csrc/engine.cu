@@ -242,8 +242,8 @@ struct cb_ctx {
 
   Batch b;
 
-  // profiling: events around phases (level >= 1), around each layer's staging copies and
-  // compute (level 2), and launch counts (always)
+  // profiling: events around phases (bit 0 of the level), around each layer's staging copies
+  // and compute (bit 1), and launch counts (always)
   int prof = 0;
   std::vector<cudaEvent_t> ev_pool;
   struct Mark {
@@ -278,7 +278,7 @@ struct PhaseScope {
   cudaEvent_t a = nullptr;
   PhaseScope(cb_ctx* c, int ph, cudaStream_t st, int kernels) : ctx(c), phase(ph), s(st) {
     ctx->launches[ph] += kernels;
-    if (ctx->prof) {
+    if (ctx->prof & 1) {
       a = ctx->get_event();
       cudaEventRecord(a, s);
     }
@@ -802,7 +802,7 @@ cb_status fetch_impl(cb_ctx* ctx, int layer, cudaStream_t cs) {
       CB_CUDA(ctx, cudaStreamWaitEvent(cs, ctx->slot_ev[slot], 0));
     }
     uint8_t* dst = ctx->staging + static_cast<size_t>(slot) * b.slot_bytes;
-    if (ctx->prof >= 2 && !load_a) {
+    if ((ctx->prof & 2) && !load_a) {
       load_a = ctx->get_event();
       CB_CUDA(ctx, cudaEventRecord(load_a, cs));
     }
@@ -816,7 +816,7 @@ cb_status fetch_impl(cb_ctx* ctx, int layer, cudaStream_t cs) {
       const size_t bytes = static_cast<size_t>(sg.n) * kvw * es;
       const size_t so = static_cast<size_t>(layer) * bytes;
       const size_t dof = (static_cast<size_t>(layer) * rh.layer_stride + static_cast<size_t>(sg.off) * kvw) * es;
-      if (ctx->prof >= 2 && !load_a) {
+      if ((ctx->prof & 2) && !load_a) {
         load_a = ctx->get_event();
         CB_CUDA(ctx, cudaEventRecord(load_a, cs));
       }
@@ -835,7 +835,7 @@ cb_status fetch_impl(cb_ctx* ctx, int layer, cudaStream_t cs) {
   return CB_OK;
 }
 
-// Per-layer profiling (level 2): events around one layer's work on the compute stream,
+// Per-layer profiling (bit 1 of the level): events around one layer's work on the compute stream,
 // from after its wait for staged KV to its last kernel.
 struct LayerScope {
   cb_ctx* ctx;
@@ -843,7 +843,7 @@ struct LayerScope {
   cudaStream_t s;
   cudaEvent_t a = nullptr;
   LayerScope(cb_ctx* c, int i, cudaStream_t st) : ctx(c), layer(i), s(st) {
-    if (ctx->prof >= 2) {
+    if (ctx->prof & 2) {
       a = ctx->get_event();
       cudaEventRecord(a, s);
     }
@@ -1645,7 +1645,7 @@ cb_status cb_get_status(cb_ctx* ctx, void* stream, int timeout_ms) {
 
 cb_status cb_set_profiling(cb_ctx* ctx, int enable) {
   if (!ctx) return fail(ctx, CB_ERR_INVALID_ARG, "null context");
-  ctx->prof = enable <= 0 ? 0 : (enable >= 2 ? 2 : 1);
+  ctx->prof = enable < 0 ? 0 : (enable > 3 ? 3 : enable);
   return CB_OK;
 }
 

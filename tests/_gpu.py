@@ -110,7 +110,7 @@ def forced_from_oracle(res, n_cached: int, n_layers: int, ratios):
     return out
 
 
-def bf16_operand_full_prefill(cfg, W, ids: np.ndarray) -> torch.Tensor:
+def bf16_operand_full_prefill(cfg, W, ids: np.ndarray, rounding: bool = True) -> torch.Tensor:
     """A plain-PyTorch full prefill on the GPU that rounds to bf16 exactly the operands a bf16
     tensor-core path must round, and computes everything else in fp32 (TF32 off): the
     normalised rows x entering each projection, q / k / v after RoPE (the cache's K and V),
@@ -120,12 +120,13 @@ def bf16_operand_full_prefill(cfg, W, ids: np.ndarray) -> torch.Tensor:
 
     It shares no code with the library or the oracle (library routines: matmul, rms_norm,
     silu).  Its distance to the oracle's fp64 prefill is the rounding floor of bf16 operands
-    for the model's depth, against which the library's own error is judged.  Returns the
-    hidden states [N, d] (fp32)."""
+    for the model's depth, against which the library's own error is judged.  rounding=False
+    gives the same prefill with no operand rounded (fp32 throughout).  Returns the hidden
+    states [N, d] (fp32)."""
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = False
     try:
-        bf = lambda t: t.to(torch.bfloat16).to(torch.float32)  # noqa: E731
+        bf = (lambda t: t.to(torch.bfloat16).to(torch.float32)) if rounding else (lambda t: t)  # noqa: E731
         dev = W["embed"].device
         t_ids = torch.from_numpy(np.asarray(ids, dtype=np.int64)).to(dev)
         N, d, H, Hkv, dh = len(ids), cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim

@@ -17,12 +17,14 @@ The expected values are the oracle's, written once by ``tests/golden/make_fullsi
   logit when the oracle's own margin is that small;
 * free-running selection: every checked set overlaps the oracle's by >= 99 %.
 
-At full depth (32 layers) the bf16 rounding of the tensor-core operands alone moves the
-hidden rows by ~3 % from the fp64 oracle.  There the GPU's own full prefill and a plain-
-PyTorch witness that rounds the same operands to bf16 (and computes the rest in fp32) are
-both compared with the oracle's full prefill first; the blend's bound at that depth is then
-max(2e-2, 1.25 x the witness's distance): the library may not lose more than a quarter
-above the rounding floor of its operand type.
+At these widths the bf16 rounding of the tensor-core operands alone moves the hidden rows
+by 2-4 % from exact arithmetic (random-init weights, six layers or more).  So each workload
+first measures that floor: a plain-PyTorch witness that rounds to bf16 exactly the operands
+a bf16 tensor-core path must round (and computes the rest in fp32) against the same prefill
+with nothing rounded; where the oracle stored its own full prefill, the GPU's full prefill
+and the unrounded witness are also held to it.  The blend's bound is then
+max(2e-2, 1.25 x that floor): the library may lose no more than a quarter above the
+rounding floor of its operand type.
 """
 from __future__ import annotations
 
@@ -89,11 +91,10 @@ def tolerance(name: str) -> float:
 
 
 # every mode of one workload runs back to back, so each model is built once; the full
-# prefill (where the oracle stored one) runs first and measures the rounding floor
+# prefill runs first and measures the rounding floor
 RUNS = []
 for _name in MF.CASES:
-    if os.path.exists(MF.full_path_of(_name)):
-        RUNS.append((_name, 0.0, "full"))
+    RUNS.append((_name, 0.0, "full"))
     RUNS += [(_name, _r, _m) for _r in MF.CASES[_name]["ratios"] for _m in ("forced", "free")]
 
 
@@ -108,28 +109,38 @@ def test_fullsize_blend_matches_oracle(name, r, mode):
 
 
 def _full(name):
-    """The GPU's full prefill and the bf16-operand witness against the oracle's full prefill."""
-    with np.load(MF.full_path_of(name)) as d:
-        gold = {k: d[k] for k in d.files}
+    """The rounding floor of bf16 operands at this depth and width, and the GPU's full prefill
+    against the oracle's (where it stored one)."""
     g, _ = gpu(name)
     spec, cfg = g.spec, g.cfg
-    assert int(gold["n_layers"]) == cfg.n_layers
     ids = np.concatenate([s.ids for s in spec.requests[0]])
-    rows, ref = gold["rows"], gold["hidden"].astype(np.float64)
+    n = len(ids)
+    rows = np.unique(np.concatenate([np.linspace(0, n - 1, 24).astype(np.int64), np.arange(n - 8, n)]))
+    w16 = to_np(bf16_operand_full_prefill(cfg, g.W, ids))
+    w32 = to_np(bf16_operand_full_prefill(cfg, g.W, ids, rounding=False))
+    FLOOR[name] = max_rel_err(w16[rows], w32[rows])
     out = g.eng.full_prefill(hd.ids_tensor(ids))
-    wit = bf16_operand_full_prefill(cfg, g.W, ids)
+    ours = to_np(out["hidden"])
     torch.cuda.synchronize()
-    err_ours = max_rel_err(to_np(out["hidden"])[rows], ref)
-    err_wit = max_rel_err(to_np(wit)[rows], ref)
-    FLOOR[name] = err_wit
-    print(f"{name} full prefill: library {err_ours:.4f}, bf16-operand witness {err_wit:.4f} "
-          f"(max over rows of ||g - o||_inf / ||o||_inf)")
-    assert err_ours <= max(TOL, FLOOR_MARGIN * err_wit), (err_ours, err_wit)
-    tok = int(out["first_token"].item())
-    ids_top, logits = gold["top_ids"], gold["top_logits"]
-    if tok != int(ids_top[0]):
-        assert tok in set(int(x) for x in ids_top), (tok, ids_top[:4])
-        assert logits[list(ids_top).index(tok)] >= logits[0] - TOL * abs(logits[0]), tok
+    err_fp32 = max_rel_err(ours[rows], w32[rows])
+    print(f"{name} full prefill ({cfg.n_layers} layers): bf16-operand floor {FLOOR[name]:.4f}, "
+          f"library vs unrounded {err_fp32:.4f} (max over rows of ||g - o||_inf / ||o||_inf)")
+    assert err_fp32 <= tolerance(name), (err_fp32, FLOOR[name])
+    if os.path.exists(MF.full_path_of(name)):
+        with np.load(MF.full_path_of(name)) as d:
+            gold = {k: d[k] for k in d.files}
+        assert int(gold["n_layers"]) == cfg.n_layers
+        r_o, ref = gold["rows"], gold["hidden"].astype(np.float64)
+        err_ours = max_rel_err(ours[r_o], ref)
+        err_w32 = max_rel_err(w32[r_o], ref)
+        print(f"  vs the oracle's full prefill: library {err_ours:.4f}, unrounded witness {err_w32:.2e}")
+        assert err_w32 < 1e-3, err_w32  # the fp32 witness is the oracle's prefill to fp32 rounding
+        assert err_ours <= tolerance(name), (err_ours, FLOOR[name])
+        tok = int(out["first_token"].item())
+        ids_top, logits = gold["top_ids"], gold["top_logits"]
+        if tok != int(ids_top[0]):
+            assert tok in set(int(x) for x in ids_top), (tok, ids_top[:4])
+            assert logits[list(ids_top).index(tok)] >= logits[0] - TOL * abs(logits[0]), tok
 
 
 def _forced(name, r):
