@@ -368,17 +368,20 @@ def _phase_ms(phases):
 GEMM_PHASES = ("qkv", "oproj", "gateup", "down")
 
 
-def measure(wl, ratio, schedule, steps, warmup, peaks, sample_clocks=False):
+def measure(wl, ratio, schedule, steps, warmup, peaks, sample_clocks=False, full_from=None):
     """Blend and full prefill of one workload at one ratio: timed steps (CUDA events on the
     launching stream, 512 MiB written between steps), one profiled run of each, and the
     roofline fractions: the projection GEMMs and the attention against the sustained bf16
-    peak, and the whole prefill as T_roof / TTFT."""
+    peak, and the whole prefill as T_roof / TTFT.  ``full_from``: an earlier measurement of
+    the same workload whose full-prefill timing and profile are reused (the full prefill does
+    not depend on the ratio)."""
     cb = wl.cb
     cfg = wl.cfg
     ratios = cb.ratio_schedule(cfg.n_layers, ratio, schedule)
     for _ in range(warmup):
         wl.blend_step(ratios)
-        wl.full_step()
+        if full_from is None:
+            wl.full_step()
     wl.eng.get_status()
     wl.eng.get_profile()  # reset the launch counters
     sampler = None
@@ -389,7 +392,7 @@ def measure(wl, ratio, schedule, steps, warmup, peaks, sample_clocks=False):
     blend_ms = wl.timed(lambda: wl.blend_step(ratios), steps, "blend_timed")
     wl.barrier()
     counts = wl.eng.get_profile()
-    full_ms = wl.timed(wl.full_step, steps, "full_timed")
+    full_ms = wl.timed(wl.full_step, steps, "full_timed") if full_from is None else full_from["full_runs"]
     wl.barrier()
     clocks = sampler.stop() if sampler else None
     wl.eng.get_status()
@@ -397,7 +400,7 @@ def measure(wl, ratio, schedule, steps, warmup, peaks, sample_clocks=False):
     # profiled full prefill
     sel_reqs = wl.make_requests(want_sel=True)
     ph_b, _ = wl.profiled(lambda: wl.blend_step(ratios, reqs=sel_reqs))
-    ph_f, _ = wl.profiled(wl.full_step)
+    ph_f = wl.profiled(wl.full_step)[0] if full_from is None else full_from["ph_full_raw"]
     L = cfg.n_layers
     pairs_b = [0.0] * L
     for req in sel_reqs:
@@ -445,6 +448,7 @@ def measure(wl, ratio, schedule, steps, warmup, peaks, sample_clocks=False):
         "gemm_bytes_blend": sum(gemm_layer_bytes(cfg, R, S) for R, S in zip(rows_R, rows_S)),
         "launches_per_step": sum(v["launches"] for v in counts.values()) / max(1, steps),
         "clocks": clocks, "rows_R": rows_R, "rows_S": rows_S, "pairs_blend": pairs_b, "checks": checks,
+        "ph_full_raw": ph_f,
     }
 
 
@@ -762,12 +766,16 @@ def run_ours(args, rank, world):
                 continue
             w2 = Workload(name, dev, world, rank)
             s2 = w2.spec.schedule if schedule is None else schedule
+            first = None
             for r in rs:
-                m2 = measure(w2, r, s2, args.config_steps, 3, peaks, sample_clocks=True)
+                m2 = measure(w2, r, s2, args.config_steps, 3, peaks, sample_clocks=True, full_from=first)
+                first = first or m2
                 e = {"workload": f"{name}: {w2.cfg.n_layers}L d{w2.cfg.d_model} H{w2.cfg.n_heads}/{w2.cfg.n_kv_heads} "
                                  f"ffn{w2.cfg.ffn_dim}; {len(w2.req_idx)} request(s) x {w2.n_tok[0]} tokens"
                                  + ("; chunk KV staged from pinned host memory" if w2.staged else ""),
                      "steps": args.config_steps, **summary(m2)}
+                if first is not m2:
+                    e["full_prefill_note"] = "full prefill timed once per workload (at the first ratio)"
                 if w2.staged:
                     e["staging"] = measure_staging(w2, m2["ratios"], s2, m2["blend_ms"], m2["full_ms"],
                                                    args.config_steps, peaks, codec=args.codec)
