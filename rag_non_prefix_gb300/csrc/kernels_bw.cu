@@ -1,6 +1,8 @@
 // Bandwidth-bound kernels of the blended prefill: embedding gather, RoPE re-rotation
 // of cached keys, RMSNorm, RoPE of fresh q/k, KV deviation, compaction + KV scatter,
 // LM head and argmax.  All use 16-byte vector accesses; rows are independent.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -120,7 +122,12 @@ cudaError_t launch_rerotate(const RerotSeg* segs, int n_segs, int max_rows, int 
   if (n_segs <= 0 || max_rows <= 0) return cudaSuccess;
   const int kvw = n_kv_heads * head_dim;
   const long long work = static_cast<long long>(max_rows) * (kvw / 16 + kvw / 8);
-  const int gx = grid_for(work, 256, 1 << 16);
+  // About 32 CTAs per SM over all segments (the stand-alone launch's size), each striding
+  // over its segment: one CTA per 256 items of every segment made hundreds of thousands of
+  // short CTAs for the 960 chunk-layers of a 60-layer batch (measured on GB300: 4.03 GB in
+  // 0.90 ms, 66 % of the copy bandwidth, against 92 % for the stand-alone launch).
+  const int per_seg = std::max(1, (152 * 32 + n_segs - 1) / n_segs);
+  const int gx = grid_for(work, 256, per_seg);
   dim3 grid(gx, n_segs);
   if (dt == CB_BF16)
     launch_chain(rerotate_batched_kernel<bf16>, dim3(grid), dim3(256), 0, s, segs, n_kv_heads, head_dim, rope_table, max_pos, status);

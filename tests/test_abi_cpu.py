@@ -103,6 +103,15 @@ def test_host_schedule_rejects_bad_ratios(lib):
         cb.ratio_schedule(8, 0.3, "linear")
 
 
+def test_tuning_hooks_reject_bad_values(lib):
+    for bad in (-1, 3, 7):
+        assert lib.cb_attention_set_tiles(bad) == 1  # CB_ERR_INVALID_ARG
+    for ok in (0, 1, 2, 0):
+        assert lib.cb_attention_set_tiles(ok) == 0
+    assert lib.cb_gemm_set_orientation(3) == 1 and lib.cb_gemm_set_orientation(0) == 0
+    assert lib.cb_k_for_ratio(0.0, 100) == 0 and lib.cb_k_for_ratio(0.15, 3136) == 471
+
+
 def test_library_fails_loudly_when_missing(tmp_path):
     with pytest.raises(RuntimeError):
         cb._lib = None

@@ -251,6 +251,35 @@ def test_host_staged_chunks_are_bit_identical(small_bf16):
     assert torch.equal(resident["sel"], staged["sel"])
 
 
+def test_layer_profile_of_a_staged_blend(small_bf16):
+    """Per-layer events (profiling level 2): every layer of a host-staged blend has staging
+    copies on the copy stream and compute on the compute stream; a resident blend stages
+    nothing; phase events alone (level 1) record no layer; the profile drains on reading."""
+    spec, g, o = small_bf16
+    cfg = spec.cfg
+    ratios = orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)
+    gh = GpuWorkload(spec, on_host=True)
+    cs = torch.cuda.Stream()
+    for level, staged in ((2, True), (2, False), (1, True)):
+        eng = gh if staged else g
+        eng.eng.get_layer_profile()
+        eng.eng.set_profiling(level)
+        out = eng.blend(ratios, copy_stream=cs if staged else None)[0]
+        lay = eng.eng.get_layer_profile()
+        eng.eng.set_profiling(0)
+        eng.eng.get_profile()
+        if level == 1:
+            assert max(lay["load_ms"]) == 0 and max(lay["compute_ms"]) == 0
+            continue
+        assert all(x > 0 for x in lay["compute_ms"]), lay
+        if staged:
+            assert all(x > 0 for x in lay["load_ms"]), lay
+        else:
+            assert max(lay["load_ms"]) == 0
+        assert eng.eng.get_layer_profile()["compute_ms"] == [0.0] * cfg.n_layers
+        assert out["sel_count"].cpu().tolist() == g.eng.plan_counts(0)
+
+
 def test_per_layer_api_matches_whole_call(small_bf16):
     spec, g, o = small_bf16
     cfg = spec.cfg
