@@ -608,6 +608,19 @@ constexpr int SMEM2 = OFF_BAR2 + 3072;          // the 227 KiB limit, as attn_tc
 constexpr uint32_t S_COL = 0;                   // S of tile t at column 128 t
 constexpr uint32_t O_COL2 = 256;                // O of tile t at column 256 + 128 t
 
+// Non-blocking test of an mbarrier phase (the MMA issuer polls several barriers in turn).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Position of K_j / V_j in the load order K0, K1, V0, K2, V1, ..., K_{n-1}, V_{n-2}, V_{n-1}
 __device__ __forceinline__ int k_item(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int v_item(int j, int nb) { return min(2 * j + 2, 2 * nb - 1); }
@@ -753,79 +766,75 @@ __global__ void __launch_bounds__(THREADS2, 1) attn_tc2_kernel(const __grid_cons
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // Lane 0 polls the two tiles' barriers and issues whatever is ready: S_t(j) once the
+    // softmax of tile t has read S_t(j-1) and K_j has landed, PV_t(j) once P_t(j) is stored
+    // and V_j has landed.  A fixed order would make a tile whose MMA is ready wait behind the
+    // other tile's softmax.  A ring slot is released once both tiles are past its block.
     bool ok = true;
-    auto wait = [&](uint64_t* b, uint32_t ph) {
-      if (ok && lane == 0) ok = mbar_wait_bounded(b, ph, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      return ok;
-    };
-    auto item_wait = [&](int x) { return wait(&full[x % SLOTS], (x / SLOTS) & 1); };
-    auto issue_s = [&](int u, int j) {  // S_u = Q_u K_j^T
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sq = smem_u32(smem + OFF_Q2 + u * 2 * ATOM);
-        const uint32_t sk = smem_u32(smem + OFF_RING + (k_item(j) % SLOTS) * SLOT);
-#pragma unroll
-        for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint64_t da = desc_kmajor(sq + (kk >> 2) * ATOM) + 2 * (kk & 3);
-          const uint64_t db = desc_kmajor(sk + (kk >> 2) * ATOM) + 2 * (kk & 3);
-          tc_mma_f16(tmem + S_COL + u * 128, da, db, idesc(false), kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&s_full[u]);
-      }
-      __syncwarp();
-    };
-    auto issue_pv = [&](int u, int j) {  // O_u (+)= P_u V_j
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t sp = smem_u32(smem + OFF_P2 + u * 2 * ATOM);
-        const uint32_t sv = smem_u32(smem + OFF_RING + (v_item(j, nb) % SLOTS) * SLOT);
-#pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          const uint64_t da = desc_kmajor(sp + (kk >> 2) * ATOM) + 2 * (kk & 3);
-          const uint64_t db = desc_mnmajor(sv + kk * 16 * 128, ATOM);
-          tc_mma_f16(tmem + O_COL2 + u * 128, da, db, idesc(true), (j > 0 || kk > 0) ? 1u : 0u);
-        }
-      }
-      __syncwarp();
-    };
-    for (int u = 0; u < 2; ++u)
-      if (nbt[u] > 0) wait(&q_full[u], 0);
-    if (nb > 0 && item_wait(k_item(0))) {
+    if (lane == 0) {
       for (int u = 0; u < 2; ++u)
-        if (nbt[u] > 0) issue_s(u, 0);
-      if (lane == 0) tc_commit(&empty[k_item(0) % SLOTS]);
-      __syncwarp();
-    }
-    for (int j = 0; ok && j < nb; ++j) {
-      // S_{j+1} of each tile as soon as its softmax has read S_j (and K_{j+1} landed) ...
-      const bool k_next = j + 1 < nb;
-      if (k_next && item_wait(k_item(j + 1))) {
-        for (int u = 0; u < 2 && ok; ++u) {
-          if (j + 1 >= nbt[u]) continue;
-          if (!wait(&s_empty[u], j & 1)) break;
-          issue_s(u, j + 1);
+        if (nbt[u] > 0 && ok) ok = mbar_wait_bounded(&q_full[u], 0, abort_flag);
+      int sn[2] = {0, 0}, pn[2] = {0, 0};  // next S / PV block of each tile
+      int k_rel = 0, v_rel = 0;            // next K / V block whose ring slot is still held
+      uint64_t t_last = global_ns();
+      while (ok && (pn[0] < nbt[0] || pn[1] < nbt[1])) {
+        bool progress = false;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int js = sn[u];
+          const int xk = k_item(js);
+          if (js < nbt[u] && (js == 0 || mbar_test(&s_empty[u], (js - 1) & 1)) &&
+              mbar_test(&full[xk % SLOTS], (xk / SLOTS) & 1)) {  // S_u = Q_u K_js^T
+            tc_fence_after();
+            const uint32_t sq = smem_u32(smem + OFF_Q2 + u * 2 * ATOM);
+            const uint32_t sk = smem_u32(smem + OFF_RING + (xk % SLOTS) * SLOT);
+#pragma unroll
+            for (int kk = 0; kk < DH / 16; ++kk) {
+              const uint64_t da = desc_kmajor(sq + (kk >> 2) * ATOM) + 2 * (kk & 3);
+              const uint64_t db = desc_kmajor(sk + (kk >> 2) * ATOM) + 2 * (kk & 3);
+              tc_mma_f16(tmem + S_COL + u * 128, da, db, idesc(false), kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&s_full[u]);
+            sn[u] = js + 1;
+            progress = true;
+          }
+          const int jp = pn[u];
+          const int xv = v_item(jp, nb);
+          if (jp < sn[u] && mbar_test(&p_full[u], jp & 1) && mbar_test(&full[xv % SLOTS], (xv / SLOTS) & 1)) {
+            tc_fence_after();  // O_u (+)= P_u V_jp
+            const uint32_t sp = smem_u32(smem + OFF_P2 + u * 2 * ATOM);
+            const uint32_t sv = smem_u32(smem + OFF_RING + (xv % SLOTS) * SLOT);
+#pragma unroll
+            for (int kk = 0; kk < BKV / 16; ++kk) {
+              const uint64_t da = desc_kmajor(sp + (kk >> 2) * ATOM) + 2 * (kk & 3);
+              const uint64_t db = desc_mnmajor(sv + kk * 16 * 128, ATOM);
+              tc_mma_f16(tmem + O_COL2 + u * 128, da, db, idesc(true), (jp > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(&pv_done[u]);
+            pn[u] = jp + 1;
+            progress = true;
+          }
         }
-        if (lane == 0 && ok) tc_commit(&empty[k_item(j + 1) % SLOTS]);
-        __syncwarp();
+        // release, in load order per slot, the blocks both tiles have consumed
+        while (k_rel < nb && (sn[0] > k_rel || k_rel >= nbt[0]) && (sn[1] > k_rel || k_rel >= nbt[1])) {
+          tc_commit(&empty[k_item(k_rel) % SLOTS]);
+          ++k_rel;
+        }
+        while (v_rel < nb && (pn[0] > v_rel || v_rel >= nbt[0]) && (pn[1] > v_rel || v_rel >= nbt[1])) {
+          tc_commit(&empty[v_item(v_rel, nb) % SLOTS]);
+          ++v_rel;
+        }
+        if (progress) {
+          t_last = global_ns();
+        } else if (*abort_flag || global_ns() - t_last > 2000000000ull) {
+          ok = false;
+        }
       }
-      // ... then PV_j of each tile once its P_j is in shared memory
-      if (!ok || !item_wait(v_item(j, nb))) break;
-      for (int u = 0; u < 2 && ok; ++u) {
-        if (j >= nbt[u]) continue;
-        if (!wait(&p_full[u], j & 1)) break;
-        issue_pv(u, j);
-        if (lane == 0) tc_commit(&pv_done[u]);
-        __syncwarp();
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(a.status, ST_WAIT_TIMEOUT);
       }
-      if (lane == 0 && ok) tc_commit(&empty[v_item(j, nb) % SLOTS]);
-      __syncwarp();
-    }
-    if (!ok && lane == 0) {
-      *abort_flag = 1;
-      set_status(a.status, ST_WAIT_TIMEOUT);
-    }
-    if (lane == 0) {  // no MMA may run when the tensor memory is released
+      // no MMA may run when the tensor memory is released
       tc_commit(drain);
       mbar_wait_bounded(drain, 0u, nullptr);
     }
@@ -1123,18 +1132,18 @@ static std::atomic<int> g_attn_tiles{0};
 void attention_set_tiles(int tiles) { g_attn_tiles.store(tiles); }
 
 // Two tiles per CTA when the waves of pair units finish sooner than the waves of single
-// tiles: a pair unit takes ~1.75x a single tile's time (measured on GB300: full causal
-// 8320 tokens, 56/8 heads 1.360 -> 1.222 ms in 25 -> 13 waves; 1357 of 8320 queries 0.232
-// -> 0.208 ms), so the pairs win only where they also save a wave or more (884 of 8256
-// queries, 64/8 heads: 3 -> 2 waves, 0.167 -> 0.194 ms).  MHA (one head per KV head) was
-// slower with pairs at every size measured.
+// tiles: a pair unit takes ~1.5x a single tile's time (measured on GB300: full causal 8320
+// tokens, 56/8 heads 1.359 -> 1.045 ms in 25 -> 13 waves; 1357 of 8320 queries 0.232 ->
+// 0.183 ms; 3200 tokens, 32/8 heads 0.140 -> 0.119 ms), so the pairs win where they save a
+// wave or more (884 of 8256 queries, 64/8 heads, 3 -> 2 waves: 0.167 ms either way).  MHA
+// (one head per KV head) was slower with pairs at every size measured.
 static bool use_pairs(long long tiles, long long pairs, int n_heads, int n_kv_heads, int n_sm) {
   const int mode = g_attn_tiles.load();
   if (mode != 0) return mode == 2;
   if (n_heads == n_kv_heads) return false;
   const long long w1 = (tiles * n_kv_heads + n_sm - 1) / n_sm;
   const long long w2 = (pairs * n_kv_heads + n_sm - 1) / n_sm;
-  return 1.75 * static_cast<double>(w2) < 0.97 * static_cast<double>(w1);
+  return 1.5 * static_cast<double>(w2) < 0.97 * static_cast<double>(w1);
 }
 
 static int sm_count_cached() {
