@@ -1135,14 +1135,16 @@ void attention_set_tiles(int tiles) { g_attn_tiles.store(tiles); }
 // tiles: a pair unit takes ~1.5x a single tile's time (measured on GB300: full causal 8320
 // tokens, 56/8 heads 1.359 -> 1.045 ms in 25 -> 13 waves; 1357 of 8320 queries 0.232 ->
 // 0.183 ms; 3200 tokens, 32/8 heads 0.140 -> 0.119 ms), so the pairs win where they save a
-// wave or more (884 of 8256 queries, 64/8 heads, 3 -> 2 waves: 0.167 ms either way).  MHA
-// (one head per KV head) was slower with pairs at every size measured.
+// wave or more (884 of 8256 queries, 64/8 heads, 3 -> 2 waves: 0.167 ms either way).  With
+// one head per KV head (MHA, 128 queries a tile) the two tiles of a sparse pair often differ
+// in length: pairs only when single tiles take four waves or more (4128 causal, 32 heads:
+// 0.216 -> 0.185 ms; 646 of 4128 queries, 2 waves: 0.067 ms alone, 0.093 paired).
 static bool use_pairs(long long tiles, long long pairs, int n_heads, int n_kv_heads, int n_sm) {
   const int mode = g_attn_tiles.load();
   if (mode != 0) return mode == 2;
-  if (n_heads == n_kv_heads) return false;
   const long long w1 = (tiles * n_kv_heads + n_sm - 1) / n_sm;
   const long long w2 = (pairs * n_kv_heads + n_sm - 1) / n_sm;
+  if (n_heads == n_kv_heads && w1 < 4) return false;
   return 1.5 * static_cast<double>(w2) < 0.97 * static_cast<double>(w1);
 }
 
