@@ -265,6 +265,25 @@ size_t cb_gemm_scratch_size(void);
  * values: CB_ERR_INVALID_ARG. */
 cb_status cb_gemm_set_orientation(int orientation);
 
+/* CTA pairs for the bf16 GEMMs, process-wide (a tuning and test hook; default 0).  A pair
+ * of CTAs on two SMs computes 256 weight rows x a tile of tokens with one 256-row
+ * tensor-core instruction (tcgen05 cta_group::2), each CTA staging 128 weight rows and half
+ * of the tokens; a cluster of two pairs also shares the weight rows by multicast.
+ * 0: chosen per shape by the library's time model (only while cb_gemm_set_orientation is
+ * 0); 1: never; 2: clusters of one pair; 4: clusters of two pairs (2 and 4 apply where the
+ * shape allows pairs: output features a multiple of 256 with the q|k|v split points
+ * multiples of 128, SwiGLU features a multiple of 128, K a multiple of 64; a token tile
+ * forced by cb_gemm_set_orientation applies to the pairs too).  Results agree to fp32
+ * rounding of the same sums.  Other values: CB_ERR_INVALID_ARG. */
+cb_status cb_gemm_set_pairing(int pairing);
+
+/* The schedule a bf16 cb_gemm of M x N x K with `epilogue` and scratch_bytes of scratch
+ * would run under the current hooks, as a NUL-terminated line of text in buf (at most len
+ * bytes, truncated): the kernel (single CTAs or CTA pairs), its tiles, grid and the time
+ * model's estimate.  For tuning and reports; no GPU work.  CB_ERR_INVALID_ARG for a null
+ * buffer, a negative size or an unknown epilogue. */
+cb_status cb_gemm_describe(int M, int N, int K, int epilogue, size_t scratch_bytes, char* buf, size_t len);
+
 /* Query tiles per CTA of the bf16 attention, process-wide (a tuning and test hook;
  * default 0).  0: two 128-row tiles of one KV head per CTA when a launch's tile pairs
  * times the KV heads fill the SMs (the tensor core then works for one tile while the

@@ -79,6 +79,8 @@ def main():
     ap.add_argument("--orientation", type=int, default=0,
                     help="GEMM tiles: 0 by the time model, 1 token rows, 2 weight rows, 16..256 weight rows "
                          "with that many tokens per tile")
+    ap.add_argument("--pairing", type=int, default=0,
+                    help="GEMM CTA pairs: 0 by the time model, 1 never, 2 clusters of one pair, 4 of two")
     a = ap.parse_args()
     cbbuild.build()
     torch.manual_seed(0)
@@ -89,6 +91,7 @@ def main():
         M, N, K = a.M, a.N, a.K
         scr = None if a.no_stream_k else cb.gemm_scratch(dev)
         cb.cb_gemm_set_orientation(a.orientation)
+        cb.cb_gemm_set_pairing(a.pairing)
         A = (torch.randn(M, K, device=dev) * 0.5).to(torch.bfloat16)
         if a.mode == "swiglu":
             G = (torch.randn(N // 2, K, device=dev) * 0.02).to(torch.bfloat16)
@@ -101,7 +104,8 @@ def main():
             fn = lambda: cb.cb_gemm(A, B, C, 1 if a.mode == "add" else 0, scratch=scr)  # noqa: E731
         avg, best = _time(fn, a.iters, a.warmup, flush, a.batch)
         fl = 2.0 * M * N * K
-        out.update(shape=[M, N, K], mode=a.mode, stream_k=scr is not None, orientation=a.orientation, ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12,
+        out.update(shape=[M, N, K], mode=a.mode, stream_k=scr is not None, orientation=a.orientation, pairing=a.pairing,
+                   plan=cb.cb_gemm_describe(M, N, K, {"store": 0, "add": 1, "swiglu": 2}[a.mode], 0 if scr is None else scr.numel()), ms=avg, best_ms=best, tflops=fl / (avg * 1e-3) / 1e12,
                    weight_bytes=N * K * 2)
     elif a.kernel == "attention":
         H, Hkv, N, m = a.H, a.Hkv, a.N, a.m

@@ -25,7 +25,7 @@ FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", 
 
 LIBS = {
     os.path.join(PKG, "libcacheblend.so"): {
-        "srcs": [os.path.join(PKG, "csrc", f) for f in ("kernels_bw.cu", "select.cu", "gemm.cu", "gemm_noalloc.cu", "attention.cu",
+        "srcs": [os.path.join(PKG, "csrc", f) for f in ("kernels_bw.cu", "select.cu", "gemm.cu", "gemm_pair.cu", "gemm_noalloc.cu", "attention.cu",
                                                                "codec.cu", "decode.cu", "gemv.cu", "engine.cu",
                                                                "controller.cpp")],
         "deps": [os.path.join(PKG, "csrc", f) for f in ("common.cuh", "internal.h")] + [os.path.join(INCLUDE, "cacheblend.h")],

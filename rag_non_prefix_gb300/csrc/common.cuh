@@ -166,6 +166,20 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 __device__ __forceinline__ void bulk_wait_read_all_but_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
+// the shared-memory source of every committed group but the most recent `keep` has been
+// read (keep: 0, 1, 3, 7 or 15; other values wait as for the next smaller one)
+__device__ __forceinline__ void bulk_wait_read_keep(int keep) {
+  if (keep >= 15)
+    asm volatile("cp.async.bulk.wait_group.read 15;" ::: "memory");
+  else if (keep >= 7)
+    asm volatile("cp.async.bulk.wait_group.read 7;" ::: "memory");
+  else if (keep >= 3)
+    asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+  else if (keep >= 1)
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+  else
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // every committed group has completed (its global writes performed)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte
@@ -268,6 +282,95 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------- PTX: CTA pairs
+// A cluster of 2 or 4 CTAs holds one or two CTA pairs (ranks 2q and 2q + 1); the even
+// CTA of a pair issues tcgen05.mma.cta_group::2 for both.  Every tcgen05 instruction of
+// a kernel that uses these forms is a cta_group::2 one.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t n_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// The shared::cluster address of the variable at shared address `smem_addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Every thread of every CTA of the cluster arrives, then waits for all of them (release /
+// acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 2-D tile load into this CTA's shared memory whose bytes complete on the mbarrier at
+// shared::cluster address `bar`, which may be this CTA's or its pair peer's.
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+// The same tile delivered to the same shared-memory offset in every CTA of `cta_mask`; in
+// each destination the bytes complete on the mbarrier at `bar`'s offset in the even CTA of
+// that destination's pair (`bar` addresses the even CTA of this CTA's pair).
+__device__ __forceinline__ void tma_load_2d_pair_mc(void* smem_dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                    int c1, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
+      : "memory");
+}
+// Tensor memory of a CTA pair: allocated, relinquished and freed by one warp of each CTA
+// of the pair, collectively (the same columns in both).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* smem_result, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_result)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D (128 lanes in each CTA of the pair) (+)= A (M = 256: 128 rows in each CTA's shared
+// memory at the descriptor's offset) . B^T (N columns: N/2 rows in each CTA's shared
+// memory at the descriptor's offset); issued by the even CTA.
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the mbarrier at `bar`'s offset in each CTA of `cta_mask` when every
+// cta_group::2 MMA issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
 
 // ----------------------------------------------------------------------------- PTX: cp.async
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {

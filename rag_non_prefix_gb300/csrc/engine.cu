@@ -1351,6 +1351,21 @@ cb_status cb_gemm_set_orientation(int orientation) {
   return CB_OK;
 }
 
+cb_status cb_gemm_describe(int M, int N, int K, int epilogue, size_t scratch_bytes, char* buf, size_t len) {
+  if (!buf || len == 0) return fail(nullptr, CB_ERR_INVALID_ARG, "null buffer");
+  if (M < 0 || N < 0 || K < 0 || epilogue < 0 || epilogue > 2)
+    return fail(nullptr, CB_ERR_INVALID_ARG, "negative size or unknown epilogue");
+  gemm_describe(M, N, K, epilogue, scratch_bytes, buf, len);
+  return CB_OK;
+}
+
+cb_status cb_gemm_set_pairing(int pairing) {
+  if (pairing != 0 && pairing != 1 && pairing != 2 && pairing != 4)
+    return fail(nullptr, CB_ERR_INVALID_ARG, "pairing must be 0, 1, 2 or 4");
+  gemm_set_pairing(pairing);
+  return CB_OK;
+}
+
 cb_status cb_attention(const void* q, const int32_t* q_pos, int m, const void* k, const void* v, int n_kv, int n_heads,
                        int n_kv_heads, int head_dim, void* out, cb_dtype dtype, void* stream) {
   if (!q || !q_pos || !k || !v || !out) return fail(nullptr, CB_ERR_INVALID_ARG, "null pointer");

@@ -17,6 +17,7 @@
 // fp32: a plain shared-memory-tiled FFMA kernel with the same epilogues (used by the
 // fp32 configuration, whose 1e-4 tolerance rules out TF32).
 #include <algorithm>
+#include <cstdio>
 #include <atomic>
 #include <mutex>
 
@@ -25,7 +26,6 @@
 
 namespace cb {
 
-enum { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_SWIGLU = 2 };
 
 // ============================================================================= tensor maps
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -46,10 +46,9 @@ static EncodeTiledFn get_encoder() {
   return fn;
 }
 
-// Row-major [rows][inner] tensor with a row pitch of `pitch` bytes (default: 128-byte swizzle).
-static bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
-                           uint64_t pitch, uint32_t box_inner, uint32_t box_rows,
-                           CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+// Row-major [rows][inner] tensor with a row pitch of `pitch` bytes.
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                 uint64_t pitch, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
   EncodeTiledFn fn = get_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
@@ -59,6 +58,12 @@ static bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void*
   CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+static bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                           uint64_t pitch, uint32_t box_inner, uint32_t box_rows,
+                           CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+  return encode_tmap(map, dt, base, inner, rows, pitch, box_inner, box_rows, swz);
 }
 
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
@@ -851,6 +856,7 @@ struct GemmPlan {
   long long sk_iters;
   int sk_group;         // CTAs per stream-K group (1: plain stream-K)
   size_t scratch_used;  // bytes of scratch the stream-K split touches (0: data-parallel)
+  double us;            // the time model's estimate
 };
 
 // Time model used to pick the orientation, the token tile and the schedule.  A tile takes
@@ -972,6 +978,7 @@ static GemmPlan plan_gemm(int M, int N, int K, int split0, int split1, long long
   g.sk_iters = c.sk_iters;
   g.sk_group = c.sk_group;
   g.scratch_used = c.scratch;
+  g.us = c.us;
   return g;
 }
 
@@ -1007,6 +1014,17 @@ static long long scratch_slots(const void* scratch, size_t scratch_bytes) {
              : 0;
 }
 
+// Whether launch_gemm runs these operands on CTA pairs (the paired kernel takes no scratch):
+// forced by the pairing hook, else when the time model prefers it and no orientation is forced.
+static bool use_pair(const GemmPlan& g, int M, int N, int K, int split0, int split1, int mode, PairPlan* pp) {
+  const int pm = gemm_pairing();
+  const int forced = g_orientation.load();
+  if (pm == 1 || (pm == 0 && forced != 0)) return false;
+  if (!plan_gemm_pair(M, N, K, split0, split1, mode, forced >= 16 ? forced : 0, pp)) return false;
+  // (the single-CTA model is optimistic: measured launches take ~1.2x its estimate)
+  return pm >= 2 || pp->us < 1.2 * g.us;
+}
+
 // Scratch bytes the schedule of launch_gemm would use for a single-tensor B of N output
 // columns with unlimited scratch (0 when the shape runs data-parallel).
 size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt) {
@@ -1018,10 +1036,29 @@ size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt) {
 // scratch: 0 on the paths that take none (no rows, the few-row GEMV, fp32), otherwise
 // what the schedule narrowed to the slots that scratch holds uses (never more than it).
 size_t gemm_scratch_used(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, int M,
-                         int N, int K, cb_dtype dt, size_t scratch_bytes) {
+                         int N, int K, int mode, cb_dtype dt, size_t scratch_bytes) {
   if (M <= 0 || dt != CB_BF16 || gemv_applies(M, K, dt, A, B0, B1, B2)) return 0;
-  return plan_gemm(M, N, K, split0, split1, scratch_slots(reinterpret_cast<const void*>(1), scratch_bytes))
-      .scratch_used;
+  const GemmPlan g = plan_gemm(M, N, K, split0, split1, scratch_slots(reinterpret_cast<const void*>(1), scratch_bytes));
+  PairPlan pp;
+  if (use_pair(g, M, N, K, split0, split1, mode, &pp)) return 0;
+  return g.scratch_used;
+}
+
+// The schedule launch_gemm picks for a bf16 GEMM with scratch_bytes of scratch, as text.
+int gemm_describe(int M, int N, int K, int mode, size_t scratch_bytes, char* buf, size_t len) {
+  if (M <= 0 || N <= 0 || K <= 0) return snprintf(buf, len, "empty");
+  const GemmPlan g = plan_gemm(M, N, K, N, N, scratch_slots(reinterpret_cast<const void*>(1), scratch_bytes));
+  PairPlan pp;
+  if (use_pair(g, M, N, K, N, N, mode, &pp)) {
+    const int stage_bytes = pp.ksub * (16384 + pp.bt * 64);
+    return snprintf(buf, len, "pairs cluster=%d token_tile=%d k_atoms_per_stage=%d stage_bytes=%d clusters=%d model_us=%.1f",
+                    pp.cl, pp.bt, pp.ksub, stage_bytes, pp.clusters, pp.us);
+  }
+  return snprintf(buf, len,
+                  "single orientation=%s token_tile=%d feature_tile=%d grid=%d data_parallel_tiles=%d stream_k_iters=%lld "
+                  "stream_k_group=%d model_us=%.1f",
+                  g.wrows ? "weight-rows" : "token-rows", g.wrows ? g.bt : 128, g.wrows ? 128 : g.bn, g.grid, g.dp_tiles,
+                  g.sk_iters, g.sk_group, g.us);
 }
 
 // mode: EPI_STORE_F32 / EPI_ADD_F32 (C fp32 [M][ldc]) or EPI_SWIGLU (C dtype [M][ldc], N/2 columns).
@@ -1051,6 +1088,9 @@ cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const voi
   }
   // bf16 on tcgen05
   const GemmPlan g = plan_gemm(M, N, K, split0, split1, scratch_slots(scratch, scratch_bytes));
+  PairPlan pp;
+  if (use_pair(g, M, N, K, split0, split1, mode, &pp))
+    return launch_gemm_pair(pp, A, B0, B1, B2, split0, split1, C, M, N, K, ldc, mode, status, s);
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   // token rows: A box 128 rows, weight box BN rows (SwiGLU BN/2 + BN/2);

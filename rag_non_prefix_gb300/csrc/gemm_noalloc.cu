@@ -96,7 +96,7 @@ extern "C" cb_status cb_gemm_noalloc(const void* A, const void* B, const void* B
   // exactly as cb_gemm does with a small caller scratch, so every shape cb_gemm accepts
   // runs here.  A schedule that asked for more than the array would be refused.
   const void* B1 = epilogue == 2 ? B2 : nullptr;
-  const size_t need = cb::gemm_scratch_used(A, B, B1, nullptr, N, N, M, N, K, dtype, CB_GEMM_STATIC_SCRATCH_BYTES);
+  const size_t need = cb::gemm_scratch_used(A, B, B1, nullptr, N, N, M, N, K, epilogue, dtype, CB_GEMM_STATIC_SCRATCH_BYTES);
   if (need > CB_GEMM_STATIC_SCRATCH_BYTES) {
     snprintf(g_noalloc_msg, sizeof(g_noalloc_msg),
              "cb_gemm_noalloc: the schedule needs %zu bytes of scratch, the built-in array holds %zu", need,
@@ -126,7 +126,7 @@ extern "C" size_t cb_gemm_noalloc_scratch_used(int M, int N, int K, int epilogue
   if (M <= 0 || N < 1 || K < 1 || epilogue < 0 || epilogue > 2) return 0;
   // aligned stand-ins for the operands: the schedule looks only at their alignment
   const void* op = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
-  return cb::gemm_scratch_used(op, op, epilogue == 2 ? op : nullptr, nullptr, N, N, M, N, K, dtype,
+  return cb::gemm_scratch_used(op, op, epilogue == 2 ? op : nullptr, nullptr, N, N, M, N, K, epilogue, dtype,
                                CB_GEMM_STATIC_SCRATCH_BYTES);
 }
 

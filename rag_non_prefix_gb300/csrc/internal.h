@@ -181,7 +181,7 @@ void gemm_set_orientation(int o);  // 0 model, 1 token rows, 2 weight rows
 size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt);
 // scratch launch_gemm uses for these operands given scratch_bytes of it (<= scratch_bytes)
 size_t gemm_scratch_used(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, int M,
-                         int N, int K, cb_dtype dt, size_t scratch_bytes);
+                         int N, int K, int mode, cb_dtype dt, size_t scratch_bytes);
 // Device address of the status word that the standalone GEMM calls (cb_gemm,
 // cb_gemm_noalloc) report device-side problems into, on the current device.
 cudaError_t standalone_gemm_status(int32_t** out);
@@ -216,7 +216,31 @@ cudaError_t launch_argmax(const float* logits, int n_req, int vocab, int32_t* co
 cudaError_t launch_write_hidden(const float* h, const int32_t* s_pos, int row0, int n, int d, float* out,
                                 cudaStream_t s);
 
+// Paired GEMM (gemm_pair.cu): clusters of one or two CTA pairs, weights on the tensor
+// core's rows, 256 weight rows x bt tokens per pair.
+struct PairPlan {
+  int cl;        // CTAs per cluster (2 or 4)
+  int bt;        // tokens per pair tile
+  int ksub;      // 64-element atoms of K per ring stage
+  int clusters;  // clusters resident at once
+  int w_tiles;   // weight tiles (256 rows; SwiGLU 128 features)
+  double us;     // the time model's estimate
+};
+// Whether the operands suit the paired kernel, and its best plan (forced_bt >= 16 fixes
+// the token tile); false when they do not, or pairing is switched off.
+bool plan_gemm_pair(int M, int N, int K, int split0, int split1, int mode, int forced_bt, PairPlan* out);
+cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, const void* B1, const void* B2,
+                             int split0, int split1, void* C, int M, int N, int K, int ldc, int mode, int32_t* status,
+                             cudaStream_t s);
+void gemm_set_pairing(int m);  // 0 model, 1 never, 2 clusters of one pair, 4 of two pairs
+// launch_gemm's schedule for a bf16 GEMM (single-tensor B) as text; snprintf's return value
+int gemm_describe(int M, int N, int K, int mode, size_t scratch_bytes, char* buf, size_t len);
+int gemm_pairing();
+enum { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_SWIGLU = 2 };
+
 // tensor-map encoder (driver entry point, resolved once)
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                 uint64_t pitch, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);
 bool encode_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                          uint32_t box_rows);
 

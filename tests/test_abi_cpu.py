@@ -109,7 +109,21 @@ def test_tuning_hooks_reject_bad_values(lib):
     for ok in (0, 1, 2, 0):
         assert lib.cb_attention_set_tiles(ok) == 0
     assert lib.cb_gemm_set_orientation(3) == 1 and lib.cb_gemm_set_orientation(0) == 0
+    for bad in (-1, 3, 5, 8):
+        assert lib.cb_gemm_set_pairing(bad) == 1
+    for ok in (1, 2, 4, 0):
+        assert lib.cb_gemm_set_pairing(ok) == 0
     assert lib.cb_k_for_ratio(0.0, 100) == 0 and lib.cb_k_for_ratio(0.15, 3136) == 471
+
+
+def test_gemm_describe_reports_a_schedule_without_a_gpu():
+    """The schedule query is host logic: on a machine without a GPU no CTA-pair cluster can be
+    resident, so the single-CTA schedule is reported; its fields follow the header."""
+    line = cb.cb_gemm_describe(1357, 7168, 7168, 1, 1 << 30)
+    assert line.startswith(("single ", "pairs ")) and "model_us=" in line
+    assert cb.cb_gemm_describe(0, 7168, 7168, 1) == "empty"
+    with pytest.raises(cb.CacheBlendError):
+        cb.cb_gemm_describe(4, 8, 8, 3)
 
 
 def test_library_fails_loudly_when_missing(tmp_path):

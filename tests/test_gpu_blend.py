@@ -99,6 +99,17 @@ def test_bf16_blend_forced_selection_matches_oracle(small_bf16, orientation):
         cb.cb_gemm_set_orientation(0)
 
 
+@pytest.mark.parametrize("pairing", [2, 4], ids=["pairs", "two-pairs"])
+def test_bf16_blend_on_cta_pairs_matches_oracle(small_bf16, pairing):
+    """Numerics with every projection on CTA pairs (q|k|v across three weight tensors,
+    output projection and down projection with the residual add, SwiGLU)."""
+    cb.cb_gemm_set_pairing(pairing)
+    try:
+        _forced_bf16(small_bf16)
+    finally:
+        cb.cb_gemm_set_pairing(0)
+
+
 @pytest.mark.parametrize("tiles", [1, 2], ids=["one-tile", "two-tiles"])
 def test_bf16_blend_attention_kernels_match_oracle(small_bf16, tiles):
     """Numerics with each attention kernel forced (one or two query tiles per CTA)."""

@@ -253,6 +253,82 @@ def test_gemm_stream_k_is_deterministic():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
+@pytest.fixture(params=[(2, 0), (4, 0), (2, 16), (4, 16), (2, 240), (4, 240), (4, 256)],
+                ids=["pair-model", "two-pairs-model", "pair-16", "two-pairs-16", "pair-240", "two-pairs-240",
+                     "two-pairs-256"])
+def pairing(request):
+    """Runs a GEMM test on CTA pairs (clusters of one or two pairs), with the time model's
+    token tile or a forced one (process-wide settings, reset after)."""
+    cl, bt = request.param
+    cb.cb_gemm_set_pairing(cl)
+    cb.cb_gemm_set_orientation(bt)
+    yield request.param
+    cb.cb_gemm_set_pairing(0)
+    cb.cb_gemm_set_orientation(0)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (17, 256, 128), (71, 256, 512), (300, 768, 1024), (535, 1024, 4096),
+                                   (1000, 512, 320), (535, 4096, 4096), (3000, 6144, 512), (256, 4096, 4096),
+                                   (200, 2560, 8192), (64, 1024, 28672), (1357, 1024, 1024), (4400, 512, 256)])
+def test_gemm_bf16_pairs_store_and_add(M, N, K, pairing):
+    """CTA-pair tiles against fp64: every token tile (a ragged last one, a pad tile of the
+    second pair when the token tiles are odd), both weight halves, K of one or many stages."""
+    rng = np.random.default_rng(M + N + K + 1)
+    A = _bf16(rng.standard_normal((M, K)))
+    B = _bf16(rng.standard_normal((N, K)) * 0.02)
+    C0 = _f32(rng.standard_normal((M, N)))
+    ref = _gemm_ref(to_np(A), to_np(B))
+    out = torch.full((M, N), np.nan, dtype=torch.float32, device="cuda")
+    cb.cb_gemm(A, B, out, epilogue=0)
+    acc = C0.clone()
+    cb.cb_gemm(A, B, acc, epilogue=1)
+    torch.cuda.synchronize()
+    scale = np.max(np.abs(ref))
+    assert np.max(np.abs(to_np(out) - ref)) < 1e-4 * scale
+    assert np.max(np.abs(to_np(acc) - (ref + to_np(C0)))) < 1e-4 * max(scale, 1.0) + 1e-5
+
+
+@pytest.mark.parametrize("M,F,K", [(2, 2048, 1024), (130, 128, 256), (535, 384, 512), (535, 14336, 4096),
+                                   (96, 2048, 4096), (3200, 1024, 256), (1005, 3584, 1024), (1357, 640, 1024)])
+def test_gemm_bf16_pairs_swiglu(M, F, K, pairing):
+    rng = np.random.default_rng(M + F + 1)
+    A = _bf16(rng.standard_normal((M, K)))
+    G = _bf16(rng.standard_normal((F, K)) * 0.05)
+    U = _bf16(rng.standard_normal((F, K)) * 0.05)
+    out = torch.zeros((M, F), dtype=torch.bfloat16, device="cuda")
+    cb.cb_gemm(A, G, out, epilogue=2, B2=U)
+    torch.cuda.synchronize()
+    g = _gemm_ref(to_np(A), to_np(G))
+    u = _gemm_ref(to_np(A), to_np(U))
+    ref = orc.silu(g) * u
+    assert np.max(np.abs(to_np(out) - ref)) <= 2 ** -7 * np.max(np.abs(ref)) + 1e-6
+
+
+def test_gemm_pairs_are_deterministic_and_match_single_ctas():
+    """The paired kernel sums each output in the same k order on every run; against the
+    single-CTA kernel it agrees to fp32 rounding of the same sums."""
+    rng = np.random.default_rng(5)
+    A = _bf16(rng.standard_normal((1357, 2048)))
+    B = _bf16(rng.standard_normal((2048, 2048)) * 0.02)
+    outs = {}
+    try:
+        for mode in (1, 2, 4):
+            cb.cb_gemm_set_pairing(mode)
+            runs = []
+            for _ in range(2):
+                o = torch.zeros((1357, 2048), dtype=torch.float32, device="cuda")
+                cb.cb_gemm(A, B, o, 0)
+                runs.append(o)
+            torch.cuda.synchronize()
+            assert torch.equal(runs[0], runs[1])
+            outs[mode] = to_np(runs[0])
+    finally:
+        cb.cb_gemm_set_pairing(0)
+    scale = np.max(np.abs(outs[1]))
+    assert np.max(np.abs(outs[2] - outs[1])) < 1e-5 * scale
+    assert np.max(np.abs(outs[4] - outs[1])) < 1e-5 * scale
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 64, 8), (2, 100, 36), (4, 100, 36), (8, 256, 1024), (77, 200, 96), (288, 1024, 256)])
 def test_gemm_f32_all_epilogues(M, N, K):
     rng = np.random.default_rng(M * 3 + N)
