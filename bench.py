@@ -730,7 +730,7 @@ def run_ours(args, rank, world):
         "speedup_vs_full_prefill": round(m["speedup"], 3),
         "full_prefill_tok_s": round(m["full_tok_s"], 1),
         "phase_ms": m["phases_blend"],
-        "roofline": {"kernel": "gemm_bf16_tc (tcgen05 projections: qkv, o, gate/up, down)", "bound": "tensor",
+        "roofline": {"kernel": "projection GEMM: gemm_pair_kernel (tcgen05 cta_group::2) / gemm_bf16_tc (qkv, o, gate/up, down)", "bound": "tensor",
                      "achieved": g["achieved_tflops"] if g else None, "peak": peaks["bf16_tflops_sustained"],
                      "unit": "TFLOP/s", "frac": g["frac"] if g else None,
                      "traffic": round(ratio_traffic * alg_per_launch) if ratio_traffic else None,
