@@ -1038,7 +1038,8 @@ size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt) {
 size_t gemm_scratch_used(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, int M,
                          int N, int K, int mode, cb_dtype dt, size_t scratch_bytes) {
   if (M <= 0 || dt != CB_BF16 || gemv_applies(M, K, dt, A, B0, B1, B2)) return 0;
-  const GemmPlan g = plan_gemm(M, N, K, split0, split1, scratch_slots(reinterpret_cast<const void*>(1), scratch_bytes));
+  const long long slots = scratch_slots(reinterpret_cast<const void*>(1), scratch_bytes);
+  const GemmPlan g = plan_gemm(M, N, K, split0, split1, slots);
   PairPlan pp;
   if (use_pair(g, M, N, K, split0, split1, mode, &pp)) return 0;
   return g.scratch_used;
@@ -1047,7 +1048,8 @@ size_t gemm_scratch_used(const void* A, const void* B0, const void* B1, const vo
 // The schedule launch_gemm picks for a bf16 GEMM with scratch_bytes of scratch, as text.
 int gemm_describe(int M, int N, int K, int mode, size_t scratch_bytes, char* buf, size_t len) {
   if (M <= 0 || N <= 0 || K <= 0) return snprintf(buf, len, "empty");
-  const GemmPlan g = plan_gemm(M, N, K, N, N, scratch_slots(reinterpret_cast<const void*>(1), scratch_bytes));
+  const long long slots = scratch_slots(reinterpret_cast<const void*>(1), scratch_bytes);
+  const GemmPlan g = plan_gemm(M, N, K, N, N, slots);
   PairPlan pp;
   if (use_pair(g, M, N, K, N, N, mode, &pp)) {
     const int stage_bytes = pp.ksub * (16384 + pp.bt * 64);
@@ -1087,7 +1089,8 @@ cudaError_t launch_gemm(const void* A, const void* B0, const void* B1, const voi
     return cudaGetLastError();
   }
   // bf16 on tcgen05
-  const GemmPlan g = plan_gemm(M, N, K, split0, split1, scratch_slots(scratch, scratch_bytes));
+  const long long slots = scratch_slots(scratch, scratch_bytes);
+  const GemmPlan g = plan_gemm(M, N, K, split0, split1, slots);
   PairPlan pp;
   if (use_pair(g, M, N, K, split0, split1, mode, &pp))
     return launch_gemm_pair(pp, A, B0, B1, B2, split0, split1, C, M, N, K, ldc, mode, status, s);

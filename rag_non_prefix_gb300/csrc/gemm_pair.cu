@@ -68,6 +68,13 @@ struct Params {
   int slabs;           // output slabs in the staging area (2, 4, 8 or 16)
 };
 
+// The idx-th unit of cluster cid, round-robin (false when there is none).
+__device__ __forceinline__ bool get_unit(const Params& p, int cid, int NC, int idx, int& u) {
+  u = cid + idx * NC;
+  return u < p.units;
+}
+
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
@@ -154,15 +161,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint16_t mc_mask = static_cast<uint16_t>((1u << h) | (1u << (2 + h)));  // (0,h) and (1,h)
-      uint32_t s = 0, ph = 0;
-      bool ok = true;
-      for (int u = cid; ok && u < p.units; u += NC) {
-        const int tt = (u % p.tok_groups) * PPC + q, wt = u / p.tok_groups;
-        const int trow = tt * p.bt + h * half_rows;  // first token this CTA stages
-        // this CTA's 128 weight rows: rows r_lo.. of map m_lo, then r_hi.. of map m_hi
-        const CUtensorMap* m_lo = &tmW0;
-        const CUtensorMap* m_hi = &tmW1;
-        int r_lo, r_hi;
+      // this CTA's 128 weight rows of unit u: rows r_lo.. of map m_lo, then r_hi.. of map m_hi
+      auto weight_rows = [&](int u, const CUtensorMap*& m_lo, const CUtensorMap*& m_hi, int& r_lo, int& r_hi) {
+        const int wt = u / p.tok_groups;
+        m_lo = &tmW0;
+        m_hi = &tmW1;
         if (p.mode == EPI_SWIGLU) {
           r_lo = r_hi = wt * 128 + h * 64;  // 64 gate rows, then the up rows of the same features
         } else {
@@ -180,29 +183,46 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           r_lo = r;
           r_hi = r + 64;
         }
+      };
+      // weight atom j of stage s (k-block kb): to this CTA, and by multicast in clusters of two pairs
+      auto load_weight_atom = [&](uint32_t s, int kb, int j, const CUtensorMap* m_lo, const CUtensorMap* m_hi, int r_lo,
+                                  int r_hi) {
+        uint8_t* aj = ring + s * static_cast<uint32_t>(p.stage_bytes) + j * A_ATOM;
+        const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead);
+        const int k0 = (kb * p.ksub + j) * BK;
+        if (PPC == 2) {
+          // half of the weight rows, to this CTA and to its counterpart in the other pair
+          if (q == 0)
+            tma_load_2d_pair_mc(aj, m_lo, bar, k0, r_lo, mc_mask);
+          else
+            tma_load_2d_pair_mc(aj + A_ATOM / 2, m_hi, bar, k0, r_hi, mc_mask);
+        } else {
+          tma_load_2d_pair(aj, m_lo, bar, k0, r_lo);
+          tma_load_2d_pair(aj + A_ATOM / 2, m_hi, bar, k0, r_hi);
+        }
+      };
+      int u = 0;
+      uint32_t s = 0, ph = 0;
+      bool ok = true;
+      for (int idx = 0; ok && get_unit(p, cid, NC, idx, u); ++idx) {
+        const int tt = (u % p.tok_groups) * PPC + q;
+        const int trow = tt * p.bt + h * half_rows;  // first token this CTA stages
+        const CUtensorMap *m_lo, *m_hi;
+        int r_lo, r_hi;
+        weight_rows(u, m_lo, m_hi, r_lo, r_hi);
         for (int kb = 0; kb < p.n_kb; ++kb) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
-          uint8_t* sa = ring + s * static_cast<uint32_t>(p.stage_bytes);
-          uint8_t* sb = sa + p.ksub * A_ATOM;
+          uint8_t* sb = ring + s * static_cast<uint32_t>(p.stage_bytes) + p.ksub * A_ATOM;
           const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead);
+          // (each atom's weights and tokens back to back: measured faster on GB300 than all
+          // weight atoms first, e.g. the Yi-34B gate/up 482 -> 465 us)
           if (even) mbar_arrive_expect_tx(&full[s], 2u * static_cast<uint32_t>(p.stage_bytes));
           for (int j = 0; j < p.ksub; ++j) {
-            const int k0 = (kb * p.ksub + j) * BK;
-            uint8_t* aj = sa + j * A_ATOM;
-            if (PPC == 2) {
-              // half of the weight rows, to this CTA and to its counterpart in the other pair
-              if (q == 0)
-                tma_load_2d_pair_mc(aj, m_lo, bar, k0, r_lo, mc_mask);
-              else
-                tma_load_2d_pair_mc(aj + A_ATOM / 2, m_hi, bar, k0, r_hi, mc_mask);
-            } else {
-              tma_load_2d_pair(aj, m_lo, bar, k0, r_lo);
-              tma_load_2d_pair(aj + A_ATOM / 2, m_hi, bar, k0, r_hi);
-            }
-            tma_load_2d_pair(sb + j * b_atom, &tmX, bar, k0, trow);
+            load_weight_atom(s, kb, j, m_lo, m_hi, r_lo, r_hi);
+            tma_load_2d_pair(sb + j * b_atom, &tmX, bar, (kb * p.ksub + j) * BK, trow);
           }
           if (++s == stages) {
             s = 0;
@@ -226,11 +246,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t sbytes = static_cast<uint32_t>(p.stage_bytes);
       const uint32_t b_off = static_cast<uint32_t>(p.ksub * A_ATOM);
       const uint64_t a_step = A_ATOM >> 4, b_step = b_atom >> 4;  // descriptor steps per atom
-      const int ksub = p.ksub, n_kb = p.n_kb;
+      const int ksub = p.ksub;
       uint32_t s = 0, ph = 0, sa = ring_u32;
       bool ok = true;
-      int i = 0;
-      for (int u = cid; ok && u < p.units; u += NC, ++i) {
+      int u = 0;
+      for (int i = 0; ok && get_unit(p, cid, NC, i, u); ++i) {
         const int b = i & 1;
         const uint32_t use = static_cast<uint32_t>(i >> 1);
         if (!mbar_wait_bounded(&acc_empty[b], (use & 1u) ^ 1u, abort_flag)) {
@@ -240,7 +260,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t tacc = tmem + static_cast<uint32_t>(b * ACC_STRIDE);
         uint32_t accum = 0u;  // the tile's first MMA overwrites the accumulator
-        for (int kb = 0; kb < n_kb; ++kb) {
+        for (int kb = 0; kb < p.n_kb; ++kb) {
           if (!mbar_try_wait(&full[s], ph) && !mbar_wait_bounded(&full[s], ph, abort_flag)) {
             ok = false;
             break;
@@ -290,9 +310,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
     const int slab_bytes = swig ? BF_SLAB : F32_SLAB;
     const int keep = p.slabs - 1;  // stores that may still read their slab when one is refilled
     int slab = 0;                  // output slabs issued so far
-    int i = 0;
-    for (int u = cid; u < p.units; u += NC, ++i) {
+    int u = 0, nx = 0;
+    for (int i = 0; get_unit(p, cid, NC, i, u); ++i) {
       const int b = i & 1;
+      // The last unit's stores are staged in the ring, which its accumulator's completion
+      // leaves idle (every copy landed and was read): one fresh slab each, none waited for
+      // (measured on GB300: 1-2 % per launch, the last unit's epilogue being the tail).
+      const bool last = !get_unit(p, cid, NC, i + 1, nx) &&
+                        (swig ? (p.bt / 16) * BF_SLAB : (p.bt / F32_SLAB_TOK) * F32_SLAB) <= p.stg_off - OFF_RING;
+      int fresh = 0;  // ring slabs used by the last unit
       const uint32_t use = static_cast<uint32_t>(i >> 1);
       bool ok = true;
       if (lane == 0) ok = mbar_wait_bounded(&acc_full[b], use & 1u, abort_flag);
@@ -320,8 +346,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
         for (int c = 0; c < nt; c += 16, ++slab) {
           float v[16];
           tmem_ld16(tbase + c, v);
-          bf16* tile = reinterpret_cast<bf16*>(slab0 + (slab % p.slabs) * slab_bytes);
-          if (et == 0) bulk_wait_read_keep(keep);  // the store that last used this slab has read it
+          bf16* tile = reinterpret_cast<bf16*>(last ? ring + (fresh++) * slab_bytes : slab0 + (slab % p.slabs) * slab_bytes);
+          if (et == 0 && !last) bulk_wait_read_keep(keep);  // the store that last used this slab has read it
           if (quarter >= 2) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) xch[(r_loc - 64) * 17 + j] = v[j];
@@ -349,9 +375,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             if (c + half * F32_SLAB_TOK >= nt) break;  // (uniform)
-            float* sbuf = reinterpret_cast<float*>(slab0 + (slab % p.slabs) * slab_bytes);
+            float* sbuf = reinterpret_cast<float*>(last ? ring + (fresh++) * slab_bytes : slab0 + (slab % p.slabs) * slab_bytes);
             ++slab;
-            if (et == 0) bulk_wait_read_keep(keep);
+            if (et == 0 && !last) bulk_wait_read_keep(keep);
             epi_bar();
 #pragma unroll
             for (int j = 0; j < F32_SLAB_TOK; ++j) sbuf[j * ROWS + r_loc] = v[half * F32_SLAB_TOK + j];
@@ -462,14 +488,13 @@ static double pair_us(int M, int K, int w_tiles, int cl, int bt, int ksub, int c
   const int tok_tiles = (M + bt - 1) / bt;
   const int groups = (tok_tiles + ppc - 1) / ppc;
   const long long units = static_cast<long long>(w_tiles) * groups;
-  const long long waves = (units + clusters - 1) / clusters;
   const double issue = ksub == 2 ? std::max(2.0 * bt + 70.0, 460.0) : std::max(2.0 * bt + 90.0, 640.0);
   const double lat = 2200.0 / ((l.stages - 1) * ksub);
   const double kb = std::max(issue, lat);
   const double main = (K / 64) * kb;
   const double epi = swiglu ? bt * 128.0 * 4.0 / 8.0 : bt * 128.0 * 4.0 / 24.0;
   const double unit = std::max(main, epi);
-  return (waves * unit + 5000.0 + epi) / 1750.0;
+  return (((units + clusters - 1) / clusters) * unit + 5000.0 + epi) / 1750.0;
 }
 
 bool plan_gemm_pair(int M, int N, int K, int split0, int split1, int mode, int forced_bt, PairPlan* out) {

@@ -219,15 +219,16 @@ cudaError_t launch_write_hidden(const float* h, const int32_t* s_pos, int row0, 
 // Paired GEMM (gemm_pair.cu): clusters of one or two CTA pairs, weights on the tensor
 // core's rows, 256 weight rows x bt tokens per pair.
 struct PairPlan {
-  int cl;        // CTAs per cluster (2 or 4)
-  int bt;        // tokens per pair tile
-  int ksub;      // 64-element atoms of K per ring stage
-  int clusters;  // clusters resident at once
-  int w_tiles;   // weight tiles (256 rows; SwiGLU 128 features)
-  double us;     // the time model's estimate
+  int cl;               // CTAs per cluster (2 or 4)
+  int bt;               // tokens per pair tile
+  int ksub;             // 64-element atoms of K per ring stage
+  int clusters;         // clusters resident at once
+  int w_tiles;          // weight tiles (256 rows; SwiGLU 128 features)
+  double us;            // the time model's estimate
 };
 // Whether the operands suit the paired kernel, and its best plan (forced_bt >= 16 fixes
-// the token tile); false when they do not, or pairing is switched off.
+// the token tile); false when they do not, or pairing is switched off.  The paired kernel
+// takes no scratch.
 bool plan_gemm_pair(int M, int N, int K, int split0, int split1, int mode, int forced_bt, PairPlan* out);
 cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, const void* B1, const void* B2,
                              int split0, int split1, void* C, int M, int N, int K, int ldc, int mode, int32_t* status,
