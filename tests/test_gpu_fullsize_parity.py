@@ -43,7 +43,16 @@ pytestmark = pytest.mark.gpu
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 TOL = 2e-2
-MIN_OVERLAP = 0.99
+# Free-running selection against the oracle's sets.  A check layer selects from what the
+# previous check layer kept (gradual filtering), so one token that flips at the selection
+# boundary of layer 1 (deviations a few bf16 ulps apart) is counted again at every later
+# check layer.  Each layer's own decision is therefore measured on the pool both sides kept
+# at the layer before (CONDITIONAL: |S_gpu & S_orc & P| / |S_orc & P| with P the previous
+# layer's common set, the whole cached range at the first check layer), and the plain
+# overlap |S_gpu & S_orc| / |S_orc|, which carries the earlier layers' flips (four check
+# layers of ~0.5 % each at the Llama-70B shape), has the looser bound.
+MIN_CONDITIONAL_OVERLAP = 0.99
+MIN_OVERLAP = 0.97
 
 
 def _golden_module():
@@ -182,13 +191,24 @@ def _free(name, r):
     tag = MF.ratio_tag(r)
     ratios = [float(x) for x in gold[f"{tag}_schedule"]]
     reqs = g.blend(ratios, copy_stream=cs)
-    worst = 1.0
+    rows = []
     for q, req in enumerate(reqs):
         sets = _sets(req, cfg.n_layers)
+        pool = None  # tokens both sides kept at the previous check layer
         for i in _check_layers(gold, tag):
             ref = gold[f"{tag}_q{q}_set_l{i}"]
             assert len(sets[i]) == len(ref), (q, i)
-            ov = len(np.intersect1d(sets[i], ref)) / len(ref)
-            worst = min(worst, ov)
-            assert ov >= MIN_OVERLAP, (q, i, ov)
-    print(f"{name} {tag}: worst set overlap {worst:.4f}")
+            both = np.intersect1d(sets[i], ref)
+            ov = len(both) / len(ref)
+            if pool is None:
+                cond = ov
+            else:
+                ref_p = np.intersect1d(ref, pool)
+                cond = len(np.intersect1d(both, pool)) / max(1, len(ref_p))
+            rows.append((q, i, ov, cond))
+            pool = both
+    for q, i, ov, cond in rows:
+        print(f"{name} {tag} request {q} layer {i}: set overlap {ov:.4f}, on the common pool {cond:.4f}")
+    for q, i, ov, cond in rows:
+        assert cond >= MIN_CONDITIONAL_OVERLAP, (q, i, cond)
+        assert ov >= MIN_OVERLAP, (q, i, ov)
