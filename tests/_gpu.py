@@ -110,7 +110,7 @@ def forced_from_oracle(res, n_cached: int, n_layers: int, ratios):
     return out
 
 
-def bf16_operand_full_prefill(cfg, W, ids: np.ndarray, rounding: bool = True) -> torch.Tensor:
+def bf16_operand_full_prefill(cfg, W, ids: np.ndarray, rounding="all") -> torch.Tensor:
     """A plain-PyTorch full prefill on the GPU that rounds to bf16 exactly the operands a bf16
     tensor-core path must round, and computes everything else in fp32 (TF32 off): the
     normalised rows x entering each projection, q / k / v after RoPE (the cache's K and V),
@@ -120,13 +120,21 @@ def bf16_operand_full_prefill(cfg, W, ids: np.ndarray, rounding: bool = True) ->
 
     It shares no code with the library or the oracle (library routines: matmul, rms_norm,
     silu).  Its distance to the oracle's fp64 prefill is the rounding floor of bf16 operands
-    for the model's depth, against which the library's own error is judged.  rounding=False
-    gives the same prefill with no operand rounded (fp32 throughout).  Returns the hidden
-    states [N, d] (fp32)."""
+    for the model's depth, against which the library's own error is judged.  rounding="none"
+    (or False) gives the same prefill with no operand rounded (fp32 throughout);
+    rounding="kv" rounds only K and V, as a bf16 cache stores them (the oracle's model of the
+    path).  Returns the hidden states [N, d] (fp32)."""
     prev = torch.backends.cuda.matmul.allow_tf32
     torch.backends.cuda.matmul.allow_tf32 = False
     try:
-        bf = (lambda t: t.to(torch.bfloat16).to(torch.float32)) if rounding else (lambda t: t)  # noqa: E731
+        if rounding is True:
+            rounding = "all"
+        elif rounding is False:
+            rounding = "none"
+        rnd = lambda t: t.to(torch.bfloat16).to(torch.float32)  # noqa: E731
+        keep = lambda t: t  # noqa: E731
+        bf = rnd if rounding == "all" else keep
+        bkv = rnd if rounding in ("all", "kv") else keep
         dev = W["embed"].device
         t_ids = torch.from_numpy(np.asarray(ids, dtype=np.int64)).to(dev)
         N, d, H, Hkv, dh = len(ids), cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
@@ -146,8 +154,8 @@ def bf16_operand_full_prefill(cfg, W, ids: np.ndarray, rounding: bool = True) ->
         for lw in W["layers"][: cfg.n_layers]:
             x = bf(torch.nn.functional.rms_norm(h, (d,), eps=cfg.rms_eps))
             q = bf(rope((x @ lw["wq"].float().T).view(N, H, dh)))
-            k = bf(rope((x @ lw["wk"].float().T).view(N, Hkv, dh)))
-            v = bf((x @ lw["wv"].float().T).view(N, Hkv, dh))
+            k = bkv(rope((x @ lw["wk"].float().T).view(N, Hkv, dh)))
+            v = bkv((x @ lw["wv"].float().T).view(N, Hkv, dh))
             att = torch.empty(N, H, dh, device=dev)
             for g in range(Hkv):
                 s = torch.einsum("ngd,md->gnm", q[:, g * G:(g + 1) * G, :], k[:, g, :]) * scale

@@ -126,7 +126,7 @@ def _full(name):
     n = len(ids)
     rows = np.unique(np.concatenate([np.linspace(0, n - 1, 24).astype(np.int64), np.arange(n - 8, n)]))
     w16 = to_np(bf16_operand_full_prefill(cfg, g.W, ids))
-    w32 = to_np(bf16_operand_full_prefill(cfg, g.W, ids, rounding=False))
+    w32 = to_np(bf16_operand_full_prefill(cfg, g.W, ids, rounding="none"))
     FLOOR[name] = max_rel_err(w16[rows], w32[rows])
     out = g.eng.full_prefill(hd.ids_tensor(ids))
     ours = to_np(out["hidden"])
@@ -140,10 +140,14 @@ def _full(name):
             gold = {k: d[k] for k in d.files}
         assert int(gold["n_layers"]) == cfg.n_layers
         r_o, ref = gold["rows"], gold["hidden"].astype(np.float64)
+        # the oracle keeps K and V in the cache's dtype: the witness that rounds only those is
+        # the oracle's prefill up to fp32 arithmetic (and the rare K/V element whose fp32 and
+        # fp64 values round to neighbouring bf16 numbers)
+        wkv = to_np(bf16_operand_full_prefill(cfg, g.W, ids, rounding="kv"))
         err_ours = max_rel_err(ours[r_o], ref)
-        err_w32 = max_rel_err(w32[r_o], ref)
-        print(f"  vs the oracle's full prefill: library {err_ours:.4f}, unrounded witness {err_w32:.2e}")
-        assert err_w32 < 1e-3, err_w32  # the fp32 witness is the oracle's prefill to fp32 rounding
+        err_wkv = max_rel_err(wkv[r_o], ref)
+        print(f"  vs the oracle's full prefill: library {err_ours:.4f}, K/V-rounded witness {err_wkv:.2e}")
+        assert err_wkv < 5e-3, err_wkv
         assert err_ours <= tolerance(name), (err_ours, FLOOR[name])
         tok = int(out["first_token"].item())
         ids_top, logits = gold["top_ids"], gold["top_logits"]
