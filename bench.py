@@ -556,15 +556,21 @@ def measure_staging(wl, ratios, schedule, blend_staged_ms, full_ms, steps, peaks
     ids0, kh, vh = wl.host_store[wl.used[0]]
     dst = torch.empty_like(kh, device=wl.dev)
     torch.cuda.synchronize()
-    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(wl.copy_stream):
-        a_ev.record(wl.copy_stream)
-        for _ in range(3):
-            dst.copy_(kh, non_blocking=True)
-        b_ev.record(wl.copy_stream)
-    b_ev.synchronize()
+    # the link's bandwidth: the best of three bursts of three copies (the host link is shared
+    # with the box's other work; one slow burst is not the link)
+    best_ms = None
+    for _ in range(3):
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(wl.copy_stream):
+            a_ev.record(wl.copy_stream)
+            for _ in range(3):
+                dst.copy_(kh, non_blocking=True)
+            b_ev.record(wl.copy_stream)
+        b_ev.synchronize()
+        ms = a_ev.elapsed_time(b_ev)
+        best_ms = ms if best_ms is None else min(best_ms, ms)
     del dst
-    h2d_gbs = 3 * kh.numel() * kh.element_size() / (a_ev.elapsed_time(b_ev) * 1e-3) / 1e9
+    h2d_gbs = 3 * kh.numel() * kh.element_size() / (best_ms * 1e-3) / 1e9
     total_bytes = sum(2 * wl.host_store[s.chunk][1].numel() * wl.host_store[s.chunk][1].element_size()
                       for r in wl.req_idx for s in wl.spec.requests[r] if s.chunk >= 0)
     t_load = total_bytes / (h2d_gbs * 1e9) * 1e3
