@@ -104,7 +104,7 @@ struct Args {
   int32_t* status;
   // key-range splits: the n_paired longest tiles get two CTAs (unit = tile * Hkv + head, tile in
   // longest-first order), the others one (n_paired 0 or part_o null: one CTA per tile)
-  float* part_o;       // [unit][2][128][128] unnormalised O
+  float* part_o;       // [unit][2 ranges] x float4 [2 halves][16][128 rows]: unnormalised O
   float2* part_ml;     // [unit][2][128] (reference max, row sum)
   int* part_cnt;       // [unit] CTAs of the unit done (reset to 0 by the second)
   int n_paired;
@@ -127,6 +127,63 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr, uint32_t lbo) {
 // kind::f16, bf16 inputs, fp32 accumulator, M = 128, N = 128; B MN-major when b_mn
 __host__ __device__ constexpr uint32_t idesc(bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+// Key-range split epilogue of attn_tc_kernel, run by its 256 softmax threads (named
+// barrier 5; thread 64 is the first of them): this range's unnormalised O (ov, one row half at
+// the reference max m) and (m, row sum of both halves) go to its partial slot; the unit's CTA that
+// finishes second combines range 0 and range 1 in that order (whichever finished first),
+// normalises and stores.  Partials are float4 [slot][half][16][128 rows]: one warp instruction
+// stores or loads 512 contiguous bytes.  The release of the partials is the CTA barrier followed
+// by one thread's device-scope fence before its ticket; the merging CTA fences after its ticket.
+__device__ __forceinline__ void split_epilogue(const Args& a, int unit, int part, int half, int r, bool valid,
+                                               const uint32_t* ov, float m, float l_all, bf16* dst,
+                                               volatile int* merge_flag) {
+  const size_t mine = static_cast<size_t>(unit) * 2 + part, other = static_cast<size_t>(unit) * 2 + (part ^ 1);
+  float4* po = reinterpret_cast<float4*>(a.part_o) + (mine * 2 + half) * 16 * ROWS + r;
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    po[c * ROWS] = make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
+                               __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
+  if (half == 0) a.part_ml[mine * ROWS + r] = make_float2(m, l_all);
+  asm volatile("bar.sync 5, 256;" ::: "memory");
+  if (threadIdx.x == 64) {
+    __threadfence();
+    *merge_flag = atomicAdd(&a.part_cnt[unit], 1) == 1;
+    __threadfence();
+  }
+  asm volatile("bar.sync 5, 256;" ::: "memory");
+  if (!*merge_flag) return;
+  const float2 oml = __ldcg(&a.part_ml[other * ROWS + r]);
+  const float m0 = part == 0 ? m : oml.x, m1 = part == 0 ? oml.x : m;
+  const float l0 = part == 0 ? l_all : oml.y, l1 = part == 0 ? oml.y : l_all;
+  const float mm = fmaxf(m0, m1);
+  const float w0 = ex2(m0 - mm), w1 = ex2(m1 - mm);
+  const float ls = __fmaf_rn(l1, w1, __fmul_rn(l0, w0));
+  const float inv = ls > 0.f ? 1.f / ls : 0.f;
+  const float4* qo = reinterpret_cast<const float4*>(a.part_o) + (other * 2 + half) * 16 * ROWS + r;
+  if (valid) {
+#pragma unroll
+    for (int c0 = 0; c0 < 16; c0 += 8) {  // eight loads in flight before their sums
+      float4 x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = __ldcg(qo + (c0 + u) * ROWS);
+#pragma unroll
+      for (int u = 0; u < 8; u += 2) {
+        const float xo[8] = {x[u].x, x[u].y, x[u].z, x[u].w, x[u + 1].x, x[u + 1].y, x[u + 1].z, x[u + 1].w};
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float mine_v = __uint_as_float(ov[(c0 + u) * 4 + e]);
+          const float o0 = part == 0 ? mine_v : xo[e];
+          const float o1 = part == 0 ? xo[e] : mine_v;
+          f[e] = __fmul_rn(__fmaf_rn(o1, w1, __fmul_rn(o0, w0)), inv);
+        }
+        store8(dst + (c0 + u) * 4, f);
+      }
+    }
+  }
+  if (threadIdx.x == 64) a.part_cnt[unit] = 0;  // for the next launch
 }
 
 // Barriers (phase of use u of a two-slot barrier b[x & 1] is (x >> 1) & 1):
@@ -410,7 +467,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       const bool need = mx > m + RESCALE_LOG2;
       const float m_new = need ? mx : m;
       const float alpha = ex2(m - m_new);
-      if (__any_sync(0xffffffffu, need) && j > 0) {  // same rows, same decision in both halves
+      // O needs the rescale only in rows that already hold mass: a row that saw no key yet
+      // (the second key range of a split tile starts past some rows' positions) has O = 0
+      if (__any_sync(0xffffffffu, need && m > -1e29f) && j > 0) {  // same rows, same decision in both halves
         // O holds PV_0..PV_{j-1}: wait for the last of them, then scale this warp's part
         wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1);
         if (ok) {
@@ -496,7 +555,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
       // This CTA's key range: O unnormalised (at the reference max m) and (m, row sum) of every
       // row go to its partial slot; the CTA of the tile that finishes second adds the two
       // ranges (each scaled to the larger max), normalises and stores.
-      const size_t mine = static_cast<size_t>(unit) * 2 + part, other = static_cast<size_t>(unit) * 2 + (part ^ 1);
       uint32_t ov[64];
       if (ok) {
         tc_fence_after();
@@ -507,46 +565,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 64; ++e) ov[e] = 0u;
       }
-      float4* po = reinterpret_cast<float4*>(a.part_o + (mine * ROWS + r) * DH + half * 64);
-#pragma unroll
-      for (int c = 0; c < 64; c += 4)
-        po[c / 4] = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]), __uint_as_float(ov[c + 2]),
-                                __uint_as_float(ov[c + 3]));
-      if (half == 0) a.part_ml[mine * ROWS + r] = make_float2(m, l_all);
-      __threadfence();  // this thread's partial before the counter below
-      asm volatile("bar.sync 5, 256;" ::: "memory");  // the eight softmax warps
-      volatile int* second = wmaxpos + 4;
-      if (threadIdx.x == 64) *second = atomicAdd(&a.part_cnt[unit], 1) == 1;
-      asm volatile("bar.sync 5, 256;" ::: "memory");
-      if (*second) {
-        // part 0 and part 1 combined in that order whichever CTA merges, so results do not
-        // depend on which finished first
-        __threadfence();
-        const float2 oml = __ldcg(&a.part_ml[other * ROWS + r]);
-        const float m0 = part == 0 ? m : oml.x, m1 = part == 0 ? oml.x : m;
-        const float l0 = part == 0 ? l_all : oml.y, l1 = part == 0 ? oml.y : l_all;
-        const float mm = fmaxf(m0, m1);
-        const float w0 = ex2(m0 - mm), w1 = ex2(m1 - mm);
-        const float ls = __fmaf_rn(l1, w1, __fmul_rn(l0, w0));
-        const float inv = ls > 0.f ? 1.f / ls : 0.f;
-        const float4* qo = reinterpret_cast<const float4*>(a.part_o + (other * ROWS + r) * DH + half * 64);
-        if (valid) {
-#pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            const float4 x0 = __ldcg(qo + c / 4), x1 = __ldcg(qo + c / 4 + 1);
-            const float xo[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const float o0 = part == 0 ? __uint_as_float(ov[c + e]) : xo[e];
-              const float o1 = part == 0 ? xo[e] : __uint_as_float(ov[c + e]);
-              f[e] = __fmul_rn(__fmaf_rn(o1, w1, __fmul_rn(o0, w0)), inv);
-            }
-            store8(dst + c, f);
-          }
-        }
-        if (threadIdx.x == 64) a.part_cnt[unit] = 0;  // for the next launch
-      }
+      split_epilogue(a, unit, part, half, r, valid, ov, m, l_all, dst, reinterpret_cast<volatile int*>(wmaxpos + 4));
     } else if (ok && nb > 0) {
       tc_fence_after();
       const float inv = l_all > 0.f ? 1.f / l_all : 0.f;
