@@ -40,7 +40,7 @@ constexpr int MAX_STAGES = 12;
 constexpr int OFF_RING = 1024;            // after the barriers
 constexpr int SMEM_ALLOC = 232448;        // the per-block maximum (227 KiB), 1 KiB of it aligns the base
 constexpr int SMEM_USE = SMEM_ALLOC - 1024;
-constexpr int XCH_BYTES = 4480;           // SwiGLU exchange: 64 rows x 17 floats, rounded to 128 B
+constexpr int XCH_BYTES = 4608;           // SwiGLU exchange: 2 x 64 rows x 9 floats
 constexpr int F32_SLAB = 8 * ROWS * 4;    // 8 tokens x 128 features fp32
 constexpr int F32_SLAB_TOK = 8;
 constexpr int BF_SLAB = 16 * 64 * 2;      // 16 tokens x 64 features bf16
@@ -305,7 +305,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t acc_empty_lead = mapa_shared(smem_u32(acc_empty), lead);
     uint8_t* stg = smem + p.stg_off;
     const bool swig = p.mode == EPI_SWIGLU;
-    float* xch = reinterpret_cast<float*>(stg);  // SwiGLU: [64][17]
+    float* xg = reinterpret_cast<float*>(stg);  // SwiGLU: gate of tokens 8-15 [64][9]
+    float* xu = xg + 64 * 9;                     //         up of tokens 0-7 [64][9]
     uint8_t* slab0 = swig ? stg + XCH_BYTES : stg;
     const int slab_bytes = swig ? BF_SLAB : F32_SLAB;
     const int keep = p.slabs - 1;  // stores that may still read their slab when one is refilled
@@ -339,25 +340,30 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t tbase = tmem + static_cast<uint32_t>(b * ACC_STRIDE) + (static_cast<uint32_t>(quarter * 32) << 16);
       if (swig) {
         // lanes 0-63 hold the gate and lanes 64-127 the up projection of features
-        // f0 .. f0 + 63: the up warps pass their values through shared memory, the gate warps
-        // write SiLU(gate) * up as a 16-token x 64-feature bf16 tile, stored by one thread
+        // f0 .. f0 + 63; per 16 tokens the gate warps pass the gate of tokens 8-15 and the up
+        // warps the up of tokens 0-7 through shared memory, then the gate warps write
+        // SiLU(gate) * up of tokens 0-7 and the up warps of tokens 8-15 into a 16-token x
+        // 64-feature bf16 tile, stored by one thread
         const int f0 = wt * 128 + h * 64;
+        const int fr = r_loc & 63;
+        const bool gate_row = quarter < 2;
 #pragma unroll 1
         for (int c = 0; c < nt; c += 16, ++slab) {
           float v[16];
           tmem_ld16(tbase + c, v);
           bf16* tile = reinterpret_cast<bf16*>(last ? ring + (fresh++) * slab_bytes : slab0 + (slab % p.slabs) * slab_bytes);
           if (et == 0 && !last) bulk_wait_read_keep(keep);  // the store that last used this slab has read it
-          if (quarter >= 2) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) xch[(r_loc - 64) * 17 + j] = v[j];
-          }
+          for (int j = 0; j < 8; ++j) (gate_row ? xg : xu)[fr * 9 + j] = v[gate_row ? 8 + j : j];
           epi_bar();
-          if (quarter < 2) {
+          if (gate_row) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) tile[j * 64 + r_loc] = __float2bfloat16_rn(silu_f(v[j]) * xch[r_loc * 17 + j]);
-            fence_proxy_async_smem();
+            for (int j = 0; j < 8; ++j) tile[j * 64 + fr] = __float2bfloat16_rn(silu_f(v[j]) * xu[fr * 9 + j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) tile[(8 + j) * 64 + fr] = __float2bfloat16_rn(silu_f(xg[fr * 9 + j]) * v[8 + j]);
           }
+          fence_proxy_async_smem();
           epi_bar();
           if (et == 0) {
             tma_store_2d(&tmC, tile, f0, t0 + c);
@@ -492,7 +498,7 @@ static double pair_us(int M, int K, int w_tiles, int cl, int bt, int ksub, int c
   const double lat = 2200.0 / ((l.stages - 1) * ksub);
   const double kb = std::max(issue, lat);
   const double main = (K / 64) * kb;
-  const double epi = swiglu ? bt * 128.0 * 4.0 / 8.0 : bt * 128.0 * 4.0 / 24.0;
+  const double epi = swiglu ? bt * 96.0 : bt * 50.0;  // per token (measured: 10.5 us / 192, 4.9 us / 176)
   const double unit = std::max(main, epi);
   return (((units + clusters - 1) / clusters) * unit + 5000.0 + epi) / 1750.0;
 }
