@@ -153,11 +153,13 @@ def gemm_flops(cfg, rows_R, rows_S):
 
 def gemm_layer_bytes(cfg, R, S):
     """Bytes the projection GEMMs of one layer must move: weights once, A read, C written
-    (fp32 q|k|v; residual read + written; bf16 SwiGLU output)."""
+    (q|k|v in fp32 where the layer checks its set (R != S), else rotated q, k, v in the model
+    dtype straight from the epilogue; residual read + written; bf16 SwiGLU output)."""
     d, qw, kvw, f = cfg.d_model, cfg.q_width, cfg.kv_width, cfg.ffn_dim
     es = 2 if cfg.dtype == "bf16" else 4
+    qkv_es = es if R == S else 4
     return (es * ((qw + 2 * kvw) * d + qw * d + 2 * f * d + f * d)
-            + R * d * es + R * (qw + 2 * kvw) * 4
+            + R * d * es + R * (qw + 2 * kvw) * qkv_es
             + S * qw * es + 2 * S * d * 4
             + S * d * es + S * f * es
             + S * f * es + 2 * S * d * 4)

@@ -284,6 +284,14 @@ cb_status cb_gemm_set_pairing(int pairing);
  * buffer, a negative size or an unknown epilogue. */
 cb_status cb_gemm_describe(int M, int N, int K, int epilogue, size_t scratch_bytes, char* buf, size_t len);
 
+/* Fused QKV of the bf16 blend, process-wide (a tuning and test hook; default 1): 1 runs,
+ * in a layer whose recomputed set is not re-selected (no check), the Q/K/V projection with
+ * RoPE and the scatter of K and V into the fused cache in the GEMM's epilogue when the paired
+ * GEMM has a plan for the shape (head_dim 128); 0 runs the projection and the post-QKV kernel
+ * separately.  Both compute the same values in the same order.  Other values:
+ * CB_ERR_INVALID_ARG. */
+cb_status cb_set_qkv_fusion(int enabled);
+
 /* Query tiles per CTA of the bf16 attention, process-wide (a tuning and test hook;
  * default 0).  0: two 128-row tiles of one KV head per CTA when a launch's tile pairs
  * times the KV heads fill the SMs (the tensor core then works for one tile while the

@@ -26,7 +26,7 @@ EXPORTED = ("cb_create", "cb_destroy", "cb_status_string", "cb_last_error", "cb_
             "cb_blend_prefill",
             "cb_full_prefill", "cb_blend_begin", "cb_fetch_kv", "cb_synchronize", "cb_prefill_layer",
             "cb_blend_layer", "cb_blend_finish", "cb_get_status", "cb_plan_counts", "cb_set_profiling",
-            "cb_get_profile", "cb_get_layer_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_noalloc_scratch_used", "cb_gemm_get_status", "cb_gemm_set_orientation", "cb_gemm_set_pairing", "cb_gemm_describe", "cb_attention_set_tiles",
+            "cb_get_profile", "cb_get_layer_profile", "cb_gemm_noalloc", "cb_gemm_noalloc_error", "cb_gemm_noalloc_scratch_used", "cb_gemm_get_status", "cb_gemm_set_orientation", "cb_gemm_set_pairing", "cb_gemm_describe", "cb_attention_set_tiles", "cb_set_qkv_fusion",
             "cb_set_launch_overlap", "cb_codec_layer_bytes", "cb_kv_encode", "cb_kv_decode", "cb_register_chunk_codec",
             "cb_set_staging", "cb_chunk_hash", "cb_chunk_info_of", "cb_plan_loading", "cb_decode_step",
             "cb_ratio_schedule", "cb_k_for_ratio")
@@ -124,6 +124,7 @@ def load_library(path: str = LIB_PATH):
         "cb_gemm_set_pairing": (st, [C.c_int]),
         "cb_gemm_describe": (st, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_size_t, C.c_char_p, C.c_size_t]),
         "cb_attention_set_tiles": (st, [C.c_int]),
+        "cb_set_qkv_fusion": (st, [C.c_int]),
         "cb_set_launch_overlap": (st, [C.c_int]),
         "cb_gemm_noalloc": (st, [vp, vp, vp, vp, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp]),
         "cb_gemm_noalloc_error": (C.c_char_p, []),
@@ -280,6 +281,12 @@ def cb_gemm_describe(M: int, N: int, K: int, epilogue: int, scratch_bytes: int =
     buf = C.create_string_buffer(256)
     _check(load_library().cb_gemm_describe(int(M), int(N), int(K), int(epilogue), int(scratch_bytes), buf, 256))
     return buf.value.decode()
+
+
+def cb_set_qkv_fusion(enabled: bool) -> None:
+    """Process-wide: Q/K/V projection with RoPE and the K/V scatter in one launch in the
+    layers without a check (default), or the projection and the post-QKV kernel (tests)."""
+    _check(load_library().cb_set_qkv_fusion(1 if enabled else 0))
 
 
 def cb_attention_set_tiles(tiles: int) -> None:

@@ -889,12 +889,22 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   int32_t* reqR = ctx->req[cur];
   float* hR = ctx->h[cur];
   // 1. QKV of R: x = RMSNorm(h_R); [q | k | v] = x W^T (RoPE of q and k is applied where
-  //    they are consumed: the deviation and the scatter)
+  //    they are consumed: the deviation and the scatter).  A layer without a check keeps its
+  //    set, so the scatter needs no compaction: RoPE and the scatter run in the GEMM's
+  //    epilogue when the paired kernel has a plan for the shape.
   {
     PhaseScope ps(ctx, CB_PH_NORM, s, 1);
     CB_CUDA(ctx, launch_rmsnorm(hR, Rn, d, c.rms_eps, ctx->x, c.dtype, s));
   }
-  {
+  bool fused = false;
+  if (!b.check[i] && c.dtype == CB_BF16 && dh == 128 && qkv_fusion()) {
+    PhaseScope ps(ctx, CB_PH_QKV, s, 1);
+    const QkvRope qr{posR, reqR, ctx->d_reqs, ctx->rope, i, c.max_positions, ctx->q, qw, kvw};
+    const cudaError_t e = launch_qkv_rope_gemm(ctx->x, ctx->wq[i], ctx->wk[i], ctx->wv[i], Rn, d, qr, ctx->status, s);
+    if (e != cudaErrorNotSupported) CB_CUDA(ctx, e);
+    fused = e == cudaSuccess;
+  }
+  if (!fused) {
     PhaseScope ps(ctx, CB_PH_QKV, s, 1);
     CB_CUDA(ctx, launch_gemm(ctx->x, ctx->wq[i], ctx->wk[i], ctx->wv[i], qw, qw + kvw, ctx->qkv, Rn, qw + 2 * kvw, d,
                              qw + 2 * kvw, 0, c.dtype, ctx->status, ctx->gemm_scratch, ctx->gemm_scratch_bytes, s));
@@ -925,7 +935,7 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
                                    c.max_positions, c.dtype, ctx->q, hR, hS, d, ctx->status, s));
     }
     b.cur ^= 1;
-  } else {
+  } else if (!fused) {
     PhaseScope ps(ctx, CB_PH_SCATTER, s, 1);
     CB_CUDA(ctx, launch_post_qkv(ctx->qkv, Sn, nullptr, posS, reqS, ctx->d_reqs, i, H, Hkv, dh, ctx->rope,
                                  c.max_positions, c.dtype, ctx->q, hR, hR, d, ctx->status, s));
@@ -1334,6 +1344,12 @@ size_t cb_gemm_scratch_size(void) { return gemm_scratch_bytes(); }
 
 cb_status cb_set_launch_overlap(int enabled) {
   cb::set_launch_overlap(enabled != 0);
+  return CB_OK;
+}
+
+cb_status cb_set_qkv_fusion(int enabled) {
+  if (enabled != 0 && enabled != 1) return fail(nullptr, CB_ERR_INVALID_ARG, "enabled must be 0 or 1");
+  set_qkv_fusion(enabled != 0);
   return CB_OK;
 }
 

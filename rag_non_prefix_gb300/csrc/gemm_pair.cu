@@ -41,14 +41,21 @@ constexpr int OFF_RING = 1024;            // after the barriers
 constexpr int SMEM_ALLOC = 232448;        // the per-block maximum (227 KiB), 1 KiB of it aligns the base
 constexpr int SMEM_USE = SMEM_ALLOC - 1024;
 constexpr int XCH_BYTES = 4608;           // SwiGLU exchange: 2 x 64 rows x 9 floats
+// RoPE epilogue: exchange of 128 rows x 17 floats, the tile's positions and its K/V destination rows
+constexpr int XCH_ROPE = 128 * 17 * 4 + 256 * 4 + 256 * 8;
 constexpr int F32_SLAB = 8 * ROWS * 4;    // 8 tokens x 128 features fp32
 constexpr int F32_SLAB_TOK = 8;
 constexpr int BF_SLAB = 16 * 64 * 2;      // 16 tokens x 64 features bf16
 constexpr uint32_t TMEM_COLS = 512;       // two accumulators of up to 256 columns
 constexpr int ACC_STRIDE = 256;
 
-// Shared memory the epilogue needs at the least (two slabs, and the SwiGLU exchange).
-__host__ __device__ constexpr int min_staging(bool swiglu) { return swiglu ? XCH_BYTES + 2 * BF_SLAB : 2 * F32_SLAB; }
+// The epilogue's exchange area and output slab (a bf16 16-token tile of the RoPE epilogue is
+// as large as an fp32 8-token slab), and the shared memory it needs at the least.
+__host__ __device__ constexpr int epi_xch(int mode) {
+  return mode == EPI_SWIGLU ? XCH_BYTES : mode == EPI_QKV_ROPE ? XCH_ROPE : 0;
+}
+__host__ __device__ constexpr int epi_slab(int mode) { return mode == EPI_SWIGLU ? BF_SLAB : F32_SLAB; }
+__host__ __device__ constexpr int min_staging(int mode) { return epi_xch(mode) + 2 * epi_slab(mode); }
 
 struct Params {
   int M, N, K, mode;
@@ -66,6 +73,7 @@ struct Params {
   int stage_bytes;     // ksub x (16 KiB of weights + bt/2 x 128 B of tokens), per CTA
   int stg_off;         // epilogue staging: offset (after the ring)
   int slabs;           // output slabs in the staging area (2, 4, 8 or 16)
+  QkvRope qr;          // EPI_QKV_ROPE only
 };
 
 // The idx-th unit of cluster cid, round-robin (false when there is none).
@@ -307,8 +315,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
     const bool swig = p.mode == EPI_SWIGLU;
     float* xg = reinterpret_cast<float*>(stg);  // SwiGLU: gate of tokens 8-15 [64][9]
     float* xu = xg + 64 * 9;                     //         up of tokens 0-7 [64][9]
-    uint8_t* slab0 = swig ? stg + XCH_BYTES : stg;
-    const int slab_bytes = swig ? BF_SLAB : F32_SLAB;
+    float* xr = reinterpret_cast<float*>(stg);   // RoPE: [128][17], then the unit's positions [256]
+    int* upos = reinterpret_cast<int*>(xr + 128 * 17);
+    bf16** udst = reinterpret_cast<bf16**>(upos + 256);
+    uint8_t* slab0 = stg + epi_xch(p.mode);
+    const int slab_bytes = epi_slab(p.mode);
     const int keep = p.slabs - 1;  // stores that may still read their slab when one is refilled
     int slab = 0;                  // output slabs issued so far
     int u = 0, nx = 0;
@@ -318,7 +329,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
       // leaves idle (every copy landed and was read): one fresh slab each, none waited for
       // (measured on GB300: 1-2 % per launch, the last unit's epilogue being the tail).
       const bool last = !get_unit(p, cid, NC, i + 1, nx) &&
-                        (swig ? (p.bt / 16) * BF_SLAB : (p.bt / F32_SLAB_TOK) * F32_SLAB) <= p.stg_off - OFF_RING;
+                        (swig ? (p.bt / 16) * BF_SLAB
+                              : (p.mode == EPI_QKV_ROPE ? p.bt / 16 : p.bt / F32_SLAB_TOK) * F32_SLAB) <=
+                            p.stg_off - OFF_RING;
       int fresh = 0;  // ring slabs used by the last unit
       const uint32_t use = static_cast<uint32_t>(i >> 1);
       bool ok = true;
@@ -368,6 +381,97 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           if (et == 0) {
             tma_store_2d(&tmC, tile, f0, t0 + c);
             bulk_commit();
+          }
+        }
+      } else if (p.mode == EPI_QKV_ROPE) {
+        // This CTA's 128 rows are one head of q, k or v.  Per 16 tokens: q and k exchange
+        // their rows through shared memory (dimension i pairs with i + 64), rotate at each
+        // token's position and round to bf16 into a 16-token x 128-dimension tile; q's tile is
+        // one TMA store into q_out, k's and v's rows are copied to the fused cache row of each
+        // token's position (256 contiguous bytes per token).
+        const int f0 = wt * 256 + h * 128;
+        const int kind = f0 < p.split0 ? 0 : f0 < p.split1 ? 1 : 2;  // q, k, v
+        const int head = (kind == 0 ? f0 : kind == 1 ? f0 - p.split0 : f0 - p.split1) / ROWS;
+        const int di = r_loc & 63;
+        const QkvRope& qr = p.qr;
+        // Once per tile: the tokens' positions (clamped for the table; out-of-range rows are not
+        // stored) and, for k and v, each token's destination row in the fused cache (null when
+        // the position is out of range).  (cos, sin) of a round's 16 tokens are loaded two
+        // rounds ahead.
+        for (int x = et; x < nt; x += 128) {
+          const int pos = __ldg(qr.s_pos + t0 + x);
+          upos[x] = min(max(pos, 0), qr.max_pos - 1);
+          if (kind > 0) {
+            const ReqDev rq = qr.reqs[__ldg(qr.s_req + t0 + x)];
+            bf16* row = nullptr;
+            if (pos >= 0 && pos < rq.n_tokens && pos < qr.max_pos) {
+              row = static_cast<bf16*>(kind == 1 ? rq.k : rq.v) + static_cast<size_t>(qr.layer) * rq.layer_stride +
+                    static_cast<size_t>(pos) * qr.kvw + head * ROWS;
+            } else {
+              set_status(p.status, ST_RANGE);
+            }
+            udst[x] = row;
+          }
+        }
+        epi_bar();
+        float2 cs1[16], cs2[16];
+        if (kind < 2) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cs1[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(j, nt - 1)]) * 64 + di);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cs2[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(16 + j, nt - 1)]) * 64 + di);
+        }
+#pragma unroll 1
+        for (int c = 0; c < nt; c += 16, ++slab) {
+          float v[16];
+          tmem_ld16(tbase + c, v);
+          bf16* tile = reinterpret_cast<bf16*>(last ? ring + (fresh++) * slab_bytes : slab0 + (slab % p.slabs) * slab_bytes);
+          if (et == 0 && !last && kind == 0) bulk_wait_read_keep(keep);  // the store that last used this slab has read it
+          if (kind < 2) {
+            float2 cs[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              cs[j] = cs1[j];
+              cs1[j] = cs2[j];
+            }
+            if (c + 32 < nt) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                cs2[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(c + 32 + j, nt - 1)]) * 64 + di);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xr[r_loc * 17 + j] = v[j];
+            epi_bar();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              // rows i and i + 64 of the head: (a, b) -> (a cos - b sin, b cos + a sin)
+              const float a = r_loc < 64 ? v[j] : xr[(r_loc - 64) * 17 + j];
+              const float b = r_loc < 64 ? xr[(r_loc + 64) * 17 + j] : v[j];
+              const float o = r_loc < 64 ? a * cs[j].x - b * cs[j].y : b * cs[j].x + a * cs[j].y;
+              tile[j * ROWS + r_loc] = __float2bfloat16_rn(o);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) tile[j * ROWS + r_loc] = __float2bfloat16_rn(v[j]);
+          }
+          fence_proxy_async_smem();
+          epi_bar();
+          if (kind == 0) {
+            if (et == 0) {
+              tma_store_2d(&tmC, tile, head * ROWS, t0 + c);
+              bulk_commit();
+            }
+          } else {
+            // two tokens per thread, 16 bytes of each
+            const int ch = et & 15;
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+              const int j = (et >> 4) + pass * 8;
+              if (c + j < nt) {
+                bf16* row = udst[c + j];
+                if (row) *reinterpret_cast<uint4*>(row + ch * 8) = *reinterpret_cast<const uint4*>(tile + j * ROWS + ch * 8);
+              }
+            }
           }
         }
       } else {
@@ -429,12 +533,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
 struct Layout {
   int stage_bytes, stages, stg_off, slabs;
 };
-__host__ inline Layout layout(int bt, int ksub, bool swiglu) {
+__host__ inline Layout layout(int bt, int ksub, int mode) {
   Layout l{};
   l.stage_bytes = ksub * (A_ATOM + bt * 64);
-  l.stages = std::min(MAX_STAGES, (SMEM_USE - OFF_RING - min_staging(swiglu)) / l.stage_bytes);
+  l.stages = std::min(MAX_STAGES, (SMEM_USE - OFF_RING - min_staging(mode)) / l.stage_bytes);
   l.stg_off = OFF_RING + l.stages * l.stage_bytes;
-  const int room = (SMEM_USE - l.stg_off - (swiglu ? XCH_BYTES : 0)) / (swiglu ? BF_SLAB : F32_SLAB);
+  const int room = (SMEM_USE - l.stg_off - epi_xch(mode)) / epi_slab(mode);
   l.slabs = room >= 16 ? 16 : room >= 8 ? 8 : room >= 4 ? 4 : 2;  // the waits take 1, 3, 7 or 15 in flight
   return l;
 }
@@ -488,8 +592,9 @@ static int max_clusters(int cl) {
 // overlaps the next unit's main loop unless it is longer, and the first stage's arrival
 // (~5000 cycles) and the last unit's epilogue are exposed.  The epilogue writes about 24
 // bytes per cycle (fp32 slabs) or the SwiGLU tile at about 8 bytes of input per cycle.
-static double pair_us(int M, int K, int w_tiles, int cl, int bt, int ksub, int clusters, bool swiglu) {
-  const pr::Layout l = pr::layout(bt, ksub, swiglu);
+static double pair_us(int M, int K, int w_tiles, int cl, int bt, int ksub, int clusters, int mode) {
+  const bool swiglu = mode == EPI_SWIGLU;
+  const pr::Layout l = pr::layout(bt, ksub, mode);
   const int ppc = cl / 2;
   const int tok_tiles = (M + bt - 1) / bt;
   const int groups = (tok_tiles + ppc - 1) / ppc;
@@ -524,8 +629,8 @@ bool plan_gemm_pair(int M, int N, int K, int split0, int split1, int mode, int f
     for (int bt = 16; bt <= 256; bt += 16) {
       if (forced_bt >= 16 && bt != forced_bt) continue;
       for (int ksub = 1; ksub <= 2; ++ksub) {
-        if (K % (64 * ksub) != 0 || pr::layout(bt, ksub, swiglu).stages < 3) continue;
-        const double us = pair_us(M, K, w_tiles, cl, bt, ksub, clusters, swiglu);
+        if (K % (64 * ksub) != 0 || pr::layout(bt, ksub, mode).stages < 3) continue;
+        const double us = pair_us(M, K, w_tiles, cl, bt, ksub, clusters, mode);
         if (us < best.us) {
           best.us = us;
           best.cl = cl;
@@ -557,7 +662,10 @@ static cudaError_t launch_pair_cl(const CUtensorMap& x, const CUtensorMap& w0, c
 
 cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, const void* B1, const void* B2,
                              int split0, int split1, void* C, int M, int N, int K, int ldc, int mode, int32_t* status,
-                             cudaStream_t s) {
+                             cudaStream_t s, const QkvRope* qr) {
+  if (mode == EPI_QKV_ROPE &&
+      (!qr || split0 != qr->q_width || split1 != qr->q_width + qr->kvw || N != split1 + qr->kvw || qr->kvw % 128 != 0))
+    return cudaErrorInvalidValue;
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   const bool swiglu = mode == EPI_SWIGLU;
@@ -581,13 +689,20 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
       return cudaErrorInvalidValue;
     if (r2 > 0 && !encode_tmap(&mw2, BF, B2, K, r2, static_cast<uint64_t>(K) * 2, pr::BK, 64, SW))
       return cudaErrorInvalidValue;
-    // fp32 C [M][ldc]: 8 tokens x 128 features per store (16-byte aligned, ldc % 4 == 0)
-    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || ldc % 4 != 0 ||
-        !encode_tmap(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, static_cast<uint64_t>(ldc) * 4, pr::ROWS,
-                     pr::F32_SLAB_TOK, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (mode == EPI_QKV_ROPE) {
+      // bf16 q_out [M][q_width]: 16 tokens x one head of 128 per store
+      if ((reinterpret_cast<uintptr_t>(qr->q_out) & 15u) != 0 ||
+          !encode_tmap(&mc, BF, qr->q_out, qr->q_width, M, static_cast<uint64_t>(qr->q_width) * 2, pr::ROWS, 16,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    } else if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || ldc % 4 != 0 ||
+               !encode_tmap(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, static_cast<uint64_t>(ldc) * 4, pr::ROWS,
+                            pr::F32_SLAB_TOK, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      // fp32 C [M][ldc]: 8 tokens x 128 features per store (16-byte aligned, ldc % 4 == 0)
       return cudaErrorInvalidValue;
+    }
   }
-  const pr::Layout l = pr::layout(g.bt, g.ksub, swiglu);
+  const pr::Layout l = pr::layout(g.bt, g.ksub, mode);
   if (l.stages < 3) return cudaErrorInvalidValue;
   pr::Params p{};
   p.M = M;
@@ -609,8 +724,25 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
   p.stages = l.stages;
   p.stg_off = l.stg_off;
   p.slabs = l.slabs;
+  if (qr) p.qr = *qr;
   if (g.cl == 4) return launch_pair_cl<4>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
   return launch_pair_cl<2>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
 }
 
+// Process-wide: the blend's uncompacted layers take QKV, RoPE and the scatter in one launch
+// (default), or the GEMM and the post-QKV kernel (tests compare the two, tuning).
+static std::atomic<bool> g_qkv_fusion{true};
+void set_qkv_fusion(bool enabled) { g_qkv_fusion.store(enabled); }
+bool qkv_fusion() { return g_qkv_fusion.load(); }
+
+cudaError_t launch_qkv_rope_gemm(const void* x, const void* wq, const void* wk, const void* wv, int M, int d,
+                                 const QkvRope& qr, int32_t* status, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  const int N = qr.q_width + 2 * qr.kvw;
+  PairPlan pp;
+  if (gemm_pairing() == 1 || !plan_gemm_pair(M, N, d, qr.q_width, qr.q_width + qr.kvw, EPI_QKV_ROPE, 0, &pp))
+    return cudaErrorNotSupported;
+  return launch_gemm_pair(pp, x, wq, wk, wv, qr.q_width, qr.q_width + qr.kvw, nullptr, M, N, d, N, EPI_QKV_ROPE, status,
+                          s, &qr);
+}
 }  // namespace cb

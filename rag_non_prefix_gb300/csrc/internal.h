@@ -216,6 +216,22 @@ cudaError_t launch_argmax(const float* logits, int n_req, int vocab, int32_t* co
 cudaError_t launch_write_hidden(const float* h, const int32_t* s_pos, int row0, int n, int d, float* out,
                                 cudaStream_t s);
 
+enum { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_SWIGLU = 2, EPI_QKV_ROPE = 3 };
+
+// EPI_QKV_ROPE (the paired GEMM only): the outputs are [q | k | v] of head_dim 128; q and k
+// are rotated at each row's position (RoPE, the table's (cos, sin) of pairs i and i + 64), q
+// goes to q_out [M][q_width] in bf16 and k, v to the fused cache row of that position, as the
+// post-QKV scatter does for an uncompacted set.
+struct QkvRope {
+  const int32_t* s_pos;  // [M] token positions
+  const int32_t* s_req;  // [M] request of each row
+  const ReqDev* reqs;
+  const float2* rope;    // [max_pos][64]
+  int layer, max_pos;
+  void* q_out;
+  int q_width, kvw;
+};
+
 // Paired GEMM (gemm_pair.cu): clusters of one or two CTA pairs, weights on the tensor
 // core's rows, 256 weight rows x bt tokens per pair.
 struct PairPlan {
@@ -232,13 +248,18 @@ struct PairPlan {
 bool plan_gemm_pair(int M, int N, int K, int split0, int split1, int mode, int forced_bt, PairPlan* out);
 cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, const void* B1, const void* B2,
                              int split0, int split1, void* C, int M, int N, int K, int ldc, int mode, int32_t* status,
-                             cudaStream_t s);
+                             cudaStream_t s, const QkvRope* qr = nullptr);
+// [q | k | v] = x [Wq; Wk; Wv]^T with RoPE and the scatter in the epilogue (EPI_QKV_ROPE) on CTA
+// pairs; cudaErrorNotSupported when the pairs have no plan for the shape (the caller then runs
+// the GEMM and the post-QKV scatter).
+cudaError_t launch_qkv_rope_gemm(const void* x, const void* wq, const void* wk, const void* wv, int M, int d,
+                                 const QkvRope& qr, int32_t* status, cudaStream_t s);
+void set_qkv_fusion(bool enabled);
+bool qkv_fusion();
 void gemm_set_pairing(int m);  // 0 model, 1 never, 2 clusters of one pair, 4 of two pairs
 // launch_gemm's schedule for a bf16 GEMM (single-tensor B) as text; snprintf's return value
 int gemm_describe(int M, int N, int K, int mode, size_t scratch_bytes, char* buf, size_t len);
 int gemm_pairing();
-enum { EPI_STORE_F32 = 0, EPI_ADD_F32 = 1, EPI_SWIGLU = 2 };
-
 // tensor-map encoder (driver entry point, resolved once)
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
                  uint64_t pitch, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);

@@ -108,6 +108,10 @@ def test_tuning_hooks_reject_bad_values(lib):
         assert lib.cb_attention_set_tiles(bad) == 1  # CB_ERR_INVALID_ARG
     for ok in (0, 1, 2, 0):
         assert lib.cb_attention_set_tiles(ok) == 0
+    for bad in (-1, 2):
+        assert lib.cb_set_qkv_fusion(bad) == 1
+    for ok in (0, 1):
+        assert lib.cb_set_qkv_fusion(ok) == 0
     assert lib.cb_gemm_set_orientation(3) == 1 and lib.cb_gemm_set_orientation(0) == 0
     for bad in (-1, 3, 5, 8):
         assert lib.cb_gemm_set_pairing(bad) == 1

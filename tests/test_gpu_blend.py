@@ -133,6 +133,37 @@ def _forced_bf16(small_bf16):
     assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 2e-2
 
 
+@pytest.mark.parametrize("name,schedule", [("small_bf16", "gradual"), ("small_mha_bf16", "fixed")])
+def test_bf16_blend_fused_qkv_matches_separate_kernels(name, schedule):
+    """The layers without a check run Q/K/V, RoPE and the K/V scatter in the paired GEMM's
+    epilogue; with the paired GEMM forced in both runs, the blend's sets, hidden rows and first
+    token are bit for bit those of the projection followed by the post-QKV kernel (the same
+    sums, the same rotation arithmetic, the same roundings).  The fixed schedule checks only
+    layer 1, so every other layer takes the fused path."""
+    spec = hz.workload(name)
+    if schedule != spec.schedule:
+        spec = hz.make_prompt(name, 12, [96, 128], 24, spec.ratio, schedule, "zipf", name=name + "_fixed")
+    g = GpuWorkload(spec)
+    cfg = spec.cfg
+    ratios = [float(x) for x in orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)]
+    outs = []
+    cb.cb_gemm_set_pairing(2)
+    try:
+        for fused in (True, False):
+            cb.cb_set_qkv_fusion(fused)
+            req = g.blend(ratios)[0]
+            torch.cuda.synchronize()
+            outs.append((to_np(req["hidden"]).copy(), _sets(req, cfg), int(req["first_token"].item())))
+    finally:
+        cb.cb_set_qkv_fusion(True)
+        cb.cb_gemm_set_pairing(0)
+    (h1, s1, t1), (h2, s2, t2) = outs
+    assert np.array_equal(h1, h2)
+    assert t1 == t2
+    for i in range(cfg.n_layers):
+        assert np.array_equal(s1[i], s2[i])
+
+
 def test_bf16_blend_long_context_matches_oracle_and_repeats():
     """A 2176-token prompt on the reduced bf16 model: tiles reach 17 key blocks, so the
     attention of every layer splits its long tiles into two key ranges merged on the device.
