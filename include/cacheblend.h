@@ -286,10 +286,10 @@ cb_status cb_gemm_describe(int M, int N, int K, int epilogue, size_t scratch_byt
 
 /* Fused QKV of the bf16 blend, process-wide (a tuning and test hook; default 1): 1 runs,
  * in a layer whose recomputed set is not re-selected (no check), the Q/K/V projection with
- * RoPE and the scatter of K and V into the fused cache in the GEMM's epilogue when the paired
- * GEMM has a plan for the shape (head_dim 128); 0 runs the projection and the post-QKV kernel
- * separately.  Both compute the same values in the same order.  Other values:
- * CB_ERR_INVALID_ARG. */
+ * RoPE and the scatter of K and V into the fused cache in the GEMM's epilogue wherever the
+ * projection runs on CTA pairs (head_dim 128), with the projection's own plan; 0 runs the
+ * projection and the post-QKV kernel separately.  Both compute the same values in the same
+ * order.  Other values: CB_ERR_INVALID_ARG. */
 cb_status cb_set_qkv_fusion(int enabled);
 
 /* Query tiles per CTA of the bf16 attention, process-wide (a tuning and test hook;

@@ -891,7 +891,7 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   // 1. QKV of R: x = RMSNorm(h_R); [q | k | v] = x W^T (RoPE of q and k is applied where
   //    they are consumed: the deviation and the scatter).  A layer without a check keeps its
   //    set, so the scatter needs no compaction: RoPE and the scatter run in the GEMM's
-  //    epilogue when the paired kernel has a plan for the shape.
+  //    epilogue where the projection runs on CTA pairs.
   {
     PhaseScope ps(ctx, CB_PH_NORM, s, 1);
     CB_CUDA(ctx, launch_rmsnorm(hR, Rn, d, c.rms_eps, ctx->x, c.dtype, s));
@@ -900,7 +900,8 @@ cb_status layer_impl(cb_ctx* ctx, int i, cudaStream_t s) {
   if (!b.check[i] && c.dtype == CB_BF16 && dh == 128 && qkv_fusion()) {
     PhaseScope ps(ctx, CB_PH_QKV, s, 1);
     const QkvRope qr{posR, reqR, ctx->d_reqs, ctx->rope, i, c.max_positions, ctx->q, qw, kvw};
-    const cudaError_t e = launch_qkv_rope_gemm(ctx->x, ctx->wq[i], ctx->wk[i], ctx->wv[i], Rn, d, qr, ctx->status, s);
+    const cudaError_t e = launch_qkv_rope_gemm(ctx->x, ctx->wq[i], ctx->wk[i], ctx->wv[i], Rn, d, qr, ctx->status,
+                                               ctx->gemm_scratch, ctx->gemm_scratch_bytes, s);
     if (e != cudaErrorNotSupported) CB_CUDA(ctx, e);
     fused = e == cudaSuccess;
   }

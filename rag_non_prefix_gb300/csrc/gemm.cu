@@ -1027,6 +1027,15 @@ static bool use_pair(const GemmPlan& g, int M, int N, int K, int split0, int spl
   return pm >= 2 || pp->us < 1.2 * g.us + 8.0;
 }
 
+// The paired plan launch_gemm takes for this bf16 store-mode GEMM (false when it would run the
+// GEMV or the single-CTA kernel).
+bool gemm_store_pair_plan(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, int M,
+                          int N, int K, const void* scratch, size_t scratch_bytes, PairPlan* pp) {
+  if (M <= 0 || gemv_applies(M, K, CB_BF16, A, B0, B1, B2)) return false;
+  const GemmPlan g = plan_gemm(M, N, K, split0, split1, scratch_slots(scratch, scratch_bytes));
+  return use_pair(g, M, N, K, split0, split1, EPI_STORE_F32, pp);
+}
+
 // Scratch bytes the schedule of launch_gemm would use for a single-tensor B of N output
 // columns with unlimited scratch (0 when the shape runs data-parallel).
 size_t gemm_scratch_needed(int N, int M, int K, cb_dtype dt) {

@@ -736,11 +736,13 @@ void set_qkv_fusion(bool enabled) { g_qkv_fusion.store(enabled); }
 bool qkv_fusion() { return g_qkv_fusion.load(); }
 
 cudaError_t launch_qkv_rope_gemm(const void* x, const void* wq, const void* wk, const void* wv, int M, int d,
-                                 const QkvRope& qr, int32_t* status, cudaStream_t s) {
+                                 const QkvRope& qr, int32_t* status, const void* scratch, size_t scratch_bytes,
+                                 cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   const int N = qr.q_width + 2 * qr.kvw;
   PairPlan pp;
-  if (gemm_pairing() == 1 || !plan_gemm_pair(M, N, d, qr.q_width, qr.q_width + qr.kvw, EPI_QKV_ROPE, 0, &pp))
+  if (!gemm_store_pair_plan(x, wq, wk, wv, qr.q_width, qr.q_width + qr.kvw, M, N, d, scratch, scratch_bytes, &pp) ||
+      pr::layout(pp.bt, pp.ksub, EPI_QKV_ROPE).stages < 3)
     return cudaErrorNotSupported;
   return launch_gemm_pair(pp, x, wq, wk, wv, qr.q_width, qr.q_width + qr.kvw, nullptr, M, N, d, N, EPI_QKV_ROPE, status,
                           s, &qr);

@@ -249,11 +249,15 @@ bool plan_gemm_pair(int M, int N, int K, int split0, int split1, int mode, int f
 cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, const void* B1, const void* B2,
                              int split0, int split1, void* C, int M, int N, int K, int ldc, int mode, int32_t* status,
                              cudaStream_t s, const QkvRope* qr = nullptr);
-// [q | k | v] = x [Wq; Wk; Wv]^T with RoPE and the scatter in the epilogue (EPI_QKV_ROPE) on CTA
-// pairs; cudaErrorNotSupported when the pairs have no plan for the shape (the caller then runs
-// the GEMM and the post-QKV scatter).
+bool gemm_store_pair_plan(const void* A, const void* B0, const void* B1, const void* B2, int split0, int split1, int M,
+                          int N, int K, const void* scratch, size_t scratch_bytes, PairPlan* pp);
+// [q | k | v] = x [Wq; Wk; Wv]^T with RoPE and the scatter in the epilogue (EPI_QKV_ROPE), on the
+// CTA-pair plan launch_gemm takes for the projection alone, so that every output is summed as
+// there; cudaErrorNotSupported when launch_gemm would not take pairs (the caller then runs the
+// GEMM and the post-QKV scatter).
 cudaError_t launch_qkv_rope_gemm(const void* x, const void* wq, const void* wk, const void* wv, int M, int d,
-                                 const QkvRope& qr, int32_t* status, cudaStream_t s);
+                                 const QkvRope& qr, int32_t* status, const void* scratch, size_t scratch_bytes,
+                                 cudaStream_t s);
 void set_qkv_fusion(bool enabled);
 bool qkv_fusion();
 void gemm_set_pairing(int m);  // 0 model, 1 never, 2 clusters of one pair, 4 of two pairs
