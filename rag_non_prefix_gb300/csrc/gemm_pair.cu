@@ -74,6 +74,8 @@ struct Params {
   int stg_off;         // epilogue staging: offset (after the ring)
   int slabs;           // output slabs in the staging area (2, 4, 8 or 16)
   QkvRope qr;          // EPI_QKV_ROPE only
+  int rope_rows;       // EPI_QKV_ROPE: map 0 (q) and map 1 (k) are 4-D maps that interleave each
+                       // head's rows i and i + 64 (the rotation's pairs in neighbouring lanes)
 };
 
 // The idx-th unit of cluster cid, round-robin (false when there is none).
@@ -170,10 +172,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const uint16_t mc_mask = static_cast<uint16_t>((1u << h) | (1u << (2 + h)));  // (0,h) and (1,h)
       // this CTA's 128 weight rows of unit u: rows r_lo.. of map m_lo, then r_hi.. of map m_hi
-      auto weight_rows = [&](int u, const CUtensorMap*& m_lo, const CUtensorMap*& m_hi, int& r_lo, int& r_hi) {
+      auto weight_rows = [&](int u, const CUtensorMap*& m_lo, const CUtensorMap*& m_hi, int& r_lo, int& r_hi,
+                             bool& inter) {
         const int wt = u / p.tok_groups;
         m_lo = &tmW0;
         m_hi = &tmW1;
+        inter = false;
         if (p.mode == EPI_SWIGLU) {
           r_lo = r_hi = wt * 128 + h * 64;  // 64 gate rows, then the up rows of the same features
         } else {
@@ -190,15 +194,25 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           m_lo = m_hi = m;
           r_lo = r;
           r_hi = r + 64;
+          inter = p.rope_rows && f < p.split1;  // q or k head: r_lo / 128 is the head
         }
       };
       // weight atom j of stage s (k-block kb): to this CTA, and by multicast in clusters of two pairs
       auto load_weight_atom = [&](uint32_t s, int kb, int j, const CUtensorMap* m_lo, const CUtensorMap* m_hi, int r_lo,
-                                  int r_hi) {
+                                  int r_hi, bool inter) {
         uint8_t* aj = ring + s * static_cast<uint32_t>(p.stage_bytes) + j * A_ATOM;
         const uint32_t bar = mapa_shared(smem_u32(&full[s]), lead);
         const int k0 = (kb * p.ksub + j) * BK;
-        if (PPC == 2) {
+        if (inter) {
+          // rows (i, i + 64) of the head for i < 32, then for i >= 32: 64 rows per box
+          const int head = r_lo / ROWS;
+          if (PPC == 2) {
+            tma_load_4d_pair_mc(aj + q * (A_ATOM / 2), m_lo, bar, k0, 0, q * 32, head, mc_mask);
+          } else {
+            tma_load_4d_pair(aj, m_lo, bar, k0, 0, 0, head);
+            tma_load_4d_pair(aj + A_ATOM / 2, m_lo, bar, k0, 0, 32, head);
+          }
+        } else if (PPC == 2) {
           // half of the weight rows, to this CTA and to its counterpart in the other pair
           if (q == 0)
             tma_load_2d_pair_mc(aj, m_lo, bar, k0, r_lo, mc_mask);
@@ -217,7 +231,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
         const int trow = tt * p.bt + h * half_rows;  // first token this CTA stages
         const CUtensorMap *m_lo, *m_hi;
         int r_lo, r_hi;
-        weight_rows(u, m_lo, m_hi, r_lo, r_hi);
+        bool inter;
+        weight_rows(u, m_lo, m_hi, r_lo, r_hi, inter);
         for (int kb = 0; kb < p.n_kb; ++kb) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
@@ -229,7 +244,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           // weight atoms first, e.g. the Yi-34B gate/up 482 -> 465 us)
           if (even) mbar_arrive_expect_tx(&full[s], 2u * static_cast<uint32_t>(p.stage_bytes));
           for (int j = 0; j < p.ksub; ++j) {
-            load_weight_atom(s, kb, j, m_lo, m_hi, r_lo, r_hi);
+            load_weight_atom(s, kb, j, m_lo, m_hi, r_lo, r_hi, inter);
             tma_load_2d_pair(sb + j * b_atom, &tmX, bar, (kb * p.ksub + j) * BK, trow);
           }
           if (++s == stages) {
@@ -392,7 +407,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
         const int f0 = wt * 256 + h * 128;
         const int kind = f0 < p.split0 ? 0 : f0 < p.split1 ? 1 : 2;  // q, k, v
         const int head = (kind == 0 ? f0 : kind == 1 ? f0 - p.split0 : f0 - p.split1) / ROWS;
-        const int di = r_loc & 63;
+        const int di = p.rope_rows ? r_loc >> 1 : r_loc & 63;  // this lane's rotation pair
         const QkvRope& qr = p.qr;
         // Once per tile: the tokens' positions (clamped for the table; out-of-range rows are not
         // stored) and, for k and v, each token's destination row in the fused cache (null when
@@ -427,7 +442,30 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           tmem_ld16(tbase + c, v);
           bf16* tile = reinterpret_cast<bf16*>(last ? ring + (fresh++) * slab_bytes : slab0 + (slab % p.slabs) * slab_bytes);
           if (et == 0 && !last && kind == 0) bulk_wait_read_keep(keep);  // the store that last used this slab has read it
-          if (kind < 2) {
+          if (kind < 2 && p.rope_rows) {
+            // lane pairs (2i, 2i + 1) hold rows i and i + 64: the partner's value by a shuffle
+            float2 cs[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              cs[j] = cs1[j];
+              cs1[j] = cs2[j];
+            }
+            if (c + 32 < nt) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                cs2[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(c + 32 + j, nt - 1)]) * 64 + di);
+            }
+            const bool lo = (r_loc & 1) == 0;
+            const int dim = (r_loc >> 1) + (lo ? 0 : 64);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float w = __shfl_xor_sync(0xffffffffu, v[j], 1);
+              const float a = lo ? v[j] : w;
+              const float b = lo ? w : v[j];
+              const float o = lo ? a * cs[j].x - b * cs[j].y : b * cs[j].x + a * cs[j].y;
+              tile[j * ROWS + dim] = __float2bfloat16_rn(o);
+            }
+          } else if (kind < 2) {
             float2 cs[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -647,6 +685,32 @@ bool plan_gemm_pair(int M, int N, int K, int split0, int split1, int mode, int f
   return true;
 }
 
+// 4-D map over a [heads x 128][K] bf16 weight whose box of 64 rows is rows (i, i + 64) of one
+// head for 32 consecutive i: dims {K, 2, 64, heads}, strides 64 rows, 1 row, 128 rows.
+static bool encode_rope_rows(CUtensorMap* map, const void* w, int K, int heads) {
+  typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<EncodeFn>(f);
+  }
+  if (heads <= 0 || (reinterpret_cast<uintptr_t>(w) & 15u) != 0) return false;
+  const cuuint64_t row = static_cast<cuuint64_t>(K) * 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(K), 2, 64, static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[3] = {64 * row, row, 128 * row};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(pr::BK), 2, 32, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(w), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int CL>
 static cudaError_t launch_pair_cl(const CUtensorMap& x, const CUtensorMap& w0, const CUtensorMap& w1,
                                   const CUtensorMap& w2, const CUtensorMap& c, pr::Params p, int clusters,
@@ -669,7 +733,8 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   const bool swiglu = mode == EPI_SWIGLU;
-  CUtensorMap mx, mw0, mw1, mw2, mc;
+  CUtensorMap mx, mw0, mw1, mw2, mc, mq4, mk4;
+  bool rope_rows = false;
   if (!encode_tmap(&mx, BF, A, K, M, static_cast<uint64_t>(K) * 2, pr::BK, g.bt / 2, SW)) return cudaErrorInvalidValue;
   if (swiglu) {
     if (!encode_tmap(&mw0, BF, B0, K, N / 2, static_cast<uint64_t>(K) * 2, pr::BK, 64, SW) ||
@@ -690,6 +755,14 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
     if (r2 > 0 && !encode_tmap(&mw2, BF, B2, K, r2, static_cast<uint64_t>(K) * 2, pr::BK, 64, SW))
       return cudaErrorInvalidValue;
     if (mode == EPI_QKV_ROPE) {
+      // q and k rows of a head interleaved as (i, i + 64): 4-D maps {K, 2 (i or i + 64), 64 (i),
+      // heads}, 64 rows per box; if the driver refuses the layout, the epilogue pairs the rows
+      // through shared memory instead
+      rope_rows = encode_rope_rows(&mq4, B0, K, split0 / 128) && encode_rope_rows(&mk4, B1, K, r1 / 128);
+      if (rope_rows) {
+        mw0 = mq4;
+        mw1 = mk4;
+      }
       // bf16 q_out [M][q_width]: 16 tokens x one head of 128 per store
       if ((reinterpret_cast<uintptr_t>(qr->q_out) & 15u) != 0 ||
           !encode_tmap(&mc, BF, qr->q_out, qr->q_width, M, static_cast<uint64_t>(qr->q_width) * 2, pr::ROWS, 16,
@@ -725,6 +798,7 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
   p.stg_off = l.stg_off;
   p.slabs = l.slabs;
   if (qr) p.qr = *qr;
+  p.rope_rows = rope_rows ? 1 : 0;
   if (g.cl == 4) return launch_pair_cl<4>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
   return launch_pair_cl<2>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
 }
