@@ -41,8 +41,8 @@ constexpr int OFF_RING = 1024;            // after the barriers
 constexpr int SMEM_ALLOC = 232448;        // the per-block maximum (227 KiB), 1 KiB of it aligns the base
 constexpr int SMEM_USE = SMEM_ALLOC - 1024;
 constexpr int XCH_BYTES = 4608;           // SwiGLU exchange: 2 x 64 rows x 9 floats
-// RoPE epilogue: exchange of 128 rows x 17 floats, the tile's positions and its K/V destination rows
-constexpr int XCH_ROPE = 128 * 17 * 4 + 256 * 4 + 256 * 8;
+// RoPE epilogue: the tile's positions and its K/V destination rows
+constexpr int XCH_ROPE = 256 * 4 + 256 * 8;
 constexpr int F32_SLAB = 8 * ROWS * 4;    // 8 tokens x 128 features fp32
 constexpr int F32_SLAB_TOK = 8;
 constexpr int BF_SLAB = 16 * 64 * 2;      // 16 tokens x 64 features bf16
@@ -74,8 +74,6 @@ struct Params {
   int stg_off;         // epilogue staging: offset (after the ring)
   int slabs;           // output slabs in the staging area (2, 4, 8 or 16)
   QkvRope qr;          // EPI_QKV_ROPE only
-  int rope_rows;       // EPI_QKV_ROPE: map 0 (q) and map 1 (k) are 4-D maps that interleave each
-                       // head's rows i and i + 64 (the rotation's pairs in neighbouring lanes)
 };
 
 // The idx-th unit of cluster cid, round-robin (false when there is none).
@@ -194,7 +192,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           m_lo = m_hi = m;
           r_lo = r;
           r_hi = r + 64;
-          inter = p.rope_rows && f < p.split1;  // q or k head: r_lo / 128 is the head
+          inter = p.mode == EPI_QKV_ROPE && f < p.split1;  // q or k head: r_lo / 128 is the head
         }
       };
       // weight atom j of stage s (k-block kb): to this CTA, and by multicast in clusters of two pairs
@@ -330,8 +328,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
     const bool swig = p.mode == EPI_SWIGLU;
     float* xg = reinterpret_cast<float*>(stg);  // SwiGLU: gate of tokens 8-15 [64][9]
     float* xu = xg + 64 * 9;                     //         up of tokens 0-7 [64][9]
-    float* xr = reinterpret_cast<float*>(stg);   // RoPE: [128][17], then the unit's positions [256]
-    int* upos = reinterpret_cast<int*>(xr + 128 * 17);
+    int* upos = reinterpret_cast<int*>(stg);     // RoPE: the tile's positions [256]
     bf16** udst = reinterpret_cast<bf16**>(upos + 256);
     uint8_t* slab0 = stg + epi_xch(p.mode);
     const int slab_bytes = epi_slab(p.mode);
@@ -399,15 +396,14 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           }
         }
       } else if (p.mode == EPI_QKV_ROPE) {
-        // This CTA's 128 rows are one head of q, k or v.  Per 16 tokens: q and k exchange
-        // their rows through shared memory (dimension i pairs with i + 64), rotate at each
-        // token's position and round to bf16 into a 16-token x 128-dimension tile; q's tile is
-        // one TMA store into q_out, k's and v's rows are copied to the fused cache row of each
-        // token's position (256 contiguous bytes per token).
+        // This CTA's 128 rows are one head of q, k or v.  Per 16 tokens: q and k rotate at each
+        // token's position (dimension i with i + 64) and round to bf16 into a 16-token x
+        // 128-dimension tile; q's tile is one TMA store into q_out, k's and v's rows are copied
+        // to the fused cache row of each token's position (256 contiguous bytes per token).
         const int f0 = wt * 256 + h * 128;
         const int kind = f0 < p.split0 ? 0 : f0 < p.split1 ? 1 : 2;  // q, k, v
         const int head = (kind == 0 ? f0 : kind == 1 ? f0 - p.split0 : f0 - p.split1) / ROWS;
-        const int di = p.rope_rows ? r_loc >> 1 : r_loc & 63;  // this lane's rotation pair
+        const int di = r_loc >> 1;  // q, k: this lane's rotation pair (rows interleaved)
         const QkvRope& qr = p.qr;
         // Once per tile: the tokens' positions (clamped for the table; out-of-range rows are not
         // stored) and, for k and v, each token's destination row in the fused cache (null when
@@ -442,8 +438,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           tmem_ld16(tbase + c, v);
           bf16* tile = reinterpret_cast<bf16*>(last ? ring + (fresh++) * slab_bytes : slab0 + (slab % p.slabs) * slab_bytes);
           if (et == 0 && !last && kind == 0) bulk_wait_read_keep(keep);  // the store that last used this slab has read it
-          if (kind < 2 && p.rope_rows) {
-            // lane pairs (2i, 2i + 1) hold rows i and i + 64: the partner's value by a shuffle
+          if (kind < 2) {
+            // q and k rows are loaded interleaved: lane pairs (2i, 2i + 1) hold rows i and i + 64
+            // of the head, which meet by a shuffle
             float2 cs[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -464,29 +461,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
               const float b = lo ? w : v[j];
               const float o = lo ? a * cs[j].x - b * cs[j].y : b * cs[j].x + a * cs[j].y;
               tile[j * ROWS + dim] = __float2bfloat16_rn(o);
-            }
-          } else if (kind < 2) {
-            float2 cs[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              cs[j] = cs1[j];
-              cs1[j] = cs2[j];
-            }
-            if (c + 32 < nt) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                cs2[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(c + 32 + j, nt - 1)]) * 64 + di);
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xr[r_loc * 17 + j] = v[j];
-            epi_bar();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              // rows i and i + 64 of the head: (a, b) -> (a cos - b sin, b cos + a sin)
-              const float a = r_loc < 64 ? v[j] : xr[(r_loc - 64) * 17 + j];
-              const float b = r_loc < 64 ? xr[(r_loc + 64) * 17 + j] : v[j];
-              const float o = r_loc < 64 ? a * cs[j].x - b * cs[j].y : b * cs[j].x + a * cs[j].y;
-              tile[j * ROWS + r_loc] = __float2bfloat16_rn(o);
             }
           } else {
 #pragma unroll
@@ -733,8 +707,7 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
   const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
   const bool swiglu = mode == EPI_SWIGLU;
-  CUtensorMap mx, mw0, mw1, mw2, mc, mq4, mk4;
-  bool rope_rows = false;
+  CUtensorMap mx, mw0, mw1, mw2, mc;
   if (!encode_tmap(&mx, BF, A, K, M, static_cast<uint64_t>(K) * 2, pr::BK, g.bt / 2, SW)) return cudaErrorInvalidValue;
   if (swiglu) {
     if (!encode_tmap(&mw0, BF, B0, K, N / 2, static_cast<uint64_t>(K) * 2, pr::BK, 64, SW) ||
@@ -756,13 +729,10 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
       return cudaErrorInvalidValue;
     if (mode == EPI_QKV_ROPE) {
       // q and k rows of a head interleaved as (i, i + 64): 4-D maps {K, 2 (i or i + 64), 64 (i),
-      // heads}, 64 rows per box; if the driver refuses the layout, the epilogue pairs the rows
-      // through shared memory instead
-      rope_rows = encode_rope_rows(&mq4, B0, K, split0 / 128) && encode_rope_rows(&mk4, B1, K, r1 / 128);
-      if (rope_rows) {
-        mw0 = mq4;
-        mw1 = mk4;
-      }
+      // heads}, 64 rows per box (a driver that refuses the layout leaves the caller the separate
+      // kernels)
+      if (!encode_rope_rows(&mw0, B0, K, split0 / 128) || !encode_rope_rows(&mw1, B1, K, r1 / 128))
+        return cudaErrorNotSupported;
       // bf16 q_out [M][q_width]: 16 tokens x one head of 128 per store
       if ((reinterpret_cast<uintptr_t>(qr->q_out) & 15u) != 0 ||
           !encode_tmap(&mc, BF, qr->q_out, qr->q_width, M, static_cast<uint64_t>(qr->q_width) * 2, pr::ROWS, 16,
@@ -798,7 +768,6 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
   p.stg_off = l.stg_off;
   p.slabs = l.slabs;
   if (qr) p.qr = *qr;
-  p.rope_rows = rope_rows ? 1 : 0;
   if (g.cl == 4) return launch_pair_cl<4>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
   return launch_pair_cl<2>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
 }
