@@ -395,7 +395,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
             bulk_commit();
           }
         }
-      } else if (p.mode == EPI_QKV_ROPE) {
+      } else if (p.mode == EPI_QKV_ROPE && nt > 0) {  // (uniform; a pad tile stores nothing)
         // This CTA's 128 rows are one head of q, k or v.  Per 16 tokens: q and k rotate at each
         // token's position (dimension i with i + 64) and round to bf16 into a 16-token x
         // 128-dimension tile; q's tile is one TMA store into q_out, k's and v's rows are copied
@@ -486,7 +486,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
             }
           }
         }
-      } else {
+      } else if (p.mode != EPI_QKV_ROPE) {
         // 8-token x 128-feature fp32 slabs, one TMA store (or add-reduction) each; a
         // 16-column tensor-memory load feeds two of them
         const int f0 = wt * 256 + h * 128;

@@ -133,13 +133,17 @@ def _forced_bf16(small_bf16):
     assert max_rel_err(to_np(req["hidden"])[ref["rows"]], ref["hidden"]) < 2e-2
 
 
-@pytest.mark.parametrize("name,schedule", [("small_bf16", "gradual"), ("small_mha_bf16", "fixed")])
-def test_bf16_blend_fused_qkv_matches_separate_kernels(name, schedule):
+@pytest.mark.parametrize("name,schedule,pairing,tile", [("small_bf16", "gradual", 2, 0), ("small_mha_bf16", "fixed", 2, 0),
+                                                      ("small_bf16", "gradual", 4, 192)],
+                         ids=["gqa-pairs", "mha-pairs-fixed", "gqa-two-pair-clusters-pad-tile"])
+def test_bf16_blend_fused_qkv_matches_separate_kernels(name, schedule, pairing, tile):
     """The layers without a check run Q/K/V, RoPE and the K/V scatter in the paired GEMM's
     epilogue; with the paired GEMM forced in both runs, the blend's sets, hidden rows and first
     token are bit for bit those of the projection followed by the post-QKV kernel (the same
     sums, the same rotation arithmetic, the same roundings).  The fixed schedule checks only
-    layer 1, so every other layer takes the fused path."""
+    layer 1, so every other layer takes the fused path; clusters of two pairs with 192-token
+    tiles give layer 0's 552 rows three token tiles, the second pair of the last cluster unit a
+    tile past the rows (nothing stored)."""
     spec = hz.workload(name)
     if schedule != spec.schedule:
         spec = hz.make_prompt(name, 12, [96, 128], 24, spec.ratio, schedule, "zipf", name=name + "_fixed")
@@ -147,7 +151,8 @@ def test_bf16_blend_fused_qkv_matches_separate_kernels(name, schedule):
     cfg = spec.cfg
     ratios = [float(x) for x in orc.ratio_schedule(cfg.n_layers, spec.ratio, spec.schedule)]
     outs = []
-    cb.cb_gemm_set_pairing(2)
+    cb.cb_gemm_set_pairing(pairing)
+    cb.cb_gemm_set_orientation(tile)
     try:
         for fused in (True, False):
             cb.cb_set_qkv_fusion(fused)
@@ -157,6 +162,7 @@ def test_bf16_blend_fused_qkv_matches_separate_kernels(name, schedule):
     finally:
         cb.cb_set_qkv_fusion(True)
         cb.cb_gemm_set_pairing(0)
+        cb.cb_gemm_set_orientation(0)
     (h1, s1, t1), (h2, s2, t2) = outs
     assert np.array_equal(h1, h2)
     assert t1 == t2
