@@ -463,6 +463,8 @@ def summary(m):
                         "full_median": r4(statistics.median(m["full_runs"]))},
             "runs_ms": {"blend": [round(x, 3) for x in m["blend_runs"]], "full_prefill": [round(x, 3) for x in m["full_runs"]]},
             "speedup_vs_full_prefill": round(m["speedup"], 3),
+            # on the medians too: a staged configuration's runs can stall on the host's copies
+            "speedup_vs_full_prefill_median": round(statistics.median(m["full_runs"]) / statistics.median(m["blend_runs"]), 3),
             "context_tok_s": {"blend": round(m["blend_tok_s"], 1), "full_prefill": round(m["full_tok_s"], 1)},
             "gemm_roofline": {"blend": m["gemm_blend"], "full_prefill": m["gemm_full"]},
             "attention_roofline": {"blend": m["attn_blend"], "full_prefill": m["attn_full"]},
