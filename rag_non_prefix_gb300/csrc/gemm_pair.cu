@@ -104,7 +104,9 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 
 // Unit u of the persistent loop: weight tile u / tok_groups, token group u % tok_groups
 // (consecutive clusters take the same weight rows, which then come from DRAM once).
-template <int CL>
+// ROPE: the EPI_QKV_ROPE instantiation (its producer loads q and k rows interleaved, its
+// epilogue rotates); the other epilogues run in the instantiation without it.
+template <int CL, bool ROPE>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW0,
                      const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW2,
@@ -192,7 +194,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
           m_lo = m_hi = m;
           r_lo = r;
           r_hi = r + 64;
-          inter = p.mode == EPI_QKV_ROPE && f < p.split1;  // q or k head: r_lo / 128 is the head
+          inter = ROPE && f < p.split1;  // q or k head: r_lo / 128 is the head
         }
       };
       // weight atom j of stage s (k-block kb): to this CTA, and by multicast in clusters of two pairs
@@ -395,98 +397,100 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1)
             bulk_commit();
           }
         }
-      } else if (p.mode == EPI_QKV_ROPE && nt > 0) {  // (uniform; a pad tile stores nothing)
-        // This CTA's 128 rows are one head of q, k or v.  Per 16 tokens: q and k rotate at each
-        // token's position (dimension i with i + 64) and round to bf16 into a 16-token x
-        // 128-dimension tile; q's tile is one TMA store into q_out, k's and v's rows are copied
-        // to the fused cache row of each token's position (256 contiguous bytes per token).
-        const int f0 = wt * 256 + h * 128;
-        const int kind = f0 < p.split0 ? 0 : f0 < p.split1 ? 1 : 2;  // q, k, v
-        const int head = (kind == 0 ? f0 : kind == 1 ? f0 - p.split0 : f0 - p.split1) / ROWS;
-        const int di = r_loc >> 1;  // q, k: this lane's rotation pair (rows interleaved)
-        const QkvRope& qr = p.qr;
-        // Once per tile: the tokens' positions (clamped for the table; out-of-range rows are not
-        // stored) and, for k and v, each token's destination row in the fused cache (null when
-        // the position is out of range).  (cos, sin) of a round's 16 tokens are loaded two
-        // rounds ahead.
-        for (int x = et; x < nt; x += 128) {
-          const int pos = __ldg(qr.s_pos + t0 + x);
-          upos[x] = min(max(pos, 0), qr.max_pos - 1);
-          if (kind > 0) {
-            const ReqDev rq = qr.reqs[__ldg(qr.s_req + t0 + x)];
-            bf16* row = nullptr;
-            if (pos >= 0 && pos < rq.n_tokens && pos < qr.max_pos) {
-              row = static_cast<bf16*>(kind == 1 ? rq.k : rq.v) + static_cast<size_t>(qr.layer) * rq.layer_stride +
-                    static_cast<size_t>(pos) * qr.kvw + head * ROWS;
-            } else {
-              set_status(p.status, ST_RANGE);
+      } else if (ROPE) {
+        if (nt > 0) {  // (uniform) a pad tile stores nothing
+          // This CTA's 128 rows are one head of q, k or v.  Per 16 tokens: q and k rotate at each
+          // token's position (dimension i with i + 64) and round to bf16 into a 16-token x
+          // 128-dimension tile; q's tile is one TMA store into q_out, k's and v's rows are copied
+          // to the fused cache row of each token's position (256 contiguous bytes per token).
+          const int f0 = wt * 256 + h * 128;
+          const int kind = f0 < p.split0 ? 0 : f0 < p.split1 ? 1 : 2;  // q, k, v
+          const int head = (kind == 0 ? f0 : kind == 1 ? f0 - p.split0 : f0 - p.split1) / ROWS;
+          const int di = r_loc >> 1;  // q, k: this lane's rotation pair (rows interleaved)
+          const QkvRope& qr = p.qr;
+          // Once per tile: the tokens' positions (clamped for the table; out-of-range rows are not
+          // stored) and, for k and v, each token's destination row in the fused cache (null when
+          // the position is out of range).  (cos, sin) of a round's 16 tokens are loaded two
+          // rounds ahead.
+          for (int x = et; x < nt; x += 128) {
+            const int pos = __ldg(qr.s_pos + t0 + x);
+            upos[x] = min(max(pos, 0), qr.max_pos - 1);
+            if (kind > 0) {
+              const ReqDev rq = qr.reqs[__ldg(qr.s_req + t0 + x)];
+              bf16* row = nullptr;
+              if (pos >= 0 && pos < rq.n_tokens && pos < qr.max_pos) {
+                row = static_cast<bf16*>(kind == 1 ? rq.k : rq.v) + static_cast<size_t>(qr.layer) * rq.layer_stride +
+                      static_cast<size_t>(pos) * qr.kvw + head * ROWS;
+              } else {
+                set_status(p.status, ST_RANGE);
+              }
+              udst[x] = row;
             }
-            udst[x] = row;
           }
-        }
-        epi_bar();
-        float2 cs1[16], cs2[16];
-        if (kind < 2) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) cs1[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(j, nt - 1)]) * 64 + di);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) cs2[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(16 + j, nt - 1)]) * 64 + di);
-        }
-#pragma unroll 1
-        for (int c = 0; c < nt; c += 16, ++slab) {
-          float v[16];
-          tmem_ld16(tbase + c, v);
-          bf16* tile = reinterpret_cast<bf16*>(last ? ring + (fresh++) * slab_bytes : slab0 + (slab % p.slabs) * slab_bytes);
-          if (et == 0 && !last && kind == 0) bulk_wait_read_keep(keep);  // the store that last used this slab has read it
-          if (kind < 2) {
-            // q and k rows are loaded interleaved: lane pairs (2i, 2i + 1) hold rows i and i + 64
-            // of the head, which meet by a shuffle
-            float2 cs[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              cs[j] = cs1[j];
-              cs1[j] = cs2[j];
-            }
-            if (c + 32 < nt) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                cs2[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(c + 32 + j, nt - 1)]) * 64 + di);
-            }
-            const bool lo = (r_loc & 1) == 0;
-            const int dim = (r_loc >> 1) + (lo ? 0 : 64);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float w = __shfl_xor_sync(0xffffffffu, v[j], 1);
-              const float a = lo ? v[j] : w;
-              const float b = lo ? w : v[j];
-              const float o = lo ? a * cs[j].x - b * cs[j].y : b * cs[j].x + a * cs[j].y;
-              tile[j * ROWS + dim] = __float2bfloat16_rn(o);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) tile[j * ROWS + r_loc] = __float2bfloat16_rn(v[j]);
-          }
-          fence_proxy_async_smem();
           epi_bar();
-          if (kind == 0) {
-            if (et == 0) {
-              tma_store_2d(&tmC, tile, head * ROWS, t0 + c);
-              bulk_commit();
+          float2 cs1[16], cs2[16];
+          if (kind < 2) {
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) cs1[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(j, nt - 1)]) * 64 + di);
+  #pragma unroll
+            for (int j = 0; j < 16; ++j) cs2[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(16 + j, nt - 1)]) * 64 + di);
+          }
+  #pragma unroll 1
+          for (int c = 0; c < nt; c += 16, ++slab) {
+            float v[16];
+            tmem_ld16(tbase + c, v);
+            bf16* tile = reinterpret_cast<bf16*>(last ? ring + (fresh++) * slab_bytes : slab0 + (slab % p.slabs) * slab_bytes);
+            if (et == 0 && !last && kind == 0) bulk_wait_read_keep(keep);  // the store that last used this slab has read it
+            if (kind < 2) {
+              // q and k rows are loaded interleaved: lane pairs (2i, 2i + 1) hold rows i and i + 64
+              // of the head, which meet by a shuffle
+              float2 cs[16];
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                cs[j] = cs1[j];
+                cs1[j] = cs2[j];
+              }
+              if (c + 32 < nt) {
+  #pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  cs2[j] = __ldg(qr.rope + static_cast<size_t>(upos[min(c + 32 + j, nt - 1)]) * 64 + di);
+              }
+              const bool lo = (r_loc & 1) == 0;
+              const int dim = (r_loc >> 1) + (lo ? 0 : 64);
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float w = __shfl_xor_sync(0xffffffffu, v[j], 1);
+                const float a = lo ? v[j] : w;
+                const float b = lo ? w : v[j];
+                const float o = lo ? a * cs[j].x - b * cs[j].y : b * cs[j].x + a * cs[j].y;
+                tile[j * ROWS + dim] = __float2bfloat16_rn(o);
+              }
+            } else {
+  #pragma unroll
+              for (int j = 0; j < 16; ++j) tile[j * ROWS + r_loc] = __float2bfloat16_rn(v[j]);
             }
-          } else {
-            // two tokens per thread, 16 bytes of each
-            const int ch = et & 15;
-#pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
-              const int j = (et >> 4) + pass * 8;
-              if (c + j < nt) {
-                bf16* row = udst[c + j];
-                if (row) *reinterpret_cast<uint4*>(row + ch * 8) = *reinterpret_cast<const uint4*>(tile + j * ROWS + ch * 8);
+            fence_proxy_async_smem();
+            epi_bar();
+            if (kind == 0) {
+              if (et == 0) {
+                tma_store_2d(&tmC, tile, head * ROWS, t0 + c);
+                bulk_commit();
+              }
+            } else {
+              // two tokens per thread, 16 bytes of each
+              const int ch = et & 15;
+  #pragma unroll
+              for (int pass = 0; pass < 2; ++pass) {
+                const int j = (et >> 4) + pass * 8;
+                if (c + j < nt) {
+                  bf16* row = udst[c + j];
+                  if (row) *reinterpret_cast<uint4*>(row + ch * 8) = *reinterpret_cast<const uint4*>(tile + j * ROWS + ch * 8);
+                }
               }
             }
           }
         }
-      } else if (p.mode != EPI_QKV_ROPE) {
+      } else {
         // 8-token x 128-feature fp32 slabs, one TMA store (or add-reduction) each; a
         // 16-column tensor-memory load feeds two of them
         const int f0 = wt * 256 + h * 128;
@@ -576,8 +580,9 @@ static int max_clusters(int cl) {
     const int v = cache[ci][dev].load();
     if (v > 0) return v;
   }
-  const void* fn = cl == 4 ? reinterpret_cast<const void*>(pr::gemm_pair_kernel<4>)
-                           : reinterpret_cast<const void*>(pr::gemm_pair_kernel<2>);
+  // (the RoPE instantiation has the same block and shared memory: one CTA per SM either way)
+  const void* fn = cl == 4 ? reinterpret_cast<const void*>(pr::gemm_pair_kernel<4, false>)
+                           : reinterpret_cast<const void*>(pr::gemm_pair_kernel<2, false>);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, pr::SMEM_ALLOC) != cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -685,16 +690,17 @@ static bool encode_rope_rows(CUtensorMap* map, const void* w, int K, int heads) 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int CL>
+template <int CL, bool ROPE>
 static cudaError_t launch_pair_cl(const CUtensorMap& x, const CUtensorMap& w0, const CUtensorMap& w1,
                                   const CUtensorMap& w2, const CUtensorMap& c, pr::Params p, int clusters,
                                   cudaStream_t s) {
   static DeviceOnce configured;
-  cudaError_t e = max_dynamic_smem_once(reinterpret_cast<const void*>(pr::gemm_pair_kernel<CL>), pr::SMEM_ALLOC,
-                                        configured);
+  cudaError_t e = max_dynamic_smem_once(reinterpret_cast<const void*>(pr::gemm_pair_kernel<CL, ROPE>),
+                                        pr::SMEM_ALLOC, configured);
   if (e != cudaSuccess) return e;
   const int n = std::min(clusters, p.units);
-  launch_chain(pr::gemm_pair_kernel<CL>, dim3(CL * n), dim3(pr::THREADS), pr::SMEM_ALLOC, s, x, w0, w1, w2, c, p);
+  launch_chain(pr::gemm_pair_kernel<CL, ROPE>, dim3(CL * n), dim3(pr::THREADS), pr::SMEM_ALLOC, s, x, w0, w1, w2, c,
+               p);
   return cudaGetLastError();
 }
 
@@ -768,8 +774,12 @@ cudaError_t launch_gemm_pair(const PairPlan& g, const void* A, const void* B0, c
   p.stg_off = l.stg_off;
   p.slabs = l.slabs;
   if (qr) p.qr = *qr;
-  if (g.cl == 4) return launch_pair_cl<4>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
-  return launch_pair_cl<2>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
+  if (mode == EPI_QKV_ROPE) {
+    if (g.cl == 4) return launch_pair_cl<4, true>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
+    return launch_pair_cl<2, true>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
+  }
+  if (g.cl == 4) return launch_pair_cl<4, false>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
+  return launch_pair_cl<2, false>(mx, mw0, mw1, mw2, mc, p, g.clusters, s);
 }
 
 // Process-wide: the blend's uncompacted layers take QKV, RoPE and the scatter in one launch
